@@ -1,0 +1,576 @@
+"""Benchmark: paged GQA decode attention over 12-bit compressed BF16 KV pages on GB300.
+
+Default workload: one Llama-3.1-8B-shaped attention layer at decode -- batch 32, 32
+query heads, 8 KV heads, head dim 128, 2048 tokens in 128 compressed 16-token pages
+per sequence (shuffled physical order) plus a raw tail of 1..15 tokens.  A step is one
+kvz_decode_attention call over the whole batch (attention + split merge).  Synthetic,
+seeded inputs (kvgen); the KV is resident in HBM before timing starts.
+
+Reported: logical-KV GB/s (BF16 K+V bytes attended / time) as `value`, µs per step,
+the in-run raw-BF16 kernel on the same pages, the compressed-block fraction, encode and
+standalone-decode GB/s, the dominant kernel's HBM roofline fraction, an end-to-end
+figure through the C ABI with host buffers, and the CPU oracle timed on host cores.
+
+Timing rules: >= 3 warm-up steps; the timed steps are one CUDA graph replay over
+rotating copies of the KV (3 copies, ~0.6 GB, > L2) so every step reads cold data;
+CUDA events on the launching stream, synchronize on both sides, max over ranks.
+`--impl reference` times the CPU oracle (the reference arm of this build).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import kvgen  # noqa: E402
+
+METRIC = "decode-attention µs/step & logical KV GB/s; % of HBM roofline; encode GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# --------------------------------------------------------------------------------------
+# helpers
+# --------------------------------------------------------------------------------------
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        return dist, rank, ws, local
+    return None, rank, ws, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        if not self.out:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in ("decode_attention_value_gb300/csrc/attention.cu", "decode_attention_value_gb300/csrc/kvz_device.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """dram bytes per launch of the compressed attention kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", f"k_attn_compressed_{workload}.md")
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    with open(p) as fh:
+        for line in fh:
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# --------------------------------------------------------------------------------------
+# workload
+# --------------------------------------------------------------------------------------
+class Workload:
+    """One decode layer: raw pool, page table, tails, queries, and `copies` compressed
+    copies of the same pages at different addresses (so consecutive steps read cold KV)."""
+
+    def __init__(self, cfg: kvgen.KVConfig, copies: int, layer: int = 0, dev="cuda"):
+        import decode_attention_value_gb300 as kvz
+
+        self.kvz, self.cfg = kvz, cfg
+        B, hq, hkv = cfg.batch, cfg.hq, cfg.hkv
+        lay = kvgen.gen_layout(cfg)
+        self.table = lay["table"].to(dev)
+        self.seq_lens = lay["seq_lens"].to(dev)
+        self.tail_len = lay["tail_len"]
+        self.full = self.table[:, : cfg.full_pages].contiguous()
+        self.tail = self.table[:, cfg.full_pages].contiguous() if cfg.tail_max > 0 else \
+            torch.full((B,), -1, dtype=torch.int32, device=dev)
+        self.raw_table = self.table.contiguous() if cfg.tail_max > 0 else \
+            torch.cat([self.table, torch.full((B, 1), -1, dtype=torch.int32, device=dev)], 1).contiguous()
+        self.q = kvgen.gen_q(cfg, layer=layer, device="cpu").to(dev)
+        pool = kvgen.gen_pages(cfg, cfg.num_pages, layer=layer, device=dev)
+        self.pools = [pool] + [pool.clone() for _ in range(copies - 1)]
+        n = B * cfg.full_pages
+        self.src = self.full.reshape(-1).contiguous()
+        self.dseq = torch.arange(B, dtype=torch.int32, device=dev).repeat_interleave(cfg.full_pages)
+        per = (cfg.full_pages + 1) * hkv * 32
+        self.arena_bytes = B * per * 256
+        self.cursor0 = torch.tensor([[b * per, (b + 1) * per] for b in range(B)], dtype=torch.int32, device=dev)
+        self.metas, self.arenas = [], []
+        self.status = kvz.new_status(dev)
+        self.enc_ws = torch.empty(kvz.encode_workspace_size(hkv, n), dtype=torch.uint8, device=dev)
+        for c in range(copies):
+            meta = torch.zeros((cfg.num_pages, hkv, 2), dtype=torch.int64, device=dev)
+            arena = torch.zeros(self.arena_bytes, dtype=torch.uint8, device=dev)
+            cur = self.cursor0.clone()
+            kvz.encode_pages(self.pools[c], self.src, self.src, self.dseq, meta, arena, cur, self.status,
+                             workspace=self.enc_ws)
+            self.metas.append(meta)
+            self.arenas.append(arena)
+        self.out = torch.empty((B, hq, 128), dtype=torch.float32, device=dev)
+        self.out_raw = torch.empty_like(self.out)
+        self.ws_c = torch.empty(kvz.attention_workspace_size(hkv, B, hq, cfg.full_pages + 1), dtype=torch.uint8,
+                                device=dev)
+        self.ws_r = torch.empty(kvz.attention_workspace_size(hkv, B, hq, self.raw_table.shape[1]),
+                                dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize()
+        if int(self.status.item()) != 0:
+            raise RuntimeError(f"encode status {int(self.status.item())}")
+        self.copies = copies
+        self._stats()
+
+    def _stats(self):
+        cfg = self.cfg
+        meta = self.metas[0][self.src.long()]  # [n][hkv][2]
+        tags = (meta >> 32) & 0xFFFFFFFF
+        raw = torch.zeros_like(tags)
+        for j in range(4):
+            raw += (((tags >> (8 * j)) & 0xFF) == 0xFF).long()
+        nblk = tags.numel() * 4
+        self.raw_blocks = int(raw.sum())
+        self.blocks = nblk
+        self.compressed_fraction = 1.0 - self.raw_blocks / nblk
+        self.block_bytes = (nblk - self.raw_blocks) * 768 + self.raw_blocks * 1024
+        B, hq, hkv = cfg.batch, cfg.hq, cfg.hkv
+        tokens = int(self.seq_lens.sum())
+        self.logical_bytes = tokens * hkv * 2 * 128 * 2
+        pages_c = B * cfg.full_pages
+        tail_bytes = int(self.tail_len.sum()) * hkv * 2 * 128 * 2
+        q_bytes = B * hq * 128 * 2
+        out_bytes = B * hq * 128 * 4
+        grid_slots = (self.ws_c.numel()) // 1  # upper bound only; partials counted below
+        del grid_slots
+        units = B * hkv
+        # partials: each (unit, CTA) segment writes G x (128 + 2) floats, the merge reads them
+        G = hq // hkv
+        segs = units + self.grid_c() - 1
+        part_bytes = 2 * segs * G * 130 * 4
+        self.alg_bytes_c = (self.block_bytes + pages_c * hkv * 16 + pages_c * hkv * 4 + tail_bytes + q_bytes +
+                            out_bytes + part_bytes)
+        raw_pages = int(((self.seq_lens + 15) // 16).sum())
+        self.alg_bytes_r = (self.logical_bytes + raw_pages * hkv * 4 + q_bytes + out_bytes + part_bytes)
+        self.pages_c, self.tail_bytes = pages_c, tail_bytes
+
+    def grid_c(self):
+        # the kernel's grid: (workspace - prefix) / (per-slot bytes) = units + C - 1 slots
+        cfg = self.cfg
+        pre = ((cfg.batch + 1) * 4 + 15) // 16 * 16
+        slots = (self.ws_c.numel() - pre) // (4 * 128 * 4 + 4 * 2 * 4)
+        return slots - cfg.batch * cfg.hkv + 1
+
+    def step_c(self, k: int, q=None, out=None):
+        c = k % self.copies
+        self.kvz.decode_attention(self.q if q is None else q, self.full, self.seq_lens, self.tail, self.metas[c],
+                                  self.arenas[c], self.pools[c], self.out if out is None else out, self.status,
+                                  workspace=self.ws_c)
+
+    def step_r(self, k: int):
+        c = k % self.copies
+        self.kvz.decode_attention_raw(self.q, self.raw_table, self.seq_lens, self.pools[c], self.out_raw,
+                                      self.status, workspace=self.ws_r)
+
+
+def graph_of(fn, steps: int):
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for k in range(steps):
+                fn(k)
+    torch.cuda.current_stream().wait_stream(s)
+    return g
+
+
+def time_graph(g, reps: int = 1) -> float:
+    """ms for `reps` replays of a captured graph, CUDA events on the current stream."""
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(st)
+    for _ in range(reps):
+        g.replay()
+    e1.record(st)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def per_launch_ms(fn, iters: int, flush: torch.Tensor) -> float:
+    """Average duration of one call, CUDA events around it, L2 flushed before each call
+    (the flush also keeps the stream busy so the events bracket only the call)."""
+    st = torch.cuda.current_stream()
+    ts = []
+    evs = []
+    for k in range(iters):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        fn(k)
+        e1.record(st)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    for e0, e1 in evs:
+        ts.append(e0.elapsed_time(e1))
+    return sum(ts) / len(ts)
+
+
+# --------------------------------------------------------------------------------------
+# CPU oracle (cpu_baseline and the reference arm)
+# --------------------------------------------------------------------------------------
+def oracle_sample(cfg: kvgen.KVConfig, budget_s: float, seqs_max: int | None = None):
+    """Time the CPU oracle's decode attention (decode of the compressed pages + fp64
+    attention) on a bounded sample of the workload's sequences, on all host cores.
+    Returns (logical GB/s, seconds, sequences, threads)."""
+    import oracle
+
+    oracle.build()
+    lay = kvgen.gen_layout(cfg)
+    table, seq_lens = lay["table"].numpy(), lay["seq_lens"].numpy()
+    pool = kvgen.bits(kvgen.gen_pages(cfg, cfg.num_pages))
+    q = kvgen.bits(kvgen.gen_q(cfg))
+    threads = os.cpu_count() or 1
+
+    def run(sel):
+        full = table[sel, : cfg.full_pages]
+        tail = table[sel, cfg.full_pages] if cfg.tail_max > 0 else np.full(len(sel), -1, np.int32)
+        meta = np.zeros((cfg.num_pages, cfg.hkv, 2), np.uint64)
+        per = (cfg.full_pages + 1) * cfg.hkv * 32
+        arena = np.zeros(len(sel) * per * 256, np.uint8)
+        cur = np.array([[i * per, (i + 1) * per] for i in range(len(sel))], np.uint32)
+        src = full.reshape(-1).astype(np.int32)
+        seq = np.repeat(np.arange(len(sel), dtype=np.int32), cfg.full_pages)
+        oracle.encode_pages(pool, src, src, seq, meta, arena, cur, cfg.hkv)
+        t0 = time.perf_counter()
+        oracle.decode_attention(q[sel], full, seq_lens[sel], tail, meta, arena, pool, cfg.hkv, nthreads=threads)
+        return time.perf_counter() - t0
+
+    # calibrate with one sequence (all its KV heads), then size the sample to the budget
+    t1 = run([0])
+    n = max(1, min(seqs_max or cfg.batch, cfg.batch, int(budget_s / max(t1, 1e-6) * min(threads, cfg.hkv))))
+    sel = list(range(n))
+    dt = run(sel)
+    logical = int(seq_lens[sel].sum()) * cfg.hkv * 2 * 128 * 2
+    return logical / dt / 1e9, dt, n, threads
+
+
+# --------------------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kvz", choices=["kvz", "reference"])
+    ap.add_argument("--workload", default="c1", choices=["c1", "c2"])
+    ap.add_argument("--copies", type=int, default=3)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    cfg = kvgen.CONFIGS[args.workload]
+    if args.workload == "c2":
+        cfg = kvgen.KVConfig(**{**cfg.__dict__, "layers": 1})  # one layer of the 32-layer stack per step
+    dist, rank, world, local = dist_setup()
+
+    if args.impl == "reference":
+        return run_reference(args, cfg, dist, rank, world)
+
+    torch.cuda.set_device(local)
+    import decode_attention_value_gb300 as kvz
+
+    dev = torch.device("cuda", local)
+    peak, peak_kind = measured_peaks()
+    W = Workload(cfg, args.copies, layer=rank, dev=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 256 MB > L2
+
+    # warm-up (also configures the kernels) and a bit-identity spot check
+    for k in range(args.warmup):
+        W.step_c(k)
+        W.step_r(k)
+    torch.cuda.synchronize()
+    if int(W.status.item()) != 0:
+        raise RuntimeError(f"attention status {int(W.status.item())}")
+    identical = bool(torch.equal(W.out, W.out_raw))
+
+    # timed region: one graph of K steps, rotating KV copies
+    K = args.steps
+    g_c = graph_of(W.step_c, K)
+    g_r = graph_of(W.step_r, K)
+    g_c.replay()
+    g_r.replay()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        soak_until = time.time() + 0.6
+        while time.time() < soak_until:
+            g_c.replay()
+            torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ms_c = time_graph(g_c)
+        if dist:
+            dist.barrier()
+        ms_r = time_graph(g_r)
+        soak_until = time.time() + 0.4
+        while time.time() < soak_until:
+            g_c.replay()
+            torch.cuda.synchronize()
+    clocks = clk.summary()
+    if dist:
+        t = torch.tensor([ms_c, ms_r], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_c, ms_r = float(t[0]), float(t[1])
+
+    us_step = ms_c * 1e3 / K
+    us_raw = ms_r * 1e3 / K
+    value = world * W.logical_bytes / (us_step * 1e-6) / 1e9
+
+    # dominant kernel: per-launch duration with L2 flushed, algorithmic bytes per launch
+    launch_ms = per_launch_ms(W.step_c, max(10, min(K, 40)), flush)
+    launch_ms_raw = per_launch_ms(W.step_r, max(10, min(K, 40)), flush)
+    achieved = W.alg_bytes_c / (launch_ms * 1e-3) / 1e9
+    achieved_raw = W.alg_bytes_r / (launch_ms_raw * 1e-3) / 1e9
+
+    # encode and standalone decode throughput (C1 full pages, cold inputs)
+    enc_meta = torch.zeros_like(W.metas[0])
+    enc_arena = torch.zeros_like(W.arenas[0])
+    enc_cur = W.cursor0.clone()
+
+    def enc(k):
+        enc_cur.copy_(W.cursor0)
+        kvz.encode_pages(W.pools[k % W.copies], W.src, W.src, W.dseq, enc_meta, enc_arena, enc_cur, W.status,
+                         workspace=W.enc_ws)
+
+    enc_ms = per_launch_ms(enc, 10, flush)
+    enc_in = W.src.numel() * cfg.hkv * 2 * 16 * 128 * 2
+    dec_out = torch.empty((W.src.numel(), cfg.hkv, 2, 16, 128), dtype=torch.bfloat16, device=dev)
+
+    def dec(k):
+        kvz.decode_blocks(W.metas[k % W.copies], W.arenas[k % W.copies], W.src, dec_out, W.status)
+
+    dec_ms = per_launch_ms(dec, 10, flush)
+    torch.cuda.synchronize()
+    if int(W.status.item()) != 0:
+        raise RuntimeError(f"status {int(W.status.item())}")
+
+    # end to end through the C ABI with host buffers: H2D of the step's inputs, D2H of the output
+    pin_q = W.q.cpu().pin_memory()
+    pin_table = W.full.cpu().pin_memory()
+    pin_lens = W.seq_lens.cpu().pin_memory()
+    pin_tail = W.tail.cpu().pin_memory()
+    pin_out = torch.empty(W.out.shape, dtype=torch.float32).pin_memory()
+    d_q, d_table, d_lens, d_tail = (torch.empty_like(W.q), torch.empty_like(W.full), torch.empty_like(W.seq_lens),
+                                    torch.empty_like(W.tail))
+    h2d = sum(t.numel() * t.element_size() for t in (pin_q, pin_table, pin_lens, pin_tail))
+    d2h = pin_out.numel() * 4
+
+    def e2e_step(k):
+        d_q.copy_(pin_q, non_blocking=True)
+        d_table.copy_(pin_table, non_blocking=True)
+        d_lens.copy_(pin_lens, non_blocking=True)
+        d_tail.copy_(pin_tail, non_blocking=True)
+        c = k % W.copies
+        kvz.decode_attention(d_q, d_table, d_lens, d_tail, W.metas[c], W.arenas[c], W.pools[c], W.out, W.status,
+                             workspace=W.ws_c)
+        pin_out.copy_(W.out, non_blocking=True)
+
+    for k in range(3):
+        e2e_step(k)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for k in range(K):
+        e2e_step(k)
+    e1.record(st)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+    e2e_value = world * W.logical_bytes * K / (e2e_ms * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        gbps, secs, nseq, threads = oracle_sample(cfg, args.cpu_budget)
+        cpu = {"value": gbps, "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"{nseq} of {cfg.batch} sequences x {cfg.hkv} KV heads of the same layer "
+                         f"(decode of compressed pages + fp64 attention), {secs:.1f} s"}
+
+    traffic = profiled_traffic(args.workload)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(us_step / 1e3, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": cfg.name, "batch": cfg.batch, "q_heads": cfg.hq, "kv_heads": cfg.hkv,
+                   "head_dim": 128, "page_tokens": 16, "context_tokens": cfg.full_pages * 16,
+                   "tail_tokens": f"{cfg.tail_min}..{cfg.tail_max}", "page_order": "shuffled",
+                   "parallelism": f"replicas{world}",
+                   "l2": f"inputs larger than L2: {args.copies} rotating KV copies "
+                         f"({args.copies * (W.block_bytes + W.tail_bytes) / 1e9:.2f} GB compressed)"},
+        "us_per_step": round(us_step, 3),
+        "raw_us_per_step": round(us_raw, 3),
+        "speedup_vs_raw": round(us_raw / us_step, 4),
+        "expected_speedup_from_fraction": round(1.0 / (W.block_bytes / (W.blocks * 1024)), 4),
+        "compressed_fraction": round(W.compressed_fraction, 5),
+        "compressed_bytes_ratio": round(W.block_bytes / (W.blocks * 1024), 5),
+        "bit_identical_compressed_vs_raw": identical,
+        "encode_GBps": round(enc_in / (enc_ms * 1e-3) / 1e9, 2),
+        "decode_GBps": round(enc_in / (dec_ms * 1e-3) / 1e9, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
+                     "kernel": "k_attn<compressed> + k_attn_merge",
+                     "launch_us": round(launch_ms * 1e3, 3),
+                     "algorithmic_bytes_per_launch": W.alg_bytes_c},
+        "roofline_raw": {"achieved": round(achieved_raw, 1), "frac": round(achieved_raw / peak, 4),
+                         "launch_us": round(launch_ms_raw * 1e3, 3), "algorithmic_bytes_per_launch": W.alg_bytes_r},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "gpu_launches": 2 * K,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_reference(args, cfg, dist, rank, world):
+    """The CPU oracle as it stands, on the host cores: each step a bounded sample."""
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    K, Wm = args.steps, args.warmup
+    per_step_budget = max(0.5, min(4.0, 150.0 / max(1, K + Wm)))
+    vals = []
+    secs = []
+    nseq = threads = 0
+    for k in range(Wm + K):
+        gbps, dt, nseq, threads = oracle_sample(cfg, per_step_budget, seqs_max=2)
+        if k >= Wm:
+            vals.append(gbps)
+            secs.append(dt)
+    value = statistics.mean(vals)
+    logical_per_seq = (cfg.full_pages * 16 + (cfg.tail_min + cfg.tail_max) / 2) * cfg.hkv * 512
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": Wm,
+        "ms_per_step": round(1e3 * statistics.mean(secs), 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": cfg.name, "batch": cfg.batch, "q_heads": cfg.hq, "kv_heads": cfg.hkv,
+                   "head_dim": 128, "page_tokens": 16, "context_tokens": cfg.full_pages * 16,
+                   "parallelism": "host"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "kind": "oracle", "cores": threads,
+                         "sample": f"{nseq} sequence(s) x {cfg.hkv} KV heads per step "
+                                   f"(~{nseq * logical_per_seq / 1e6:.0f} MB logical KV)"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

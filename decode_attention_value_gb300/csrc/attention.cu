@@ -1,0 +1,658 @@
+// attention.cu -- split-KV GQA paged decode attention over 12-bit compressed pages
+// plus a raw BF16 tail (kCompressed = true), and the same kernel over plain BF16
+// pages (kCompressed = false, the in-run uncompressed baseline).
+//
+// GAAC ("Attention with On-the-Fly Decompression"): the kernel reads compressed tiles
+// and their metadata, rebuilds BF16 only in registers, and compressed blocks and the
+// raw tail share one softmax.  ZipFusion ("How it works"): the restored values feed
+// the tensor cores for QK^T and PV.
+//
+// GB300 design:
+//  * one wave of C = SMs x k CTAs; the (sequence, KV head, page) list is flattened and
+//    cut into C equal page ranges (the split depends only on shapes and seq_lens);
+//  * per CTA one producer warp and four consumer warps; the producer resolves page
+//    ids and metadata 32-64 pages ahead and streams each page into an 8-stage shared
+//    memory ring with TMA: two 1-D bulk copies (the K and V groups, 3-4 KB each) for a
+//    compressed page, two 2-D tensor copies with 128-byte swizzle for a raw page;
+//  * each consumer warp takes whole pages: per 512-value block one 16-byte and one
+//    8-byte shared load per lane, an integer restore into bf16x2 fragments, and
+//    mma.sync m16n8k16 with K (QK^T, tokens x dims) and V^T (PV, dims x tokens) as the
+//    A operand and the G query heads in the N columns.  G <= 4 leaves four spare N
+//    columns: Q is duplicated there for QK^T, and for PV they carry the low part of
+//    P = hi + lo (both bf16), so the PV product keeps ~16 bits of P for free;
+//  * warps merge their online-softmax states per (sequence, KV head) segment, and a
+//    small follow-up kernel (programmatic dependent launch) merges the segments in a
+//    fixed order.
+#include <cuda.h>
+
+#include <cstring>
+
+#include "kvz_internal.h"
+
+namespace kvz {
+
+constexpr int kStages = 8;
+constexpr int kStageBytes = 8192;
+constexpr int kConsumers = 4;
+constexpr int kThreads = (kConsumers + 1) * 32;
+static_assert(kStages % kConsumers == 0, "a stage's consecutive fills must go to the same consumer warp");
+
+enum : uint32_t { kKindPair = 0, kKindRaw = 1, kKindSkip = 2 };
+
+struct __align__(16) StageInfo {
+    uint32_t kind, valid, tagsK, tagsV;
+};
+
+// dynamic shared memory layout (offsets from a 1024-aligned base)
+struct Smem {
+    static constexpr int stage = 0;
+    static constexpr int full = stage + kStages * kStageBytes;
+    static constexpr int empty = full + kStages * 8;
+    static constexpr int qfull = empty + kStages * 8;
+    static constexpr int qempty = qfull + 2 * 8;
+    static constexpr int info = qempty + 2 * 8;
+    static constexpr int q = info + kStages * 16;
+    static constexpr int mm = q + 2 * 4 * 256;
+    static constexpr int ml = mm + kConsumers * 4 * 4;
+    static constexpr int mo = ml + kConsumers * 4 * 4;
+    static constexpr int pref = mo + kConsumers * 4 * 128 * 4;
+    __host__ __device__ static int lens(int batch) { return pref + (batch + 1) * 4; }
+    __host__ __device__ static int bytes(int batch) { return lens(batch) + batch * 4 + 1024; }
+};
+
+__device__ __forceinline__ uint32_t swz128(int row, int col)
+{
+    // byte offset of element (row, col) of a [32][128] BF16 tile loaded as two
+    // 64-column boxes with the 128-byte swizzle (16-byte chunk index ^= row % 8)
+    return (uint32_t)((col >> 6) * 4096 + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4) + (col & 7) * 2);
+}
+
+struct PageLoc {
+    int b, kvh, p;
+};
+
+// Largest b in [0, batch) with hkv * pref[b] <= x, then the KV head and page.
+__device__ __forceinline__ PageLoc locate(const int32_t *pref, int batch, int hkv, int64_t x)
+{
+    int lo = 0, hi = batch - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)hkv * pref[mid] <= x) lo = mid;
+        else hi = mid - 1;
+    }
+    const int n = pref[lo + 1] - pref[lo];
+    const int64_t r = x - (int64_t)hkv * pref[lo];
+    PageLoc L;
+    L.b = lo;
+    L.kvh = (int)(r / n);
+    L.p = (int)(r - (int64_t)L.kvh * n);
+    return L;
+}
+
+__device__ __forceinline__ int64_t unit_end(const int32_t *pref, int hkv, const PageLoc &L)
+{
+    const int n = pref[L.b + 1] - pref[L.b];
+    return (int64_t)hkv * pref[L.b] + (int64_t)(L.kvh + 1) * n;
+}
+
+// ---------------------------------------------------------------------------------
+// consumer-side fragment loads
+// ---------------------------------------------------------------------------------
+// One 512-value block of a compressed group in shared memory -> the two A fragments.
+__device__ __forceinline__ void block_frags(const uint8_t *blk, uint32_t tag, int lane, uint32_t (&a0)[4],
+                                            uint32_t (&a1)[4])
+{
+    if (tag == 0xFFu) {
+        const uint4 x = *reinterpret_cast<const uint4 *>(blk + 32 * lane);
+        const uint4 y = *reinterpret_cast<const uint4 *>(blk + 32 * lane + 16);
+        a0[0] = x.x; a0[1] = x.y; a0[2] = x.z; a0[3] = x.w;
+        a1[0] = y.x; a1[1] = y.y; a1[2] = y.z; a1[3] = y.w;
+    } else {
+        const uint4 low = *reinterpret_cast<const uint4 *>(blk + 16 * lane);
+        const uint2 code = *reinterpret_cast<const uint2 *>(blk + 512 + 8 * lane);
+        const uint32_t bb = tag * 0x01010101u;
+        restore_fragment(low.x, low.y, code.x, bb, a0);
+        restore_fragment(low.z, low.w, code.y, bb, a1);
+    }
+}
+
+// K operand (tokens x 16 dims) of k-tile (j, f) from a swizzled raw page.
+__device__ __forceinline__ void raw_k_frag(uint32_t st, int j, int f, int lane, uint32_t (&a)[4])
+{
+    const int mi = lane >> 3, rr = lane & 7;
+    const int tok = rr + 8 * (mi & 1), col = 32 * j + 16 * f + 8 * (mi >> 1);
+    ldmatrix_x4(st + swz128(tok, col), a);
+}
+
+// V^T operand (16 dims x tokens) of tile (j, f) from a swizzled raw page.
+__device__ __forceinline__ void raw_v_frag(uint32_t st, int j, int f, int lane, uint32_t (&a)[4])
+{
+    const int mi = lane >> 3, rr = lane & 7;
+    const int tok = rr + 8 * (mi >> 1), col = 32 * j + 16 * f + 8 * (mi & 1);
+    ldmatrix_x4_trans(st + swz128(16 + tok, col), a);
+}
+
+// Zero the V^T operand halves of tokens >= valid (a partial tail page may hold stale
+// values beyond its last token; P is 0 there but 0 * NaN is not 0).
+__device__ __forceinline__ void mask_v_frag(uint32_t (&a)[4], int lane, int valid)
+{
+    const int t = lane & 3;
+    const int t0 = 2 * t, t1 = 2 * t + 1, t8 = 2 * t + 8, t9 = 2 * t + 9;
+    const uint32_t mlo = (t0 < valid ? 0x0000FFFFu : 0u) | (t1 < valid ? 0xFFFF0000u : 0u);
+    const uint32_t mhi = (t8 < valid ? 0x0000FFFFu : 0u) | (t9 < valid ? 0xFFFF0000u : 0u);
+    a[0] &= mlo;
+    a[1] &= mlo;
+    a[2] &= mhi;
+    a[3] &= mhi;
+}
+
+// ---------------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------------
+template <bool kCompressed>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams P, const __grid_constant__ CUtensorMap tmap)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_addr(smem);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int32_t *pref = reinterpret_cast<int32_t *>(smem + Smem::pref);
+    int32_t *lens = reinterpret_cast<int32_t *>(smem + Smem::lens(P.batch));
+    StageInfo *info = reinterpret_cast<StageInfo *>(smem + Smem::info);
+    const int B = P.batch, hkv = P.hkv, G = P.G;
+
+    // ---- per-sequence page counts and their prefix ----
+    uint32_t bad_len = 0;
+    for (int b = tid; b < B; b += kThreads) {
+        int L = P.seq_lens[b];
+        if (L < 0) {
+            L = 0;
+            bad_len = 1;
+        }
+        lens[b] = L;
+    }
+    if (bad_len) atomicOr(P.status, KVZ_STATUS_BAD_INDEX);
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(sbase + Smem::full + 8 * s, 1);
+            mbar_init(sbase + Smem::empty + 8 * s, 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(sbase + Smem::qfull + 8 * s, 1);
+            mbar_init(sbase + Smem::qempty + 8 * s, kConsumers);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int chunk = (B + 31) / 32;
+        const int b0 = min(B, lane * chunk), b1 = min(B, b0 + chunk);
+        int s = 0;
+        for (int b = b0; b < b1; ++b) s += (lens[b] + kPage - 1) / kPage;
+        int incl = s;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        int run = incl - s;
+        for (int b = b0; b < b1; ++b) {
+            pref[b] = run;
+            run += (lens[b] + kPage - 1) / kPage;
+        }
+        if (lane == 31) pref[B] = incl;
+    }
+    __syncthreads();
+    if (blockIdx.x == 0)
+        for (int b = tid; b <= B; b += kThreads) P.prefix[b] = pref[b];
+
+    const int64_t T = (int64_t)hkv * pref[B];
+    const int64_t C = gridDim.x, c = blockIdx.x;
+    const int64_t lo = (c * T + C - 1) / C, hi = ((c + 1) * T + C - 1) / C;
+    pdl_launch_dependents();
+
+    if (warp == kConsumers) {
+        // =============================== producer ===============================
+        prefetch_tensormap(&tmap);
+        const int64_t npage = hi - lo;
+        // lookahead: lane l owns pages i = l (mod 32); A = its next page, N = the one after
+        PageLoc A{0, 0, 0}, N{0, 0, 0};
+        int32_t pidA = -1, pidN = -1;
+        uint64_t mA0 = 0, mA1 = 0;
+        auto page_pid = [&](const PageLoc &L) -> int32_t {
+            const int len = lens[L.b];
+            const bool from_table = kCompressed ? (L.p < len / kPage) : true;
+            if (!from_table) return P.tail_page[L.b];
+            if (L.p >= P.max_pages) return INT32_MIN;
+            return P.page_ids[(int64_t)L.b * P.max_pages + L.p];
+        };
+        auto load_meta = [&](const PageLoc &L, int32_t pid, uint64_t &m0, uint64_t &m1) {
+            m0 = m1 = 0;
+            if (kCompressed && L.p < lens[L.b] / kPage && pid >= 0 && pid < P.num_meta_pages) {
+                const ulonglong2 v =
+                    *reinterpret_cast<const ulonglong2 *>(P.meta + ((int64_t)pid * hkv + L.kvh) * 2);
+                m0 = v.x;
+                m1 = v.y;
+            }
+        };
+        if (lane < npage) {
+            A = locate(pref, B, hkv, lo + lane);
+            pidA = page_pid(A);
+        }
+        if (lane + 32 < npage) {
+            N = locate(pref, B, hkv, lo + lane + 32);
+            pidN = page_pid(N);
+        }
+        if (lane < npage) load_meta(A, pidA, mA0, mA1);
+
+        int64_t seg_end = lo;
+        int seg = 0;
+        bool ok = true;
+        for (int64_t i = 0; i < npage; ++i) {
+            const int64_t x = lo + i;
+            if (x == seg_end) {  // new (sequence, KV head) segment: stage its queries
+                const PageLoc L = locate(pref, B, hkv, x);
+                seg_end = min(hi, unit_end(pref, hkv, L));
+                if (lane == 0 && ok) {
+                    const int qb = seg & 1, use = seg >> 1;
+                    ok = mbar_wait(sbase + Smem::qempty + 8 * qb, (use & 1) ^ 1, P.status);
+                    if (ok) {
+                        const uint32_t bytes = (uint32_t)G * kDim * 2;
+                        mbar_arrive_expect_tx(sbase + Smem::qfull + 8 * qb, bytes);
+                        bulk_copy_g2s(sbase + Smem::q + qb * 1024,
+                                      P.q + ((int64_t)L.b * hkv * G + (int64_t)L.kvh * G) * kDim, bytes,
+                                      sbase + Smem::qfull + 8 * qb);
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                ++seg;
+            }
+            if (lane == (int)(i & 31)) {
+                const int s = (int)(i % kStages);
+                const int64_t fill = i / kStages;
+                if (ok) ok = mbar_wait(sbase + Smem::empty + 8 * s, (uint32_t)((fill & 1) ^ 1), P.status);
+                StageInfo inf{kKindSkip, 0, 0, 0};
+                uint32_t bad = 0;
+                const int len = lens[A.b];
+                const uint32_t fullbar = sbase + Smem::full + 8 * s;
+                const uint32_t dst = sbase + Smem::stage + s * kStageBytes;
+                const bool compressed_page = kCompressed && (A.p < len / kPage);
+                if (compressed_page) {
+                    const uint32_t offK = (uint32_t)mA0, offV = (uint32_t)mA1;
+                    const uint32_t tK = (uint32_t)(mA0 >> 32), tV = (uint32_t)(mA1 >> 32);
+                    if (pidA < 0 || pidA >= P.num_meta_pages) {
+                        bad = KVZ_STATUS_BAD_INDEX;
+                    } else if (!tags_valid(tK) || !tags_valid(tV) || offK == KVZ_OFFSET_INVALID ||
+                               offV == KVZ_OFFSET_INVALID ||
+                               ((uint64_t)offK + group_granules(tK)) * kGranule > P.arena_bytes ||
+                               ((uint64_t)offV + group_granules(tV)) * kGranule > P.arena_bytes) {
+                        bad = KVZ_STATUS_BAD_META;
+                    } else {
+                        inf = StageInfo{kKindPair, kPage, tK, tV};
+                    }
+                    if (ok) {
+                        info[s] = inf;
+                        if (inf.kind == kKindPair) {
+                            const uint32_t bK = group_granules(tK) * kGranule, bV = group_granules(tV) * kGranule;
+                            mbar_arrive_expect_tx(fullbar, bK + bV);
+                            bulk_copy_g2s(dst, P.arena + (uint64_t)offK * kGranule, bK, fullbar);
+                            bulk_copy_g2s(dst + 4096, P.arena + (uint64_t)offV * kGranule, bV, fullbar);
+                        } else {
+                            mbar_arrive(fullbar);
+                        }
+                    }
+                } else {
+                    const int valid = min(kPage, len - kPage * A.p);
+                    if (pidA < 0 || pidA >= P.num_raw_pages) {
+                        bad = (kCompressed && pidA == -1) ? KVZ_STATUS_BAD_TAIL : KVZ_STATUS_BAD_INDEX;
+                    } else {
+                        inf = StageInfo{kKindRaw, (uint32_t)valid, 0, 0};
+                    }
+                    if (ok) {
+                        info[s] = inf;
+                        if (inf.kind == kKindRaw) {
+                            const int row = (int)(((int64_t)pidA * hkv + A.kvh) * 32);
+                            mbar_arrive_expect_tx(fullbar, kStageBytes);
+                            tensor_copy_2d_g2s(dst, &tmap, 0, row, fullbar);
+                            tensor_copy_2d_g2s(dst + 4096, &tmap, 64, row, fullbar);
+                        } else {
+                            mbar_arrive(fullbar);
+                        }
+                    }
+                }
+                if (bad) atomicOr(P.status, bad);
+                // slide the lookahead window
+                A = N;
+                pidA = pidN;
+                if (i + 32 < npage) load_meta(A, pidA, mA0, mA1);
+                if (i + 64 < npage) {
+                    N = locate(pref, B, hkv, lo + i + 64);
+                    pidN = page_pid(N);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, (int)(i & 31));
+        }
+        // never leave with copies in flight: wait for the last fill of every stage
+        if (lane == 0) {
+            for (int s = 0; s < kStages && s < npage; ++s) {
+                const int64_t last = (npage - 1 - s) / kStages;
+                mbar_wait(sbase + Smem::full + 8 * s, (uint32_t)(last & 1), P.status);
+            }
+            for (int qb = 0; qb < 2 && qb < seg; ++qb) {
+                const int last = (seg - 1 - qb) / 2;
+                mbar_wait(sbase + Smem::qfull + 8 * qb, (uint32_t)(last & 1), P.status);
+            }
+        }
+        return;
+    }
+
+    // =============================== consumers ===============================
+    const int g = lane >> 2, t = lane & 3;
+    const float NEG_INF = -INFINITY;
+    float *mm = reinterpret_cast<float *>(smem + Smem::mm);
+    float *mlv = reinterpret_cast<float *>(smem + Smem::ml);
+    float *mo = reinterpret_cast<float *>(smem + Smem::mo);
+    bool ok = true;
+    int64_t x = lo, ibase = 0;
+    int seg = 0;
+    while (x < hi) {
+        const PageLoc L = locate(pref, B, hkv, x);
+        const int64_t send = min(hi, unit_end(pref, hkv, L));
+        const int64_t cnt = send - x;
+
+        // queries of this segment: B operand of QK^T, column n = head n % 4 (zero if >= G)
+        uint32_t qf[8][2];
+        {
+            const int qb = seg & 1, use = seg >> 1;
+            if (ok) ok = mbar_wait(sbase + Smem::qfull + 8 * qb, (uint32_t)(use & 1), P.status);
+            const int head = g & 3;
+            const uint8_t *qs = smem + Smem::q + qb * 1024 + head * 256;
+#pragma unroll
+            for (int kt = 0; kt < 8; ++kt) {
+                uint32_t b0 = 0, b1 = 0;
+                if (ok && head < G) {
+                    b0 = *reinterpret_cast<const uint32_t *>(qs + (16 * kt + 2 * t) * 2);
+                    b1 = *reinterpret_cast<const uint32_t *>(qs + (16 * kt + 2 * t + 8) * 2);
+                }
+                qf[kt][0] = b0;
+                qf[kt][1] = b1;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sbase + Smem::qempty + 8 * qb);
+        }
+
+        float o[8][4];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) o[a][0] = o[a][1] = o[a][2] = o[a][3] = 0.f;
+        float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
+
+        for (int64_t k = warp; k < cnt; k += kConsumers) {
+            const int64_t i = ibase + k;
+            const int s = (int)(i % kStages);
+            const int64_t fill = i / kStages;
+            if (ok) ok = mbar_wait(sbase + Smem::full + 8 * s, (uint32_t)(fill & 1), P.status);
+            const StageInfo inf = info[s];
+            if (ok && inf.kind != kKindSkip) {
+                const uint8_t *st = smem + Smem::stage + s * kStageBytes;
+                const uint32_t sta = sbase + Smem::stage + s * kStageBytes;
+                // ---- S^T = K Q^T over the page's 16 tokens ----
+                float sc[4] = {0.f, 0.f, 0.f, 0.f};
+                if (kCompressed && inf.kind == kKindPair) {
+                    uint32_t off = 0;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t tag = (inf.tagsK >> (8 * j)) & 0xFFu;
+                        uint32_t a0[4], a1[4];
+                        block_frags(st + off, tag, lane, a0, a1);
+                        mma_bf16_16816(sc, a0, qf[2 * j][0], qf[2 * j][1]);
+                        mma_bf16_16816(sc, a1, qf[2 * j + 1][0], qf[2 * j + 1][1]);
+                        off += tag_granules(tag) * kGranule;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t a0[4], a1[4];
+                        raw_k_frag(sta, j, 0, lane, a0);
+                        raw_k_frag(sta, j, 1, lane, a1);
+                        mma_bf16_16816(sc, a0, qf[2 * j][0], qf[2 * j][1]);
+                        mma_bf16_16816(sc, a1, qf[2 * j + 1][0], qf[2 * j + 1][1]);
+                    }
+                }
+                // sc: (token g, col 2t), (token g, col 2t+1), (token g+8, col 2t), (token g+8, col 2t+1)
+                const int valid = (int)inf.valid;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sc[e] *= P.scale_log2;
+                if (valid < kPage) {
+                    if (g >= valid) sc[0] = sc[1] = NEG_INF;
+                    if (g + 8 >= valid) sc[2] = sc[3] = NEG_INF;
+                }
+                // ---- online softmax (column max over the 16 tokens: lanes with equal t) ----
+                float x0 = fmaxf(sc[0], sc[2]), x1 = fmaxf(sc[1], sc[3]);
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, off));
+                    x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, off));
+                }
+                const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+                if (__any_sync(0xffffffffu, (n0 > m0) || (n1 > m1))) {
+                    const float a0 = (n0 == NEG_INF) ? 1.f : exp2f(m0 - n0);
+                    const float a1 = (n1 == NEG_INF) ? 1.f : exp2f(m1 - n1);
+#pragma unroll
+                    for (int a = 0; a < 8; ++a) {
+                        o[a][0] *= a0;
+                        o[a][2] *= a0;
+                        o[a][1] *= a1;
+                        o[a][3] *= a1;
+                    }
+                    l0 *= a0;
+                    l1 *= a1;
+                    m0 = n0;
+                    m1 = n1;
+                }
+                const float u0 = (m0 == NEG_INF) ? 0.f : m0, u1 = (m1 == NEG_INF) ? 0.f : m1;
+                const float p0 = exp2f(sc[0] - u0), p1 = exp2f(sc[1] - u1);
+                const float p2 = exp2f(sc[2] - u0), p3 = exp2f(sc[3] - u1);
+                l0 += p0 + p2;
+                l1 += p1 + p3;
+                // P split: columns 0..3 (t < 2) carry bf16(p), columns 4..7 carry bf16(p - bf16(p))
+                float v0 = p0, v1 = p1, v2 = p2, v3 = p3;
+                if (t >= 2) {
+                    v0 = p0 - bf16_round(p0);
+                    v1 = p1 - bf16_round(p1);
+                    v2 = p2 - bf16_round(p2);
+                    v3 = p3 - bf16_round(p3);
+                }
+                const uint32_t pb0 = movmatrix_trans(pack_bf16x2(v0, v1));  // tokens 0..7
+                const uint32_t pb1 = movmatrix_trans(pack_bf16x2(v2, v3));  // tokens 8..15
+                // ---- O^T += V^T P^T ----
+                if (kCompressed && inf.kind == kKindPair) {
+                    uint32_t off = 4096;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint32_t tag = (inf.tagsV >> (8 * j)) & 0xFFu;
+                        uint32_t a0[4], a1[4];
+                        block_frags(st + off, tag, lane, a0, a1);
+                        mma_bf16_16816(o[2 * j], a0, pb0, pb1);
+                        mma_bf16_16816(o[2 * j + 1], a1, pb0, pb1);
+                        off += tag_granules(tag) * kGranule;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t a0[4], a1[4];
+                        raw_v_frag(sta, j, 0, lane, a0);
+                        raw_v_frag(sta, j, 1, lane, a1);
+                        if (valid < kPage) {
+                            mask_v_frag(a0, lane, valid);
+                            mask_v_frag(a1, lane, valid);
+                        }
+                        mma_bf16_16816(o[2 * j], a0, pb0, pb1);
+                        mma_bf16_16816(o[2 * j + 1], a1, pb0, pb1);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sbase + Smem::empty + 8 * s);
+        }
+
+        // ---- warp state -> shared memory (columns h and h+4 summed) ----
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        }
+#pragma unroll
+        for (int a = 0; a < 8; ++a)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[a][e] += __shfl_xor_sync(0xffffffffu, o[a][e], 2);
+        if (t < 2) {
+            const int h0 = 2 * t, h1 = 2 * t + 1;
+            if (g == 0) {
+                mm[warp * 4 + h0] = m0;
+                mm[warp * 4 + h1] = m1;
+                mlv[warp * 4 + h0] = l0;
+                mlv[warp * 4 + h1] = l1;
+            }
+#pragma unroll
+            for (int a = 0; a < 8; ++a) {
+                const int d0 = 16 * a + g, d1 = 16 * a + g + 8;
+                mo[(warp * 4 + h0) * 128 + d0] = o[a][0];
+                mo[(warp * 4 + h1) * 128 + d0] = o[a][1];
+                mo[(warp * 4 + h0) * 128 + d1] = o[a][2];
+                mo[(warp * 4 + h1) * 128 + d1] = o[a][3];
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");
+        {
+            // ---- merge the four warps (fixed order) and write this segment's partial ----
+            const int d = tid;  // 0..127
+            const int64_t slot = (int64_t)(L.b * hkv + L.kvh) + c;
+            for (int h = 0; h < G; ++h) {
+                float M = NEG_INF;
+#pragma unroll
+                for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, mm[w * 4 + h]);
+                float Lsum = 0.f, Osum = 0.f;
+                if (M != NEG_INF) {
+#pragma unroll
+                    for (int w = 0; w < kConsumers; ++w) {
+                        const float sw = exp2f(mm[w * 4 + h] - M);
+                        Lsum += sw * mlv[w * 4 + h];
+                        Osum += sw * mo[(w * 4 + h) * 128 + d];
+                    }
+                }
+                P.part_o[(slot * 4 + h) * 128 + d] = Osum;
+                if (d == 0) {
+                    P.part_ml[(slot * 4 + h) * 2 + 0] = M;
+                    P.part_ml[(slot * 4 + h) * 2 + 1] = Lsum;
+                }
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");
+        x = send;
+        ibase += cnt;
+        ++seg;
+    }
+}
+
+// ---------------------------------------------------------------------------------
+// merge the per-segment partials of each (sequence, KV head): fixed order over CTAs
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(128) k_attn_merge(const AttnParams P)
+{
+    pdl_wait_primary();
+    const int u = blockIdx.x, hkv = P.hkv, G = P.G;
+    const int b = u / hkv, kvh = u % hkv, d = threadIdx.x;
+    const int64_t n = P.prefix[b + 1] - P.prefix[b];
+    const int64_t T = (int64_t)hkv * P.prefix[P.batch];
+    const int64_t C = P.grid;
+    float *out = P.out + ((int64_t)b * hkv * G + (int64_t)kvh * G) * kDim;
+    if (n == 0) {
+        for (int h = 0; h < G; ++h) out[h * kDim + d] = 0.f;
+        return;
+    }
+    const int64_t S = (int64_t)hkv * P.prefix[b] + (int64_t)kvh * n, E = S + n;
+    // CTA c covers pages [ceil(cT/C), ceil((c+1)T/C)); page x belongs to CTA floor(xC/T).
+    // CTAs between the first and last owner with an empty range (T < C) wrote nothing.
+    const int64_t c0 = (S * C) / T, c1 = ((E - 1) * C) / T;
+    auto written = [&](int64_t c) { return (c * T + C - 1) / C < ((c + 1) * T + C - 1) / C; };
+    for (int h = 0; h < G; ++h) {
+        float M = -INFINITY;
+        for (int64_t c = c0; c <= c1; ++c)
+            if (written(c)) M = fmaxf(M, P.part_ml[((u + c) * 4 + h) * 2]);
+        float Ls = 0.f, Os = 0.f;
+        if (M != -INFINITY) {
+            for (int64_t c = c0; c <= c1; ++c) {
+                if (!written(c)) continue;
+                const int64_t slot = u + c;
+                const float w = exp2f(P.part_ml[(slot * 4 + h) * 2] - M);
+                Ls += w * P.part_ml[(slot * 4 + h) * 2 + 1];
+                Os += w * P.part_o[(slot * 4 + h) * 128 + d];
+            }
+        }
+        out[h * kDim + d] = Ls > 0.f ? Os / Ls : 0.f;
+    }
+}
+
+// ---------------------------------------------------------------------------------
+// launcher
+// ---------------------------------------------------------------------------------
+int attn_smem_bytes(int batch) { return Smem::bytes(batch); }
+
+template <bool kCompressed>
+static cudaError_t configure(int dev)
+{
+    // per process and device: allow the full shared-memory carve-out (attributes are per function)
+    static unsigned long long done = 0;  // bit per device ordinal < 64
+    if (dev < 64 && (__atomic_load_n(&done, __ATOMIC_ACQUIRE) >> dev) & 1ull) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(k_attn<kCompressed>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_attn<kCompressed>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e == cudaSuccess && dev < 64) __atomic_fetch_or(&done, 1ull << dev, __ATOMIC_ACQ_REL);
+    return e;
+}
+
+cudaError_t attn_ctas_per_sm(int batch, int *out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = configure<true>(dev);
+    if (e == cudaSuccess) e = configure<false>(dev);
+    int a = 0, b = 0;
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, k_attn<true>, kThreads, Smem::bytes(batch));
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_attn<false>, kThreads, Smem::bytes(batch));
+    *out = e == cudaSuccess ? (a < b ? a : b) : 0;
+    return e;
+}
+
+template <bool kCompressed>
+static cudaError_t launch_impl(const AttnParams &P, const void *tmap, cudaStream_t stream)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = configure<kCompressed>(dev);
+    if (e != cudaSuccess) return e;
+    CUtensorMap map;
+    memcpy(&map, tmap, sizeof(map));
+    k_attn<kCompressed><<<P.grid, kThreads, Smem::bytes(P.batch), stream>>>(P, map);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(P.batch * P.hkv);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_attn_merge, P);
+}
+
+cudaError_t launch_attention(const AttnParams &P, bool compressed, const void *tmap, cudaStream_t stream)
+{
+    return compressed ? launch_impl<true>(P, tmap, stream) : launch_impl<false>(P, tmap, stream);
+}
+
+}  // namespace kvz

@@ -1,0 +1,436 @@
+// codec.cu -- page encoder (three launches: block sizes, segmented placement scan,
+// pack) and standalone decoder for the 12-bit BF16 block format.
+//
+// Format (ZipFusion, "How it works" steps 1-4, layout and metadata paragraphs): a
+// 16-token page slice of one KV head, K or V, is four 512-value blocks (dims
+// [32j, 32j+32) x 16 tokens).  A block whose exponents all lie in [b, b+15], b the
+// even floor of the minimum, keeps every value's low byte and a 4-bit (sign, d)
+// code, d = (e-b)/2: 768 bytes.  Any other block stays raw: 1024 bytes.  Values are
+// stored in the tensor-core fragment order of the block's role (K rows = tokens for
+// QK^T, V rows = dims for PV), so the attention kernel restores each lane's eight
+// operand elements from one 8-byte low run and one 4-byte code word.
+#include "kvz_internal.h"
+
+namespace kvz {
+
+// ---------------------------------------------------------------------------------
+// storage order: element (lane, f, i) of block j  ->  (token, dim) of the page slice
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ int frag_row(int lane, int i) { return (lane >> 2) + 8 * ((i >> 1) & 1); }
+__device__ __forceinline__ int frag_col(int lane, int i) { return 2 * (lane & 3) + (i & 1) + 8 * (i >> 2); }
+
+// Page slice staging in shared memory: 32 rows (K tokens 0..15, V tokens 16..31) of
+// 128 BF16 with a 272-byte pitch, so the fragment gathers below hit 32 distinct banks.
+constexpr int kStagePitch = 272;
+
+// Gather this lane's 16 values of block (kv, j) in storage order as 8 bf16x2 words
+// (w[0..3] = fragment 0 elements (0,1),(2,3),(4,5),(6,7); w[4..7] = fragment 1).
+__device__ __forceinline__ void gather_block(const uint8_t *stage, int kv, int j, int lane, uint32_t (&w)[8])
+{
+#pragma unroll
+    for (int f = 0; f < 2; ++f)
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            const int r = frag_row(lane, i), c = frag_col(lane, i);
+            const int dim0 = 32 * j + 16 * f;
+            uint32_t v;
+            if (kv == 0) {  // K: token r, dims c and c+1 are adjacent
+                v = *reinterpret_cast<const uint32_t *>(stage + r * kStagePitch + (dim0 + c) * 2);
+            } else {  // V: tokens c and c+1 of dim r
+                const uint8_t *base = stage + (16 + c) * kStagePitch + (dim0 + r) * 2;
+                uint32_t lo = *reinterpret_cast<const uint16_t *>(base);
+                uint32_t hi = *reinterpret_cast<const uint16_t *>(base + kStagePitch);
+                v = lo | (hi << 16);
+            }
+            w[f * 4 + i / 2] = v;
+        }
+}
+
+__device__ __forceinline__ void load_slice_to_stage(const uint16_t *src, uint8_t *stage, int tid, int nthreads)
+{
+    // 8 KB slice: 512 chunks of 16 B; chunk q -> row q/16, byte (q%16)*16
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(src);
+    for (int q = tid; q < 512; q += nthreads) {
+        uint4 v = s4[q];
+        *reinterpret_cast<uint4 *>(stage + (q >> 4) * kStagePitch + (q & 15) * 16) = v;
+    }
+}
+
+__device__ __forceinline__ void exponent_range(const uint32_t (&w)[8], uint32_t &mn, uint32_t &mx)
+{
+    mn = 255;
+    mx = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        uint32_t e0 = (w[k] >> 7) & 0xFFu, e1 = (w[k] >> 23) & 0xFFu;
+        mn = min(mn, min(e0, e1));
+        mx = max(mx, max(e0, e1));
+    }
+    mn = __reduce_min_sync(0xffffffffu, mn);
+    mx = __reduce_max_sync(0xffffffffu, mx);
+}
+
+// ---------------------------------------------------------------------------------
+// launch 1: group sizes.  One CTA per (entry, head); warp w = block (kv = w/4, j = w%4)
+// reads its 16 x 32 slab (row = lane/2, 32 B per lane) and reduces the exponent range.
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_enc_sizes(EncodeParams P)
+{
+    const int entry = blockIdx.x / P.hkv, head = blockIdx.x % P.hkv;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kv = warp >> 2, j = warp & 3;
+    __shared__ uint32_t gran[8];
+    const int src = P.src_page[entry];
+    uint32_t g = 0;
+    if (src >= 0 && src < P.num_raw_pages) {
+        const uint16_t *slab = P.raw_pool + (((int64_t)src * P.hkv + head) * 2 + kv) * kPage * kDim;
+        const uint4 *p = reinterpret_cast<const uint4 *>(slab + (lane >> 1) * kDim + 32 * j + 16 * (lane & 1));
+        uint4 a = p[0], b = p[1];
+        uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        uint32_t mn, mx;
+        exponent_range(w, mn, mx);
+        const uint32_t base = mn & ~1u;
+        g = (mx <= base + 15) ? 3u : 4u;
+    }
+    if (lane == 0) gran[warp] = g;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t s = 0;
+        for (int k = 0; k < 8; ++k) s += gran[k];
+        P.ws_pair_size[blockIdx.x] = s;
+    }
+}
+
+// ---------------------------------------------------------------------------------
+// launch 2: one CTA validates the call and places every (entry, head) K+V pair at its
+// cursor: a segmented exclusive scan of pair sizes in call order, segments = runs of
+// equal dst_seq.  The segment head reads its cursor; the segment end writes it back.
+// ---------------------------------------------------------------------------------
+constexpr int kScanThreads = 1024;
+constexpr int kScanItems = 8;  // items per thread per tile
+
+__global__ void __launch_bounds__(kScanThreads) k_enc_scan(EncodeParams P)
+{
+    __shared__ uint32_t s_err;
+    __shared__ uint32_t s_flag[kScanThreads / 32];
+    __shared__ uint64_t s_sum[kScanThreads / 32];
+    __shared__ uint32_t s_carry_flag;
+    __shared__ uint64_t s_carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        s_err = 0;
+        s_carry = 0;
+        s_carry_flag = 0;
+    }
+    __syncthreads();
+    uint32_t err = 0;
+    for (int e = tid; e < P.n; e += kScanThreads) {
+        const int s = P.src_page[e], d = P.dst_page[e], q = P.dst_seq[e];
+        if (s < 0 || s >= P.num_raw_pages || d < 0 || d >= P.num_meta_pages || q < 0 || q >= P.num_cursors)
+            err |= KVZ_STATUS_BAD_INDEX;
+        if (e > 0 && q < P.dst_seq[e - 1]) err |= KVZ_STATUS_BAD_ORDER;
+    }
+    if (err) atomicOr(&s_err, err);
+    __syncthreads();
+    if (s_err) {
+        if (tid == 0) {
+            atomicOr(P.status, s_err);
+            *P.ws_call_ok = 0;
+        }
+        return;
+    }
+    const int64_t M = (int64_t)P.n * P.hkv;
+    for (int64_t t0 = 0; t0 < M; t0 += (int64_t)kScanThreads * kScanItems) {
+        // this thread's run of items
+        const int64_t i0 = t0 + (int64_t)tid * kScanItems;
+        uint64_t val[kScanItems];
+        uint32_t head[kScanItems];
+        uint32_t any_head = 0;
+        uint64_t run = 0;
+#pragma unroll
+        for (int k = 0; k < kScanItems; ++k) {
+            const int64_t it = i0 + k;
+            val[k] = 0;
+            head[k] = 0;
+            if (it < M) {
+                const int e = (int)(it / P.hkv), h = (int)(it % P.hkv);
+                const int seq = P.dst_seq[e];
+                const bool is_head = (h == 0) && (e == 0 || P.dst_seq[e - 1] != seq);
+                uint64_t v = P.ws_pair_size[it];
+                if (is_head) v += P.cursors[2 * seq];  // absolute granule position
+                head[k] = is_head;
+                val[k] = v;
+            }
+            // inclusive segmented scan within the run
+            run = head[k] ? val[k] : run + val[k];
+            any_head |= head[k];
+            val[k] = run;
+        }
+        // warp-level inclusive segmented scan of (flag, run total)
+        uint32_t f = any_head;
+        uint64_t s = run;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            uint64_t so = __shfl_up_sync(0xffffffffu, s, off);
+            uint32_t fo = __shfl_up_sync(0xffffffffu, f, off);
+            if (lane >= off) {
+                if (!f) s += so;
+                f |= fo;
+            }
+        }
+        if (lane == 31) {
+            s_flag[warp] = f;
+            s_sum[warp] = s;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            uint32_t wf = s_flag[lane];
+            uint64_t ws = s_sum[lane];
+            if (lane == 0) {  // fold in the carry from the previous tile
+                if (!wf) ws += s_carry;
+                wf |= s_carry_flag;
+            }
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                uint64_t so = __shfl_up_sync(0xffffffffu, ws, off);
+                uint32_t fo = __shfl_up_sync(0xffffffffu, wf, off);
+                if (lane >= off) {
+                    if (!wf) ws += so;
+                    wf |= fo;
+                }
+            }
+            s_flag[lane] = wf;
+            s_sum[lane] = ws;
+        }
+        __syncthreads();
+        // exclusive prefix of this thread's run = inclusive of previous lane (this warp)
+        // combined with the previous warps' inclusive total
+        uint64_t prev_s = __shfl_up_sync(0xffffffffu, s, 1);
+        uint32_t prev_f = __shfl_up_sync(0xffffffffu, f, 1);
+        const uint64_t wpre_s = warp > 0 ? s_sum[warp - 1] : s_carry;
+        uint64_t excl;
+        if (lane == 0) {
+            excl = wpre_s;
+        } else {
+            excl = prev_f ? prev_s : prev_s + wpre_s;
+        }
+        // write item positions: item k's exclusive position = (run prefix) - own size
+#pragma unroll
+        for (int k = 0; k < kScanItems; ++k) {
+            const int64_t it = i0 + k;
+            if (it >= M) break;
+            // inclusive value of item k including the carry-in
+            bool seen_head = false;
+            for (int q = 0; q <= k; ++q) seen_head |= head[q];
+            const uint64_t incl = seen_head ? val[k] : val[k] + excl;
+            const uint64_t own = P.ws_pair_size[it];
+            const uint64_t pos = incl - own;
+            P.ws_pair_base[it] = (uint32_t)min(pos, (uint64_t)0xFFFFFFFFu);
+            // the last item of a segment writes the cursor back
+            const int e = (int)(it / P.hkv), h = (int)(it % P.hkv);
+            const bool last = (h == P.hkv - 1) && (e == P.n - 1 || P.dst_seq[e + 1] != P.dst_seq[e]);
+            if (last) P.cursors[2 * P.dst_seq[e]] = (uint32_t)min(incl, (uint64_t)0xFFFFFFFFu);
+        }
+        __syncthreads();
+        if (tid == kScanThreads - 1) {
+            // carry = inclusive total of the whole tile (previous carry folded in)
+            s_carry = s_sum[31];
+            s_carry_flag = s_flag[31];
+        }
+        __syncthreads();
+    }
+    if (tid == 0) *P.ws_call_ok = 1;
+}
+
+// ---------------------------------------------------------------------------------
+// launch 3: pack.  One CTA per (entry, head): stage the K+V slice, each warp gathers
+// its block in storage order, recomputes the tag and writes 768 or 1024 bytes at its
+// place in the group; warps 0 and 4 write the two metadata words.
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_enc_pack(EncodeParams P)
+{
+    __shared__ __align__(16) uint8_t stage[32 * kStagePitch];
+    __shared__ uint32_t tags[8];
+    if (*P.ws_call_ok == 0) return;
+    const int entry = blockIdx.x / P.hkv, head = blockIdx.x % P.hkv;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kv = warp >> 2, j = warp & 3;
+    const int src = P.src_page[entry], dst = P.dst_page[entry], seq = P.dst_seq[entry];
+    const uint16_t *slice = P.raw_pool + ((int64_t)src * P.hkv + head) * 2 * kPage * kDim;
+    load_slice_to_stage(slice, stage, threadIdx.x, blockDim.x);
+    __syncthreads();
+
+    uint32_t w[8];
+    gather_block(stage, kv, j, lane, w);
+    uint32_t mn, mx;
+    exponent_range(w, mn, mx);
+    const uint32_t b = mn & ~1u;
+    const bool eligible = mx <= b + 15;
+    const uint32_t tag = eligible ? (b >> 1) : 0xFFu;
+    if (lane == 0) tags[warp] = tag;
+    __syncthreads();
+
+    uint32_t group_tags = 0, before = 0, gsize = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t t = tags[kv * 4 + k];
+        group_tags |= t << (8 * k);
+        if (k < j) before += tag_granules(t);
+        gsize += tag_granules(t);
+    }
+    uint32_t k_size = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) k_size += tag_granules(tags[k]);
+    const uint64_t pair_base = P.ws_pair_base[blockIdx.x];
+    const uint64_t offset0 = pair_base + (kv ? k_size : 0);
+    const uint64_t end = min((uint64_t)P.cursors[2 * seq + 1], P.arena_bytes / kGranule);
+    const bool fits = offset0 + gsize <= end;
+
+    if (fits) {
+        uint8_t *blk = P.arena + (offset0 + before) * kGranule;
+        if (eligible) {
+            uint32_t low[4], code[2];
+#pragma unroll
+            for (int f = 0; f < 2; ++f) {
+                uint32_t lo03 = 0, lo47 = 0, cw = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint32_t v = (w[f * 4 + i / 2] >> (16 * (i & 1))) & 0xFFFFu;
+                    const uint32_t s = v >> 15, e = (v >> 7) & 0xFFu, d = (e - b) >> 1;
+                    const uint32_t lowbyte = v & 0xFFu;
+                    if (i < 4) {
+                        lo03 |= lowbyte << (8 * i);
+                        cw |= ((s << 7) | d) << (8 * i);
+                    } else {
+                        lo47 |= lowbyte << (8 * (i - 4));
+                        cw |= ((s << 3) | (d << 4)) << (8 * (i - 4));
+                    }
+                }
+                low[2 * f] = lo03;
+                low[2 * f + 1] = lo47;
+                code[f] = cw;
+            }
+            *reinterpret_cast<uint4 *>(blk + 16 * lane) = make_uint4(low[0], low[1], low[2], low[3]);
+            *reinterpret_cast<uint2 *>(blk + 512 + 8 * lane) = make_uint2(code[0], code[1]);
+        } else {
+            *reinterpret_cast<uint4 *>(blk + 32 * lane) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4 *>(blk + 32 * lane + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+    }
+    if (lane == 0 && j == 0) {
+        const uint64_t off_word = fits ? offset0 : (uint64_t)KVZ_OFFSET_INVALID;
+        P.meta[((int64_t)dst * P.hkv + head) * 2 + kv] = off_word | ((uint64_t)group_tags << 32);
+        if (!fits) atomicOr(P.status, KVZ_STATUS_ARENA_FULL);
+    }
+}
+
+// ---------------------------------------------------------------------------------
+// standalone decode: one CTA per (entry, head); warp w restores block (w/4, w%4) with
+// the same register restore the attention kernel uses, scatters it to a staged page
+// slice, and the CTA writes the 8 KB slice back in the plain page layout.
+// ---------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_decode(DecodeParams P)
+{
+    __shared__ __align__(16) uint8_t stage[32 * kStagePitch];
+    const int entry = blockIdx.x / P.hkv, head = blockIdx.x % P.hkv;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kv = warp >> 2, j = warp & 3;
+    const int page = P.page[entry];
+    uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    uint32_t bad = 0;
+    if (page < 0 || page >= P.num_meta_pages) {
+        bad = KVZ_STATUS_BAD_INDEX;
+    } else {
+        const uint64_t word = P.meta[((int64_t)page * P.hkv + head) * 2 + kv];
+        const uint32_t offset0 = (uint32_t)word, tags = (uint32_t)(word >> 32);
+        if (!tags_valid(tags) || offset0 == KVZ_OFFSET_INVALID ||
+            ((uint64_t)offset0 + group_granules(tags)) * kGranule > P.arena_bytes) {
+            bad = KVZ_STATUS_BAD_META;
+        } else {
+            uint32_t before = 0;
+            for (int k = 0; k < j; ++k) before += tag_granules((tags >> (8 * k)) & 0xFFu);
+            const uint32_t tag = (tags >> (8 * j)) & 0xFFu;
+            const uint8_t *blk = P.arena + ((uint64_t)offset0 + before) * kGranule;
+            if (tag == 0xFFu) {
+                uint4 a = *reinterpret_cast<const uint4 *>(blk + 32 * lane);
+                uint4 c = *reinterpret_cast<const uint4 *>(blk + 32 * lane + 16);
+                w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+                w[4] = c.x; w[5] = c.y; w[6] = c.z; w[7] = c.w;
+            } else {
+                const uint4 low = *reinterpret_cast<const uint4 *>(blk + 16 * lane);
+                const uint2 code = *reinterpret_cast<const uint2 *>(blk + 512 + 8 * lane);
+                const uint32_t bb = tag * 0x01010101u;
+                uint32_t f0[4], f1[4];
+                restore_fragment(low.x, low.y, code.x, bb, f0);
+                restore_fragment(low.z, low.w, code.y, bb, f1);
+                w[0] = f0[0]; w[1] = f0[1]; w[2] = f0[2]; w[3] = f0[3];
+                w[4] = f1[0]; w[5] = f1[1]; w[6] = f1[2]; w[7] = f1[3];
+            }
+        }
+    }
+    if (bad && lane == 0) atomicOr(P.status, bad);
+    // scatter to the staged slice (inverse of gather_block)
+#pragma unroll
+    for (int f = 0; f < 2; ++f)
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            const int r = frag_row(lane, i), c = frag_col(lane, i);
+            const int dim0 = 32 * j + 16 * f;
+            const uint32_t v = w[f * 4 + i / 2];
+            if (kv == 0) {
+                *reinterpret_cast<uint32_t *>(stage + r * kStagePitch + (dim0 + c) * 2) = v;
+            } else {
+                uint8_t *base = stage + (16 + c) * kStagePitch + (dim0 + r) * 2;
+                *reinterpret_cast<uint16_t *>(base) = (uint16_t)(v & 0xFFFFu);
+                *reinterpret_cast<uint16_t *>(base + kStagePitch) = (uint16_t)(v >> 16);
+            }
+        }
+    __syncthreads();
+    uint4 *out = reinterpret_cast<uint4 *>(P.out + ((int64_t)entry * P.hkv + head) * 2 * kPage * kDim);
+    for (int q = threadIdx.x; q < 512; q += blockDim.x)
+        out[q] = *reinterpret_cast<const uint4 *>(stage + (q >> 4) * kStagePitch + (q & 15) * 16);
+}
+
+// ---------------------------------------------------------------------------------
+// cursor updates from the host allocator
+// ---------------------------------------------------------------------------------
+__global__ void k_apply_cursor_updates(const int32_t *idx, const uint32_t *pos, const uint32_t *end, int n,
+                                       uint32_t *cursors, int num_cursors)
+{
+    const int k = blockIdx.x * blockDim.x + threadIdx.x;
+    if (k < n) {
+        const int c = idx[k];
+        if (c >= 0 && c < num_cursors) {
+            cursors[2 * c] = pos[k];
+            cursors[2 * c + 1] = end[k];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------
+// host launchers
+// ---------------------------------------------------------------------------------
+cudaError_t launch_encode(const EncodeParams &P, cudaStream_t stream)
+{
+    const int pairs = P.n * P.hkv;
+    k_enc_sizes<<<pairs, 256, 0, stream>>>(P);
+    k_enc_scan<<<1, kScanThreads, 0, stream>>>(P);
+    k_enc_pack<<<pairs, 256, 0, stream>>>(P);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const DecodeParams &P, cudaStream_t stream)
+{
+    k_decode<<<P.n * P.hkv, 256, 0, stream>>>(P);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_apply_cursor_updates(const int32_t *idx, const uint32_t *pos, const uint32_t *end, int n,
+                                        uint32_t *cursors, int num_cursors, cudaStream_t stream)
+{
+    if (n <= 0) return cudaSuccess;
+    k_apply_cursor_updates<<<(n + 255) / 256, 256, 0, stream>>>(idx, pos, end, n, cursors, num_cursors);
+    return cudaGetLastError();
+}
+
+}  // namespace kvz

@@ -1,0 +1,309 @@
+// kvz_api.cu -- the C ABI (include/kvz.h): host-side argument checks, launch
+// configuration and the TMA tensor map for raw pages.  All compute runs in the
+// kernels of codec.cu and attention.cu; nothing here touches device data.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "kvz_internal.h"
+
+using namespace kvz;
+
+namespace {
+
+thread_local int g_last_cuda = 0;
+
+int fail_cuda(cudaError_t e)
+{
+    g_last_cuda = static_cast<int>(e);
+    return KVZ_ERR_CUDA;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool dims_ok(const kvz_dims &d) { return d.num_kv_heads >= 1 && d.head_dim == kDim && d.page_size == kPage; }
+
+int sm_count()
+{
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+// Number of attention CTAs: one wave of the CTAs the device holds, but at least
+// kMinPagesPerCta pages each.  Depends only on shapes and the device.
+int attention_grid(int batch, int hkv, int table_pages, int *grid)
+{
+    int per_sm = 0;
+    cudaError_t e = attn_ctas_per_sm(batch, &per_sm);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (per_sm < 1) return KVZ_ERR_UNSUPPORTED;
+    const int sms = sm_count();
+    if (sms < 1) return KVZ_ERR_DEVICE;
+    const int64_t wave = (int64_t)sms * per_sm;
+    const int64_t pages = (int64_t)batch * hkv * (int64_t)(table_pages > 0 ? table_pages : 1);
+    int64_t c = (pages + kMinPagesPerCta - 1) / kMinPagesPerCta;
+    if (c > wave) c = wave;
+    if (c < 1) c = 1;
+    *grid = (int)c;
+    return KVZ_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Raw pool as a 2-D tensor [num_raw_pages * hkv * 32 rows][128 BF16]; box = 64 columns
+// x 32 rows (the K and V rows of one page and head), 128-byte swizzle.
+int raw_tensor_map(const void *raw_pool, int64_t num_raw_pages, int hkv, CUtensorMap *map)
+{
+    thread_local const void *c_ptr = nullptr;
+    thread_local int64_t c_rows = -1;
+    thread_local CUtensorMap c_map;
+    const int64_t rows = num_raw_pages * hkv * 32;
+    if (c_ptr == raw_pool && c_rows == rows) {
+        *map = c_map;
+        return KVZ_OK;
+    }
+    auto enc = tensor_map_encoder();
+    if (!enc) return KVZ_ERR_DEVICE;
+    cuuint64_t dims[2] = {(cuuint64_t)kDim, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)kDim * 2};
+    cuuint32_t box[2] = {64, 32};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(raw_pool), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        g_last_cuda = (int)r;
+        return KVZ_ERR_CUDA;
+    }
+    c_ptr = raw_pool;
+    c_rows = rows;
+    c_map = *map;
+    return KVZ_OK;
+}
+
+int check_attention_common(const kvz_dims &d, int batch, int hq, const void *q, const int32_t *seq_lens,
+                           const void *raw_pool, int64_t num_raw_pages, const float *out, const void *ws,
+                           const uint32_t *status, int max_pages, const int32_t *page_ids)
+{
+    if (!dims_ok(d)) return d.num_kv_heads >= 1 ? KVZ_ERR_UNSUPPORTED : KVZ_ERR_INVALID_ARG;
+    if (batch < 0 || hq < 1 || max_pages < 0 || num_raw_pages < 0) return KVZ_ERR_INVALID_ARG;
+    if (hq % d.num_kv_heads != 0) return KVZ_ERR_INVALID_ARG;
+    const int G = hq / d.num_kv_heads;
+    if (G != 1 && G != 2 && G != 4) return KVZ_ERR_UNSUPPORTED;
+    if (batch > kMaxBatch) return KVZ_ERR_UNSUPPORTED;
+    if (batch == 0) return KVZ_OK;
+    if (!q || !seq_lens || !out || !ws || !status || (max_pages > 0 && !page_ids)) return KVZ_ERR_INVALID_ARG;
+    if (num_raw_pages > 0 && !raw_pool) return KVZ_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(ws, 16) || !aligned(out, 4) || !aligned(raw_pool, 16) || !aligned(seq_lens, 4) ||
+        !aligned(status, 4))
+        return KVZ_ERR_ALIGNMENT;
+    if (num_raw_pages * d.num_kv_heads * 32 >= (int64_t)1 << 31) return KVZ_ERR_UNSUPPORTED;
+    return KVZ_OK;
+}
+
+int run_attention(bool compressed, const kvz_dims &d, int batch, int hq, const void *q, const int32_t *page_ids,
+                  int max_pages, const int32_t *seq_lens, const int32_t *tail_page, const uint64_t *meta,
+                  int64_t num_meta_pages, const uint8_t *arena, uint64_t arena_bytes, const void *raw_pool,
+                  int64_t num_raw_pages, float *out, void *ws, size_t ws_bytes, uint32_t *status, cudaStream_t stream)
+{
+    const int hkv = d.num_kv_heads;
+    const int table_pages = compressed ? max_pages + 1 : max_pages;
+    int grid = 0;
+    int rc = attention_grid(batch, hkv, table_pages, &grid);
+    if (rc) return rc;
+    if (attn_ws_bytes(batch, hkv, grid) > ws_bytes) return KVZ_ERR_WORKSPACE;
+    CUtensorMap map;
+    // a pool with no pages still needs a valid map object; it is never dereferenced
+    rc = raw_tensor_map(raw_pool ? raw_pool : ws, num_raw_pages > 0 ? num_raw_pages : 1, hkv, &map);
+    if (rc) return rc;
+    AttnParams P;
+    memset(&P, 0, sizeof P);
+    P.batch = batch;
+    P.hkv = hkv;
+    P.G = hq / hkv;
+    P.max_pages = max_pages;
+    P.grid = grid;
+    P.q = static_cast<const uint16_t *>(q);
+    P.page_ids = page_ids;
+    P.seq_lens = seq_lens;
+    P.tail_page = tail_page;
+    P.meta = meta;
+    P.num_meta_pages = num_meta_pages;
+    P.arena = arena;
+    P.arena_bytes = arena_bytes;
+    P.num_raw_pages = num_raw_pages;
+    P.out = out;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    P.prefix = reinterpret_cast<int32_t *>(w);
+    w += attn_ws_prefix_bytes(batch);
+    const size_t slots = attn_slots(batch, hkv, grid);
+    P.part_o = reinterpret_cast<float *>(w);
+    w += slots * 4 * 128 * 4;
+    P.part_ml = reinterpret_cast<float *>(w);
+    P.status = status;
+    P.scale_log2 = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e) / sqrt(128)
+    cudaError_t e = launch_attention(P, compressed, &map, stream);
+    return e == cudaSuccess ? KVZ_OK : fail_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kvz_strerror(int code)
+{
+    switch (code) {
+    case KVZ_OK: return "ok";
+    case KVZ_ERR_INVALID_ARG: return "invalid argument";
+    case KVZ_ERR_UNSUPPORTED: return "unsupported shape";
+    case KVZ_ERR_ALIGNMENT: return "pointer misaligned";
+    case KVZ_ERR_WORKSPACE: return "workspace too small";
+    case KVZ_ERR_CUDA: return "CUDA error (see kvz_last_cuda_error)";
+    case KVZ_ERR_DEVICE: return "no usable CUDA device";
+    case KVZ_ERR_OUT_OF_SPACE: return "no free arena chunk";
+    default: return "unknown error";
+    }
+}
+
+int kvz_last_cuda_error(void) { return g_last_cuda; }
+
+int kvz_device_sm_count(void) { return sm_count(); }
+
+size_t kvz_encode_workspace_size(kvz_dims dims, int32_t n)
+{
+    if (!dims_ok(dims) || n < 0) return 0;
+    return 16 + ((size_t)n * dims.num_kv_heads * 4 + 15) / 16 * 16 * 2;
+}
+
+int kvz_encode_pages(kvz_dims dims, const void *raw_pool, int64_t num_raw_pages, const int32_t *src_page,
+                     const int32_t *dst_page, const int32_t *dst_seq, int32_t n, uint64_t *meta,
+                     int64_t num_meta_pages, uint8_t *arena, uint64_t arena_bytes, uint32_t *cursors,
+                     int32_t num_cursors, void *workspace, size_t workspace_bytes, uint32_t *status,
+                     kvz_stream_t stream)
+{
+    if (!dims_ok(dims)) return dims.num_kv_heads >= 1 ? KVZ_ERR_UNSUPPORTED : KVZ_ERR_INVALID_ARG;
+    if (n < 0 || num_raw_pages < 0 || num_meta_pages < 0 || num_cursors < 0) return KVZ_ERR_INVALID_ARG;
+    if (n == 0) return KVZ_OK;
+    if (!raw_pool || !src_page || !dst_page || !dst_seq || !meta || !arena || !cursors || !workspace || !status)
+        return KVZ_ERR_INVALID_ARG;
+    if (!aligned(raw_pool, 16) || !aligned(meta, 16) || !aligned(arena, 256) || !aligned(cursors, 8) ||
+        !aligned(workspace, 16) || !aligned(status, 4))
+        return KVZ_ERR_ALIGNMENT;
+    if ((int64_t)n * dims.num_kv_heads > (int64_t)1 << 30) return KVZ_ERR_UNSUPPORTED;
+    if (workspace_bytes < kvz_encode_workspace_size(dims, n)) return KVZ_ERR_WORKSPACE;
+    EncodeParams P;
+    P.hkv = dims.num_kv_heads;
+    P.n = n;
+    P.raw_pool = static_cast<const uint16_t *>(raw_pool);
+    P.num_raw_pages = num_raw_pages;
+    P.src_page = src_page;
+    P.dst_page = dst_page;
+    P.dst_seq = dst_seq;
+    P.meta = meta;
+    P.num_meta_pages = num_meta_pages;
+    P.arena = arena;
+    P.arena_bytes = arena_bytes;
+    P.cursors = cursors;
+    P.num_cursors = num_cursors;
+    P.status = status;
+    uint8_t *w = static_cast<uint8_t *>(workspace);
+    const size_t arr = ((size_t)n * dims.num_kv_heads * 4 + 15) / 16 * 16;
+    P.ws_call_ok = reinterpret_cast<uint32_t *>(w);
+    P.ws_pair_size = reinterpret_cast<uint32_t *>(w + 16);
+    P.ws_pair_base = reinterpret_cast<uint32_t *>(w + 16 + arr);
+    cudaError_t e = launch_encode(P, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KVZ_OK : fail_cuda(e);
+}
+
+int kvz_decode_blocks(kvz_dims dims, const uint64_t *meta, int64_t num_meta_pages, const uint8_t *arena,
+                      uint64_t arena_bytes, const int32_t *page, int32_t n, void *out_pages, uint32_t *status,
+                      kvz_stream_t stream)
+{
+    if (!dims_ok(dims)) return dims.num_kv_heads >= 1 ? KVZ_ERR_UNSUPPORTED : KVZ_ERR_INVALID_ARG;
+    if (n < 0 || num_meta_pages < 0) return KVZ_ERR_INVALID_ARG;
+    if (n == 0) return KVZ_OK;
+    if (!meta || !arena || !page || !out_pages || !status) return KVZ_ERR_INVALID_ARG;
+    if (!aligned(meta, 8) || !aligned(arena, 256) || !aligned(out_pages, 16) || !aligned(status, 4))
+        return KVZ_ERR_ALIGNMENT;
+    if ((int64_t)n * dims.num_kv_heads > (int64_t)1 << 30) return KVZ_ERR_UNSUPPORTED;
+    DecodeParams P;
+    P.hkv = dims.num_kv_heads;
+    P.n = n;
+    P.meta = meta;
+    P.num_meta_pages = num_meta_pages;
+    P.arena = arena;
+    P.arena_bytes = arena_bytes;
+    P.page = page;
+    P.out = static_cast<uint16_t *>(out_pages);
+    P.status = status;
+    cudaError_t e = launch_decode(P, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KVZ_OK : fail_cuda(e);
+}
+
+size_t kvz_attention_workspace_size(kvz_dims dims, int32_t batch, int32_t num_q_heads, int32_t table_pages)
+{
+    if (!dims_ok(dims) || batch < 0 || num_q_heads < 1 || table_pages < 0) return 0;
+    if (batch == 0) return 16;
+    int grid = 0;
+    if (attention_grid(batch, dims.num_kv_heads, table_pages, &grid) != KVZ_OK) return 0;
+    return attn_ws_bytes(batch, dims.num_kv_heads, grid);
+}
+
+int kvz_decode_attention(kvz_dims dims, int32_t batch, int32_t num_q_heads, const void *q, const int32_t *page_ids,
+                         int32_t max_pages, const int32_t *seq_lens, const int32_t *tail_page, const uint64_t *meta,
+                         int64_t num_meta_pages, const uint8_t *arena, uint64_t arena_bytes, const void *raw_pool,
+                         int64_t num_raw_pages, float *out, void *workspace, size_t workspace_bytes,
+                         uint32_t *status, kvz_stream_t stream)
+{
+    int rc = check_attention_common(dims, batch, num_q_heads, q, seq_lens, raw_pool, num_raw_pages, out, workspace,
+                                    status, max_pages, page_ids);
+    if (rc || batch == 0) return rc;
+    if (!tail_page || !meta || !arena || num_meta_pages < 0) return KVZ_ERR_INVALID_ARG;
+    if (!aligned(meta, 16) || !aligned(arena, 256) || !aligned(tail_page, 4)) return KVZ_ERR_ALIGNMENT;
+    return run_attention(true, dims, batch, num_q_heads, q, page_ids, max_pages, seq_lens, tail_page, meta,
+                         num_meta_pages, arena, arena_bytes, raw_pool, num_raw_pages, out, workspace,
+                         workspace_bytes, status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kvz_decode_attention_raw(kvz_dims dims, int32_t batch, int32_t num_q_heads, const void *q,
+                             const int32_t *page_ids, int32_t max_pages, const int32_t *seq_lens,
+                             const void *raw_pool, int64_t num_raw_pages, float *out, void *workspace,
+                             size_t workspace_bytes, uint32_t *status, kvz_stream_t stream)
+{
+    int rc = check_attention_common(dims, batch, num_q_heads, q, seq_lens, raw_pool, num_raw_pages, out, workspace,
+                                    status, max_pages, page_ids);
+    if (rc || batch == 0) return rc;
+    return run_attention(false, dims, batch, num_q_heads, q, page_ids, max_pages, seq_lens, nullptr, nullptr, 0,
+                         nullptr, 0, raw_pool, num_raw_pages, out, workspace, workspace_bytes, status,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kvz_apply_cursor_updates(const int32_t *idx, const uint32_t *pos, const uint32_t *end, int32_t n,
+                             uint32_t *cursors, int32_t num_cursors, kvz_stream_t stream)
+{
+    if (n < 0 || num_cursors < 0) return KVZ_ERR_INVALID_ARG;
+    if (n == 0) return KVZ_OK;
+    if (!idx || !pos || !end || !cursors) return KVZ_ERR_INVALID_ARG;
+    cudaError_t e = launch_apply_cursor_updates(idx, pos, end, n, cursors, num_cursors,
+                                                reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KVZ_OK : fail_cuda(e);
+}
+
+}  // extern "C"

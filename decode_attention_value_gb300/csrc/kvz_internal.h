@@ -1,0 +1,89 @@
+// kvz_internal.h -- parameter blocks and launchers shared by the host runtime
+// (kvz_api.cu) and the kernels (codec.cu, attention.cu).  Not installed.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kvz_device.cuh"
+
+namespace kvz {
+
+struct EncodeParams {
+    int hkv;
+    int n;
+    const uint16_t *raw_pool;
+    int64_t num_raw_pages;
+    const int32_t *src_page, *dst_page, *dst_seq;
+    uint64_t *meta;
+    int64_t num_meta_pages;
+    uint8_t *arena;
+    uint64_t arena_bytes;
+    uint32_t *cursors;
+    int num_cursors;
+    uint32_t *status;
+    // workspace
+    uint32_t *ws_pair_size;  // [n*hkv]
+    uint32_t *ws_pair_base;  // [n*hkv]
+    uint32_t *ws_call_ok;    // [1]
+};
+
+struct DecodeParams {
+    int hkv;
+    int n;
+    const uint64_t *meta;
+    int64_t num_meta_pages;
+    const uint8_t *arena;
+    uint64_t arena_bytes;
+    const int32_t *page;
+    uint16_t *out;
+    uint32_t *status;
+};
+
+// Attention work split: grid = C CTAs over the flattened (sequence, KV head, page)
+// list; partial results live in U + C - 1 slots (U = batch * Hkv units).
+constexpr int kCtasPerSm = 3;
+constexpr int kMinPagesPerCta = 4;
+constexpr int kMaxBatch = 1024;
+
+struct AttnParams {
+    int batch, hkv, G, max_pages;
+    int grid;  // C
+    const uint16_t *q;
+    const int32_t *page_ids, *seq_lens, *tail_page;
+    const uint64_t *meta;
+    int64_t num_meta_pages;
+    const uint8_t *arena;
+    uint64_t arena_bytes;
+    int64_t num_raw_pages;
+    float *out;
+    float *part_o;     // [slots][4][128]
+    float *part_ml;    // [slots][4][2]
+    int32_t *prefix;   // [batch + 1] page prefix per sequence, written by CTA 0
+    uint32_t *status;
+    float scale_log2;  // log2(e) / sqrt(128)
+};
+
+inline size_t attn_slots(int batch, int hkv, int grid) { return (size_t)batch * hkv + grid - 1; }
+
+// workspace layout: prefix (batch+1 int32, rounded to 16 B), part_o, part_ml
+inline size_t attn_ws_prefix_bytes(int batch) { return ((size_t)(batch + 1) * 4 + 15) / 16 * 16; }
+inline size_t attn_ws_bytes(int batch, int hkv, int grid)
+{
+    size_t pre = attn_ws_prefix_bytes(batch);
+    size_t slots = attn_slots(batch, hkv, grid);
+    return pre + slots * 4 * 128 * 4 + slots * 4 * 2 * 4;
+}
+
+cudaError_t launch_encode(const EncodeParams &P, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeParams &P, cudaStream_t stream);
+cudaError_t launch_apply_cursor_updates(const int32_t *idx, const uint32_t *pos, const uint32_t *end, int n,
+                                        uint32_t *cursors, int num_cursors, cudaStream_t stream);
+// tmap: a CUtensorMap (128-byte object) over the raw pool viewed as
+// [num_raw_pages*Hkv*32 rows][128 BF16], box 64 x 32, 128-byte swizzle.
+cudaError_t launch_attention(const AttnParams &P, bool compressed, const void *tmap, cudaStream_t stream);
+int attn_smem_bytes(int batch);
+// CTAs per SM both attention kernels can hold at this batch size (the smaller of the two)
+cudaError_t attn_ctas_per_sm(int batch, int *out);
+
+}  // namespace kvz

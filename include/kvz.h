@@ -1,0 +1,229 @@
+/*
+ * kvz.h -- C ABI of libkvz: lossless 12-bit BF16 KV-cache pages and paged GQA decode
+ * attention that reads them, for one NVIDIA GB300 (sm_103a).
+ *
+ * The block format is the one fixed on the page "ZipFusion: Fusing Lossless KV
+ * Decompression with Attention for Efficient LLM Decoding" (section "How it works",
+ * steps 1-4, the operand-role layout paragraph and the metadata paragraph); the
+ * page lifecycle (encode once on completion, raw BF16 tail until then) and the one
+ * shared softmax over compressed pages and the raw tail follow "GAAC: Lossless KV
+ * Compression for Bandwidth-Efficient LLM Inference on Personal Devices" (sections
+ * "Attention with On-the-Fly Decompression" and "Block-Wise Compression Scheduling").
+ *
+ * ---------------------------------------------------------------------------------
+ * Data layouts (all little-endian; every pointer is DEVICE memory owned by the
+ * caller unless stated otherwise; the library never allocates device memory):
+ *
+ *  raw pool   BF16 [num_raw_pages][Hkv][2][16][128]; [2] = K, V; a page slice is
+ *             [token][dim].  Base 16-byte aligned.
+ *  block      One (page, KV head, K|V) slice splits into 4 blocks of 512 values;
+ *             block j holds dims [32j, 32j+32) of all 16 tokens.  Inside a block the
+ *             values are in "storage order": lane L (0..31), fragment f (0..1),
+ *             element i (0..7); with g = L/4, t = L%4, r = g + 8*((i/2)%2),
+ *             c = 2t + i%2 + 8*(i/4):  K value (token r, dim 32j+16f+c), V value
+ *             (token c, dim 32j+16f+r).  This is the per-lane A operand of a 16x16
+ *             tensor-core tile in each block's role: K for QK^T, V^T for PV.
+ *  eligible   b = min exponent rounded down to even; every exponent in [b, b+15].
+ *  block (768 B)  bytes [0,512): low byte of element (L,f,i) at 16L+8f+i (exponent
+ *             LSB + 7 fraction bits); bytes [512,768): code byte 512+8L+4f+k pairs
+ *             elements k and k+4:  sign_k<<7 | d_(k+4)<<4 | sign_(k+4)<<3 | d_k,
+ *             d = (e-b)/2.  Restore: e = b + 2d + r (r = exponent LSB).
+ *  raw block (1024 B)  512 BF16 words in storage order.
+ *  meta       uint64 [num_meta_pages][Hkv][2]: per (page, head, K|V) group of 4
+ *             blocks, bits 0..31 = offset of the group's first block in 256-byte
+ *             granules from the arena base, bits 32..63 = one tag byte per block:
+ *             b/2 (0..127) or 0xFF = raw.  Block j starts at offset0 + sum over
+ *             k<j of (3 or 4) granules.  offset0 = 0xFFFFFFFF marks an unwritten group.
+ *  arena      uint8 buffer, 256-byte aligned; groups are placed back to back at
+ *             per-cursor positions.
+ *  cursors    uint32 [num_cursors][2] = {next free granule, end granule (excl.)}.
+ *
+ * Error behaviour: every call validates its arguments on the host and returns 0 or
+ * a negative KVZ_ERR_* code without launching anything.  Calls are asynchronous on
+ * `stream` and never synchronise.  Conditions only the device can see (an index out
+ * of range, unusable metadata, a full cursor region, a bounded wait that expired)
+ * are OR-ed as KVZ_STATUS_* bits into *status (a device uint32 the caller zeroes and
+ * reads when it wants); the offending page or group is skipped, never trapped on.
+ */
+#ifndef KVZ_H
+#define KVZ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVZ_PAGE_TOKENS 16
+#define KVZ_HEAD_DIM 128
+#define KVZ_GRANULE_BYTES 256
+#define KVZ_BLOCK_BYTES_ELIGIBLE 768
+#define KVZ_BLOCK_BYTES_RAW 1024
+#define KVZ_TAG_RAW 0xFF
+#define KVZ_OFFSET_INVALID 0xFFFFFFFFu
+
+/* host-side return codes */
+#define KVZ_OK 0
+#define KVZ_ERR_INVALID_ARG -1
+#define KVZ_ERR_UNSUPPORTED -2
+#define KVZ_ERR_ALIGNMENT -3
+#define KVZ_ERR_WORKSPACE -4
+#define KVZ_ERR_CUDA -5
+#define KVZ_ERR_DEVICE -6
+#define KVZ_ERR_OUT_OF_SPACE -7
+
+/* device-side status bits */
+#define KVZ_STATUS_ARENA_FULL 1u
+#define KVZ_STATUS_BAD_INDEX 2u
+#define KVZ_STATUS_BAD_ORDER 4u
+#define KVZ_STATUS_BAD_META 8u
+#define KVZ_STATUS_TIMEOUT 16u
+#define KVZ_STATUS_BAD_TAIL 32u
+
+/* A CUDA stream (same object as cudaStream_t / CUstream); NULL = legacy stream. */
+typedef struct CUstream_st *kvz_stream_t;
+
+/* Shapes shared by every call.  head_dim must be 128 and page_size 16. */
+typedef struct {
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t page_size;
+} kvz_dims;
+
+/* ---------------------------------------------------------------------------------
+ * kvz_encode_pages -- compress completed pages of one layer (ZipFusion "How it
+ * works" steps 1-3 and the metadata paragraph; GAAC "Block-Wise Compression
+ * Scheduling": each page is encoded once, when it completes).
+ *
+ *  raw_pool         raw pool of this layer (see layouts), num_raw_pages pages
+ *  src_page[n]      raw page to encode, per entry
+ *  dst_page[n]      meta page index the result is recorded under
+ *  dst_seq[n]       cursor the groups are appended at; must be non-decreasing
+ *  meta             this layer's metadata table, num_meta_pages pages (16-B aligned)
+ *  arena            compressed storage, arena_bytes long (256-B aligned)
+ *  cursors          num_cursors cursor pairs, advanced in place
+ *  workspace        >= kvz_encode_workspace_size(n) bytes of scratch (16-B aligned)
+ * Placement: entries in call order, then KV head, then K before V; each group's four
+ * blocks are contiguous at its cursor, which then advances by the group's size.  A
+ * group that would pass its cursor's end or the arena is not written (offset0 set to
+ * KVZ_OFFSET_INVALID, KVZ_STATUS_ARENA_FULL), the cursor still advances.  An index out
+ * of range (KVZ_STATUS_BAD_INDEX) or a decreasing dst_seq (KVZ_STATUS_BAD_ORDER) makes
+ * the whole call write nothing.
+ * --------------------------------------------------------------------------------- */
+size_t kvz_encode_workspace_size(kvz_dims dims, int32_t n);
+int kvz_encode_pages(kvz_dims dims, const void *raw_pool, int64_t num_raw_pages,
+                     const int32_t *src_page, const int32_t *dst_page, const int32_t *dst_seq,
+                     int32_t n, uint64_t *meta, int64_t num_meta_pages, uint8_t *arena,
+                     uint64_t arena_bytes, uint32_t *cursors, int32_t num_cursors,
+                     void *workspace, size_t workspace_bytes, uint32_t *status,
+                     kvz_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * kvz_decode_blocks -- standalone bit-exact decompression (ZipFusion "How it works"
+ * step 4), used to check the format and to time decoding on its own.
+ *  page[n]     meta page indices;  out_pages: BF16 [n][Hkv][2][16][128] (16-B aligned)
+ * A group with unusable metadata is written as zeros (KVZ_STATUS_BAD_META); an out of
+ * range page index zero-fills that page (KVZ_STATUS_BAD_INDEX).
+ * --------------------------------------------------------------------------------- */
+int kvz_decode_blocks(kvz_dims dims, const uint64_t *meta, int64_t num_meta_pages,
+                      const uint8_t *arena, uint64_t arena_bytes, const int32_t *page, int32_t n,
+                      void *out_pages, uint32_t *status, kvz_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * kvz_decode_attention -- GQA paged decode attention over compressed pages plus an
+ * uncompressed tail page, one softmax over both (GAAC "Attention with On-the-Fly
+ * Decompression"; ZipFusion "How it works": restore in registers, tensor-core QK^T
+ * and PV, no decompressed copy in memory).
+ *
+ *  q            BF16 [batch][num_q_heads][128]; query head h reads KV head h/G,
+ *               G = num_q_heads / num_kv_heads (G in {1, 2, 4})
+ *  page_ids     int32 [batch][max_pages] meta page ids of each sequence's completed pages
+ *  seq_lens     int32 [batch] tokens in context; the first seq_lens/16 pages come from
+ *               page_ids, the last seq_lens%16 tokens from raw page tail_page[b]
+ *  tail_page    int32 [batch] raw page id of the tail (-1 when seq_lens%16 == 0)
+ *  out          float32 [batch][num_q_heads][128]:
+ *               softmax(q.K^T / sqrt(128)) V over the sequence's tokens
+ *  workspace    >= kvz_attention_workspace_size(dims, batch, num_q_heads, max_pages + 1)
+ *               bytes (16-B aligned); the split-KV partial results
+ * Output for an empty sequence is zero.  A page with unusable metadata or an index out
+ * of range is left out of the softmax and flagged.
+ * Determinism: the work split depends only on (batch, num_kv_heads, seq_lens, the
+ * block-table width counted with its tail slot, and the device's SM count), so for
+ * the same data this call and kvz_decode_attention_raw (given a table one column
+ * wider that ends in the tail page) return bit-identical outputs.
+ * --------------------------------------------------------------------------------- */
+size_t kvz_attention_workspace_size(kvz_dims dims, int32_t batch, int32_t num_q_heads,
+                                    int32_t table_pages);
+int kvz_decode_attention(kvz_dims dims, int32_t batch, int32_t num_q_heads, const void *q,
+                         const int32_t *page_ids, int32_t max_pages, const int32_t *seq_lens,
+                         const int32_t *tail_page, const uint64_t *meta, int64_t num_meta_pages,
+                         const uint8_t *arena, uint64_t arena_bytes, const void *raw_pool,
+                         int64_t num_raw_pages, float *out, void *workspace,
+                         size_t workspace_bytes, uint32_t *status, kvz_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * kvz_decode_attention_raw -- the same kernel over plain BF16 pages: the in-run
+ * uncompressed baseline.  page_ids [batch][max_pages] are raw page ids covering all
+ * ceil(seq_lens/16) pages (the last one possibly partial).  workspace >=
+ * kvz_attention_workspace_size(dims, batch, num_q_heads, max_pages).
+ * --------------------------------------------------------------------------------- */
+int kvz_decode_attention_raw(kvz_dims dims, int32_t batch, int32_t num_q_heads, const void *q,
+                             const int32_t *page_ids, int32_t max_pages, const int32_t *seq_lens,
+                             const void *raw_pool, int64_t num_raw_pages, float *out,
+                             void *workspace, size_t workspace_bytes, uint32_t *status,
+                             kvz_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * Host-side chunk allocator for the arena (GAAC "Block-Wise Compression Scheduling":
+ * two fixed storage classes, 768-byte and 1024-byte block slots; ZipFusion: the memory
+ * manager tracks the space left, hands chunks freed by one layer or sequence to
+ * another, and reports capacity).  Pure host code, no device memory is touched.
+ *
+ * The arena is cut into fixed chunks of chunk_granules granules.  Each cursor (one per
+ * sequence, shared by all its layers) owns a chain of chunks and a device cursor pair.
+ * Before an encode call the caller asks kvz_alloc_reserve for room for `pages` pages
+ * on each cursor: the allocator keeps an upper bound of every cursor's position
+ * (pos + worst case of every reservation since the last observation), and when the
+ * worst case of the new pages does not fit the current chunk it takes a fresh chunk.
+ * The cursor pairs the device must hold before the encode are returned as updates
+ * (cursor index, pos, end) for the caller to copy to the device.  kvz_alloc_observe
+ * feeds back a device snapshot of the cursors taken after reservation `ticket`, which
+ * tightens the bounds.  kvz_alloc_release returns a finished sequence's chunks.
+ * --------------------------------------------------------------------------------- */
+typedef struct kvz_alloc kvz_alloc;
+int kvz_alloc_create(uint64_t arena_bytes, uint32_t chunk_granules, int32_t num_cursors,
+                     int32_t num_kv_heads, kvz_alloc **out);
+void kvz_alloc_destroy(kvz_alloc *a);
+/* pages[k] pages for cursor cursor_ids[k] (host arrays, k < count, each cursor at most
+ * once).  upd_idx/upd_pos/upd_end (host, capacity `count`) receive *n_upd updates;
+ * *ticket identifies the reservation.  Returns KVZ_ERR_OUT_OF_SPACE (nothing changed)
+ * when no free chunk is left for a cursor that needs one. */
+int kvz_alloc_reserve(kvz_alloc *a, const int32_t *cursor_ids, const int32_t *pages, int32_t count,
+                      int32_t *upd_idx, uint32_t *upd_pos, uint32_t *upd_end, int32_t *n_upd,
+                      uint64_t *ticket);
+/* cursors_snapshot: host copy of the device cursors [num_cursors][2] taken after the
+ * encode that used reservation `ticket` completed. */
+int kvz_alloc_observe(kvz_alloc *a, uint64_t ticket, const uint32_t *cursors_snapshot);
+int kvz_alloc_release(kvz_alloc *a, int32_t cursor_id);
+/* bytes in chunks held by cursors, bytes in free chunks, bytes known used (observed
+ * cursor positions), chunks held, chunks free */
+int kvz_alloc_stats(const kvz_alloc *a, uint64_t *held_bytes, uint64_t *free_bytes,
+                    uint64_t *used_bytes_bound, int32_t *chunks_held, int32_t *chunks_free);
+
+/* Copy n cursor updates (device arrays idx[n], pos[n], end[n]) into cursors. */
+int kvz_apply_cursor_updates(const int32_t *idx, const uint32_t *pos, const uint32_t *end,
+                             int32_t n, uint32_t *cursors, int32_t num_cursors,
+                             kvz_stream_t stream);
+
+/* Text for a KVZ_ERR_* code. */
+const char *kvz_strerror(int code);
+/* The last CUDA error seen by a failed call on this thread (a cudaError_t value). */
+int kvz_last_cuda_error(void);
+/* SM count of the current device, as used for the attention work split. */
+int kvz_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,199 @@
+"""CPU checks of the C-ABI boundary: libkvz.so loads, exports every function that
+include/kvz.h declares, rejects bad arguments on the host before any launch, and its
+host-side chunk allocator (GAAC "Block-Wise Compression Scheduling"; ZipFusion memory
+manager paragraph) keeps every encoded group inside its sequence's chunk when the
+CPU oracle stands in for the device."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import kvgen
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kvz():
+    from decode_attention_value_gb300 import _build
+
+    _build.build()
+    import decode_attention_value_gb300 as m
+
+    return m
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"\b(kvz_[a-z0-9_]+)\s*\(", text):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_four_calls():
+    names = declared_functions()
+    for call in ("kvz_encode_pages", "kvz_decode_blocks", "kvz_decode_attention", "kvz_decode_attention_raw"):
+        assert call in names
+
+
+def test_library_exports_every_declared_symbol(kvz):
+    lib = ctypes.CDLL(kvz._build.LIB)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(kvz.EXPORTS) <= set(declared_functions())
+
+
+def test_strerror(kvz):
+    lib = kvz.lib()
+    assert lib.kvz_strerror(0) == b"ok"
+    for code in range(-7, 0):
+        assert lib.kvz_strerror(code) not in (b"", b"unknown error")
+
+
+def _dims(kvz, hkv=8, d=128, p=16):
+    return kvz.Dims(hkv, d, p)
+
+
+def test_host_rejects_bad_arguments(kvz):
+    lib = kvz.lib()
+    E = dict(inval=-1, unsup=-2, align=-3, ws=-4)
+    fake = 1 << 20  # never dereferenced: every call below returns before any launch
+    # shapes other than head_dim 128 / page 16 are unsupported, Hkv < 1 is invalid
+    assert lib.kvz_encode_pages(_dims(kvz, d=64), fake, 1, fake, fake, fake, 1, fake, 1, fake, 1 << 20, fake, 1,
+                                fake, 1 << 20, fake, None) == E["unsup"]
+    assert lib.kvz_encode_pages(_dims(kvz, hkv=0), fake, 1, fake, fake, fake, 1, fake, 1, fake, 1 << 20, fake, 1,
+                                fake, 1 << 20, fake, None) == E["inval"]
+    # n = 0 is a no-op, negative n invalid
+    assert lib.kvz_encode_pages(_dims(kvz), None, 0, None, None, None, 0, None, 0, None, 0, None, 0, None, 0,
+                                None, None) == 0
+    assert lib.kvz_encode_pages(_dims(kvz), fake, 1, fake, fake, fake, -1, fake, 1, fake, 1 << 20, fake, 1,
+                                fake, 1 << 20, fake, None) == E["inval"]
+    # null pointer / misaligned arena / short workspace
+    assert lib.kvz_encode_pages(_dims(kvz), fake, 1, None, fake, fake, 1, fake, 1, fake, 1 << 20, fake, 1,
+                                fake, 1 << 20, fake, None) == E["inval"]
+    assert lib.kvz_encode_pages(_dims(kvz), fake, 1, fake, fake, fake, 1, fake, 1, fake + 16, 1 << 20, fake, 1,
+                                fake, 1 << 20, fake, None) == E["align"]
+    ws = kvz.encode_workspace_size(8, 10)
+    assert ws >= 2 * 10 * 8 * 4
+    assert lib.kvz_encode_pages(_dims(kvz), fake, 10, fake, fake, fake, 10, fake, 10, fake, 1 << 20, fake, 1,
+                                fake, ws - 1, fake, None) == E["ws"]
+    # decode: misaligned output
+    assert lib.kvz_decode_blocks(_dims(kvz), fake, 1, fake, 1 << 20, fake, 1, fake + 2, fake, None) == E["align"]
+    assert lib.kvz_decode_blocks(_dims(kvz), None, 0, None, 0, None, 0, None, None, None) == 0
+    # attention: GQA group must divide and be 1, 2 or 4
+    assert lib.kvz_decode_attention(_dims(kvz), 2, 12, fake, fake, 4, fake, fake, fake, 1, fake, 1 << 20, fake, 1,
+                                    fake, fake, 1 << 20, fake, None) == E["inval"]
+    assert lib.kvz_decode_attention(_dims(kvz), 2, 64, fake, fake, 4, fake, fake, fake, 1, fake, 1 << 20, fake, 1,
+                                    fake, fake, 1 << 20, fake, None) == E["unsup"]
+    assert lib.kvz_decode_attention_raw(_dims(kvz), 2, 32, fake + 8, fake, 4, fake, fake, 1, fake, fake, 1 << 20,
+                                        fake, None) == E["align"]
+    assert lib.kvz_decode_attention_raw(_dims(kvz), 0, 32, None, None, 0, None, None, 0, None, None, 0, None,
+                                        None) == 0
+    assert lib.kvz_apply_cursor_updates(None, None, None, 0, None, 0, None) == 0
+
+
+# --------------------------------------------------------------------------------------
+# allocator
+# --------------------------------------------------------------------------------------
+def test_allocator_reserve_release_stats(kvz):
+    hkv = 2
+    chunk = 4 * 64  # granules: room for 4 worst-case pages (64 granules each at Hkv 2)
+    a = kvz.Allocator(arena_bytes=chunk * 256 * 3, chunk_granules=chunk, num_cursors=4, num_kv_heads=hkv)
+    assert a.stats()["chunks_free"] == 3
+    t1, up = a.reserve([0, 1], [2, 1])
+    assert up == [(0, 0, chunk), (1, chunk, 2 * chunk)]  # chunk 0 first, then chunk 1
+    t2, up = a.reserve([0], [2])  # 2 + 2 worst-case pages still fit chunk 0
+    assert up == []
+    t3, up = a.reserve([0], [1])  # a fifth worst-case page does not
+    assert up == [(0, 2 * chunk, 3 * chunk)]
+    with pytest.raises(kvz.KvzError) as e:
+        a.reserve([2], [1])  # no chunk left
+    assert e.value.code == kvz.ERR_OUT_OF_SPACE
+    with pytest.raises(kvz.KvzError):
+        a.reserve([3], [5])  # more than a chunk in one call
+    st = a.stats()
+    assert st["chunks_held"] == 3 and st["chunks_free"] == 0
+    a.release(1)
+    assert a.stats()["chunks_free"] == 1
+    t4, up = a.reserve([2], [1])
+    assert up == [(2, chunk, 2 * chunk)]  # the released chunk is reused
+
+
+def test_allocator_observe_tightens_bound(kvz):
+    hkv = 1  # worst case per page: 2 groups x 16 granules = 32 granules
+    chunk = 90
+    a = kvz.Allocator(arena_bytes=chunk * 256 * 2, chunk_granules=chunk, num_cursors=1, num_kv_heads=hkv)
+    t, up = a.reserve([0], [2])
+    assert up == [(0, 0, chunk)]
+    assert a.stats()["used_bytes_bound"] == 64 * 256
+    # the device used 2 pages x 24 granules (every block eligible): bound drops to 48
+    a.observe(t, np.array([[48, chunk]], np.uint32))
+    assert a.stats()["used_bytes_bound"] == 48 * 256
+    t2, up = a.reserve([0], [1])  # 48 + 32 <= 90 fits; without the observation 64 + 32 would not
+    assert up == []
+    # an observation taken before the latest reservation is ignored
+    a.observe(t, np.array([[48, chunk]], np.uint32))
+    assert a.stats()["used_bytes_bound"] == 80 * 256
+    t3, up = a.reserve([0], [1])  # 80 + 32 > 90: next chunk
+    assert up == [(0, chunk, 2 * chunk)]
+
+
+def test_allocator_with_oracle_stream(kvz, oracle):
+    """Streaming page completions for several sequences, the oracle encoding into the
+    cursors the allocator hands out: no group ever overflows, chunks are recycled."""
+    cfg = kvgen.KVConfig("alloc-sim", 1, 4, 8, 2, 24, seed=21, block_outlier_frac=0.3)
+    hkv = cfg.hkv
+    pool = kvgen.bits(kvgen.gen_pages(cfg, 24))
+    chunk = 5 * 64  # 5 worst-case pages per chunk
+    nchunks = 12
+    arena = np.zeros(nchunks * chunk * 256, np.uint8)
+    a = kvz.Allocator(arena.size, chunk, num_cursors=cfg.batch, num_kv_heads=hkv)
+    cursors = np.zeros((cfg.batch, 2), np.uint32)
+    meta = np.zeros((200, hkv, 2), np.uint64)
+    next_meta = 0
+    owner = {}
+    for step in range(12):
+        seqs = [s for s in range(cfg.batch) if (step + s) % 3 != 0]
+        pages = [1 + (s % 2) for s in seqs]
+        t, ups = a.reserve(seqs, pages)
+        for c, pos, end in ups:
+            cursors[c] = (pos, end)
+        src, dst, dseq = [], [], []
+        for s, n in zip(seqs, pages):
+            for _ in range(n):
+                src.append((step * 7 + s * 5 + len(src)) % 24)
+                dst.append(next_meta)
+                owner[next_meta] = s
+                next_meta += 1
+                dseq.append(s)
+        st = oracle.encode_pages(pool, src, dst, dseq, meta, arena, cursors, hkv)
+        assert st == 0, step
+        a.observe(t, cursors)
+        if step == 6:  # sequence 1 finishes; its chunks go back to the pool
+            a.release(1)
+            cursors[1] = (0, 0)
+            for m_id in [k for k, v in owner.items() if v == 1]:
+                meta[m_id] = 0
+                owner.pop(m_id)
+    # every recorded group lies inside a chunk and no two groups overlap
+    spans = []
+    for m_id in owner:
+        for h in range(hkv):
+            for kv in range(2):
+                w = int(meta[m_id, h, kv])
+                off = w & 0xFFFFFFFF
+                size = sum(4 if (w >> (32 + 8 * j)) & 0xFF == 0xFF else 3 for j in range(4))
+                assert off // chunk == (off + size - 1) // chunk
+                spans.append((off, off + size))
+    spans.sort()
+    assert all(spans[k][1] <= spans[k + 1][0] for k in range(len(spans) - 1))
+    st = a.stats()
+    assert st["chunks_held"] + st["chunks_free"] == nchunks

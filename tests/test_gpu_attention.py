@@ -1,0 +1,122 @@
+"""GPU decode-attention parity (GAAC "Attention with On-the-Fly Decompression";
+ZipFusion "How it works"): the compressed and raw kernels against the fp64 CPU oracle
+within the stated tolerance, and against each other bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import kvgen
+from helpers import Layer, check_attention
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kvz():
+    from decode_attention_value_gb300 import _build
+
+    _build.build()
+    import decode_attention_value_gb300 as m
+
+    return m
+
+
+def run_and_check(layer, oracle, what):
+    out_c = layer.run_compressed()
+    out_r = layer.run_raw()
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == 0, f"{what}: status {int(layer.status.item())}"
+    ref, st = layer.oracle_attention(oracle)
+    assert st == 0
+    check_attention(out_c, ref, what + " compressed")
+    check_attention(out_r, ref, what + " raw")
+    assert torch.equal(out_c, out_r), f"{what}: compressed and raw outputs differ"
+    return out_c, ref
+
+
+CASES = [
+    kvgen.C0,
+    kvgen.C0_TAIL,
+    kvgen.KVConfig("ragged-b6", 1, 6, 16, 4, 9, tail_min=1, tail_max=15, k_log2_sigma=(-4, 3),
+                   v_log2_sigma=(-3, 1), k_outlier_channels=4, k_outlier_scale=32.0, block_outlier_frac=0.05,
+                   block_outlier_log2=14, seed=31),
+    kvgen.KVConfig("gqa1", 1, 3, 4, 4, 7, tail_min=3, tail_max=9, seed=32),
+    kvgen.KVConfig("gqa2", 1, 3, 8, 4, 7, tail_min=3, tail_max=9, seed=33),
+    kvgen.KVConfig("spread", 1, 2, 32, 8, 12, tail_min=1, tail_max=15, spread=(8, 20), seed=34),
+]
+
+
+@pytest.mark.parametrize("cfg", CASES, ids=lambda c: c.name)
+def test_attention_matches_oracle(kvz, oracle, cfg):
+    run_and_check(Layer(cfg, oracle), oracle, cfg.name)
+
+
+def test_ragged_lengths_and_every_tail(kvz, oracle):
+    """Lengths 0..(pages*16): empty, tail-only, every tail length 0..15, full pages."""
+    cfg = kvgen.KVConfig("lengths", 1, 20, 8, 2, 6, tail_min=1, tail_max=15, seed=41)
+    lens = [0, 1, 15, 16, 17, 31, 32, 33, 47, 48, 50, 63, 64, 70, 80, 89, 95, 96, 97, 100]
+    layer = Layer(cfg, oracle, seq_lens=lens)
+    out, ref = run_and_check(layer, oracle, "lengths")
+    assert not out[0].any()  # empty context -> zero output
+
+
+def test_many_splits_long_context(kvz, oracle):
+    """Few long sequences: every (sequence, head) unit is cut across many CTAs."""
+    cfg = kvgen.KVConfig("long", 1, 2, 8, 2, 300, tail_min=5, tail_max=11, k_log2_sigma=(-4, 3),
+                         v_log2_sigma=(-3, 1), seed=42)
+    run_and_check(Layer(cfg, oracle), oracle, "long")
+
+
+def test_bad_metadata_page_is_skipped(kvz, oracle):
+    cfg = kvgen.C0_TAIL
+    layer = Layer(cfg, oracle)
+    bad_o = layer.o_meta.copy()
+    victim = int(layer.full[0, 3])
+    bad_o[victim, 1, 1] = np.uint64(0xFFFFFFFF) | (bad_o[victim, 1, 1] & np.uint64(0xFFFFFFFF00000000))
+    bad_g = layer.meta.clone()
+    bad_g[victim, 1, 1] = torch.from_numpy(bad_o[victim, 1, 1:2].view(np.int64)).cuda()
+    st = kvz.new_status()
+    out = layer.run_compressed(meta=bad_g, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == kvz.STATUS_BAD_META
+    ref, o_st = layer.oracle_attention(oracle, meta=bad_o)
+    assert o_st == oracle.BAD_META
+    check_attention(out, ref, "bad meta")
+
+
+def test_missing_tail_page_is_flagged(kvz, oracle):
+    cfg = kvgen.C0_TAIL
+    layer = Layer(cfg, oracle)
+    layer.tail = torch.full_like(layer.tail, -1)
+    st = kvz.new_status()
+    layer.run_compressed(status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & kvz.STATUS_BAD_TAIL
+
+
+def test_full_size_layer_sampled(kvz, oracle):
+    """The Llama-3.1-8B-shaped layer (batch 32, 32/8 heads, 2048 + tail tokens, shuffled
+    pages) in the bench's launch configuration; the fp64 oracle on a sample of sequences."""
+    cfg = kvgen.C1
+    layer = Layer(cfg, None)
+    out_c = layer.run_compressed()
+    out_r = layer.run_raw()
+    torch.cuda.synchronize()
+    assert int(layer.status.item()) == 0
+    assert torch.equal(out_c, out_r)
+    pick = [0, 7, 19, 31]
+    sub = kvgen.KVConfig(cfg.name, 1, len(pick), cfg.hq, cfg.hkv, cfg.full_pages, cfg.tail_min, cfg.tail_max)
+    pool = kvgen.bits(layer.g_pool.cpu())
+    o_meta = np.zeros((cfg.num_pages, cfg.hkv, 2), np.uint64)
+    per = (cfg.full_pages + 1) * cfg.hkv * 32
+    o_arena = np.zeros(len(pick) * per * 256, np.uint8)
+    cur = np.array([[i * per, (i + 1) * per] for i in range(len(pick))], np.uint32)
+    src = np.concatenate([layer.full[b].numpy() for b in pick]).astype(np.int32)
+    seq = np.repeat(np.arange(len(pick), dtype=np.int32), cfg.full_pages)
+    assert oracle.encode_pages(pool, src, src, seq, o_meta, o_arena, cur, cfg.hkv) == 0
+    ref, st = oracle.decode_attention(kvgen.bits(layer.q[pick]), layer.full[pick].numpy(),
+                                      layer.seq_lens[pick].numpy(), layer.tail[pick].numpy(), o_meta, o_arena,
+                                      pool, cfg.hkv, nthreads=8)
+    assert st == 0
+    check_attention(out_c[pick], ref, "C1 sample")
+    del sub

@@ -1,0 +1,161 @@
+"""GPU codec parity: libkvz's encoder, placement scan and decoder against the CPU
+oracle, bit for bit (ZipFusion "How it works" steps 1-4, metadata paragraph)."""
+import numpy as np
+import pytest
+import torch
+
+import kvgen
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kvz():
+    from decode_attention_value_gb300 import _build
+
+    _build.build()
+    import decode_attention_value_gb300 as m
+
+    return m
+
+
+def encode_both(kvz, oracle, pool, src, dst, seq, n_meta, arena_bytes, cursors0):
+    hkv = pool.shape[1]
+    g_meta = torch.zeros((n_meta, hkv, 2), dtype=torch.int64, device="cuda")
+    g_arena = torch.zeros(arena_bytes, dtype=torch.uint8, device="cuda")
+    g_cur = torch.from_numpy(np.asarray(cursors0, np.uint32).view(np.int32).copy()).cuda()
+    st = kvz.new_status()
+    kvz.encode_pages(pool.cuda(), torch.as_tensor(src, dtype=torch.int32).cuda(),
+                     torch.as_tensor(dst, dtype=torch.int32).cuda(), torch.as_tensor(seq, dtype=torch.int32).cuda(),
+                     g_meta, g_arena, g_cur, st)
+    torch.cuda.synchronize()
+    o_meta = np.zeros((n_meta, hkv, 2), np.uint64)
+    o_arena = np.zeros(arena_bytes, np.uint8)
+    o_cur = np.asarray(cursors0, np.uint32).copy()
+    o_st = oracle.encode_pages(kvgen.bits(pool), src, dst, seq, o_meta, o_arena, o_cur, hkv)
+    gpu = (g_meta.cpu().numpy().view(np.uint64), g_arena.cpu().numpy(), g_cur.cpu().numpy().view(np.uint32),
+           int(st.item()))
+    return gpu, (o_meta, o_arena, o_cur, o_st)
+
+
+def assert_same(gpu, ora):
+    assert gpu[3] == ora[3], f"status {gpu[3]} vs oracle {ora[3]}"
+    assert np.array_equal(gpu[2], ora[2]), "cursors differ"
+    assert np.array_equal(gpu[0], ora[0]), "metadata differs"
+    diff = np.nonzero(gpu[1] != ora[1])[0]
+    assert diff.size == 0, f"arena differs at {diff[:8]} ({diff.size} bytes)"
+
+
+def spread_cfg(lo, hi, seed, hkv=2):
+    return kvgen.KVConfig(f"spread{lo}-{hi}", 1, 1, 4 * hkv, hkv, 8, spread=(lo, hi), seed=seed)
+
+
+@pytest.mark.parametrize("cfg", [kvgen.C0, spread_cfg(8, 20, 5), spread_cfg(8, 14, 6), spread_cfg(16, 20, 7),
+                                 kvgen.KVConfig("llama-like", 1, 1, 32, 8, 6, k_log2_sigma=(-4, 3),
+                                                v_log2_sigma=(-3, 1), k_outlier_channels=4,
+                                                k_outlier_scale=32.0, seed=9)],
+                         ids=lambda c: c.name)
+def test_encode_bit_exact(kvz, oracle, cfg):
+    n = cfg.num_pages
+    pool = kvgen.gen_pages(cfg, n)
+    src = np.random.default_rng(cfg.seed).permutation(n).astype(np.int32)
+    dst = np.arange(n, dtype=np.int32)
+    seq = np.zeros(n, np.int32)
+    gpu, ora = encode_both(kvz, oracle, pool, src, dst, seq, n, n * cfg.hkv * 8192 + 4096, [[3, 1 << 30]])
+    assert_same(gpu, ora)
+
+
+def test_encode_extremes_all_eligible_and_all_raw(kvz, oracle):
+    # spread 8 -> every block eligible; spread 20 -> every block raw
+    for lo_hi, expect_raw in (((8, 8), False), ((20, 20), True)):
+        cfg = spread_cfg(*lo_hi, seed=11, hkv=4)
+        pool = kvgen.gen_pages(cfg, cfg.num_pages)
+        n = cfg.num_pages
+        gpu, ora = encode_both(kvz, oracle, pool, np.arange(n, dtype=np.int32), np.arange(n, dtype=np.int32),
+                               np.zeros(n, np.int32), n, n * 4 * 8192, [[0, 1 << 30]])
+        assert_same(gpu, ora)
+        tags = ora[0] >> np.uint64(32)
+        all_raw = np.all(tags == np.uint64(0xFFFFFFFF))
+        assert bool(all_raw) == expect_raw
+        per_group = 16 if expect_raw else 12
+        assert int(ora[2][0, 0]) == n * 4 * 2 * per_group
+
+
+def test_encode_many_cursors_and_scan_tiles(kvz, oracle):
+    """Thousands of (page, head) pairs -> several scan tiles, segments crossing tiles."""
+    cfg = kvgen.KVConfig("scan", 1, 1, 32, 8, 1200, k_log2_sigma=(-4, 3), v_log2_sigma=(-3, 1),
+                         block_outlier_frac=0.2, seed=13)
+    n = cfg.num_pages
+    pool = kvgen.gen_pages(cfg, n)
+    rng = np.random.default_rng(2)
+    sizes = np.array([100, 150, 7, 149, 1, 133, 150, 150, 150, 210], np.int64)  # 10 cursors, 1200 pages
+    assert sizes.sum() == n
+    seq = np.repeat(np.arange(10, dtype=np.int32), sizes)
+    worst = sizes * cfg.hkv * 2 * 16
+    starts = np.concatenate([[5], 5 + np.cumsum(worst + 3)[:-1]])
+    cursors = np.stack([starts, starts + worst], 1).astype(np.uint32)
+    src = rng.permutation(n).astype(np.int32)
+    dst = rng.permutation(n).astype(np.int32)
+    arena_bytes = int(cursors[-1, 1]) * 256
+    gpu, ora = encode_both(kvz, oracle, pool, src, dst, seq, n, arena_bytes, cursors)
+    assert_same(gpu, ora)
+
+
+def test_encode_error_paths_match_oracle(kvz, oracle):
+    cfg = kvgen.C0
+    n = 6
+    pool = kvgen.gen_pages(cfg, n)
+    ar = n * cfg.hkv * 8192
+    # cursor region too small: later groups are marked invalid, nothing written past the end
+    gpu, ora = encode_both(kvz, oracle, pool, np.arange(n, dtype=np.int32), np.arange(n, dtype=np.int32),
+                           np.zeros(n, np.int32), n, ar, [[0, 100]])
+    assert ora[3] == oracle.ARENA_FULL
+    assert_same(gpu, ora)
+    # arena smaller than the cursor claims
+    gpu, ora = encode_both(kvz, oracle, pool, np.arange(n, dtype=np.int32), np.arange(n, dtype=np.int32),
+                           np.zeros(n, np.int32), n, 90 * 256, [[0, 1 << 20]])
+    assert ora[3] == oracle.ARENA_FULL
+    assert_same(gpu, ora)
+    # decreasing cursor order: nothing happens
+    gpu, ora = encode_both(kvz, oracle, pool, np.arange(n, dtype=np.int32), np.arange(n, dtype=np.int32),
+                           np.array([0, 0, 1, 1, 0, 1], np.int32), n, ar, [[0, 4000], [4000, 8000]])
+    assert ora[3] == oracle.BAD_ORDER
+    assert_same(gpu, ora)
+    assert not gpu[0].any() and not gpu[1].any()
+    # index out of range: nothing happens
+    gpu, ora = encode_both(kvz, oracle, pool, np.array([0, 1, 2, 3, 4, 99], np.int32),
+                           np.arange(n, dtype=np.int32), np.zeros(n, np.int32), n, ar, [[0, 4000]])
+    assert ora[3] == oracle.BAD_INDEX
+    assert_same(gpu, ora)
+
+
+@pytest.mark.parametrize("cfg", [kvgen.C0, spread_cfg(8, 20, 17, hkv=8)], ids=lambda c: c.name)
+def test_decode_bit_exact_and_bad_metadata(kvz, oracle, cfg):
+    n = cfg.num_pages
+    pool = kvgen.gen_pages(cfg, n)
+    src = np.arange(n, dtype=np.int32)
+    gpu, ora = encode_both(kvz, oracle, pool, src, src, np.zeros(n, np.int32), n, n * cfg.hkv * 8192, [[0, 1 << 30]])
+    assert_same(gpu, ora)
+    meta = torch.from_numpy(gpu[0].view(np.int64).copy()).cuda()
+    arena = torch.from_numpy(gpu[1]).cuda()
+    order = torch.from_numpy(np.random.default_rng(1).permutation(n).astype(np.int32)).cuda()
+    out = torch.full((n, cfg.hkv, 2, 16, 128), 7, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    st = kvz.new_status()
+    kvz.decode_blocks(meta, arena, order, out, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(out.cpu().view(torch.int16), pool[order.cpu().long()].view(torch.int16))
+    # corrupt metadata: bad tag byte, invalid offset, offset past the arena, page id out of range
+    bad = gpu[0].copy()
+    bad[0, 0, 1] = (bad[0, 0, 1] & np.uint64(0x00FFFFFFFFFFFFFF)) | np.uint64(0x9A << 56)
+    bad[1, cfg.hkv - 1, 0] = np.uint64(0xFFFFFFFF) | (bad[1, cfg.hkv - 1, 0] & np.uint64(0xFFFFFFFF00000000))
+    bad[2, 0, 0] = np.uint64(arena.numel() // 256 - 5) | (bad[2, 0, 0] & np.uint64(0xFFFFFFFF00000000))
+    pages = np.array([0, 1, 2, 3, n + 4], np.int32)
+    o_out, o_st = oracle.decode_pages(bad, gpu[1], pages, cfg.hkv)
+    st.zero_()
+    out = torch.empty((5, cfg.hkv, 2, 16, 128), dtype=torch.bfloat16, device="cuda")
+    kvz.decode_blocks(torch.from_numpy(bad.view(np.int64).copy()).cuda(), arena, torch.from_numpy(pages).cuda(),
+                      out, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == o_st == (oracle.BAD_META | oracle.BAD_INDEX)
+    assert np.array_equal(out.cpu().view(torch.int16).numpy().view(np.uint16), o_out)
