@@ -404,11 +404,13 @@ def main():
     us_raw = ms_r * 1e3 / K
     value = world * W.logical_bytes / (us_step * 1e-6) / 1e9
 
-    # dominant kernel: per-launch duration with L2 flushed, algorithmic bytes per launch
+    # dominant kernel: algorithmic bytes per launch / average launch duration over the
+    # timed region (one attention launch + its merge per step); a cold single launch
+    # (L2 flushed, nothing before or after it) is reported beside it
+    achieved = W.alg_bytes_c / (us_step * 1e-6) / 1e9
+    achieved_raw = W.alg_bytes_r / (us_raw * 1e-6) / 1e9
     launch_ms = per_launch_ms(W.step_c, max(10, min(K, 40)), flush)
     launch_ms_raw = per_launch_ms(W.step_r, max(10, min(K, 40)), flush)
-    achieved = W.alg_bytes_c / (launch_ms * 1e-3) / 1e9
-    achieved_raw = W.alg_bytes_r / (launch_ms_raw * 1e-3) / 1e9
 
     # encode and standalone decode throughput (C1 full pages, cold inputs)
     enc_meta = torch.zeros_like(W.metas[0])
@@ -511,10 +513,11 @@ def main():
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
                      "kernel": "k_attn<compressed> + k_attn_merge",
-                     "launch_us": round(launch_ms * 1e3, 3),
+                     "launch_us": round(us_step, 3), "cold_single_launch_us": round(launch_ms * 1e3, 3),
                      "algorithmic_bytes_per_launch": W.alg_bytes_c},
         "roofline_raw": {"achieved": round(achieved_raw, 1), "frac": round(achieved_raw / peak, 4),
-                         "launch_us": round(launch_ms_raw * 1e3, 3), "algorithmic_bytes_per_launch": W.alg_bytes_r},
+                         "launch_us": round(us_raw, 3), "cold_single_launch_us": round(launch_ms_raw * 1e3, 3),
+                         "algorithmic_bytes_per_launch": W.alg_bytes_r},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "cpu_baseline": cpu,
         "clocks": clocks,

@@ -56,8 +56,7 @@ struct Smem {
     static constexpr int ml = mm + kConsumers * 4 * 4;
     static constexpr int mo = ml + kConsumers * 4 * 4;
     static constexpr int pref = mo + kConsumers * 4 * 128 * 4;
-    __host__ __device__ static int lens(int batch) { return pref + (batch + 1) * 4; }
-    __host__ __device__ static int bytes(int batch) { return lens(batch) + batch * 4 + 1024; }
+    __host__ __device__ static int bytes(int batch) { return pref + (batch + 1) * 4; }
 };
 
 __device__ __forceinline__ uint32_t swz128(int row, int col)
@@ -152,26 +151,18 @@ __device__ __forceinline__ void mask_v_frag(uint32_t (&a)[4], int lane, int vali
 template <bool kCompressed>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams P, const __grid_constant__ CUtensorMap tmap)
 {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_addr(smem);
+    if (sbase & 1023u) {  // the swizzled TMA destinations need 1024-byte alignment
+        if (threadIdx.x == 0) atomicOr(P.status, KVZ_STATUS_BAD_INDEX);
+        return;
+    }
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int32_t *pref = reinterpret_cast<int32_t *>(smem + Smem::pref);
-    int32_t *lens = reinterpret_cast<int32_t *>(smem + Smem::lens(P.batch));
     StageInfo *info = reinterpret_cast<StageInfo *>(smem + Smem::info);
     const int B = P.batch, hkv = P.hkv, G = P.G;
 
-    // ---- per-sequence page counts and their prefix ----
-    uint32_t bad_len = 0;
-    for (int b = tid; b < B; b += kThreads) {
-        int L = P.seq_lens[b];
-        if (L < 0) {
-            L = 0;
-            bad_len = 1;
-        }
-        lens[b] = L;
-    }
-    if (bad_len) atomicOr(P.status, KVZ_STATUS_BAD_INDEX);
+    // ---- barriers, and the per-sequence page-count prefix ----
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(sbase + Smem::full + 8 * s, 1);
@@ -183,12 +174,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
         }
         fence_barrier_init();
     }
-    __syncthreads();
     if (warp == 0) {
         const int chunk = (B + 31) / 32;
         const int b0 = min(B, lane * chunk), b1 = min(B, b0 + chunk);
         int s = 0;
-        for (int b = b0; b < b1; ++b) s += (lens[b] + kPage - 1) / kPage;
+        uint32_t bad_len = 0;
+        for (int b = b0; b < b1; ++b) {
+            const int L = P.seq_lens[b];
+            bad_len |= L < 0;
+            s += L > 0 ? (L + kPage - 1) / kPage : 0;
+        }
+        if (bad_len) atomicOr(P.status, KVZ_STATUS_BAD_INDEX);
         int incl = s;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -198,7 +194,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
         int run = incl - s;
         for (int b = b0; b < b1; ++b) {
             pref[b] = run;
-            run += (lens[b] + kPage - 1) / kPage;
+            const int L = P.seq_lens[b];
+            run += L > 0 ? (L + kPage - 1) / kPage : 0;
         }
         if (lane == 31) pref[B] = incl;
     }
@@ -213,124 +210,143 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
 
     if (warp == kConsumers) {
         // =============================== producer ===============================
+        // Page ids and metadata are fetched for 32 pages at a time, one page per lane,
+        // a batch ahead of use (warp-wide loads, so no lane waits on another's load).
+        // For each page the lane derives the stage descriptor; lane 0 then issues the
+        // copies page by page into the ring as stages free up.
         prefetch_tensormap(&tmap);
         const int64_t npage = hi - lo;
-        // lookahead: lane l owns pages i = l (mod 32); A = its next page, N = the one after
-        PageLoc A{0, 0, 0}, N{0, 0, 0};
-        int32_t pidA = -1, pidN = -1;
-        uint64_t mA0 = 0, mA1 = 0;
-        auto page_pid = [&](const PageLoc &L) -> int32_t {
-            const int len = lens[L.b];
-            const bool from_table = kCompressed ? (L.p < len / kPage) : true;
-            if (!from_table) return P.tail_page[L.b];
-            if (L.p >= P.max_pages) return INT32_MIN;
-            return P.page_ids[(int64_t)L.b * P.max_pages + L.p];
+        struct Pre {
+            PageLoc L;
+            int32_t pid, len;
         };
-        auto load_meta = [&](const PageLoc &L, int32_t pid, uint64_t &m0, uint64_t &m1) {
+        auto prep = [&](int64_t x, Pre &r) {  // locate + page id (global load)
+            r.pid = INT32_MIN;
+            r.len = 0;
+            r.L = PageLoc{0, 0, 0};
+            if (x >= hi) return;
+            r.L = locate(pref, B, hkv, x);
+            r.len = max(0, P.seq_lens[r.L.b]);
+            const bool from_table = kCompressed ? (r.L.p < r.len / kPage) : true;
+            if (!from_table) r.pid = P.tail_page[r.L.b];
+            else if (r.L.p < P.max_pages) r.pid = P.page_ids[(int64_t)r.L.b * P.max_pages + r.L.p];
+        };
+        auto load_meta = [&](const Pre &r, uint64_t &m0, uint64_t &m1) {  // metadata (global load)
             m0 = m1 = 0;
-            if (kCompressed && L.p < lens[L.b] / kPage && pid >= 0 && pid < P.num_meta_pages) {
+            if (kCompressed && r.L.p < r.len / kPage && r.pid >= 0 && r.pid < P.num_meta_pages) {
                 const ulonglong2 v =
-                    *reinterpret_cast<const ulonglong2 *>(P.meta + ((int64_t)pid * hkv + L.kvh) * 2);
+                    *reinterpret_cast<const ulonglong2 *>(P.meta + ((int64_t)r.pid * hkv + r.L.kvh) * 2);
                 m0 = v.x;
                 m1 = v.y;
             }
         };
-        if (lane < npage) {
-            A = locate(pref, B, hkv, lo + lane);
-            pidA = page_pid(A);
-        }
-        if (lane + 32 < npage) {
-            N = locate(pref, B, hkv, lo + lane + 32);
-            pidN = page_pid(N);
-        }
-        if (lane < npage) load_meta(A, pidA, mA0, mA1);
+        Pre cur, nxt;
+        uint64_t cm0 = 0, cm1 = 0;
+        prep(lo + lane, cur);
+        prep(lo + 32 + lane, nxt);
+        load_meta(cur, cm0, cm1);
 
         int64_t seg_end = lo;
         int seg = 0;
         bool ok = true;
-        for (int64_t i = 0; i < npage; ++i) {
-            const int64_t x = lo + i;
-            if (x == seg_end) {  // new (sequence, KV head) segment: stage its queries
-                const PageLoc L = locate(pref, B, hkv, x);
-                seg_end = min(hi, unit_end(pref, hkv, L));
-                if (lane == 0 && ok) {
-                    const int qb = seg & 1, use = seg >> 1;
-                    ok = mbar_wait(sbase + Smem::qempty + 8 * qb, (use & 1) ^ 1, P.status);
-                    if (ok) {
-                        const uint32_t bytes = (uint32_t)G * kDim * 2;
-                        mbar_arrive_expect_tx(sbase + Smem::qfull + 8 * qb, bytes);
-                        bulk_copy_g2s(sbase + Smem::q + qb * 1024,
-                                      P.q + ((int64_t)L.b * hkv * G + (int64_t)L.kvh * G) * kDim, bytes,
-                                      sbase + Smem::qfull + 8 * qb);
-                    }
-                }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                ++seg;
-            }
-            if (lane == (int)(i & 31)) {
-                const int s = (int)(i % kStages);
-                const int64_t fill = i / kStages;
-                if (ok) ok = mbar_wait(sbase + Smem::empty + 8 * s, (uint32_t)((fill & 1) ^ 1), P.status);
-                StageInfo inf{kKindSkip, 0, 0, 0};
-                uint32_t bad = 0;
-                const int len = lens[A.b];
-                const uint32_t fullbar = sbase + Smem::full + 8 * s;
-                const uint32_t dst = sbase + Smem::stage + s * kStageBytes;
-                const bool compressed_page = kCompressed && (A.p < len / kPage);
+        for (int64_t base = 0; base < npage; base += 32) {
+            // ---- this lane's page descriptor: kind | valid << 8 | status << 16, source, sizes, tags ----
+            uint32_t d_kind = kKindSkip, d_valid = 0, d_bad = 0, d_tK = 0, d_tV = 0, d_bytes = 0;
+            uint64_t d_srcK = 0, d_srcV = 0;
+            if (base + lane < npage) {
+                const bool compressed_page = kCompressed && (cur.L.p < cur.len / kPage);
                 if (compressed_page) {
-                    const uint32_t offK = (uint32_t)mA0, offV = (uint32_t)mA1;
-                    const uint32_t tK = (uint32_t)(mA0 >> 32), tV = (uint32_t)(mA1 >> 32);
-                    if (pidA < 0 || pidA >= P.num_meta_pages) {
-                        bad = KVZ_STATUS_BAD_INDEX;
+                    const uint32_t offK = (uint32_t)cm0, offV = (uint32_t)cm1;
+                    const uint32_t tK = (uint32_t)(cm0 >> 32), tV = (uint32_t)(cm1 >> 32);
+                    if (cur.pid < 0 || cur.pid >= P.num_meta_pages) {
+                        d_bad = KVZ_STATUS_BAD_INDEX;
                     } else if (!tags_valid(tK) || !tags_valid(tV) || offK == KVZ_OFFSET_INVALID ||
                                offV == KVZ_OFFSET_INVALID ||
                                ((uint64_t)offK + group_granules(tK)) * kGranule > P.arena_bytes ||
                                ((uint64_t)offV + group_granules(tV)) * kGranule > P.arena_bytes) {
-                        bad = KVZ_STATUS_BAD_META;
+                        d_bad = KVZ_STATUS_BAD_META;
                     } else {
-                        inf = StageInfo{kKindPair, kPage, tK, tV};
-                    }
-                    if (ok) {
-                        info[s] = inf;
-                        if (inf.kind == kKindPair) {
-                            const uint32_t bK = group_granules(tK) * kGranule, bV = group_granules(tV) * kGranule;
-                            mbar_arrive_expect_tx(fullbar, bK + bV);
-                            bulk_copy_g2s(dst, P.arena + (uint64_t)offK * kGranule, bK, fullbar);
-                            bulk_copy_g2s(dst + 4096, P.arena + (uint64_t)offV * kGranule, bV, fullbar);
-                        } else {
-                            mbar_arrive(fullbar);
-                        }
+                        d_kind = kKindPair;
+                        d_valid = kPage;
+                        d_tK = tK;
+                        d_tV = tV;
+                        d_srcK = (uint64_t)offK * kGranule;
+                        d_srcV = (uint64_t)offV * kGranule;
+                        d_bytes = (group_granules(tK) * kGranule) | ((group_granules(tV) * kGranule) << 16);
                     }
                 } else {
-                    const int valid = min(kPage, len - kPage * A.p);
-                    if (pidA < 0 || pidA >= P.num_raw_pages) {
-                        bad = (kCompressed && pidA == -1) ? KVZ_STATUS_BAD_TAIL : KVZ_STATUS_BAD_INDEX;
+                    if (cur.pid < 0 || cur.pid >= P.num_raw_pages) {
+                        d_bad = (kCompressed && cur.pid == -1) ? KVZ_STATUS_BAD_TAIL : KVZ_STATUS_BAD_INDEX;
                     } else {
-                        inf = StageInfo{kKindRaw, (uint32_t)valid, 0, 0};
+                        d_kind = kKindRaw;
+                        d_valid = (uint32_t)min(kPage, cur.len - kPage * cur.L.p);
+                        d_srcK = (uint64_t)(((int64_t)cur.pid * hkv + cur.L.kvh) * 32);  // tensor row
                     }
+                }
+                if (d_bad) atomicOr(P.status, d_bad);
+            }
+            const uint32_t d_word = d_kind | (d_valid << 8);
+            // ---- next batches: metadata of batch +1 (its page ids arrived a batch ago), ids of batch +2 ----
+            uint64_t nm0 = 0, nm1 = 0;
+            load_meta(nxt, nm0, nm1);
+            Pre nn;
+            prep(lo + base + 64 + lane, nn);
+
+            const int cnt = (int)(npage - base < 32 ? npage - base : 32);
+            for (int j = 0; j < cnt; ++j) {
+                const int64_t i = base + j;
+                const int64_t x = lo + i;
+                const uint32_t w = __shfl_sync(0xffffffffu, d_word, j);
+                const uint64_t sK = __shfl_sync(0xffffffffu, d_srcK, j);
+                const uint64_t sV = __shfl_sync(0xffffffffu, d_srcV, j);
+                const uint32_t tK = __shfl_sync(0xffffffffu, d_tK, j);
+                const uint32_t tV = __shfl_sync(0xffffffffu, d_tV, j);
+                const uint32_t nb = __shfl_sync(0xffffffffu, d_bytes, j);
+                if (x == seg_end) {  // new (sequence, KV head) segment: stage its queries
+                    const PageLoc L = locate(pref, B, hkv, x);
+                    seg_end = min(hi, unit_end(pref, hkv, L));
+                    if (lane == 0 && ok) {
+                        const int qb = seg & 1, use = seg >> 1;
+                        ok = mbar_wait(sbase + Smem::qempty + 8 * qb, (use & 1) ^ 1, P.status);
+                        if (ok) {
+                            const uint32_t bytes = (uint32_t)G * kDim * 2;
+                            mbar_arrive_expect_tx(sbase + Smem::qfull + 8 * qb, bytes);
+                            bulk_copy_g2s(sbase + Smem::q + qb * 1024,
+                                          P.q + ((int64_t)L.b * hkv * G + (int64_t)L.kvh * G) * kDim, bytes,
+                                          sbase + Smem::qfull + 8 * qb);
+                        }
+                    }
+                    ++seg;
+                }
+                if (lane == 0 && ok) {
+                    const int s = (int)(i % kStages);
+                    const int64_t fill = i / kStages;
+                    ok = mbar_wait(sbase + Smem::empty + 8 * s, (uint32_t)((fill & 1) ^ 1), P.status);
                     if (ok) {
-                        info[s] = inf;
-                        if (inf.kind == kKindRaw) {
-                            const int row = (int)(((int64_t)pidA * hkv + A.kvh) * 32);
+                        const uint32_t kind = w & 0xFFu;
+                        info[s] = StageInfo{kind, (w >> 8) & 0xFFu, tK, tV};
+                        const uint32_t fullbar = sbase + Smem::full + 8 * s;
+                        const uint32_t dst = sbase + Smem::stage + s * kStageBytes;
+                        if (kind == kKindPair) {
+                            const uint32_t bK = nb & 0xFFFFu, bV = nb >> 16;
+                            mbar_arrive_expect_tx(fullbar, bK + bV);
+                            bulk_copy_g2s(dst, P.arena + sK, bK, fullbar);
+                            bulk_copy_g2s(dst + 4096, P.arena + sV, bV, fullbar);
+                        } else if (kind == kKindRaw) {
                             mbar_arrive_expect_tx(fullbar, kStageBytes);
-                            tensor_copy_2d_g2s(dst, &tmap, 0, row, fullbar);
-                            tensor_copy_2d_g2s(dst + 4096, &tmap, 64, row, fullbar);
+                            tensor_copy_2d_g2s(dst, &tmap, 0, (int32_t)sK, fullbar);
+                            tensor_copy_2d_g2s(dst + 4096, &tmap, 64, (int32_t)sK, fullbar);
                         } else {
                             mbar_arrive(fullbar);
                         }
                     }
                 }
-                if (bad) atomicOr(P.status, bad);
-                // slide the lookahead window
-                A = N;
-                pidA = pidN;
-                if (i + 32 < npage) load_meta(A, pidA, mA0, mA1);
-                if (i + 64 < npage) {
-                    N = locate(pref, B, hkv, lo + i + 64);
-                    pidN = page_pid(N);
-                }
             }
-            ok = __shfl_sync(0xffffffffu, ok, (int)(i & 31));
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            cur = nxt;
+            cm0 = nm0;
+            cm1 = nm1;
+            nxt = nn;
         }
         // never leave with copies in flight: wait for the last fill of every stage
         if (lane == 0) {
@@ -557,40 +573,76 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
 // ---------------------------------------------------------------------------------
 // merge the per-segment partials of each (sequence, KV head): fixed order over CTAs
 // ---------------------------------------------------------------------------------
+constexpr int kMergeChunk = 8;  // slots whose partials one thread keeps in flight at once
+
 __global__ void __launch_bounds__(128) k_attn_merge(const AttnParams P)
 {
     pdl_wait_primary();
     const int u = blockIdx.x, hkv = P.hkv, G = P.G;
     const int b = u / hkv, kvh = u % hkv, d = threadIdx.x;
-    const int64_t n = P.prefix[b + 1] - P.prefix[b];
-    const int64_t T = (int64_t)hkv * P.prefix[P.batch];
+    const int32_t pb = P.prefix[b], pb1 = P.prefix[b + 1], pB = P.prefix[P.batch];
+    const int64_t n = pb1 - pb;
+    const int64_t T = (int64_t)hkv * pB;
     const int64_t C = P.grid;
     float *out = P.out + ((int64_t)b * hkv * G + (int64_t)kvh * G) * kDim;
     if (n == 0) {
         for (int h = 0; h < G; ++h) out[h * kDim + d] = 0.f;
         return;
     }
-    const int64_t S = (int64_t)hkv * P.prefix[b] + (int64_t)kvh * n, E = S + n;
     // CTA c covers pages [ceil(cT/C), ceil((c+1)T/C)); page x belongs to CTA floor(xC/T).
     // CTAs between the first and last owner with an empty range (T < C) wrote nothing.
+    const int64_t S = (int64_t)hkv * pb + (int64_t)kvh * n, E = S + n;
     const int64_t c0 = (S * C) / T, c1 = ((E - 1) * C) / T;
-    auto written = [&](int64_t c) { return (c * T + C - 1) / C < ((c + 1) * T + C - 1) / C; };
-    for (int h = 0; h < G; ++h) {
-        float M = -INFINITY;
-        for (int64_t c = c0; c <= c1; ++c)
-            if (written(c)) M = fmaxf(M, P.part_ml[((u + c) * 4 + h) * 2]);
-        float Ls = 0.f, Os = 0.f;
-        if (M != -INFINITY) {
-            for (int64_t c = c0; c <= c1; ++c) {
-                if (!written(c)) continue;
-                const int64_t slot = u + c;
-                const float w = exp2f(P.part_ml[(slot * 4 + h) * 2] - M);
-                Ls += w * P.part_ml[(slot * 4 + h) * 2 + 1];
-                Os += w * P.part_o[(slot * 4 + h) * 128 + d];
+    float M[4], Ls[4], Os[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        M[h] = -INFINITY;
+        Ls[h] = 0.f;
+        Os[h] = 0.f;
+    }
+    // running merge over chunks of slots; within a chunk every load is independent
+    for (int64_t cb = c0; cb <= c1; cb += kMergeChunk) {
+        float mv[kMergeChunk][4], lv[kMergeChunk][4], ov[kMergeChunk][4];
+#pragma unroll
+        for (int k = 0; k < kMergeChunk; ++k) {
+            const int64_t c = cb + k;
+            const bool w = c <= c1 && (c * T + C - 1) / C < ((c + 1) * T + C - 1) / C;
+            const int64_t slot = u + c;
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                mv[k][h] = -INFINITY;
+                lv[k][h] = 0.f;
+                ov[k][h] = 0.f;
+                if (w && h < G) {
+                    const float2 ml = *reinterpret_cast<const float2 *>(P.part_ml + (slot * 4 + h) * 2);
+                    mv[k][h] = ml.x;
+                    lv[k][h] = ml.y;
+                    ov[k][h] = P.part_o[(slot * 4 + h) * 128 + d];
+                }
             }
         }
-        out[h * kDim + d] = Ls > 0.f ? Os / Ls : 0.f;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            float m = M[h];
+#pragma unroll
+            for (int k = 0; k < kMergeChunk; ++k) m = fmaxf(m, mv[k][h]);
+            if (m == -INFINITY) continue;
+            const float r = exp2f(M[h] - m);  // M[h] = -inf -> 0
+            float l = Ls[h] * r, o = Os[h] * r;
+#pragma unroll
+            for (int k = 0; k < kMergeChunk; ++k) {
+                const float wgt = exp2f(mv[k][h] - m);
+                l += wgt * lv[k][h];
+                o += wgt * ov[k][h];
+            }
+            M[h] = m;
+            Ls[h] = l;
+            Os[h] = o;
+        }
     }
+#pragma unroll
+    for (int h = 0; h < 4; ++h)
+        if (h < G) out[h * kDim + d] = Ls[h] > 0.f ? Os[h] / Ls[h] : 0.f;
 }
 
 // ---------------------------------------------------------------------------------
@@ -637,14 +689,16 @@ static cudaError_t launch_impl(const AttnParams &P, const void *tmap, cudaStream
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
+    // the merge is a programmatic dependent: its CTAs take SM slots as attention CTAs
+    // drain and start as soon as the attention grid has completed
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(P.batch * P.hkv);
     cfg.blockDim = dim3(128);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, k_attn_merge, P);
