@@ -163,6 +163,35 @@ int run_attention(bool compressed, const kvz_dims &d, int batch, int hq, const v
     return e == cudaSuccess ? KVZ_OK : fail_cuda(e);
 }
 
+// ---------------------------------------------------------------------------------
+// Fixed scratch for kvz_decode_attention_noalloc.  In host code the array's name is
+// only a host-side stand-in; its device address comes from cudaGetSymbolAddress, looked
+// up once per device (with that device current) and cached.
+// ---------------------------------------------------------------------------------
+static __device__ __align__(256) uint8_t g_noalloc_scratch[KVZ_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[kMaxDevices] = {};
+
+int noalloc_scratch(void **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail_cuda(e);
+    if (dev < 0 || dev >= kMaxDevices) return KVZ_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return fail_cuda(e);
+        if (!p) return KVZ_ERR_DEVICE;
+        g_noalloc_addr[dev] = p;
+    }
+    *out = g_noalloc_addr[dev];
+    return KVZ_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -178,6 +207,7 @@ const char *kvz_strerror(int code)
     case KVZ_ERR_CUDA: return "CUDA error (see kvz_last_cuda_error)";
     case KVZ_ERR_DEVICE: return "no usable CUDA device";
     case KVZ_ERR_OUT_OF_SPACE: return "no free arena chunk";
+    case KVZ_ERR_NOALLOC_LIMIT: return "problem needs more split-KV scratch than the fixed no-alloc array holds";
     default: return "unknown error";
     }
 }
@@ -293,6 +323,31 @@ int kvz_decode_attention_raw(kvz_dims dims, int32_t batch, int32_t num_q_heads, 
     return run_attention(false, dims, batch, num_q_heads, q, page_ids, max_pages, seq_lens, nullptr, nullptr, 0,
                          nullptr, 0, raw_pool, num_raw_pages, out, workspace, workspace_bytes, status,
                          reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kvz_decode_attention_noalloc(kvz_dims dims, int32_t batch, int32_t num_q_heads, const void *q,
+                                 const int32_t *page_ids, int32_t max_pages, const int32_t *seq_lens,
+                                 const int32_t *tail_page, const uint64_t *meta, int64_t num_meta_pages,
+                                 const uint8_t *arena, uint64_t arena_bytes, const void *raw_pool,
+                                 int64_t num_raw_pages, float *out, uint32_t *status, kvz_stream_t stream)
+{
+    void *scratch = nullptr;
+    if (batch > 0) {
+        int src = noalloc_scratch(&scratch);  // device address of the fixed array
+        if (src) return src;
+    }
+    int rc = check_attention_common(dims, batch, num_q_heads, q, seq_lens, raw_pool, num_raw_pages, out, scratch,
+                                    status, max_pages, page_ids);
+    if (rc || batch == 0) return rc;
+    if (!tail_page || !meta || !arena || num_meta_pages < 0) return KVZ_ERR_INVALID_ARG;
+    if (!aligned(meta, 16) || !aligned(arena, 256) || !aligned(tail_page, 4)) return KVZ_ERR_ALIGNMENT;
+    int grid = 0;
+    rc = attention_grid(batch, dims.num_kv_heads, max_pages + 1, &grid);
+    if (rc) return rc;
+    if (attn_ws_bytes(batch, dims.num_kv_heads, grid) > (size_t)KVZ_NOALLOC_SCRATCH_BYTES) return KVZ_ERR_NOALLOC_LIMIT;
+    return run_attention(true, dims, batch, num_q_heads, q, page_ids, max_pages, seq_lens, tail_page, meta,
+                         num_meta_pages, arena, arena_bytes, raw_pool, num_raw_pages, out, scratch,
+                         KVZ_NOALLOC_SCRATCH_BYTES, status, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int kvz_apply_cursor_updates(const int32_t *idx, const uint32_t *pos, const uint32_t *end, int32_t n,

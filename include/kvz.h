@@ -72,6 +72,7 @@ extern "C" {
 #define KVZ_ERR_CUDA -5
 #define KVZ_ERR_DEVICE -6
 #define KVZ_ERR_OUT_OF_SPACE -7
+#define KVZ_ERR_NOALLOC_LIMIT -8
 
 /* device-side status bits */
 #define KVZ_STATUS_ARENA_FULL 1u
@@ -173,6 +174,33 @@ int kvz_decode_attention_raw(kvz_dims dims, int32_t batch, int32_t num_q_heads, 
                              const void *raw_pool, int64_t num_raw_pages, float *out,
                              void *workspace, size_t workspace_bytes, uint32_t *status,
                              kvz_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * kvz_decode_attention_noalloc -- kvz_decode_attention for callers that cannot
+ * allocate device memory.  The pages describe no such variant; it exists for callers
+ * such as runtime plugins whose host framework owns every device allocation, code that
+ * must not grow the device footprint while it runs, or work recorded into CUDA graphs
+ * under an allocation-free policy.  Arguments and results are those of
+ * kvz_decode_attention without the workspace: the split-KV partial results go to a
+ * fixed array compiled into libkvz (KVZ_NOALLOC_SCRATCH_BYTES, on every device that
+ * loads the library, held until the process exits).  The library allocates nothing.
+ *  - A problem whose kvz_attention_workspace_size(dims, batch, num_q_heads,
+ *    max_pages + 1) exceeds KVZ_NOALLOC_SCRATCH_BYTES returns KVZ_ERR_NOALLOC_LIMIT
+ *    before anything is launched.
+ *  - The first call on a device looks up that device's address of the array; make
+ *    that first call before any stream capture on that device.
+ *  - Every call on a device uses the same array and leaves its contents behind; each
+ *    call rewrites all of it that it reads, nothing needs to start at zero.  Calls
+ *    whose kernels overlap on the GPU (different streams, no ordering) race on the
+ *    array: order them on one stream or use kvz_decode_attention with separate
+ *    workspaces.
+ * --------------------------------------------------------------------------------- */
+#define KVZ_NOALLOC_SCRATCH_BYTES (4u << 20)
+int kvz_decode_attention_noalloc(kvz_dims dims, int32_t batch, int32_t num_q_heads, const void *q,
+                                 const int32_t *page_ids, int32_t max_pages, const int32_t *seq_lens,
+                                 const int32_t *tail_page, const uint64_t *meta, int64_t num_meta_pages,
+                                 const uint8_t *arena, uint64_t arena_bytes, const void *raw_pool,
+                                 int64_t num_raw_pages, float *out, uint32_t *status, kvz_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
  * Host-side chunk allocator for the arena (GAAC "Block-Wise Compression Scheduling":
