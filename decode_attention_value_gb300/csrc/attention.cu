@@ -21,8 +21,7 @@
 //    columns: Q is duplicated there for QK^T, and for PV they carry the low part of
 //    P = hi + lo (both bf16), so the PV product keeps ~16 bits of P for free;
 //  * warps merge their online-softmax states per (sequence, KV head) segment, and a
-//    small follow-up kernel (programmatic dependent launch) merges the segments in a
-//    fixed order.
+//    small follow-up kernel merges the segments in a fixed order.
 #include <cuda.h>
 
 #include <cstring>
@@ -56,7 +55,8 @@ struct Smem {
     static constexpr int ml = mm + kConsumers * 4 * 4;
     static constexpr int mo = ml + kConsumers * 4 * 4;
     static constexpr int pref = mo + kConsumers * 4 * 128 * 4;
-    __host__ __device__ static int bytes(int batch) { return pref + (batch + 1) * 4; }
+    __host__ __device__ static int tail(int batch) { return pref + (batch + 1) * 4; }
+    __host__ __device__ static int bytes(int batch) { return tail(batch) + ((batch + 15) & ~15); }
 };
 
 __device__ __forceinline__ uint32_t swz128(int row, int col)
@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
     }
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int32_t *pref = reinterpret_cast<int32_t *>(smem + Smem::pref);
+    uint8_t *tail_len = smem + Smem::tail(P.batch);  // tokens in each sequence's last page if partial, else 0
     StageInfo *info = reinterpret_cast<StageInfo *>(smem + Smem::info);
     const int B = P.batch, hkv = P.hkv, G = P.G;
 
@@ -179,8 +180,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
         const int b0 = min(B, lane * chunk), b1 = min(B, b0 + chunk);
         int s = 0;
         uint32_t bad_len = 0;
+        const uint64_t keep = l2_evict_last();
         for (int b = b0; b < b1; ++b) {
-            const int L = P.seq_lens[b];
+            const int L = ld_keep_s32(P.seq_lens + b, keep);
             bad_len |= L < 0;
             s += L > 0 ? (L + kPage - 1) / kPage : 0;
         }
@@ -194,8 +196,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
         int run = incl - s;
         for (int b = b0; b < b1; ++b) {
             pref[b] = run;
-            const int L = P.seq_lens[b];
+            const int L = ld_keep_s32(P.seq_lens + b, keep);
             run += L > 0 ? (L + kPage - 1) / kPage : 0;
+            tail_len[b] = (uint8_t)(L > 0 ? L % kPage : 0);
         }
         if (lane == 31) pref[B] = incl;
     }
@@ -206,7 +209,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
     const int64_t T = (int64_t)hkv * pref[B];
     const int64_t C = gridDim.x, c = blockIdx.x;
     const int64_t lo = (c * T + C - 1) / C, hi = ((c + 1) * T + C - 1) / C;
-    pdl_launch_dependents();
 
     if (warp == kConsumers) {
         // =============================== producer ===============================
@@ -216,29 +218,33 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
         // copies page by page into the ring as stages free up.
         prefetch_tensormap(&tmap);
         const int64_t npage = hi - lo;
+        // the KV stream is read once per step; the tables each step starts from stay in L2
+        const uint64_t keep = l2_evict_last(), stream_once = l2_evict_first();
         struct Pre {
             PageLoc L;
-            int32_t pid, len;
+            int32_t pid, n, tl;  // page id, pages in the sequence, tail tokens (0 = none)
         };
-        auto prep = [&](int64_t x, Pre &r) {  // locate + page id (global load)
+        // locate + page id: the table entry and the tail id do not wait on each other
+        auto prep = [&](int64_t x, Pre &r) {
             r.pid = INT32_MIN;
-            r.len = 0;
+            r.n = 0;
+            r.tl = 0;
             r.L = PageLoc{0, 0, 0};
             if (x >= hi) return;
             r.L = locate(pref, B, hkv, x);
-            r.len = max(0, P.seq_lens[r.L.b]);
-            const bool from_table = kCompressed ? (r.L.p < r.len / kPage) : true;
-            if (!from_table) r.pid = P.tail_page[r.L.b];
-            else if (r.L.p < P.max_pages) r.pid = P.page_ids[(int64_t)r.L.b * P.max_pages + r.L.p];
+            r.n = pref[r.L.b + 1] - pref[r.L.b];
+            r.tl = tail_len[r.L.b];
+            const bool last_partial = (r.L.p == r.n - 1) && r.tl != 0;
+            const int32_t tab =
+                r.L.p < P.max_pages ? ld_keep_s32(P.page_ids + (int64_t)r.L.b * P.max_pages + r.L.p, keep) : INT32_MIN;
+            if (kCompressed && last_partial) r.pid = ld_keep_s32(P.tail_page + r.L.b, keep);
+            else r.pid = tab;
         };
+        auto is_compressed = [&](const Pre &r) { return kCompressed && !((r.L.p == r.n - 1) && r.tl != 0); };
         auto load_meta = [&](const Pre &r, uint64_t &m0, uint64_t &m1) {  // metadata (global load)
             m0 = m1 = 0;
-            if (kCompressed && r.L.p < r.len / kPage && r.pid >= 0 && r.pid < P.num_meta_pages) {
-                const ulonglong2 v =
-                    *reinterpret_cast<const ulonglong2 *>(P.meta + ((int64_t)r.pid * hkv + r.L.kvh) * 2);
-                m0 = v.x;
-                m1 = v.y;
-            }
+            if (is_compressed(r) && r.pid >= 0 && r.pid < P.num_meta_pages)
+                ld_keep_u64x2(P.meta + ((int64_t)r.pid * hkv + r.L.kvh) * 2, keep, m0, m1);
         };
         Pre cur, nxt;
         uint64_t cm0 = 0, cm1 = 0;
@@ -254,8 +260,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
             uint32_t d_kind = kKindSkip, d_valid = 0, d_bad = 0, d_tK = 0, d_tV = 0, d_bytes = 0;
             uint64_t d_srcK = 0, d_srcV = 0;
             if (base + lane < npage) {
-                const bool compressed_page = kCompressed && (cur.L.p < cur.len / kPage);
-                if (compressed_page) {
+                if (is_compressed(cur)) {
                     const uint32_t offK = (uint32_t)cm0, offV = (uint32_t)cm1;
                     const uint32_t tK = (uint32_t)(cm0 >> 32), tV = (uint32_t)(cm1 >> 32);
                     if (cur.pid < 0 || cur.pid >= P.num_meta_pages) {
@@ -279,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                         d_bad = (kCompressed && cur.pid == -1) ? KVZ_STATUS_BAD_TAIL : KVZ_STATUS_BAD_INDEX;
                     } else {
                         d_kind = kKindRaw;
-                        d_valid = (uint32_t)min(kPage, cur.len - kPage * cur.L.p);
+                        d_valid = (cur.L.p == cur.n - 1 && cur.tl != 0) ? (uint32_t)cur.tl : (uint32_t)kPage;
                         d_srcK = (uint64_t)(((int64_t)cur.pid * hkv + cur.L.kvh) * 32);  // tensor row
                     }
                 }
@@ -330,12 +335,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                         if (kind == kKindPair) {
                             const uint32_t bK = nb & 0xFFFFu, bV = nb >> 16;
                             mbar_arrive_expect_tx(fullbar, bK + bV);
-                            bulk_copy_g2s(dst, P.arena + sK, bK, fullbar);
-                            bulk_copy_g2s(dst + 4096, P.arena + sV, bV, fullbar);
+                            bulk_copy_g2s_hint(dst, P.arena + sK, bK, fullbar, stream_once);
+                            bulk_copy_g2s_hint(dst + 4096, P.arena + sV, bV, fullbar, stream_once);
                         } else if (kind == kKindRaw) {
                             mbar_arrive_expect_tx(fullbar, kStageBytes);
-                            tensor_copy_2d_g2s(dst, &tmap, 0, (int32_t)sK, fullbar);
-                            tensor_copy_2d_g2s(dst + 4096, &tmap, 64, (int32_t)sK, fullbar);
+                            tensor_copy_2d_g2s_hint(dst, &tmap, 0, (int32_t)sK, fullbar, stream_once);
+                            tensor_copy_2d_g2s_hint(dst + 4096, &tmap, 64, (int32_t)sK, fullbar, stream_once);
                         } else {
                             mbar_arrive(fullbar);
                         }
@@ -577,7 +582,6 @@ constexpr int kMergeChunk = 8;  // slots whose partials one thread keeps in flig
 
 __global__ void __launch_bounds__(128) k_attn_merge(const AttnParams P)
 {
-    pdl_wait_primary();
     const int u = blockIdx.x, hkv = P.hkv, G = P.G;
     const int b = u / hkv, kvh = u % hkv, d = threadIdx.x;
     const int32_t pb = P.prefix[b], pb1 = P.prefix[b + 1], pB = P.prefix[P.batch];
@@ -659,6 +663,8 @@ static cudaError_t configure(int dev)
     cudaError_t e = cudaFuncSetAttribute(k_attn<kCompressed>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k_attn<kCompressed>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    // the merge runs between attention launches: same carve-out, no reconfiguration
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn_merge, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e == cudaSuccess && dev < 64) __atomic_fetch_or(&done, 1ull << dev, __ATOMIC_ACQ_REL);
     return e;
 }
@@ -688,20 +694,8 @@ static cudaError_t launch_impl(const AttnParams &P, const void *tmap, cudaStream
     k_attn<kCompressed><<<P.grid, kThreads, Smem::bytes(P.batch), stream>>>(P, map);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-
-    // the merge is a programmatic dependent: its CTAs take SM slots as attention CTAs
-    // drain and start as soon as the attention grid has completed
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(P.batch * P.hkv);
-    cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_attn_merge, P);
+    k_attn_merge<<<P.batch * P.hkv, 128, 0, stream>>>(P);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_attention(const AttnParams &P, bool compressed, const void *tmap, cudaStream_t stream)

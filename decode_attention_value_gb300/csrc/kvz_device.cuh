@@ -140,6 +140,55 @@ __device__ __forceinline__ void tensor_copy_2d_g2s(uint32_t dst, const void *tma
         : "memory");
 }
 
+// L2 cache policies: the KV stream is read once per step (evict first), while the
+// small tables every step starts from (lengths, page ids, metadata) should stay
+// resident across steps (evict last).
+__device__ __forceinline__ uint64_t l2_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void bulk_copy_g2s_hint(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                                   uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tensor_copy_2d_g2s_hint(uint32_t dst, const void *tmap, int32_t c0, int32_t c1,
+                                                        uint32_t bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+        "{%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ int32_t ld_keep_s32(const int32_t *p, uint64_t policy)
+{
+    int32_t v;
+    asm volatile("ld.global.L2::cache_hint.b32 %0, [%1], %2;" : "=r"(v) : "l"(p), "l"(policy));
+    return v;
+}
+
+__device__ __forceinline__ void ld_keep_u64x2(const uint64_t *p, uint64_t policy, uint64_t &a, uint64_t &b)
+{
+    asm volatile("ld.global.L2::cache_hint.v2.b64 {%0, %1}, [%2], %3;" : "=l"(a), "=l"(b) : "l"(p), "l"(policy));
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const void *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
