@@ -134,26 +134,35 @@ def gen_pages(cfg: KVConfig, num_pages: int, layer: int = 0, device="cpu", seed_
     return pool
 
 
+_SPREAD_CHUNK = 1 << 18  # blocks generated per chunk (bounds the temporaries to ~0.5 GB)
+
+
 def _spread_pages(cfg: KVConfig, g, num_pages: int, device) -> torch.Tensor:
     """Per block: spread S ~ U{lo..hi}; exponents uniform in [E0, E0+S] with both ends
     present, E0 = 127 - S + (random parity bit); random sign and fraction."""
     lo, hi = cfg.spread
     nblk = num_pages * cfg.hkv * 2 * 4
-    S = torch.randint(lo, hi + 1, (nblk, 1), generator=g, device=device)
-    E0 = 127 - S + torch.randint(0, 2, (nblk, 1), generator=g, device=device)
-    u = torch.rand((nblk, 512), generator=g, device=device)
-    e = torch.minimum(E0 + torch.floor(u * (S + 1).float()).long(), E0 + S)
-    # force both ends of the window to occur
-    pos = torch.randint(0, 512, (nblk, 2), generator=g, device=device)
-    pos[:, 1] = (pos[:, 0] + 1 + torch.randint(0, 511, (nblk,), generator=g, device=device)) % 512
-    e.scatter_(1, pos[:, :1], E0)
-    e.scatter_(1, pos[:, 1:], E0 + S)
-    sign = torch.randint(0, 2, (nblk, 512), generator=g, device=device)
-    frac = torch.randint(0, 128, (nblk, 512), generator=g, device=device)
-    w = (sign << 15) | (e << 7) | frac
-    w = torch.where(w >= 32768, w - 65536, w).to(torch.int16)
+    words = torch.empty((nblk, 512), dtype=torch.int16, device=device)
+    for b0 in range(0, nblk, _SPREAD_CHUNK):
+        n = min(_SPREAD_CHUNK, nblk - b0)
+        S = torch.randint(lo, hi + 1, (n, 1), generator=g, device=device, dtype=torch.int32)
+        E0 = 127 - S + torch.randint(0, 2, (n, 1), generator=g, device=device, dtype=torch.int32)
+        u = torch.rand((n, 512), generator=g, device=device)
+        e = torch.minimum(E0 + torch.floor(u * (S + 1).float()).to(torch.int32), E0 + S)
+        del u
+        # force both ends of the window to occur
+        pos = torch.randint(0, 512, (n, 2), generator=g, device=device)
+        pos[:, 1] = (pos[:, 0] + 1 + torch.randint(0, 511, (n,), generator=g, device=device)) % 512
+        e.scatter_(1, pos[:, :1], E0)
+        e.scatter_(1, pos[:, 1:], E0 + S)
+        sign = torch.randint(0, 2, (n, 512), generator=g, device=device, dtype=torch.int32)
+        frac = torch.randint(0, 128, (n, 512), generator=g, device=device, dtype=torch.int32)
+        w = (sign << 15) | (e << 7) | frac
+        del sign, frac, e
+        words[b0: b0 + n] = torch.where(w >= 32768, w - 65536, w).to(torch.int16)
+        del w
     # block order (page, head, kv, j) with values [16 tok][32 dims] -> page layout
-    w = w.view(num_pages, cfg.hkv, 2, 4, PAGE, 32).permute(0, 1, 2, 4, 3, 5).contiguous()
+    w = words.view(num_pages, cfg.hkv, 2, 4, PAGE, 32).permute(0, 1, 2, 4, 3, 5).contiguous()
     return w.view(num_pages, cfg.hkv, 2, PAGE, HEAD_DIM).view(torch.bfloat16)
 
 
