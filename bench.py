@@ -372,12 +372,14 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kvz", choices=["kvz", "reference"])
-    ap.add_argument("--workload", default="c1", choices=["c1", "c2", "c4"])
+    ap.add_argument("--workload", default="c1", choices=["c1", "c2", "c3", "c4"])
+    ap.add_argument("--budget-gb", type=float, default=60.0, help="KV budget for the c3 capacity count (1e9 B)")
     ap.add_argument("--sweep", action="store_true",
                     help="encode / standalone-decode throughput over 64 MB .. 4 GB of pages (exponent-spread KV)")
     ap.add_argument("--copies", type=int, default=3)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-steps", type=int, default=256, help="decode steps of the c3 streaming run")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -387,6 +389,8 @@ def main():
     dist, rank, world, local = dist_setup()
     if args.sweep:
         return run_sweep(args, dist, rank, local)
+    if args.workload == "c3":
+        return run_stream(args, cfg, dist, rank, world, local)
 
     if args.impl == "reference":
         return run_reference(args, cfg, dist, rank, world)
@@ -558,6 +562,163 @@ def main():
     if dist:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def run_stream(args, cfg, dist, rank, world, local):
+    """Streaming decode, Qwen3-8B shape (36 layers, 32/8 heads, batch 64): a 2048-token
+    prompt (128 pages per sequence and layer, encoded at prefill), then `decode_steps`
+    steps that each append one token per sequence and layer and run attention in every
+    layer.  When a sequence's tail page fills (every 16th step) the page is encoded in
+    every layer before that step's attention, into chunk slots handed out by the host
+    allocator; per-step latency includes the encoding.  The same loop on raw pages gives
+    the uncompressed step time.  At the end: sequences that fit in the KV budget."""
+    torch.cuda.set_device(local)
+    import decode_attention_value_gb300 as kvz
+
+    dev = torch.device("cuda", local)
+    B, L, hkv, hq = cfg.batch, cfg.layers, cfg.hkv, cfg.hq
+    prompt_pages = cfg.full_pages
+    T = args.decode_steps
+    dec_pages = (T + 15) // 16
+    ppseq = prompt_pages + dec_pages + 1  # raw page slots per sequence: prompt, decode pages, spare
+    P = B * ppseq
+    # raw pool of every layer; page b*ppseq + k is sequence b's k-th page (meta ids are the same)
+    raw = torch.empty((L, P, hkv, 2, 16, 128), dtype=torch.bfloat16, device=dev)
+    for layer in range(L):
+        raw[layer] = kvgen.gen_pages(cfg, P, layer=layer, device=dev)
+    new_kv = kvgen.gen_new_tokens(cfg, T, device=dev)  # [T][L][B][hkv][2][128]
+    qs = [kvgen.gen_q(cfg, layer=layer).to(dev) for layer in range(L)]
+    ids = torch.arange(B, device=dev, dtype=torch.int32) * ppseq
+    table = (ids[:, None] + torch.arange(ppseq - 1, device=dev, dtype=torch.int32)[None]).contiguous()
+    full_table = table[:, : prompt_pages + dec_pages].contiguous()
+    lens_h = [2048 + t + 1 for t in range(T)]
+    seq_lens = torch.tensor([[x] * B for x in lens_h], dtype=torch.int32, device=dev)  # [T][B]
+    tails = torch.stack([(ids + prompt_pages + t // 16) if x % 16 else torch.full_like(ids, -1)
+                         for t, x in enumerate(lens_h)]).contiguous()
+    status = kvz.new_status(dev)
+    meta = torch.zeros((L, P, hkv, 2), dtype=torch.int64, device=dev)
+    chunk = 32768  # granules (8 MiB)
+    worst_seq = L * (prompt_pages + dec_pages) * hkv * 32 * 256
+    nchunks = B * (worst_seq // (chunk * 256) + 2)
+    arena = torch.zeros(nchunks * chunk * 256, dtype=torch.uint8, device=dev)
+    alloc = kvz.Allocator(arena.numel(), chunk, B, hkv)
+    cursors = torch.zeros((B, 2), dtype=torch.int32, device=dev)
+    enc_ws = torch.empty(kvz.encode_workspace_size(hkv, B * 16), dtype=torch.uint8, device=dev)
+    seqs = np.arange(B, dtype=np.int32)
+
+    def apply(updates):
+        if updates:
+            u = torch.tensor(updates, dtype=torch.int64)
+            kvz.apply_cursor_updates(u[:, 0].to(torch.int32).to(dev), u[:, 1].to(torch.int32).to(dev),
+                                     u[:, 2].to(torch.int32).to(dev), cursors)
+
+    # ---- prefill: encode every prompt page of every layer, 16 pages per sequence per call ----
+    for k0 in range(0, prompt_pages, 16):
+        n = min(16, prompt_pages - k0)
+        for layer in range(L):
+            ticket, ups = alloc.reserve(seqs, [n] * B)
+            apply(ups)
+            src = (ids[:, None] + torch.arange(k0, k0 + n, device=dev, dtype=torch.int32)[None]).reshape(-1).contiguous()
+            dseq = torch.arange(B, device=dev, dtype=torch.int32).repeat_interleave(n)
+            kvz.encode_pages(raw[layer], src, src, dseq, meta[layer], arena, cursors, status, workspace=enc_ws)
+            alloc.observe(ticket, cursors.cpu().numpy().view(np.uint32))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, int(status.item())
+
+    out_c = torch.empty((B, hq, 128), dtype=torch.float32, device=dev)
+    out_r = torch.empty_like(out_c)
+    ws_c = torch.empty(kvz.attention_workspace_size(hkv, B, hq, full_table.shape[1] + 1), dtype=torch.uint8, device=dev)
+    ws_r = torch.empty(kvz.attention_workspace_size(hkv, B, hq, table.shape[1]), dtype=torch.uint8, device=dev)
+    pin_cur = torch.empty((B, 2), dtype=torch.int32).pin_memory()
+    pending = None  # (ticket, event) of the last cursor snapshot in flight
+
+    def append(t):
+        j, pos = t // 16, t % 16
+        raw[:, (ids + prompt_pages + j).long(), :, :, pos, :] = new_kv[t]
+
+    def step_compressed(t):
+        nonlocal pending
+        append(t)
+        if lens_h[t] % 16 == 0:  # every sequence's tail page just filled: encode it in every layer
+            if pending is not None and pending[1].query():
+                alloc.observe(pending[0], pin_cur.numpy().view(np.uint32))
+                pending = None
+            ticket, ups = alloc.reserve(seqs, [L] * B)
+            apply(ups)
+            page = (ids + prompt_pages + t // 16).contiguous()
+            dseq = torch.arange(B, device=dev, dtype=torch.int32)
+            for layer in range(L):
+                kvz.encode_pages(raw[layer], page, page, dseq, meta[layer], arena, cursors, status,
+                                 workspace=enc_ws)
+            pin_cur.copy_(cursors, non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record()
+            pending = (ticket, ev)
+        for layer in range(L):
+            kvz.decode_attention(qs[layer], full_table, seq_lens[t], tails[t], meta[layer], arena, raw[layer], out_c,
+                                 status, workspace=ws_c)
+
+    def step_raw(t):
+        append(t)
+        for layer in range(L):
+            kvz.decode_attention_raw(qs[layer], table, seq_lens[t], raw[layer], out_r, status, workspace=ws_r)
+
+    def run(step_fn):
+        times = []
+        for t in range(T):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            step_fn(t)
+            torch.cuda.synchronize()
+            times.append((time.perf_counter() - t0) * 1e6)
+        return times
+
+    # the raw loop re-appends the same tokens at the same places, so both loops see the same KV
+    with ClockSampler(local) as clk:
+        t_c = run(step_compressed)
+        t_r = run(step_raw)
+    clocks = clk.summary()
+    torch.cuda.synchronize()
+    st = int(status.item())
+    assert st == 0, st
+    identical = bool(torch.equal(out_c, out_r))  # last step: same pages, same split -> same bits
+    if pending is not None:
+        alloc.observe(pending[0], cursors.cpu().numpy().view(np.uint32))
+    stats = alloc.stats()
+    enc_steps = [t for t in range(T) if lens_h[t] % 16 == 0]
+    plain = [t for t in range(T) if lens_h[t] % 16 != 0]
+    meta_per_seq = L * (prompt_pages + dec_pages) * hkv * 16
+    used_per_seq = stats["used_bytes_bound"] / B
+    held_per_seq = stats["held_bytes"] / B
+    raw_per_seq = L * (2048 + T) * hkv * 2 * 128 * 2
+    budget = args.budget_gb * 1e9
+    logical = [L * B * lens_h[t] * hkv * 512 for t in range(T)]
+    mean_c = statistics.mean(t_c)
+    line = {
+        "metric": METRIC, "value": round(statistics.mean(logical) / (mean_c * 1e-6) / 1e9, 2), "unit": "GB/s",
+        "n_gpus": world, "steps": T, "warmup": 0, "ms_per_step": round(mean_c / 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": cfg.name, "layers": L, "batch": B, "q_heads": hq, "kv_heads": hkv, "head_dim": 128,
+                   "prompt_tokens": 2048, "decode_steps": T, "chunk_bytes": chunk * 256,
+                   "timing": "wall time per step, synchronised (an engine reading logits every step)"},
+        "us_per_step": round(mean_c, 1),
+        "us_per_step_with_encode": round(statistics.mean([t_c[t] for t in enc_steps]), 1),
+        "us_per_step_without_encode": round(statistics.mean([t_c[t] for t in plain]), 1),
+        "raw_us_per_step": round(statistics.mean(t_r), 1),
+        "speedup_vs_raw": round(statistics.mean(t_r) / mean_c, 4),
+        "bit_identical_last_step": identical,
+        "capacity": {"budget_bytes": budget, "raw_bytes_per_seq": raw_per_seq,
+                     "compressed_bytes_per_seq": round(used_per_seq + meta_per_seq),
+                     "compressed_bytes_per_seq_chunk_granular": round(held_per_seq + meta_per_seq),
+                     "raw_seqs": int(budget // raw_per_seq),
+                     "compressed_seqs": int(budget // (used_per_seq + meta_per_seq)),
+                     "compressed_seqs_chunk_granular": int(budget // (held_per_seq + meta_per_seq))},
+        "clocks": clocks,
+        # attention + merge per layer per step, plus 3 encode launches per layer at each page completion
+        "gpu_launches": T * L * 2 + len(enc_steps) * L * 3,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
 
 
 def run_sweep(args, dist, rank, local):

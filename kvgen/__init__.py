@@ -166,6 +166,20 @@ def _spread_pages(cfg: KVConfig, g, num_pages: int, device) -> torch.Tensor:
     return w.view(num_pages, cfg.hkv, 2, PAGE, HEAD_DIM).view(torch.bfloat16)
 
 
+def gen_new_tokens(cfg: KVConfig, steps: int, device="cpu") -> torch.Tensor:
+    """K/V of the tokens appended during `steps` decode steps, all layers:
+    BF16 [steps][layers][B][Hkv][2][128], same per-channel scales as the prompt pages."""
+    out = torch.empty((steps, cfg.layers, cfg.batch, cfg.hkv, 2, HEAD_DIM), dtype=torch.bfloat16, device=device)
+    for layer in range(cfg.layers):
+        ks, vs = channel_sigmas(cfg, layer, device)
+        g = _gen(device, cfg.seed * 4241 + layer * 97 + 11)
+        x = torch.randn((steps, cfg.batch, cfg.hkv, 2, HEAD_DIM), generator=g, device=device)
+        x[:, :, :, 0] *= ks[None, None]
+        x[:, :, :, 1] *= vs[None, None]
+        out[:, layer] = x.to(torch.bfloat16)
+    return out
+
+
 def gen_q(cfg: KVConfig, layer: int = 0, device="cpu", step: int = 0) -> torch.Tensor:
     g = _gen(device, cfg.seed * 31 + layer * 1009 + step * 65537 + 5)
     return torch.randn((cfg.batch, cfg.hq, HEAD_DIM), generator=g, device=device).to(torch.bfloat16)
