@@ -1,5 +1,5 @@
-// codec.cu -- page encoder (three launches: block sizes, segmented placement scan,
-// pack) and standalone decoder for the 12-bit BF16 block format.
+// codec.cu -- page encoder (validation, block sizes, segmented placement scan over
+// pages, pack) and standalone decoder for the 12-bit BF16 block format.
 //
 // Format (ZipFusion, "How it works" steps 1-4, layout and metadata paragraphs): a
 // 16-token page slice of one KV head, K or V, is four 512-value blocks (dims
@@ -74,15 +74,16 @@ __device__ __forceinline__ void exponent_range(const uint32_t (&w)[8], uint32_t 
 // launch 1: group sizes.  One CTA per (entry, head); warp w = block (kv = w/4, j = w%4)
 // reads its 16 x 32 slab (row = lane/2, 32 B per lane) and reduces the exponent range.
 // ---------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_enc_sizes(EncodeParams P)
+__global__ void __launch_bounds__(256) k_enc_sizes(EncodeParams P, int e0)
 {
-    const int entry = blockIdx.x / P.hkv, head = blockIdx.x % P.hkv;
+    if (P.ws_hdr[0] != 0) return;  // the call failed validation: nothing is read or written
+    const int entry = e0 + (int)(blockIdx.x / P.hkv), head = (int)(blockIdx.x % P.hkv);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kv = warp >> 2, j = warp & 3;
     __shared__ uint32_t gran[8];
     const int src = P.src_page[entry];
     uint32_t g = 0;
-    if (src >= 0 && src < P.num_raw_pages) {
+    {
         const uint16_t *slab = P.raw_pool + (((int64_t)src * P.hkv + head) * 2 + kv) * kPage * kDim;
         const uint4 *p = reinterpret_cast<const uint4 *>(slab + (lane >> 1) * kDim + 32 * j + 16 * (lane & 1));
         uint4 a = p[0], b = p[1];
@@ -97,90 +98,90 @@ __global__ void __launch_bounds__(256) k_enc_sizes(EncodeParams P)
     if (threadIdx.x == 0) {
         uint32_t s = 0;
         for (int k = 0; k < 8; ++k) s += gran[k];
-        P.ws_pair_size[blockIdx.x] = s;
+        P.ws_pair_size[(int64_t)entry * P.hkv + head] = s;
+        atomicAdd(P.ws_page_size + entry, s);  // integer sum: the same whatever the order
     }
 }
 
-// ---------------------------------------------------------------------------------
-// launch 2: one CTA validates the call and places every (entry, head) K+V pair at its
-// cursor: a segmented exclusive scan of pair sizes in call order, segments = runs of
-// equal dst_seq.  The segment head reads its cursor; the segment end writes it back.
-// ---------------------------------------------------------------------------------
-constexpr int kScanThreads = 1024;
-constexpr int kScanItems = 8;  // items per thread per tile
-
-__global__ void __launch_bounds__(kScanThreads) k_enc_scan(EncodeParams P)
+// Validation before anything is written: an index out of range or a decreasing
+// dst_seq makes the whole call a no-op.
+__global__ void __launch_bounds__(256) k_enc_validate(EncodeParams P)
 {
-    __shared__ uint32_t s_err;
-    __shared__ uint32_t s_flag[kScanThreads / 32];
-    __shared__ uint64_t s_sum[kScanThreads / 32];
-    __shared__ uint32_t s_carry_flag;
-    __shared__ uint64_t s_carry;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) {
-        s_err = 0;
-        s_carry = 0;
-        s_carry_flag = 0;
-    }
-    __syncthreads();
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
     uint32_t err = 0;
-    for (int e = tid; e < P.n; e += kScanThreads) {
+    if (e < P.n) {
         const int s = P.src_page[e], d = P.dst_page[e], q = P.dst_seq[e];
         if (s < 0 || s >= P.num_raw_pages || d < 0 || d >= P.num_meta_pages || q < 0 || q >= P.num_cursors)
             err |= KVZ_STATUS_BAD_INDEX;
         if (e > 0 && q < P.dst_seq[e - 1]) err |= KVZ_STATUS_BAD_ORDER;
     }
-    if (err) atomicOr(&s_err, err);
-    __syncthreads();
-    if (s_err) {
-        if (tid == 0) {
-            atomicOr(P.status, s_err);
-            *P.ws_call_ok = 0;
-        }
-        return;
+    err = __reduce_or_sync(0xffffffffu, err);
+    if (err && (threadIdx.x & 31) == 0) {
+        atomicOr(P.ws_hdr, err);
+        atomicOr(P.status, err);
     }
-    const int64_t M = (int64_t)P.n * P.hkv;
-    for (int64_t t0 = 0; t0 < M; t0 += (int64_t)kScanThreads * kScanItems) {
-        // this thread's run of items
-        const int64_t i0 = t0 + (int64_t)tid * kScanItems;
+}
+
+// ---------------------------------------------------------------------------------
+// Placement: one CTA scans the pages [e0, e1) in call order -- a segmented exclusive
+// scan of page sizes (per page, summed over heads by the size pass), segments = runs
+// of equal dst_seq.  A segment's first page reads its cursor, its last page writes it
+// back.
+// ---------------------------------------------------------------------------------
+constexpr int kScanThreads = 1024;
+constexpr int kScanItems = 4;  // pages per thread per tile
+
+__global__ void __launch_bounds__(kScanThreads) k_enc_scan(EncodeParams P, int e0, int e1)
+{
+    __shared__ uint32_t s_flag[kScanThreads / 32];
+    __shared__ uint64_t s_sum[kScanThreads / 32];
+    __shared__ uint32_t s_carry_flag;
+    __shared__ uint64_t s_carry;
+    if (P.ws_hdr[0] != 0) return;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        s_carry = 0;
+        s_carry_flag = 0;
+    }
+    __syncthreads();
+    for (int t0 = e0; t0 < e1; t0 += kScanThreads * kScanItems) {
+        const int i0 = t0 + tid * kScanItems;
         uint64_t val[kScanItems];
         uint32_t head[kScanItems];
         uint32_t any_head = 0;
         uint64_t run = 0;
 #pragma unroll
         for (int k = 0; k < kScanItems; ++k) {
-            const int64_t it = i0 + k;
+            const int e = i0 + k;
             val[k] = 0;
             head[k] = 0;
-            if (it < M) {
-                const int e = (int)(it / P.hkv), h = (int)(it % P.hkv);
+            if (e < e1) {
                 const int seq = P.dst_seq[e];
-                const bool is_head = (h == 0) && (e == 0 || P.dst_seq[e - 1] != seq);
-                uint64_t v = P.ws_pair_size[it];
+                const bool is_head = e == e0 || P.dst_seq[e - 1] != seq;
+                uint64_t v = P.ws_page_size[e];
                 if (is_head) v += P.cursors[2 * seq];  // absolute granule position
                 head[k] = is_head;
                 val[k] = v;
             }
-            // inclusive segmented scan within the run
-            run = head[k] ? val[k] : run + val[k];
+            run = head[k] ? val[k] : run + val[k];  // inclusive segmented scan within the run
             any_head |= head[k];
             val[k] = run;
         }
         // warp-level inclusive segmented scan of (flag, run total)
         uint32_t f = any_head;
-        uint64_t s = run;
+        uint64_t sm = run;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            uint64_t so = __shfl_up_sync(0xffffffffu, s, off);
-            uint32_t fo = __shfl_up_sync(0xffffffffu, f, off);
+            const uint64_t so = __shfl_up_sync(0xffffffffu, sm, off);
+            const uint32_t fo = __shfl_up_sync(0xffffffffu, f, off);
             if (lane >= off) {
-                if (!f) s += so;
+                if (!f) sm += so;
                 f |= fo;
             }
         }
         if (lane == 31) {
             s_flag[warp] = f;
-            s_sum[warp] = s;
+            s_sum[warp] = sm;
         }
         __syncthreads();
         if (warp == 0) {
@@ -192,8 +193,8 @@ __global__ void __launch_bounds__(kScanThreads) k_enc_scan(EncodeParams P)
             }
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
-                uint64_t so = __shfl_up_sync(0xffffffffu, ws, off);
-                uint32_t fo = __shfl_up_sync(0xffffffffu, wf, off);
+                const uint64_t so = __shfl_up_sync(0xffffffffu, ws, off);
+                const uint32_t fo = __shfl_up_sync(0xffffffffu, wf, off);
                 if (lane >= off) {
                     if (!wf) ws += so;
                     wf |= fo;
@@ -203,43 +204,31 @@ __global__ void __launch_bounds__(kScanThreads) k_enc_scan(EncodeParams P)
             s_sum[lane] = ws;
         }
         __syncthreads();
-        // exclusive prefix of this thread's run = inclusive of previous lane (this warp)
-        // combined with the previous warps' inclusive total
-        uint64_t prev_s = __shfl_up_sync(0xffffffffu, s, 1);
-        uint32_t prev_f = __shfl_up_sync(0xffffffffu, f, 1);
+        // exclusive prefix of this thread's run: inclusive of the previous lane, combined
+        // with the previous warps' inclusive total
+        const uint64_t prev_s = __shfl_up_sync(0xffffffffu, sm, 1);
+        const uint32_t prev_f = __shfl_up_sync(0xffffffffu, f, 1);
         const uint64_t wpre_s = warp > 0 ? s_sum[warp - 1] : s_carry;
-        uint64_t excl;
-        if (lane == 0) {
-            excl = wpre_s;
-        } else {
-            excl = prev_f ? prev_s : prev_s + wpre_s;
-        }
-        // write item positions: item k's exclusive position = (run prefix) - own size
+        const uint64_t excl = lane == 0 ? wpre_s : (prev_f ? prev_s : prev_s + wpre_s);
+        bool seen_head = false;
 #pragma unroll
         for (int k = 0; k < kScanItems; ++k) {
-            const int64_t it = i0 + k;
-            if (it >= M) break;
-            // inclusive value of item k including the carry-in
-            bool seen_head = false;
-            for (int q = 0; q <= k; ++q) seen_head |= head[q];
+            const int e = i0 + k;
+            if (e >= e1) break;
+            seen_head |= head[k] != 0;
             const uint64_t incl = seen_head ? val[k] : val[k] + excl;
-            const uint64_t own = P.ws_pair_size[it];
-            const uint64_t pos = incl - own;
-            P.ws_pair_base[it] = (uint32_t)min(pos, (uint64_t)0xFFFFFFFFu);
-            // the last item of a segment writes the cursor back
-            const int e = (int)(it / P.hkv), h = (int)(it % P.hkv);
-            const bool last = (h == P.hkv - 1) && (e == P.n - 1 || P.dst_seq[e + 1] != P.dst_seq[e]);
-            if (last) P.cursors[2 * P.dst_seq[e]] = (uint32_t)min(incl, (uint64_t)0xFFFFFFFFu);
+            const uint64_t pos = incl - P.ws_page_size[e];
+            P.ws_page_base[e] = (uint32_t)(pos < 0xFFFFFFFFull ? pos : 0xFFFFFFFFull);
+            const bool last = e == e1 - 1 || P.dst_seq[e + 1] != P.dst_seq[e];
+            if (last) P.cursors[2 * P.dst_seq[e]] = (uint32_t)(incl < 0xFFFFFFFFull ? incl : 0xFFFFFFFFull);
         }
         __syncthreads();
         if (tid == kScanThreads - 1) {
-            // carry = inclusive total of the whole tile (previous carry folded in)
-            s_carry = s_sum[31];
+            s_carry = s_sum[31];  // inclusive total of the whole tile (previous carry folded in)
             s_carry_flag = s_flag[31];
         }
         __syncthreads();
     }
-    if (tid == 0) *P.ws_call_ok = 1;
 }
 
 // ---------------------------------------------------------------------------------
@@ -247,12 +236,12 @@ __global__ void __launch_bounds__(kScanThreads) k_enc_scan(EncodeParams P)
 // its block in storage order, recomputes the tag and writes 768 or 1024 bytes at its
 // place in the group; warps 0 and 4 write the two metadata words.
 // ---------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_enc_pack(EncodeParams P)
+__global__ void __launch_bounds__(256) k_enc_pack(EncodeParams P, int e0)
 {
     __shared__ __align__(16) uint8_t stage[32 * kStagePitch];
     __shared__ uint32_t tags[8];
-    if (*P.ws_call_ok == 0) return;
-    const int entry = blockIdx.x / P.hkv, head = blockIdx.x % P.hkv;
+    if (P.ws_hdr[0] != 0) return;
+    const int entry = e0 + (int)(blockIdx.x / P.hkv), head = (int)(blockIdx.x % P.hkv);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kv = warp >> 2, j = warp & 3;
     const int src = P.src_page[entry], dst = P.dst_page[entry], seq = P.dst_seq[entry];
@@ -281,7 +270,8 @@ __global__ void __launch_bounds__(256) k_enc_pack(EncodeParams P)
     uint32_t k_size = 0;
 #pragma unroll
     for (int k = 0; k < 4; ++k) k_size += tag_granules(tags[k]);
-    const uint64_t pair_base = P.ws_pair_base[blockIdx.x];
+    uint64_t pair_base = P.ws_page_base[entry];  // the page's position, then the heads before this one
+    for (int h = 0; h < head; ++h) pair_base += P.ws_pair_size[(int64_t)entry * P.hkv + h];
     const uint64_t offset0 = pair_base + (kv ? k_size : 0);
     const uint64_t end = min((uint64_t)P.cursors[2 * seq + 1], P.arena_bytes / kGranule);
     const bool fits = offset0 + gsize <= end;
@@ -412,10 +402,13 @@ __global__ void k_apply_cursor_updates(const int32_t *idx, const uint32_t *pos, 
 // ---------------------------------------------------------------------------------
 cudaError_t launch_encode(const EncodeParams &P, cudaStream_t stream)
 {
-    const int pairs = P.n * P.hkv;
-    k_enc_sizes<<<pairs, 256, 0, stream>>>(P);
-    k_enc_scan<<<1, kScanThreads, 0, stream>>>(P);
-    k_enc_pack<<<pairs, 256, 0, stream>>>(P);
+    cudaError_t e = cudaMemsetAsync(P.ws_hdr, 0, 16 + (size_t)P.n * 4, stream);  // header + page sizes
+    if (e != cudaSuccess) return e;
+    k_enc_validate<<<(P.n + 255) / 256, 256, 0, stream>>>(P);
+    const unsigned items = (unsigned)((size_t)P.n * P.hkv);
+    k_enc_sizes<<<items, 256, 0, stream>>>(P, 0);
+    k_enc_scan<<<1, kScanThreads, 0, stream>>>(P, 0, P.n);
+    k_enc_pack<<<items, 256, 0, stream>>>(P, 0);
     return cudaGetLastError();
 }
 

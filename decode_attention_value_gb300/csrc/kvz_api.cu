@@ -219,7 +219,7 @@ int kvz_device_sm_count(void) { return sm_count(); }
 size_t kvz_encode_workspace_size(kvz_dims dims, int32_t n)
 {
     if (!dims_ok(dims) || n < 0) return 0;
-    return 16 + ((size_t)n * dims.num_kv_heads * 4 + 15) / 16 * 16 * 2;
+    return encode_ws_bytes(n, dims.num_kv_heads);
 }
 
 int kvz_encode_pages(kvz_dims dims, const void *raw_pool, int64_t num_raw_pages, const int32_t *src_page,
@@ -254,10 +254,11 @@ int kvz_encode_pages(kvz_dims dims, const void *raw_pool, int64_t num_raw_pages,
     P.num_cursors = num_cursors;
     P.status = status;
     uint8_t *w = static_cast<uint8_t *>(workspace);
-    const size_t arr = ((size_t)n * dims.num_kv_heads * 4 + 15) / 16 * 16;
-    P.ws_call_ok = reinterpret_cast<uint32_t *>(w);
-    P.ws_pair_size = reinterpret_cast<uint32_t *>(w + 16);
-    P.ws_pair_base = reinterpret_cast<uint32_t *>(w + 16 + arr);
+    const size_t a = ((size_t)n * 4 + 15) / 16 * 16;
+    P.ws_hdr = reinterpret_cast<uint32_t *>(w);
+    P.ws_page_size = reinterpret_cast<uint32_t *>(w + 16);  // contiguous with the header: one memset
+    P.ws_page_base = reinterpret_cast<uint32_t *>(w + 16 + a);
+    P.ws_pair_size = reinterpret_cast<uint32_t *>(w + 16 + 2 * a);
     cudaError_t e = launch_encode(P, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KVZ_OK : fail_cuda(e);
 }

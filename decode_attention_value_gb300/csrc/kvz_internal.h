@@ -23,10 +23,17 @@ struct EncodeParams {
     int num_cursors;
     uint32_t *status;
     // workspace
-    uint32_t *ws_pair_size;  // [n*hkv]
-    uint32_t *ws_pair_base;  // [n*hkv]
-    uint32_t *ws_call_ok;    // [1]
+    uint32_t *ws_hdr;        // [4]: validation failure bits (zeroed each call)
+    uint32_t *ws_page_size;  // [n] granules per page, summed over heads (zeroed each call)
+    uint32_t *ws_page_base;  // [n] granule position of each page's first group
+    uint32_t *ws_pair_size;  // [n*hkv] granules per (page, head) K+V pair
 };
+
+inline size_t encode_ws_bytes(int n, int hkv)
+{
+    const size_t a = ((size_t)n * 4 + 15) / 16 * 16;
+    return 16 + 2 * a + ((size_t)n * hkv * 4 + 15) / 16 * 16;
+}
 
 struct DecodeParams {
     int hkv;

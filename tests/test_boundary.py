@@ -82,7 +82,7 @@ def test_host_rejects_bad_arguments(kvz):
     assert lib.kvz_encode_pages(_dims(kvz), fake, 1, fake, fake, fake, 1, fake, 1, fake + 16, 1 << 20, fake, 1,
                                 fake, 1 << 20, fake, None) == E["align"]
     ws = kvz.encode_workspace_size(8, 10)
-    assert ws >= 2 * 10 * 8 * 4
+    assert ws >= 10 * 8 * 4 + 2 * 10 * 4  # per-(page, head) sizes, per-page sizes and positions
     assert lib.kvz_encode_pages(_dims(kvz), fake, 10, fake, fake, fake, 10, fake, 10, fake, 1 << 20, fake, 1,
                                 fake, ws - 1, fake, None) == E["ws"]
     # decode: misaligned output
