@@ -340,10 +340,12 @@ static double bf16_to_double(uint16_t w)
 double oref_bf16_value(uint16_t w) { return bf16_to_double(w); }
 
 typedef struct {
-    int hkv, batch, hq, max_pages, compressed;
+    int hkv, batch, hq, max_pages, compressed; /* compressed: 0 raw, 1 12-bit blocks, 2 GA tiles */
     const uint16_t *q;
     const int32_t *page_ids, *seq_lens, *tail_page;
     const uint64_t *meta;
+    const uint32_t *meta32; /* GA tile entries */
+    const uint8_t *bases;   /* GA bases [hkv][2][2][128] */
     int64_t num_meta_pages;
     const uint8_t *arena;
     uint64_t arena_bytes;
@@ -378,9 +380,17 @@ static int attend_unit(attn_job *J, int unit)
                 status |= OREF_BAD_INDEX;
                 ok = 0;
             } else {
-                const uint64_t *m = J->meta + ((int64_t)pid * J->hkv + kvh) * 2;
-                int st = decode_group(m[0], J->arena, J->arena_bytes, 0, kp);
-                st |= decode_group(m[1], J->arena, J->arena_bytes, 1, vp);
+                int st;
+                if (J->compressed == 2) {
+                    const uint32_t *m = J->meta32 + ((int64_t)pid * J->hkv + kvh) * 2;
+                    const uint8_t *bb = J->bases + (size_t)kvh * 2 * 256;
+                    st = oga_decode_entry(m[0], J->arena, J->arena_bytes, 0, bb, kp);
+                    st |= oga_decode_entry(m[1], J->arena, J->arena_bytes, 1, bb + 256, vp);
+                } else {
+                    const uint64_t *m = J->meta + ((int64_t)pid * J->hkv + kvh) * 2;
+                    st = decode_group(m[0], J->arena, J->arena_bytes, 0, kp);
+                    st |= decode_group(m[1], J->arena, J->arena_bytes, 1, vp);
+                }
                 if (st) {
                     status |= st;
                     ok = 0;
@@ -512,6 +522,37 @@ int oref_attention_raw(int hkv, int batch, int hq, const uint16_t *q, const int3
     J.q = q;
     J.page_ids = page_ids;
     J.seq_lens = seq_lens;
+    J.raw_pool = raw_pool;
+    J.num_raw_pages = num_raw_pages;
+    J.out = out;
+    return run_attention(&J, nthreads);
+}
+
+/* The same attention over group-adaptive tiles (GAAC, "Attention with On-the-Fly
+ * Decompression"): finalized pages come from tiles, the partial last page from the
+ * raw pool. */
+int oref_ga_decode_attention(int hkv, int batch, int hq, const uint16_t *q, const int32_t *page_ids,
+                             int max_pages, const int32_t *seq_lens, const int32_t *tail_page,
+                             const uint32_t *meta, int64_t num_meta_pages, const uint8_t *arena,
+                             uint64_t arena_bytes, const uint8_t *bases, const uint16_t *raw_pool,
+                             int64_t num_raw_pages, double *out, int nthreads)
+{
+    attn_job J;
+    memset(&J, 0, sizeof J);
+    J.hkv = hkv;
+    J.batch = batch;
+    J.hq = hq;
+    J.max_pages = max_pages;
+    J.compressed = 2;
+    J.q = q;
+    J.page_ids = page_ids;
+    J.seq_lens = seq_lens;
+    J.tail_page = tail_page;
+    J.meta32 = meta;
+    J.bases = bases;
+    J.num_meta_pages = num_meta_pages;
+    J.arena = arena;
+    J.arena_bytes = arena_bytes;
     J.raw_pool = raw_pool;
     J.num_raw_pages = num_raw_pages;
     J.out = out;

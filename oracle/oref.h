@@ -43,6 +43,25 @@ int oref_attention_raw(int hkv, int batch, int hq, const uint16_t *q, const int3
                        int max_pages, const int32_t *seq_lens, const uint16_t *raw_pool,
                        int64_t num_raw_pages, double *out, int nthreads);
 
+/* group-adaptive additive tiles (oga.c) */
+void oga_calibrate(const uint16_t *pages, int64_t n, uint8_t *b3, uint8_t *b4);
+int oga_group_mode(const unsigned e[8], const unsigned b3[8], const unsigned b4[8]);
+int oga_encode_tile(const uint16_t *page, int is_v, const uint8_t *b3, const uint8_t *b4, uint8_t *out);
+void oga_decode_tile(const uint8_t *in, int raw, int is_v, const uint8_t *b3, const uint8_t *b4, uint16_t *page);
+int oga_encode_pages(int hkv, const uint16_t *raw_pool, int64_t num_raw_pages, const uint8_t *bases,
+                     const int32_t *src_page, const int32_t *dst_page, const int32_t *dst_seq, int32_t n,
+                     uint32_t *meta, int64_t num_meta_pages, uint8_t *arena, uint64_t arena_bytes,
+                     uint32_t *cursors, int32_t num_cursors);
+int oga_decode_entry(uint32_t entry, const uint8_t *arena, uint64_t arena_bytes, int is_v, const uint8_t *bb,
+                     uint16_t *half_page);
+int oga_decode_pages(int hkv, const uint32_t *meta, int64_t num_meta_pages, const uint8_t *arena,
+                     uint64_t arena_bytes, const uint8_t *bases, const int32_t *page, int32_t n, uint16_t *out);
+int oref_ga_decode_attention(int hkv, int batch, int hq, const uint16_t *q, const int32_t *page_ids,
+                             int max_pages, const int32_t *seq_lens, const int32_t *tail_page,
+                             const uint32_t *meta, int64_t num_meta_pages, const uint8_t *arena,
+                             uint64_t arena_bytes, const uint8_t *bases, const uint16_t *raw_pool,
+                             int64_t num_raw_pages, double *out, int nthreads);
+
 #ifdef __cplusplus
 }
 #endif
