@@ -403,6 +403,8 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="encode / standalone-decode throughput over 64 MB .. 4 GB of pages (exponent-spread KV)")
     ap.add_argument("--copies", type=int, default=3)
+    ap.add_argument("--format", default="zf", choices=["zf", "ga"],
+                    help="ga: group-adaptive additive tiles instead of 12-bit block groups (c1, c2, c4)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-steps", type=int, default=256, help="decode steps of the c3 streaming run")
@@ -422,6 +424,8 @@ def main():
 
     if args.impl == "reference":
         return run_reference(args, cfg, dist, rank, world)
+    if args.format == "ga":
+        return run_ga(args, cfg, dist, rank, world, local)
 
     torch.cuda.set_device(local)
     import decode_attention_value_gb300 as kvz
@@ -591,6 +595,158 @@ def main():
                          "algorithmic_bytes_per_launch": W.alg_bytes_r},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "cpu_baseline": cpu,
+        "clocks": clocks,
+        "gpu_launches": 2 * K,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+class GaCopies:
+    """The workload's pages as group-adaptive tiles: bases calibrated on the GPU from
+    every 8th encoded page of the layer, then one tile copy per KV copy."""
+
+    def __init__(self, W: Workload, sample_step: int = 8):
+        kvz, cfg, dev = W.kvz, W.cfg, W.full.device
+        B, hkv = cfg.batch, cfg.hkv
+        self.W = W
+        self.bases = torch.zeros((hkv, 2, 2, 128), dtype=torch.uint8, device=dev)
+        self.sample = W.src[::sample_step].contiguous()
+        kvz.ga_calibrate(W.pools[0], self.sample, self.bases, W.status)
+        per = max(cfg.full_pages, 1) * hkv * 2 * 64
+        self.arena_bytes = B * per * 64
+        self.cursor0 = torch.tensor([[b * per, (b + 1) * per] for b in range(B)], dtype=torch.int32, device=dev)
+        self.metas, self.arenas = [], []
+        for c in range(W.copies):
+            meta = torch.zeros((cfg.num_pages, hkv, 2), dtype=torch.int32, device=dev)
+            arena = torch.zeros(self.arena_bytes, dtype=torch.uint8, device=dev)
+            cur = self.cursor0.clone()
+            kvz.ga_encode_pages(W.pools[c], self.bases, W.src, W.src, W.dseq, meta, arena, cur, W.status,
+                                workspace=W.enc_ws)
+            self.metas.append(meta)
+            self.arenas.append(arena)
+        self.out = torch.empty_like(W.out)
+        torch.cuda.synchronize()
+        if int(W.status.item()) != 0:
+            raise RuntimeError(f"tile encode status {int(W.status.item())}")
+        e = self.metas[0][W.src.long()].view(-1)
+        raw = ((e.view(torch.int32) < 0) & (e != -1)).sum().item()  # bit 31 set: raw tile
+        self.tiles = e.numel()
+        self.raw_tiles = int(raw)
+        self.tile_bytes = (self.tiles - self.raw_tiles) * 3008 + self.raw_tiles * 4096
+        G = cfg.hq // hkv
+        segs = B * hkv + W.grid_c() - 1
+        part_bytes = 2 * segs * G * 130 * 4
+        self.alg_bytes = (self.tile_bytes + W.pages_c * hkv * 8 + W.pages_c * hkv * 4 + hkv * 512 + W.tail_bytes +
+                          B * cfg.hq * 128 * 2 + B * cfg.hq * 128 * 4 + part_bytes)
+
+    def step(self, k: int):
+        W = self.W
+        c = k % W.copies
+        W.kvz.ga_decode_attention(W.q, W.full, W.seq_lens, W.tail, self.metas[c], self.arenas[c], self.bases,
+                                  W.pools[c], self.out, W.status, workspace=W.ws_c)
+
+
+def run_ga(args, cfg, dist, rank, world, local):
+    """The workload through the group-adaptive tile format, timed beside the 12-bit
+    format and the raw kernel on the same pages."""
+    torch.cuda.set_device(local)
+    import decode_attention_value_gb300 as kvz
+
+    dev = torch.device("cuda", local)
+    peak, peak_kind = measured_peaks()
+    W = Workload(cfg, args.copies, layer=rank, dev=dev)
+    GA = GaCopies(W)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for k in range(args.warmup):
+        GA.step(k)
+        W.step_c(k)
+        W.step_r(k)
+    torch.cuda.synchronize()
+    if int(W.status.item()) != 0:
+        raise RuntimeError(f"attention status {int(W.status.item())}")
+    identical = bool(torch.equal(GA.out, W.out_raw))
+    K = args.steps
+    g_g, g_c, g_r = graph_of(GA.step, K), graph_of(W.step_c, K), graph_of(W.step_r, K)
+    for g in (g_g, g_c, g_r):
+        g.replay()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        soak_until = time.time() + 0.6
+        while time.time() < soak_until:
+            g_g.replay()
+            torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        ms_g = time_graph(g_g)
+        ms_c = time_graph(g_c)
+        ms_r = time_graph(g_r)
+    clocks = clk.summary()
+    ms_g, ms_c, ms_r = max_over_ranks(dist, [ms_g, ms_c, ms_r], device=dev)
+    us_g, us_c, us_r = (m * 1e3 / K for m in (ms_g, ms_c, ms_r))
+    value = job_throughput(world, W.logical_bytes, K, ms_g)
+    achieved = GA.alg_bytes / (us_g * 1e-6) / 1e9
+    launch_ms = per_launch_ms(GA.step, max(10, min(K, 40)), flush)
+
+    enc_meta = torch.zeros_like(GA.metas[0])
+    enc_arena = torch.zeros_like(GA.arenas[0])
+    enc_cur = GA.cursor0.clone()
+
+    def enc(k):
+        enc_cur.copy_(GA.cursor0)
+        kvz.ga_encode_pages(W.pools[k % W.copies], GA.bases, W.src, W.src, W.dseq, enc_meta, enc_arena, enc_cur,
+                            W.status, workspace=W.enc_ws)
+
+    enc_ms = per_launch_ms(enc, 10, flush)
+    enc_in = W.src.numel() * cfg.hkv * 2 * 16 * 128 * 2
+    dec_out = torch.empty((W.src.numel(), cfg.hkv, 2, 16, 128), dtype=torch.bfloat16, device=dev)
+
+    def dec(k):
+        kvz.ga_decode_blocks(GA.metas[k % W.copies], GA.arenas[k % W.copies], GA.bases, W.src, dec_out, W.status)
+
+    dec_ms = per_launch_ms(dec, 10, flush)
+    torch.cuda.synchronize()
+    if int(W.status.item()) != 0:
+        raise RuntimeError(f"status {int(W.status.item())}")
+    if not torch.equal(dec_out.view(torch.int16), W.pools[(10 - 1) % W.copies][W.src.long()].view(torch.int16)):
+        raise RuntimeError("tile decode differs from the input pages")
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(us_g / 1e3, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": cfg.name, "format": "group-adaptive tiles", "batch": cfg.batch, "q_heads": cfg.hq,
+                   "kv_heads": cfg.hkv, "head_dim": 128, "page_tokens": 16, "context_tokens": cfg.full_pages * 16,
+                   "tail_tokens": f"{cfg.tail_min}..{cfg.tail_max}", "page_order": "shuffled",
+                   "calibration": "every 8th encoded page of the layer", "parallelism": f"replicas{world}",
+                   "l2": f"inputs larger than L2: {args.copies} rotating KV copies"},
+        "us_per_step": round(us_g, 3),
+        "zf_us_per_step": round(us_c, 3),
+        "raw_us_per_step": round(us_r, 3),
+        "speedup_vs_raw": round(us_r / us_g, 4),
+        "speedup_vs_zf": round(us_c / us_g, 4),
+        "tile_bytes_ratio": round(GA.tile_bytes / (GA.tiles * 4096), 5),
+        "raw_tile_fraction": round(GA.raw_tiles / GA.tiles, 5),
+        "zf_bytes_ratio": round(W.block_bytes / (W.blocks * 1024), 5),
+        "bit_identical_tiles_vs_raw": identical,
+        "encode_GBps": round(enc_in / (enc_ms * 1e-3) / 1e9, 2),
+        "decode_GBps": round(enc_in / (dec_ms * 1e-3) / 1e9, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "k_attn<tiles> + k_attn_merge", "launch_us": round(us_g, 3),
+                     "cold_single_launch_us": round(launch_ms * 1e3, 3),
+                     "algorithmic_bytes_per_launch": GA.alg_bytes},
         "clocks": clocks,
         "gpu_launches": 2 * K,
     }

@@ -1,5 +1,5 @@
-"""Python binding of libkvz: lossless 12-bit BF16 KV pages and paged GQA decode
-attention over them on one GB300 (sm_103a).
+"""Python binding of libkvz: lossless 12-bit BF16 KV pages, group-adaptive additive
+tiles, and paged GQA decode attention over either on one GB300 (sm_103a).
 
 Argument marshalling only: every step runs in the CUDA kernels of ``libkvz.so``
 (built in-tree by ``_build.build()``).  Tensors are torch CUDA tensors; the binding
@@ -29,11 +29,18 @@ STATUS_BAD_TAIL = 32
 
 ERR_OUT_OF_SPACE = -7
 
+GA_GRANULE = 64
+GA_TILE_BYTES = 3008
+GA_RAW_TILE_BYTES = 4096
+GA_ENTRY_RAW = 0x80000000
+GA_ENTRY_INVALID = 0xFFFFFFFF
+
 EXPORTS = (
     "kvz_encode_workspace_size", "kvz_encode_pages", "kvz_decode_blocks", "kvz_attention_workspace_size",
     "kvz_decode_attention", "kvz_decode_attention_raw", "kvz_alloc_create", "kvz_alloc_destroy",
     "kvz_alloc_reserve", "kvz_alloc_observe", "kvz_alloc_release", "kvz_alloc_stats",
     "kvz_apply_cursor_updates", "kvz_strerror", "kvz_last_cuda_error", "kvz_device_sm_count",
+    "kvz_ga_calibrate", "kvz_ga_encode_pages", "kvz_ga_decode_blocks", "kvz_ga_decode_attention",
 )
 
 
@@ -71,6 +78,11 @@ def _load() -> ctypes.CDLL:
         "kvz_alloc_release": (ctypes.c_int, [P, i32]),
         "kvz_alloc_stats": (ctypes.c_int, [P, P, P, P, P, P]),
         "kvz_apply_cursor_updates": (ctypes.c_int, [P, P, P, i32, P, i32, P]),
+        "kvz_ga_calibrate": (ctypes.c_int, [Dims, P, i64, P, i32, P, P, P]),
+        "kvz_ga_encode_pages": (ctypes.c_int, [Dims, P, i64, P, P, P, P, i32, P, i64, P, u64, P, i32, P, sz, P, P]),
+        "kvz_ga_decode_blocks": (ctypes.c_int, [Dims, P, i64, P, u64, P, P, i32, P, P, P]),
+        "kvz_ga_decode_attention": (ctypes.c_int, [Dims, i32, i32, P, P, i32, P, P, P, i64, P, u64, P, P, i64, P, P,
+                                                   sz, P, P]),
         "kvz_strerror": (ctypes.c_char_p, [ctypes.c_int]),
         "kvz_last_cuda_error": (ctypes.c_int, []),
         "kvz_device_sm_count": (ctypes.c_int, []),
@@ -228,6 +240,69 @@ def apply_cursor_updates(idx, pos, end, cursors, stream=None):
         _ptr(cursors, _U32, "cursors"), cursors.numel() // 2, _stream(stream),
     )
     _check("kvz_apply_cursor_updates", rc)
+
+
+# ------------------------------------------------------------------------------------
+# group-adaptive additive tiles
+# ------------------------------------------------------------------------------------
+def ga_calibrate(raw_pool, pages, bases, status, stream=None):
+    """Window bases of one layer from the sample pages (int32 raw page ids) into bases:
+    uint8 [Hkv][2][2][128]."""
+    hkv = raw_pool.shape[1]
+    rc = _lib.kvz_ga_calibrate(
+        _dims(hkv), _ptr(raw_pool, _BF16, "raw_pool"), _pages_of(raw_pool), _ptr(pages, torch.int32, "pages"),
+        pages.numel(), _ptr(bases, _U8, "bases"), _ptr(status, _U32, "status"), _stream(stream),
+    )
+    _check("kvz_ga_calibrate", rc)
+
+
+def ga_encode_pages(raw_pool, bases, src_page, dst_page, dst_seq, meta, arena, cursors, status, workspace=None,
+                    stream=None):
+    """encode_pages for tiles: meta int32/uint32 [M][Hkv][2] entries, cursors in 64-byte
+    granules."""
+    hkv = raw_pool.shape[1]
+    n = src_page.numel()
+    if workspace is None:
+        workspace = torch.empty(encode_workspace_size(hkv, n), dtype=torch.uint8, device=raw_pool.device)
+    rc = _lib.kvz_ga_encode_pages(
+        _dims(hkv), _ptr(raw_pool, _BF16, "raw_pool"), _pages_of(raw_pool), _ptr(bases, _U8, "bases"),
+        _ptr(src_page, torch.int32, "src_page"), _ptr(dst_page, torch.int32, "dst_page"),
+        _ptr(dst_seq, torch.int32, "dst_seq"), n, _ptr(meta, _U32, "meta"), meta.numel() // (hkv * 2),
+        _ptr(arena, _U8, "arena"), arena.numel(), _ptr(cursors, _U32, "cursors"), cursors.numel() // 2,
+        _ptr(workspace, _U8, "workspace"), workspace.numel(), _ptr(status, _U32, "status"), _stream(stream),
+    )
+    _check("kvz_ga_encode_pages", rc)
+
+
+def ga_decode_blocks(meta, arena, bases, pages, out, status, stream=None):
+    """Decompress tiles of pages (meta page ids) into out: BF16 [n][Hkv][2][16][128]."""
+    hkv = out.shape[1]
+    rc = _lib.kvz_ga_decode_blocks(
+        _dims(hkv), _ptr(meta, _U32, "meta"), meta.numel() // (hkv * 2), _ptr(arena, _U8, "arena"), arena.numel(),
+        _ptr(bases, _U8, "bases"), _ptr(pages, torch.int32, "pages"), pages.numel(), _ptr(out, _BF16, "out"),
+        _ptr(status, _U32, "status"), _stream(stream),
+    )
+    _check("kvz_ga_decode_blocks", rc)
+
+
+def ga_decode_attention(q, page_ids, seq_lens, tail_page, meta, arena, bases, raw_pool, out, status,
+                        workspace=None, stream=None):
+    """decode_attention over tiles (meta: int32/uint32 [M][Hkv][2] entries)."""
+    B, hq = q.shape[0], q.shape[1]
+    hkv = meta.shape[1] if meta.dim() >= 2 else raw_pool.shape[1]
+    max_pages = page_ids.shape[1] if page_ids.dim() == 2 else 0
+    if workspace is None:
+        workspace = torch.empty(attention_workspace_size(hkv, B, hq, max_pages + 1), dtype=torch.uint8,
+                                device=q.device)
+    rc = _lib.kvz_ga_decode_attention(
+        _dims(hkv), B, hq, _ptr(q, _BF16, "q"), _ptr(page_ids, torch.int32, "page_ids"), max_pages,
+        _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(tail_page, torch.int32, "tail_page"),
+        _ptr(meta, _U32, "meta"), meta.numel() // (hkv * 2), _ptr(arena, _U8, "arena"), arena.numel(),
+        _ptr(bases, _U8, "bases"), _ptr(raw_pool, _BF16, "raw_pool"), _pages_of(raw_pool),
+        _ptr(out, torch.float32, "out"), _ptr(workspace, _U8, "workspace"), workspace.numel(),
+        _ptr(status, _U32, "status"), _stream(stream),
+    )
+    _check("kvz_ga_decode_attention", rc)
 
 
 # ------------------------------------------------------------------------------------

@@ -1,6 +1,7 @@
-// attention.cu -- split-KV GQA paged decode attention over 12-bit compressed pages
-// plus a raw BF16 tail (kCompressed = true), and the same kernel over plain BF16
-// pages (kCompressed = false, the in-run uncompressed baseline).
+// attention.cu -- split-KV GQA paged decode attention over compressed pages plus a raw
+// BF16 tail (12-bit block groups, kFmt = kFmtZf; group-adaptive tiles, kFmt = kFmtGa),
+// and the same kernel over plain BF16 pages (kFmt = kFmtRaw, the in-run uncompressed
+// baseline).
 //
 // GAAC ("Attention with On-the-Fly Decompression"): the kernel reads compressed tiles
 // and their metadata, rebuilds BF16 only in registers, and compressed blocks and the
@@ -26,6 +27,7 @@
 
 #include <cstring>
 
+#include "ga.cuh"
 #include "kvz_internal.h"
 
 namespace kvz {
@@ -148,9 +150,11 @@ __device__ __forceinline__ void mask_v_frag(uint32_t (&a)[4], int lane, int vali
 // ---------------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------------
-template <bool kCompressed>
+template <int kFmt>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams P, const __grid_constant__ CUtensorMap tmap)
 {
+    constexpr bool kCompressed = kFmt != kFmtRaw;
+    constexpr bool kGa = kFmt == kFmtGa;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_addr(smem);
     if (sbase & 1023u) {  // the swizzled TMA destinations need 1024-byte alignment
@@ -243,8 +247,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
         auto is_compressed = [&](const Pre &r) { return kCompressed && !((r.L.p == r.n - 1) && r.tl != 0); };
         auto load_meta = [&](const Pre &r, uint64_t &m0, uint64_t &m1) {  // metadata (global load)
             m0 = m1 = 0;
-            if (is_compressed(r) && r.pid >= 0 && r.pid < P.num_meta_pages)
-                ld_keep_u64x2(P.meta + ((int64_t)r.pid * hkv + r.L.kvh) * 2, keep, m0, m1);
+            if (is_compressed(r) && r.pid >= 0 && r.pid < P.num_meta_pages) {
+                if (kGa)  // the K and V tile entries
+                    m0 = ld_keep_u64(reinterpret_cast<const uint64_t *>(P.meta32 + ((int64_t)r.pid * hkv + r.L.kvh) * 2),
+                                     keep);
+                else
+                    ld_keep_u64x2(P.meta + ((int64_t)r.pid * hkv + r.L.kvh) * 2, keep, m0, m1);
+            }
         };
         Pre cur, nxt;
         uint64_t cm0 = 0, cm1 = 0;
@@ -260,7 +269,25 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
             uint32_t d_kind = kKindSkip, d_valid = 0, d_bad = 0, d_tK = 0, d_tV = 0, d_bytes = 0;
             uint64_t d_srcK = 0, d_srcV = 0;
             if (base + lane < npage) {
-                if (is_compressed(cur)) {
+                if (kGa && is_compressed(cur)) {
+                    const uint32_t eK = (uint32_t)cm0, eV = (uint32_t)(cm0 >> 32);
+                    const uint64_t oK = eK & kGaOffsetMask, oV = eV & kGaOffsetMask;
+                    if (cur.pid < 0 || cur.pid >= P.num_meta_pages) {
+                        d_bad = KVZ_STATUS_BAD_INDEX;
+                    } else if (eK == kGaEntryInvalid || eV == kGaEntryInvalid ||
+                               oK * kGaGranule + ga_entry_bytes(eK) > P.arena_bytes ||
+                               oV * kGaGranule + ga_entry_bytes(eV) > P.arena_bytes) {
+                        d_bad = KVZ_STATUS_BAD_META;
+                    } else {
+                        d_kind = kKindPair;
+                        d_valid = kPage;
+                        d_tK = eK >> 31;  // 1: raw tile
+                        d_tV = eV >> 31;
+                        d_srcK = oK * kGaGranule;
+                        d_srcV = oV * kGaGranule;
+                        d_bytes = ga_entry_bytes(eK) | (ga_entry_bytes(eV) << 16);
+                    }
+                } else if (is_compressed(cur)) {
                     const uint32_t offK = (uint32_t)cm0, offV = (uint32_t)cm1;
                     const uint32_t tK = (uint32_t)(cm0 >> 32), tV = (uint32_t)(cm1 >> 32);
                     if (cur.pid < 0 || cur.pid >= P.num_meta_pages) {
@@ -380,6 +407,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
         const PageLoc L = locate(pref, B, hkv, x);
         const int64_t send = min(hi, unit_end(pref, hkv, L));
         const int64_t cnt = send - x;
+        const uint8_t *ga_row = kGa ? P.ga_bases + (size_t)L.kvh * 512 : nullptr;  // K b3 row; V at +256
 
         // queries of this segment: B operand of QK^T, column n = head n % 4 (zero if >= G)
         uint32_t qf[8][2];
@@ -412,13 +440,31 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
             const int s = (int)(i % kStages);
             const int64_t fill = i / kStages;
             if (ok) ok = mbar_wait(sbase + Smem::full + 8 * s, (uint32_t)(fill & 1), P.status);
+            ok = __all_sync(0xffffffffu, ok);  // warp-uniform: the page body uses warp collectives
             const StageInfo inf = info[s];
             if (ok && inf.kind != kKindSkip) {
                 const uint8_t *st = smem + Smem::stage + s * kStageBytes;
                 const uint32_t sta = sbase + Smem::stage + s * kStageBytes;
                 // ---- S^T = K Q^T over the page's 16 tokens ----
                 float sc[4] = {0.f, 0.f, 0.f, 0.f};
-                if (kCompressed && inf.kind == kKindPair) {
+                if (kGa && inf.kind == kKindPair && !inf.tagsK) {
+                    GaLane gs = ga_lane_load(st, lane);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t a0[4], a1[4];
+                        ga_block_frags<false>(st, ga_row, gs, lane, j, a0, a1);
+                        mma_bf16_16816(sc, a0, qf[2 * j][0], qf[2 * j][1]);
+                        mma_bf16_16816(sc, a1, qf[2 * j + 1][0], qf[2 * j + 1][1]);
+                    }
+                } else if (kGa && inf.kind == kKindPair) {  // raw tile: 4 raw 1024-byte blocks
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t a0[4], a1[4];
+                        block_frags(st + 1024 * j, 0xFFu, lane, a0, a1);
+                        mma_bf16_16816(sc, a0, qf[2 * j][0], qf[2 * j][1]);
+                        mma_bf16_16816(sc, a1, qf[2 * j + 1][0], qf[2 * j + 1][1]);
+                    }
+                } else if (!kGa && kCompressed && inf.kind == kKindPair) {
                     uint32_t off = 0;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -486,7 +532,25 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                 const uint32_t pb0 = movmatrix_trans(pack_bf16x2(v0, v1));  // tokens 0..7
                 const uint32_t pb1 = movmatrix_trans(pack_bf16x2(v2, v3));  // tokens 8..15
                 // ---- O^T += V^T P^T ----
-                if (kCompressed && inf.kind == kKindPair) {
+                if (kGa && inf.kind == kKindPair && !inf.tagsV) {
+                    const uint8_t *tv = st + 4096;
+                    GaLane gs = ga_lane_load(tv, lane);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t a0[4], a1[4];
+                        ga_block_frags<true>(tv, ga_row + 256, gs, lane, j, a0, a1);
+                        mma_bf16_16816(o[2 * j], a0, pb0, pb1);
+                        mma_bf16_16816(o[2 * j + 1], a1, pb0, pb1);
+                    }
+                } else if (kGa && inf.kind == kKindPair) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t a0[4], a1[4];
+                        block_frags(st + 4096 + 1024 * j, 0xFFu, lane, a0, a1);
+                        mma_bf16_16816(o[2 * j], a0, pb0, pb1);
+                        mma_bf16_16816(o[2 * j + 1], a1, pb0, pb1);
+                    }
+                } else if (!kGa && kCompressed && inf.kind == kKindPair) {
                     uint32_t off = 4096;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -654,15 +718,14 @@ __global__ void __launch_bounds__(128) k_attn_merge(const AttnParams P)
 // ---------------------------------------------------------------------------------
 int attn_smem_bytes(int batch) { return Smem::bytes(batch); }
 
-template <bool kCompressed>
+template <int kFmt>
 static cudaError_t configure(int dev)
 {
     // per process and device: allow the full shared-memory carve-out (attributes are per function)
     static unsigned long long done = 0;  // bit per device ordinal < 64
     if (dev < 64 && (__atomic_load_n(&done, __ATOMIC_ACQUIRE) >> dev) & 1ull) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(k_attn<kCompressed>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_attn<kCompressed>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    cudaError_t e = cudaFuncSetAttribute(k_attn<kFmt>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn<kFmt>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     // the merge runs between attention launches: same carve-out, no reconfiguration
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn_merge, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e == cudaSuccess && dev < 64) __atomic_fetch_or(&done, 1ull << dev, __ATOMIC_ACQ_REL);
@@ -671,36 +734,44 @@ static cudaError_t configure(int dev)
 
 cudaError_t attn_ctas_per_sm(int batch, int *out)
 {
+    // the same split for every format: the smallest occupancy of the three kernels
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = configure<true>(dev);
-    if (e == cudaSuccess) e = configure<false>(dev);
-    int a = 0, b = 0;
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, k_attn<true>, kThreads, Smem::bytes(batch));
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_attn<false>, kThreads, Smem::bytes(batch));
-    *out = e == cudaSuccess ? (a < b ? a : b) : 0;
+    if (e == cudaSuccess) e = configure<kFmtRaw>(dev);
+    if (e == cudaSuccess) e = configure<kFmtZf>(dev);
+    if (e == cudaSuccess) e = configure<kFmtGa>(dev);
+    int a = 0, b = 0, c = 0;
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, k_attn<kFmtRaw>, kThreads, Smem::bytes(batch));
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_attn<kFmtZf>, kThreads, Smem::bytes(batch));
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, k_attn<kFmtGa>, kThreads, Smem::bytes(batch));
+    *out = e == cudaSuccess ? min(a, min(b, c)) : 0;
     return e;
 }
 
-template <bool kCompressed>
+template <int kFmt>
 static cudaError_t launch_impl(const AttnParams &P, const void *tmap, cudaStream_t stream)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = configure<kCompressed>(dev);
+    if (e == cudaSuccess) e = configure<kFmt>(dev);
     if (e != cudaSuccess) return e;
     CUtensorMap map;
     memcpy(&map, tmap, sizeof(map));
-    k_attn<kCompressed><<<P.grid, kThreads, Smem::bytes(P.batch), stream>>>(P, map);
+    k_attn<kFmt><<<P.grid, kThreads, Smem::bytes(P.batch), stream>>>(P, map);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     k_attn_merge<<<P.batch * P.hkv, 128, 0, stream>>>(P);
     return cudaGetLastError();
 }
 
-cudaError_t launch_attention(const AttnParams &P, bool compressed, const void *tmap, cudaStream_t stream)
+cudaError_t launch_attention(const AttnParams &P, int format, const void *tmap, cudaStream_t stream)
 {
-    return compressed ? launch_impl<true>(P, tmap, stream) : launch_impl<false>(P, tmap, stream);
+    switch (format) {
+    case kFmtRaw: return launch_impl<kFmtRaw>(P, tmap, stream);
+    case kFmtZf: return launch_impl<kFmtZf>(P, tmap, stream);
+    case kFmtGa: return launch_impl<kFmtGa>(P, tmap, stream);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace kvz

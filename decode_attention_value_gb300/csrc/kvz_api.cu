@@ -1,6 +1,6 @@
 // kvz_api.cu -- the C ABI (include/kvz.h): host-side argument checks, launch
 // configuration and the TMA tensor map for raw pages.  All compute runs in the
-// kernels of codec.cu and attention.cu; nothing here touches device data.
+// kernels of codec.cu, ga_codec.cu and attention.cu; nothing here touches device data.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -118,13 +118,20 @@ int check_attention_common(const kvz_dims &d, int batch, int hq, const void *q, 
     return KVZ_OK;
 }
 
-int run_attention(bool compressed, const kvz_dims &d, int batch, int hq, const void *q, const int32_t *page_ids,
-                  int max_pages, const int32_t *seq_lens, const int32_t *tail_page, const uint64_t *meta,
-                  int64_t num_meta_pages, const uint8_t *arena, uint64_t arena_bytes, const void *raw_pool,
-                  int64_t num_raw_pages, float *out, void *ws, size_t ws_bytes, uint32_t *status, cudaStream_t stream)
+struct FormatArgs {
+    int format;  // AttnFormat
+    const uint64_t *meta;
+    const uint32_t *meta32;
+    const uint8_t *ga_bases;
+};
+
+int run_attention(const FormatArgs &F, const kvz_dims &d, int batch, int hq, const void *q, const int32_t *page_ids,
+                  int max_pages, const int32_t *seq_lens, const int32_t *tail_page, int64_t num_meta_pages,
+                  const uint8_t *arena, uint64_t arena_bytes, const void *raw_pool, int64_t num_raw_pages, float *out,
+                  void *ws, size_t ws_bytes, uint32_t *status, cudaStream_t stream)
 {
     const int hkv = d.num_kv_heads;
-    const int table_pages = compressed ? max_pages + 1 : max_pages;
+    const int table_pages = F.format != kFmtRaw ? max_pages + 1 : max_pages;
     int grid = 0;
     int rc = attention_grid(batch, hkv, table_pages, &grid);
     if (rc) return rc;
@@ -144,7 +151,9 @@ int run_attention(bool compressed, const kvz_dims &d, int batch, int hq, const v
     P.page_ids = page_ids;
     P.seq_lens = seq_lens;
     P.tail_page = tail_page;
-    P.meta = meta;
+    P.meta = F.meta;
+    P.meta32 = F.meta32;
+    P.ga_bases = F.ga_bases;
     P.num_meta_pages = num_meta_pages;
     P.arena = arena;
     P.arena_bytes = arena_bytes;
@@ -159,7 +168,7 @@ int run_attention(bool compressed, const kvz_dims &d, int batch, int hq, const v
     P.part_ml = reinterpret_cast<float *>(w);
     P.status = status;
     P.scale_log2 = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e) / sqrt(128)
-    cudaError_t e = launch_attention(P, compressed, &map, stream);
+    cudaError_t e = launch_attention(P, F.format, &map, stream);
     return e == cudaSuccess ? KVZ_OK : fail_cuda(e);
 }
 
@@ -239,6 +248,7 @@ int kvz_encode_pages(kvz_dims dims, const void *raw_pool, int64_t num_raw_pages,
     if ((int64_t)n * dims.num_kv_heads > (int64_t)1 << 30) return KVZ_ERR_UNSUPPORTED;
     if (workspace_bytes < kvz_encode_workspace_size(dims, n)) return KVZ_ERR_WORKSPACE;
     EncodeParams P;
+    memset(&P, 0, sizeof P);
     P.hkv = dims.num_kv_heads;
     P.n = n;
     P.raw_pool = static_cast<const uint16_t *>(raw_pool);
@@ -275,6 +285,7 @@ int kvz_decode_blocks(kvz_dims dims, const uint64_t *meta, int64_t num_meta_page
         return KVZ_ERR_ALIGNMENT;
     if ((int64_t)n * dims.num_kv_heads > (int64_t)1 << 30) return KVZ_ERR_UNSUPPORTED;
     DecodeParams P;
+    memset(&P, 0, sizeof P);
     P.hkv = dims.num_kv_heads;
     P.n = n;
     P.meta = meta;
@@ -308,9 +319,9 @@ int kvz_decode_attention(kvz_dims dims, int32_t batch, int32_t num_q_heads, cons
     if (rc || batch == 0) return rc;
     if (!tail_page || !meta || !arena || num_meta_pages < 0) return KVZ_ERR_INVALID_ARG;
     if (!aligned(meta, 16) || !aligned(arena, 256) || !aligned(tail_page, 4)) return KVZ_ERR_ALIGNMENT;
-    return run_attention(true, dims, batch, num_q_heads, q, page_ids, max_pages, seq_lens, tail_page, meta,
-                         num_meta_pages, arena, arena_bytes, raw_pool, num_raw_pages, out, workspace,
-                         workspace_bytes, status, reinterpret_cast<cudaStream_t>(stream));
+    return run_attention(FormatArgs{kFmtZf, meta, nullptr, nullptr}, dims, batch, num_q_heads, q, page_ids,
+                         max_pages, seq_lens, tail_page, num_meta_pages, arena, arena_bytes, raw_pool, num_raw_pages,
+                         out, workspace, workspace_bytes, status, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int kvz_decode_attention_raw(kvz_dims dims, int32_t batch, int32_t num_q_heads, const void *q,
@@ -321,9 +332,9 @@ int kvz_decode_attention_raw(kvz_dims dims, int32_t batch, int32_t num_q_heads, 
     int rc = check_attention_common(dims, batch, num_q_heads, q, seq_lens, raw_pool, num_raw_pages, out, workspace,
                                     status, max_pages, page_ids);
     if (rc || batch == 0) return rc;
-    return run_attention(false, dims, batch, num_q_heads, q, page_ids, max_pages, seq_lens, nullptr, nullptr, 0,
-                         nullptr, 0, raw_pool, num_raw_pages, out, workspace, workspace_bytes, status,
-                         reinterpret_cast<cudaStream_t>(stream));
+    return run_attention(FormatArgs{kFmtRaw, nullptr, nullptr, nullptr}, dims, batch, num_q_heads, q, page_ids,
+                         max_pages, seq_lens, nullptr, 0, nullptr, 0, raw_pool, num_raw_pages, out, workspace,
+                         workspace_bytes, status, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int kvz_decode_attention_noalloc(kvz_dims dims, int32_t batch, int32_t num_q_heads, const void *q,
@@ -346,9 +357,114 @@ int kvz_decode_attention_noalloc(kvz_dims dims, int32_t batch, int32_t num_q_hea
     rc = attention_grid(batch, dims.num_kv_heads, max_pages + 1, &grid);
     if (rc) return rc;
     if (attn_ws_bytes(batch, dims.num_kv_heads, grid) > (size_t)KVZ_NOALLOC_SCRATCH_BYTES) return KVZ_ERR_NOALLOC_LIMIT;
-    return run_attention(true, dims, batch, num_q_heads, q, page_ids, max_pages, seq_lens, tail_page, meta,
-                         num_meta_pages, arena, arena_bytes, raw_pool, num_raw_pages, out, scratch,
-                         KVZ_NOALLOC_SCRATCH_BYTES, status, reinterpret_cast<cudaStream_t>(stream));
+    return run_attention(FormatArgs{kFmtZf, meta, nullptr, nullptr}, dims, batch, num_q_heads, q, page_ids,
+                         max_pages, seq_lens, tail_page, num_meta_pages, arena, arena_bytes, raw_pool, num_raw_pages,
+                         out, scratch, KVZ_NOALLOC_SCRATCH_BYTES, status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------------------------
+// group-adaptive additive tiles
+// ---------------------------------------------------------------------------------
+int kvz_ga_calibrate(kvz_dims dims, const void *raw_pool, int64_t num_raw_pages, const int32_t *pages, int32_t n,
+                     uint8_t *bases, uint32_t *status, kvz_stream_t stream)
+{
+    if (!dims_ok(dims)) return dims.num_kv_heads >= 1 ? KVZ_ERR_UNSUPPORTED : KVZ_ERR_INVALID_ARG;
+    if (n < 0 || num_raw_pages < 0) return KVZ_ERR_INVALID_ARG;
+    if (!bases || !status || (n > 0 && (!raw_pool || !pages))) return KVZ_ERR_INVALID_ARG;
+    if (!aligned(raw_pool, 16) || !aligned(pages, 4) || !aligned(status, 4)) return KVZ_ERR_ALIGNMENT;
+    if ((int64_t)n * kPage >= (int64_t)1 << 40 || dims.num_kv_heads > (1 << 20)) return KVZ_ERR_UNSUPPORTED;
+    cudaError_t e = launch_ga_calibrate(dims.num_kv_heads, static_cast<const uint16_t *>(raw_pool), num_raw_pages,
+                                        pages, n, bases, status, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KVZ_OK : fail_cuda(e);
+}
+
+int kvz_ga_encode_pages(kvz_dims dims, const void *raw_pool, int64_t num_raw_pages, const uint8_t *bases,
+                        const int32_t *src_page, const int32_t *dst_page, const int32_t *dst_seq, int32_t n,
+                        uint32_t *meta, int64_t num_meta_pages, uint8_t *arena, uint64_t arena_bytes,
+                        uint32_t *cursors, int32_t num_cursors, void *workspace, size_t workspace_bytes,
+                        uint32_t *status, kvz_stream_t stream)
+{
+    if (!dims_ok(dims)) return dims.num_kv_heads >= 1 ? KVZ_ERR_UNSUPPORTED : KVZ_ERR_INVALID_ARG;
+    if (n < 0 || num_raw_pages < 0 || num_meta_pages < 0 || num_cursors < 0) return KVZ_ERR_INVALID_ARG;
+    if (n == 0) return KVZ_OK;
+    if (!raw_pool || !bases || !src_page || !dst_page || !dst_seq || !meta || !arena || !cursors || !workspace ||
+        !status)
+        return KVZ_ERR_INVALID_ARG;
+    if (!aligned(raw_pool, 16) || !aligned(bases, 16) || !aligned(meta, 8) || !aligned(arena, 64) ||
+        !aligned(cursors, 8) || !aligned(workspace, 16) || !aligned(status, 4))
+        return KVZ_ERR_ALIGNMENT;
+    if ((int64_t)n * dims.num_kv_heads > (int64_t)1 << 30) return KVZ_ERR_UNSUPPORTED;
+    if (workspace_bytes < kvz_encode_workspace_size(dims, n)) return KVZ_ERR_WORKSPACE;
+    EncodeParams P;
+    memset(&P, 0, sizeof P);
+    P.hkv = dims.num_kv_heads;
+    P.n = n;
+    P.raw_pool = static_cast<const uint16_t *>(raw_pool);
+    P.num_raw_pages = num_raw_pages;
+    P.src_page = src_page;
+    P.dst_page = dst_page;
+    P.dst_seq = dst_seq;
+    P.meta32 = meta;
+    P.ga_bases = bases;
+    P.num_meta_pages = num_meta_pages;
+    P.arena = arena;
+    P.arena_bytes = arena_bytes;
+    P.cursors = cursors;
+    P.num_cursors = num_cursors;
+    P.status = status;
+    uint8_t *w = static_cast<uint8_t *>(workspace);
+    const size_t a = ((size_t)n * 4 + 15) / 16 * 16;
+    P.ws_hdr = reinterpret_cast<uint32_t *>(w);
+    P.ws_page_size = reinterpret_cast<uint32_t *>(w + 16);
+    P.ws_page_base = reinterpret_cast<uint32_t *>(w + 16 + a);
+    P.ws_pair_size = reinterpret_cast<uint32_t *>(w + 16 + 2 * a);
+    cudaError_t e = launch_ga_encode(P, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KVZ_OK : fail_cuda(e);
+}
+
+int kvz_ga_decode_blocks(kvz_dims dims, const uint32_t *meta, int64_t num_meta_pages, const uint8_t *arena,
+                         uint64_t arena_bytes, const uint8_t *bases, const int32_t *page, int32_t n, void *out_pages,
+                         uint32_t *status, kvz_stream_t stream)
+{
+    if (!dims_ok(dims)) return dims.num_kv_heads >= 1 ? KVZ_ERR_UNSUPPORTED : KVZ_ERR_INVALID_ARG;
+    if (n < 0 || num_meta_pages < 0) return KVZ_ERR_INVALID_ARG;
+    if (n == 0) return KVZ_OK;
+    if (!meta || !arena || !bases || !page || !out_pages || !status) return KVZ_ERR_INVALID_ARG;
+    if (!aligned(meta, 4) || !aligned(arena, 64) || !aligned(out_pages, 16) || !aligned(status, 4))
+        return KVZ_ERR_ALIGNMENT;
+    if ((int64_t)n * dims.num_kv_heads > (int64_t)1 << 30) return KVZ_ERR_UNSUPPORTED;
+    DecodeParams P;
+    memset(&P, 0, sizeof P);
+    P.hkv = dims.num_kv_heads;
+    P.n = n;
+    P.meta32 = meta;
+    P.ga_bases = bases;
+    P.num_meta_pages = num_meta_pages;
+    P.arena = arena;
+    P.arena_bytes = arena_bytes;
+    P.page = page;
+    P.out = static_cast<uint16_t *>(out_pages);
+    P.status = status;
+    cudaError_t e = launch_ga_decode(P, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KVZ_OK : fail_cuda(e);
+}
+
+int kvz_ga_decode_attention(kvz_dims dims, int32_t batch, int32_t num_q_heads, const void *q,
+                            const int32_t *page_ids, int32_t max_pages, const int32_t *seq_lens,
+                            const int32_t *tail_page, const uint32_t *meta, int64_t num_meta_pages,
+                            const uint8_t *arena, uint64_t arena_bytes, const uint8_t *bases, const void *raw_pool,
+                            int64_t num_raw_pages, float *out, void *workspace, size_t workspace_bytes,
+                            uint32_t *status, kvz_stream_t stream)
+{
+    int rc = check_attention_common(dims, batch, num_q_heads, q, seq_lens, raw_pool, num_raw_pages, out, workspace,
+                                    status, max_pages, page_ids);
+    if (rc || batch == 0) return rc;
+    if (!tail_page || !meta || !arena || !bases || num_meta_pages < 0) return KVZ_ERR_INVALID_ARG;
+    if (!aligned(meta, 8) || !aligned(arena, 64) || !aligned(tail_page, 4) || !aligned(bases, 2))
+        return KVZ_ERR_ALIGNMENT;
+    return run_attention(FormatArgs{kFmtGa, nullptr, meta, bases}, dims, batch, num_q_heads, q, page_ids, max_pages,
+                         seq_lens, tail_page, num_meta_pages, arena, arena_bytes, raw_pool, num_raw_pages, out,
+                         workspace, workspace_bytes, status, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int kvz_apply_cursor_updates(const int32_t *idx, const uint32_t *pos, const uint32_t *end, int32_t n,

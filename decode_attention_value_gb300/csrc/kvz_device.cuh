@@ -189,6 +189,13 @@ __device__ __forceinline__ void ld_keep_u64x2(const uint64_t *p, uint64_t policy
     asm volatile("ld.global.L2::cache_hint.v2.b64 {%0, %1}, [%2], %3;" : "=l"(a), "=l"(b) : "l"(p), "l"(policy));
 }
 
+__device__ __forceinline__ uint64_t ld_keep_u64(const uint64_t *p, uint64_t policy)
+{
+    uint64_t v;
+    asm volatile("ld.global.L2::cache_hint.b64 %0, [%1], %2;" : "=l"(v) : "l"(p), "l"(policy));
+    return v;
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const void *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");

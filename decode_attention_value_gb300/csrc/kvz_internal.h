@@ -22,6 +22,9 @@ struct EncodeParams {
     uint32_t *cursors;
     int num_cursors;
     uint32_t *status;
+    // group-adaptive tiles: 4-byte entries instead of meta, bases [hkv][2][2][128]
+    uint32_t *meta32;
+    const uint8_t *ga_bases;
     // workspace
     uint32_t *ws_hdr;        // [4]: validation failure bits (zeroed each call)
     uint32_t *ws_page_size;  // [n] granules per page, summed over heads (zeroed each call)
@@ -45,6 +48,8 @@ struct DecodeParams {
     const int32_t *page;
     uint16_t *out;
     uint32_t *status;
+    const uint32_t *meta32;  // group-adaptive tiles
+    const uint8_t *ga_bases;
 };
 
 // Attention work split: grid = C CTAs over the flattened (sequence, KV head, page)
@@ -59,6 +64,8 @@ struct AttnParams {
     const uint16_t *q;
     const int32_t *page_ids, *seq_lens, *tail_page;
     const uint64_t *meta;
+    const uint32_t *meta32;   // group-adaptive tiles: entries
+    const uint8_t *ga_bases;  // group-adaptive tiles: [hkv][2][2][128]
     int64_t num_meta_pages;
     const uint8_t *arena;
     uint64_t arena_bytes;
@@ -83,12 +90,20 @@ inline size_t attn_ws_bytes(int batch, int hkv, int grid)
 }
 
 cudaError_t launch_encode(const EncodeParams &P, cudaStream_t stream);
+cudaError_t launch_enc_validate(const EncodeParams &P, cudaStream_t stream);
+cudaError_t launch_enc_scan(const EncodeParams &P, cudaStream_t stream);
+cudaError_t launch_ga_encode(const EncodeParams &P, cudaStream_t stream);
+cudaError_t launch_ga_decode(const DecodeParams &P, cudaStream_t stream);
+cudaError_t launch_ga_calibrate(int hkv, const uint16_t *raw_pool, int64_t num_raw_pages, const int32_t *pages, int n,
+                                uint8_t *bases, uint32_t *status, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams &P, cudaStream_t stream);
 cudaError_t launch_apply_cursor_updates(const int32_t *idx, const uint32_t *pos, const uint32_t *end, int n,
                                         uint32_t *cursors, int num_cursors, cudaStream_t stream);
 // tmap: a CUtensorMap (128-byte object) over the raw pool viewed as
 // [num_raw_pages*Hkv*32 rows][128 BF16], box 64 x 32, 128-byte swizzle.
-cudaError_t launch_attention(const AttnParams &P, bool compressed, const void *tmap, cudaStream_t stream);
+// format: 0 plain BF16 pages, 1 12-bit block groups, 2 group-adaptive tiles
+enum AttnFormat : int { kFmtRaw = 0, kFmtZf = 1, kFmtGa = 2 };
+cudaError_t launch_attention(const AttnParams &P, int format, const void *tmap, cudaStream_t stream);
 int attn_smem_bytes(int batch);
 // CTAs per SM both attention kernels can hold at this batch size (the smaller of the two)
 cudaError_t attn_ctas_per_sm(int batch, int *out);

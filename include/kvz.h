@@ -203,6 +203,74 @@ int kvz_decode_attention_noalloc(kvz_dims dims, int32_t batch, int32_t num_q_hea
                                  int64_t num_raw_pages, float *out, uint32_t *status, kvz_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
+ * Group-adaptive additive tiles: a second compressed format, from the page "GAAC:
+ * Lossless KV Compression for Bandwidth-Efficient LLM Inference on Personal Devices"
+ * (section "Lossless KV Compression": "Contiguous exponent concentration" and
+ * "Group-adaptive additive coding"; Table 9 "Storage"; "Block-Wise Compression
+ * Scheduling" for the two storage classes and the 4-byte block-table entry).
+ *
+ *  bases      uint8 [Hkv][2][2][128] per layer: (head, K|V, b3|b4, channel); b3 is the
+ *             start of the 8-exponent window, b4 of the 16-exponent window.
+ *  tile       one (page, head, K|V) slice of 2048 values in the storage order above;
+ *             group q = 8L + 2j + f is the 8 elements (L, f, i) of block j.  A group
+ *             takes mode 0 if every e - b3[channel] is in [0,8), else mode 1 if every
+ *             e - b4[channel] is in [0,16), else mode 2 (code = e).  Layout (3008 B):
+ *               [0,2048)    sign<<7 | fraction of element (L,f,i) of block j at
+ *                           512j + 16L + 8f + i
+ *               [2048,2816) 3-bit codes, group q at 2048+3q, element i at bits 3i..3i+2
+ *               [2816,2880) 2-bit modes, group q at byte 2816+q/4, bits 2(q%4)
+ *               [2880,3008) escape bytes of the mode-1 (1 byte: bit i = bit 3 of code
+ *                           i) and mode-2 (5 bytes: bits 3..7 of code i at 5i..5i+4)
+ *                           groups in q order, then zeros
+ *             A tile needing more than 128 escape bytes is kept raw: 4096 bytes, BF16
+ *             words in storage order (the 4 blocks of a raw 12-bit group).
+ *  meta32     uint32 [num_meta_pages][Hkv][2] entries: bits 0..30 = tile offset in
+ *             64-byte granules from the arena base, bit 31 = raw tile;
+ *             KVZ_GA_ENTRY_INVALID = not written.
+ *  arena      64-byte aligned; cursors count 64-byte granules (47 per compressed tile,
+ *             64 per raw tile).  Offsets above 2^31-1 granules are not representable:
+ *             space beyond 128 GiB of one arena is never used.
+ * --------------------------------------------------------------------------------- */
+#define KVZ_GA_GRANULE_BYTES 64
+#define KVZ_GA_TILE_BYTES 3008
+#define KVZ_GA_RAW_TILE_BYTES 4096
+#define KVZ_GA_ENTRY_RAW 0x80000000u
+#define KVZ_GA_ENTRY_INVALID 0xFFFFFFFFu
+
+/* kvz_ga_calibrate -- window bases of one layer ("Contiguous exponent concentration":
+ * per head-channel pair and separately for K and V, the 8- and 16-wide exponent windows
+ * that cover the most sample values; ties go to the lowest start).
+ *  pages[n]   raw page ids of the sample (device int32); bases: uint8 [Hkv][2][2][128]
+ * A sample page id out of range is skipped (KVZ_STATUS_BAD_INDEX).  n = 0 gives zeros. */
+int kvz_ga_calibrate(kvz_dims dims, const void *raw_pool, int64_t num_raw_pages, const int32_t *pages,
+                     int32_t n, uint8_t *bases, uint32_t *status, kvz_stream_t stream);
+
+/* kvz_ga_encode_pages -- kvz_encode_pages for tiles: same arguments, placement and
+ * error behaviour, with `bases` (16-B aligned) and uint32 entries (8-B aligned) in
+ * 64-byte granules.  workspace: kvz_encode_workspace_size(dims, n). */
+int kvz_ga_encode_pages(kvz_dims dims, const void *raw_pool, int64_t num_raw_pages, const uint8_t *bases,
+                        const int32_t *src_page, const int32_t *dst_page, const int32_t *dst_seq, int32_t n,
+                        uint32_t *meta, int64_t num_meta_pages, uint8_t *arena, uint64_t arena_bytes,
+                        uint32_t *cursors, int32_t num_cursors, void *workspace, size_t workspace_bytes,
+                        uint32_t *status, kvz_stream_t stream);
+
+/* kvz_ga_decode_blocks -- kvz_decode_blocks for tiles (bit-exact BF16 pages). */
+int kvz_ga_decode_blocks(kvz_dims dims, const uint32_t *meta, int64_t num_meta_pages, const uint8_t *arena,
+                         uint64_t arena_bytes, const uint8_t *bases, const int32_t *page, int32_t n,
+                         void *out_pages, uint32_t *status, kvz_stream_t stream);
+
+/* kvz_ga_decode_attention -- kvz_decode_attention over tiles (GAAC "Attention with
+ * On-the-Fly Decompression"): same arguments with uint32 entries and `bases`; same
+ * workspace, work split and determinism (bit-identical to kvz_decode_attention_raw on
+ * the same data). */
+int kvz_ga_decode_attention(kvz_dims dims, int32_t batch, int32_t num_q_heads, const void *q,
+                            const int32_t *page_ids, int32_t max_pages, const int32_t *seq_lens,
+                            const int32_t *tail_page, const uint32_t *meta, int64_t num_meta_pages,
+                            const uint8_t *arena, uint64_t arena_bytes, const uint8_t *bases,
+                            const void *raw_pool, int64_t num_raw_pages, float *out, void *workspace,
+                            size_t workspace_bytes, uint32_t *status, kvz_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
  * Host-side chunk allocator for the arena (GAAC "Block-Wise Compression Scheduling":
  * two fixed storage classes, 768-byte and 1024-byte block slots; ZipFusion: the memory
  * manager tracks the space left, hands chunks freed by one layer or sequence to
