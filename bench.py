@@ -616,8 +616,8 @@ class GaCopies:
         self.bases = torch.zeros((hkv, 2, 2, 128), dtype=torch.uint8, device=dev)
         self.sample = W.src[::sample_step].contiguous()
         kvz.ga_calibrate(W.pools[0], self.sample, self.bases, W.status)
-        per = max(cfg.full_pages, 1) * hkv * 2 * 64
-        self.arena_bytes = B * per * 64
+        per = max(cfg.full_pages, 1) * hkv * 2 * (4096 // kvz.GA_GRANULE)  # granules: worst case per sequence
+        self.arena_bytes = B * per * kvz.GA_GRANULE
         self.cursor0 = torch.tensor([[b * per, (b + 1) * per] for b in range(B)], dtype=torch.int32, device=dev)
         self.metas, self.arenas = [], []
         for c in range(W.copies):

@@ -449,10 +449,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                 float sc[4] = {0.f, 0.f, 0.f, 0.f};
                 if (kGa && inf.kind == kKindPair && !inf.tagsK) {
                     GaLane gs = ga_lane_load(st, lane);
+                    const bool any2 = ga_tile_any_raw_groups(gs);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         uint32_t a0[4], a1[4];
-                        ga_block_frags<false>(st, ga_row, gs, lane, j, a0, a1);
+                        ga_block_frags<false>(st, ga_row, gs, any2, lane, j, a0, a1);
                         mma_bf16_16816(sc, a0, qf[2 * j][0], qf[2 * j][1]);
                         mma_bf16_16816(sc, a1, qf[2 * j + 1][0], qf[2 * j + 1][1]);
                     }
@@ -535,10 +536,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                 if (kGa && inf.kind == kKindPair && !inf.tagsV) {
                     const uint8_t *tv = st + 4096;
                     GaLane gs = ga_lane_load(tv, lane);
+                    const bool any2 = ga_tile_any_raw_groups(gs);
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         uint32_t a0[4], a1[4];
-                        ga_block_frags<true>(tv, ga_row + 256, gs, lane, j, a0, a1);
+                        ga_block_frags<true>(tv, ga_row + 256, gs, any2, lane, j, a0, a1);
                         mma_bf16_16816(o[2 * j], a0, pb0, pb1);
                         mma_bf16_16816(o[2 * j + 1], a1, pb0, pb1);
                     }

@@ -66,36 +66,79 @@ __device__ __forceinline__ uint32_t ga_lane_escape_base(uint32_t modes16, int la
 
 // Per-element bases of one group as two byte vectors (elements 0..3, 4..7).
 // K: element i is channel 32j+16f + 2t + i%2 + 8(i/4); V: channel 32j+16f + g + 8((i/2)%2).
-// row: this head's b3 row (b4 row = row + 128) for this K|V.  Mode 2 has base 0.
+// row: this head's b3 row (b4 row = row + 128) for this K|V; w = 0 (b3) or 1 (b4).
 template <bool kV>
-__device__ __forceinline__ void ga_bases(const uint8_t *row, uint32_t mode, int lane, int j, int f, uint32_t &b0,
+__device__ __forceinline__ void ga_bases(const uint8_t *row, uint32_t w, int lane, int j, int f, uint32_t &b0,
                                          uint32_t &b1)
 {
-    b0 = b1 = 0;
-    if (mode < 2) {
-        const uint8_t *r = row + mode * 128 + 32 * j + 16 * f;
-        if (!kV) {
-            const int c = 2 * (lane & 3);
-            const uint32_t x = __ldg(reinterpret_cast<const uint16_t *>(r + c));
-            const uint32_t y = __ldg(reinterpret_cast<const uint16_t *>(r + c + 8));
-            b0 = __byte_perm(x, 0, 0x1010);
-            b1 = __byte_perm(y, 0, 0x1010);
-        } else {
-            const int g = lane >> 2;
-            const uint32_t x = __ldg(r + g), y = __ldg(r + g + 8);
-            b0 = b1 = __byte_perm(x, y, 0x4400);
-        }
+    const uint8_t *r = row + w * 128 + 32 * j + 16 * f;
+    if (!kV) {
+        const int c = 2 * (lane & 3);
+        const uint32_t x = __ldg(reinterpret_cast<const uint16_t *>(r + c));
+        const uint32_t y = __ldg(reinterpret_cast<const uint16_t *>(r + c + 8));
+        b0 = x * 0x00010001u;  // [x0 x1 x0 x1]: multiplies run beside the byte ops
+        b1 = y * 0x00010001u;
+    } else {
+        const int g = lane >> 2;
+        const uint32_t x = __ldg(r + g), y = __ldg(r + g + 8);
+        b0 = b1 = (x + y * 0x10000u) * 0x0101u;  // [x x y y]
     }
 }
 
-// Restore one group: sf0/sf1 = sign/fraction bytes of elements 0..3 / 4..7, code =
-// 24-bit field, esc = pointer to the tile's escape area, off = running offset of this
-// lane's next escape byte.  Writes the four bf16x2 fragment registers.
+// Exponent bytes + sign/fraction bytes -> the four bf16x2 fragment registers.
+__device__ __forceinline__ void ga_assemble(uint32_t sf0, uint32_t sf1, uint32_t e0, uint32_t e1, uint32_t (&a)[4])
+{
+    const uint32_t h0 = ((e0 >> 1) & 0x7F7F7F7Fu) | (sf0 & 0x80808080u);
+    const uint32_t l0 = ((e0 << 7) & 0x80808080u) | (sf0 & 0x7F7F7F7Fu);
+    const uint32_t h1 = ((e1 >> 1) & 0x7F7F7F7Fu) | (sf1 & 0x80808080u);
+    const uint32_t l1 = ((e1 << 7) & 0x80808080u) | (sf1 & 0x7F7F7F7Fu);
+    a[0] = __byte_perm(l0, h0, 0x5140);
+    a[1] = __byte_perm(l0, h0, 0x7362);
+    a[2] = __byte_perm(l1, h1, 0x5140);
+    a[3] = __byte_perm(l1, h1, 0x7362);
+}
+
+// Restore one group.  Modes 0 and 1 take no branch: a 3-bit group reads no escape
+// byte and adds its b3 vector, a 4-bit group adds bit 3 from its escape byte and its b4
+// vector.  Raw-exponent groups (mode 2, rare) are patched in a branch that only tiles
+// holding such groups enter (any2, warp-uniform).  sf0/sf1: sign/fraction bytes of
+// elements 0..3 / 4..7; code: 24-bit field; esc: the tile's escape area; off: running
+// offset of this lane's next escape byte.
+template <bool kV>
+__device__ __forceinline__ void ga_restore_group_fast(uint32_t sf0, uint32_t sf1, uint32_t code, uint32_t mode,
+                                                      bool any2, const uint8_t *esc, uint32_t &off,
+                                                      const uint8_t *row, int lane, int j, int f, uint32_t (&a)[4])
+{
+    const uint32_t m1 = mode & 1u;
+    uint32_t h = 0;
+    if (m1) h = esc[min(off, kGaEscCap - 1)];
+    off += m1;
+    uint32_t b0, b1;
+    ga_bases<kV>(row, m1, lane, j, f, b0, b1);
+    const uint32_t l0 = ga_spread3(code & 0xFFFu), l1 = ga_spread3((code >> 12) & 0xFFFu);
+    uint32_t c0 = l0 | ga_spread1_hi(h), c1 = l1 | ga_spread1_hi(h >> 4);
+    if (any2) {
+        if (mode >= 2) {
+            const uint8_t *p = esc + min(off, kGaEscCap - 5);
+            const uint32_t lo =
+                (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+            c0 = l0 | ga_spread5_hi(lo & 0xFFFFFu);
+            c1 = l1 | ga_spread5_hi((lo >> 20) | ((uint32_t)p[4] << 12));
+            b0 = b1 = 0;
+            off += 5;
+        }
+    }
+    ga_assemble(sf0, sf1, c0 + b0, c1 + b1, a);  // byte adds never carry (every e <= 255)
+}
+
+// Restore one group of any mode (tiles holding raw-exponent groups).
+template <bool kV>
 __device__ __forceinline__ void ga_restore_group(uint32_t sf0, uint32_t sf1, uint32_t code, uint32_t mode,
-                                                 const uint8_t *esc, uint32_t &off, uint32_t b0, uint32_t b1,
-                                                 uint32_t (&a)[4])
+                                                 const uint8_t *esc, uint32_t &off, const uint8_t *row, int lane,
+                                                 int j, int f, uint32_t (&a)[4])
 {
     uint32_t c0 = ga_spread3(code & 0xFFFu), c1 = ga_spread3((code >> 12) & 0xFFFu);
+    uint32_t b0 = 0, b1 = 0;
     if (mode == 1) {
         const uint32_t h = esc[min(off, kGaEscCap - 1)];
         c0 |= ga_spread1_hi(h);
@@ -109,15 +152,8 @@ __device__ __forceinline__ void ga_restore_group(uint32_t sf0, uint32_t sf1, uin
         c1 |= ga_spread5_hi((lo >> 20) | (hi8 << 12));
         off += 5;
     }
-    const uint32_t e0 = c0 + b0, e1 = c1 + b1;  // per byte; never carries (every e <= 255)
-    const uint32_t h0 = ((e0 >> 1) & 0x7F7F7F7Fu) | (sf0 & 0x80808080u);
-    const uint32_t l0 = ((e0 << 7) & 0x80808080u) | (sf0 & 0x7F7F7F7Fu);
-    const uint32_t h1 = ((e1 >> 1) & 0x7F7F7F7Fu) | (sf1 & 0x80808080u);
-    const uint32_t l1 = ((e1 << 7) & 0x80808080u) | (sf1 & 0x7F7F7F7Fu);
-    a[0] = __byte_perm(l0, h0, 0x5140);
-    a[1] = __byte_perm(l0, h0, 0x7362);
-    a[2] = __byte_perm(l1, h1, 0x5140);
-    a[3] = __byte_perm(l1, h1, 0x7362);
+    if (mode < 2) ga_bases<kV>(row, mode, lane, j, f, b0, b1);
+    ga_assemble(sf0, sf1, c0 + b0, c1 + b1, a);
 }
 
 // This lane's 24 code bytes (groups 8L..8L+7) as six words; group k's field.
@@ -149,27 +185,33 @@ __device__ __forceinline__ GaLane ga_lane_load(const uint8_t *tile, int lane)
     return s;
 }
 
-// Fragments of block j (both f) of a compressed tile; row = this head's b3 row.
+// Fragments of block j (both f) of a compressed tile; row = this head's b3 row;
+// any2: some lane's group of this tile has mode 2 (warp-uniform).
 template <bool kV>
-__device__ __forceinline__ void ga_block_frags(const uint8_t *tile, const uint8_t *row, GaLane &s, int lane, int j,
-                                               uint32_t (&a0)[4], uint32_t (&a1)[4])
+__device__ __forceinline__ void ga_block_frags(const uint8_t *tile, const uint8_t *row, GaLane &s, bool any2, int lane,
+                                               int j, uint32_t (&a0)[4], uint32_t (&a1)[4])
 {
     const uint4 sf = *reinterpret_cast<const uint4 *>(tile + 512 * j + 16 * lane);
     const uint8_t *esc = tile + kGaEscOff;
-    {
-        const int k = 2 * j;
-        const uint32_t mode = (s.modes >> (2 * k)) & 3u;
-        uint32_t b0, b1;
-        ga_bases<kV>(row, mode, lane, j, 0, b0, b1);
-        ga_restore_group(sf.x, sf.y, ga_code_field(s.code, k), mode, esc, s.off, b0, b1, a0);
-    }
-    {
-        const int k = 2 * j + 1;
-        const uint32_t mode = (s.modes >> (2 * k)) & 3u;
-        uint32_t b0, b1;
-        ga_bases<kV>(row, mode, lane, j, 1, b0, b1);
-        ga_restore_group(sf.z, sf.w, ga_code_field(s.code, k), mode, esc, s.off, b0, b1, a1);
-    }
+    const uint32_t m0 = (s.modes >> (4 * j)) & 3u, m1 = (s.modes >> (4 * j + 2)) & 3u;
+    ga_restore_group_fast<kV>(sf.x, sf.y, ga_code_field(s.code, 2 * j), m0, any2, esc, s.off, row, lane, j, 0, a0);
+    ga_restore_group_fast<kV>(sf.z, sf.w, ga_code_field(s.code, 2 * j + 1), m1, any2, esc, s.off, row, lane, j, 1, a1);
 }
+
+// Fragment of group k = 2j + f (any mode) with run-time k, reading the code field from
+// the tile: the compact path for tiles that hold raw-exponent groups.
+template <bool kV>
+__device__ __forceinline__ void ga_group_frag_any(const uint8_t *tile, const uint8_t *row, uint32_t modes,
+                                                  uint32_t &off, int lane, int k, uint32_t (&a)[4])
+{
+    const int j = k >> 1, f = k & 1;
+    const uint2 sf = *reinterpret_cast<const uint2 *>(tile + 512 * j + 16 * lane + 8 * f);
+    const uint8_t *c = tile + kGaCodeOff + 24 * lane + 3 * k;
+    const uint32_t code = (uint32_t)c[0] | ((uint32_t)c[1] << 8) | ((uint32_t)c[2] << 16);
+    ga_restore_group<kV>(sf.x, sf.y, code, (modes >> (2 * k)) & 3u, tile + kGaEscOff, off, row, lane, j, f, a);
+}
+
+// Whether any lane's groups of this tile use the raw-exponent mode.  Warp-collective.
+__device__ __forceinline__ bool ga_tile_any_raw_groups(const GaLane &s) { return __any_sync(0xffffffffu, s.modes & 0xAAAAu); }
 
 }  // namespace kvz

@@ -309,8 +309,13 @@ __global__ void __launch_bounds__(256) k_ga_decode(DecodeParams P)
             const uint32_t mask = (1u << (4 * j)) - 1u;  // groups k < 2j of this lane
             s.off += __popc(s.modes & 0x5555u & mask) + 5u * __popc(s.modes & 0xAAAAu & mask);
             uint32_t f0[4], f1[4];
-            if (kv == 0) ga_block_frags<false>(tile, row, s, lane, j, f0, f1);
-            else ga_block_frags<true>(tile, row, s, lane, j, f0, f1);
+            if (kv == 0) {
+                ga_group_frag_any<false>(tile, row, s.modes, s.off, lane, 2 * j, f0);
+                ga_group_frag_any<false>(tile, row, s.modes, s.off, lane, 2 * j + 1, f1);
+            } else {
+                ga_group_frag_any<true>(tile, row, s.modes, s.off, lane, 2 * j, f0);
+                ga_group_frag_any<true>(tile, row, s.modes, s.off, lane, 2 * j + 1, f1);
+            }
             w[0] = f0[0]; w[1] = f0[1]; w[2] = f0[2]; w[3] = f0[3];
             w[4] = f1[0]; w[5] = f1[1]; w[6] = f1[2]; w[7] = f1[3];
         }
