@@ -136,16 +136,18 @@ class ClockSampler:
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for rel in ("decode_attention_value_gb300/csrc/attention.cu", "decode_attention_value_gb300/csrc/kvz_device.cuh"):
+    for rel in ("decode_attention_value_gb300/csrc/attention.cu", "decode_attention_value_gb300/csrc/kvz_device.cuh",
+                "decode_attention_value_gb300/csrc/ga.cuh"):
         with open(os.path.join(ROOT, rel), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    """dram bytes per launch of the compressed attention kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
-    p = os.path.join(ROOT, "profiles", f"k_attn_compressed_{workload}.md")
+def profiled_traffic(workload: str, kernel: str = "compressed"):
+    """dram bytes per launch of an attention kernel ("compressed" = 12-bit groups,
+    "tiles" = group-adaptive tiles) from the committed ncu summary, if it was taken on
+    the current kernel source."""
+    p = os.path.join(ROOT, "profiles", f"k_attn_{kernel}_{workload}.md")
     if not os.path.exists(p):
         return None
     vals = {}
@@ -743,8 +745,8 @@ def run_ga(args, cfg, dist, rank, world, local):
         "encode_GBps": round(enc_in / (enc_ms * 1e-3) / 1e9, 2),
         "decode_GBps": round(enc_in / (dec_ms * 1e-3) / 1e9, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None, "peak_kind": peak_kind,
-                     "kernel": "k_attn<tiles> + k_attn_merge", "launch_us": round(us_g, 3),
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(args.workload, "tiles"),
+                     "peak_kind": peak_kind, "kernel": "k_attn<tiles> + k_attn_merge", "launch_us": round(us_g, 3),
                      "cold_single_launch_us": round(launch_ms * 1e3, 3),
                      "algorithmic_bytes_per_launch": GA.alg_bytes},
         "clocks": clocks,
