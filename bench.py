@@ -398,7 +398,9 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kvz", choices=["kvz", "reference"])
-    ap.add_argument("--workload", default="c1", choices=["c1", "c2", "c3", "c4"])
+    ap.add_argument("--workload", default="c1", choices=["c1", "c2", "c3", "c4", "serve"])
+    ap.add_argument("--serve-budget-gb", type=float, default=4.0, help="serve: KV budget of both caches (1e9 B)")
+    ap.add_argument("--serve-requests", type=int, default=256, help="serve: requests in the queue")
     ap.add_argument("--budget-gb", type=float, default=60.0, help="KV budget for the c3 capacity count (1e9 B)")
     ap.add_argument("--stack", action="store_true",
                     help="c2: one step = all layers of the stack, each with its own KV (else one layer per step)")
@@ -413,7 +415,7 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    cfg = kvgen.CONFIGS[args.workload]
+    cfg = kvgen.CONFIGS.get(args.workload, kvgen.C3)
     if args.workload in ("c2", "c4"):
         cfg = kvgen.KVConfig(**{**cfg.__dict__, "layers": 1})  # one layer of the 32-layer stack per step
     dist, rank, world, local = dist_setup()
@@ -421,6 +423,8 @@ def main():
         return run_sweep(args, dist, rank, local)
     if args.workload == "c3":
         return run_stream(args, cfg, dist, rank, world, local)
+    if args.workload == "serve":
+        return run_serve(args, dist, rank, world, local)
     if args.stack:
         return run_stack(args, kvgen.CONFIGS[args.workload], dist, rank, world, local)
 
@@ -751,6 +755,180 @@ def run_ga(args, cfg, dist, rank, world, local):
                      "algorithmic_bytes_per_launch": GA.alg_bytes},
         "clocks": clocks,
         "gpu_launches": 2 * K,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_serve(args, dist, rank, world, local):
+    """Toy admission loop over a fixed KV budget (GAAC "Block-Wise Compression
+    Scheduling", ZipFusion's memory manager): a FIFO queue of requests (seeded prompt and
+    generation lengths) is admitted while the cache reports room for them, each running
+    sequence gains one token per step in every layer (pages encoded as they fill,
+    attention in every layer), and finished sequences are released so their storage serves
+    the next requests.  Run twice on the same requests: compressed pages (12-bit groups in
+    recycled arena chunks) and raw pages from a slot free list, both holding the same
+    budget.  Reports decode tokens/s, mean and peak concurrency, prefill encode time and
+    preemptions."""
+    import collections
+    import dataclasses
+
+    torch.cuda.set_device(local)
+    import decode_attention_value_gb300 as kvz
+    from decode_attention_value_gb300.cache import CompressedKVCache, OutOfSpace, RawKVCache
+
+    dev = torch.device("cuda", local)
+    L, hkv, hq = 8, 8, 32
+    cfg = dataclasses.replace(kvgen.C1, layers=L, seed=77)
+    rng = np.random.default_rng(77)
+    N = args.serve_requests
+    reqs = [(int(rng.integers(512, 2049)), int(rng.integers(64, 257))) for _ in range(N)]
+    max_pages = (2048 + 256) // 16 + 1
+    max_seqs = 192  # slots (tail pages, meta rows); concurrency stays below
+    budget = int(args.serve_budget_gb * 1e9)
+    page_layer_raw = hkv * 2 * 16 * 128 * 2  # one page of one layer, BF16
+    sig = [kvgen.channel_sigmas(cfg, layer, dev) for layer in range(L)]
+    qs = [torch.randn((max_seqs, hq, 128), device=dev).to(torch.bfloat16) for _ in range(L)]
+    out = torch.empty((max_seqs, hq, 128), dtype=torch.float32, device=dev)
+
+    def pages_of(r):
+        return (r[0] + r[1] + 15) // 16
+
+    def run(kind):
+        if kind == "compressed":
+            tails_bytes = L * max_seqs * page_layer_raw
+            meta_bytes = L * max_seqs * max_pages * hkv * 16
+            chunk = 8192  # granules of 256 B = 2 MiB
+            arena = (budget - tails_bytes - meta_bytes) // (chunk * 256) * (chunk * 256)
+            cache = CompressedKVCache(L, hkv, max_seqs, max_pages, arena, chunk_granules=chunk, device=dev)
+        else:
+            cache = RawKVCache(L, hkv, max_seqs, max_pages, budget // (L * page_layer_raw), device=dev)
+        ws = cache.workspace(max_seqs, hq)
+        queue = collections.deque(range(N))
+        running = {}  # slot -> [request id, tokens generated]
+        free = list(range(max_seqs - 1, -1, -1))
+        order = []  # running slots in admission order (newest last)
+        gen_rng = torch.Generator(device=dev)
+        gen_rng.manual_seed(1234)
+        t_decode = t_prefill = t_attn = 0.0
+        tokens = steps = preempt = peak = 0
+        conc = []
+
+        def worst_left(slot):
+            rid, done = running[slot]
+            return pages_of(reqs[rid]) - (reqs[rid][0] + done) // 16
+
+        def can_admit(rid):
+            if kind == "raw":
+                need = pages_of(reqs[rid]) + sum(pages_of(reqs[running[s][0]]) - len(cache.pages[s]) for s in running)
+                return cache.free_pages() >= need
+            st = cache.stats()
+            bpl = (cache.mean_page_layer_bytes() or 32 * hkv * 256) * 1.03  # + chunk-end waste
+            committed = sum(worst_left(s) for s in running) * L * bpl
+            need = pages_of(reqs[rid]) * L * bpl + cache.chunk_bytes
+            return st["free_bytes"] - committed >= need
+
+        while queue or running:
+            while queue and free and can_admit(queue[0]):
+                rid = queue.popleft()
+                slot = free.pop()
+                n_tok = reqs[rid][0]
+                prompt = torch.stack([kvgen.gen_pages(cfg, (n_tok + 15) // 16, layer=layer, device=dev,
+                                                      seed_offset=7919 * rid) for layer in range(L)])
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+                try:
+                    cache.admit(slot, prompt, n_tok)
+                except OutOfSpace:
+                    cache.release(slot)
+                    free.append(slot)
+                    queue.appendleft(rid)
+                    break
+                torch.cuda.synchronize()
+                t_prefill += time.perf_counter() - t0
+                running[slot] = [rid, 0]
+                order.append(slot)
+            if not running:
+                raise RuntimeError(f"request {queue[0]} does not fit the budget alone")
+            slots = sorted(running)
+            x = torch.randn((L, len(slots), hkv, 2, 128), device=dev, generator=gen_rng)
+            for layer in range(L):
+                x[layer, :, :, 0] *= sig[layer][0]
+                x[layer, :, :, 1] *= sig[layer][1]
+            kv = x.to(torch.bfloat16)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            while True:
+                try:
+                    cache.append(slots, kv[:, : len(slots)])
+                    break
+                except OutOfSpace:  # preempt the newest sequence and retry (its request restarts later)
+                    victim = order.pop()
+                    cache.release(victim)
+                    queue.appendleft(running.pop(victim)[0])
+                    free.append(victim)
+                    preempt += 1
+                    keep = [i for i, s in enumerate(slots) if s != victim]
+                    slots = [slots[i] for i in keep]
+                    kv = kv[:, keep].contiguous()
+            n = len(slots)
+            args_b = cache.batch_args(slots)
+            q_b = [qs[layer][:n].contiguous() for layer in range(L)]
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for layer in range(L):
+                cache.attention(layer, q_b[layer], args_b, out[:n], workspace=ws)
+            e1.record()
+            torch.cuda.synchronize()
+            t_decode += time.perf_counter() - t0
+            t_attn += e0.elapsed_time(e1) * 1e-3
+            steps += 1
+            tokens += n
+            conc.append(n)
+            peak = max(peak, n)
+            for s in slots:
+                running[s][1] += 1
+                if running[s][1] == reqs[running[s][0]][1]:
+                    cache.release(s)
+                    del running[s]
+                    order.remove(s)
+                    free.append(s)
+        if int(cache.status.item()) != 0:
+            raise RuntimeError(f"{kind}: status {int(cache.status.item())}")
+        res = {"decode_tokens_per_s": round(tokens / t_decode, 1), "steps": steps, "tokens": tokens,
+               "mean_concurrency": round(statistics.mean(conc), 2), "peak_concurrency": peak,
+               "decode_s": round(t_decode, 3), "attention_s": round(t_attn, 4),
+               "attention_us_per_step": round(t_attn * 1e6 / steps, 1),
+               "attention_us_per_token": round(t_attn * 1e6 / tokens, 3),
+               "prefill_encode_s": round(t_prefill, 3), "preemptions": preempt}
+        if kind == "compressed":
+            res["arena_bytes"] = cache.arena.numel()
+            res["mean_page_layer_bytes"] = round(cache.mean_page_layer_bytes(), 1)
+            res["raw_page_layer_bytes"] = page_layer_raw
+            res["chunk_grants"] = cache.chunk_grants
+            res["arena_chunks"] = cache.arena.numel() // cache.chunk_bytes
+        return res
+
+    with ClockSampler(local) as clk:
+        comp = run("compressed")
+        raw = run("raw")
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": comp["decode_tokens_per_s"], "unit": "tokens/s", "n_gpus": world,
+        "steps": comp["steps"], "warmup": 0, "ms_per_step": round(comp["decode_s"] * 1e3 / comp["steps"], 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "toy admission loop", "layers": L, "q_heads": hq, "kv_heads": hkv, "head_dim": 128,
+                   "requests": N, "prompt_tokens": "512..2048", "generated_tokens": "64..256",
+                   "kv_budget_bytes": budget, "timing": "wall time of decode steps (append + encodes + attention in "
+                   "every layer), synchronised; prefill encodes timed apart"},
+        "compressed": comp, "raw": raw,
+        "speedup_vs_raw": round(comp["decode_tokens_per_s"] / raw["decode_tokens_per_s"], 4),
+        "attention_speedup_per_token_vs_raw": round(raw["attention_us_per_token"] / comp["attention_us_per_token"], 4),
+        "concurrency_gain_vs_raw": round(comp["mean_concurrency"] / raw["mean_concurrency"], 4),
+        "clocks": clocks,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -41,6 +41,7 @@ EXPORTS = (
     "kvz_alloc_reserve", "kvz_alloc_observe", "kvz_alloc_release", "kvz_alloc_stats",
     "kvz_apply_cursor_updates", "kvz_strerror", "kvz_last_cuda_error", "kvz_device_sm_count",
     "kvz_ga_calibrate", "kvz_ga_encode_pages", "kvz_ga_decode_blocks", "kvz_ga_decode_attention",
+    "kvz_selftest_bounded_wait", "kvz_encode_sizes", "kvz_alloc_reserve_granules", "kvz_alloc_room",
 )
 
 
@@ -83,6 +84,10 @@ def _load() -> ctypes.CDLL:
         "kvz_ga_decode_blocks": (ctypes.c_int, [Dims, P, i64, P, u64, P, P, i32, P, P, P]),
         "kvz_ga_decode_attention": (ctypes.c_int, [Dims, i32, i32, P, P, i32, P, P, P, i64, P, u64, P, P, i64, P, P,
                                                    sz, P, P]),
+        "kvz_selftest_bounded_wait": (ctypes.c_int, [u64, P, P, P]),
+        "kvz_encode_sizes": (ctypes.c_int, [Dims, P, i64, P, i32, P, P, sz, P, P]),
+        "kvz_alloc_reserve_granules": (ctypes.c_int, [P, P, P, i32, P, P, P, P, P]),
+        "kvz_alloc_room": (ctypes.c_int, [P, i32, P]),
         "kvz_strerror": (ctypes.c_char_p, [ctypes.c_int]),
         "kvz_last_cuda_error": (ctypes.c_int, []),
         "kvz_device_sm_count": (ctypes.c_int, []),
@@ -183,6 +188,20 @@ def encode_pages(raw_pool, src_page, dst_page, dst_seq, meta, arena, cursors, st
         _ptr(workspace, _U8, "workspace"), workspace.numel(), _ptr(status, _U32, "status"), _stream(stream),
     )
     _check("kvz_encode_pages", rc)
+
+
+def encode_sizes(raw_pool, src_page, granules, status, workspace=None, stream=None):
+    """Granules (int32 [n], device) each page raw_pool[src_page[i]] will take when encoded."""
+    hkv = raw_pool.shape[1]
+    n = src_page.numel()
+    if workspace is None:
+        workspace = torch.empty(encode_workspace_size(hkv, n), dtype=torch.uint8, device=raw_pool.device)
+    rc = _lib.kvz_encode_sizes(
+        _dims(hkv), _ptr(raw_pool, _BF16, "raw_pool"), _pages_of(raw_pool), _ptr(src_page, torch.int32, "src_page"),
+        n, _ptr(granules, _U32, "granules"), _ptr(workspace, _U8, "workspace"), workspace.numel(),
+        _ptr(status, _U32, "status"), _stream(stream),
+    )
+    _check("kvz_encode_sizes", rc)
 
 
 def decode_blocks(meta, arena, pages, out, status, stream=None):
@@ -305,6 +324,13 @@ def ga_decode_attention(q, page_ids, seq_lens, tail_page, meta, arena, bases, ra
     _check("kvz_ga_decode_attention", rc)
 
 
+def selftest_bounded_wait(limit_ns: int, status, out, stream=None):
+    """Device check of the bounded barrier wait (see kvz_selftest_bounded_wait); out:
+    int64 [3] on the device."""
+    _check("kvz_selftest_bounded_wait", _lib.kvz_selftest_bounded_wait(
+        int(limit_ns), _ptr(status, _U32, "status"), _ptr(out, _U64, "out"), _stream(stream)))
+
+
 # ------------------------------------------------------------------------------------
 # host allocator
 # ------------------------------------------------------------------------------------
@@ -340,6 +366,29 @@ class Allocator:
         _check("kvz_alloc_reserve", rc)
         k = nu.value
         return tk.value, list(zip(ui[:k].tolist(), up[:k].tolist(), ue[:k].tolist()))
+
+    def reserve_granules(self, cursor_ids, granules):
+        """Exact reservation: granules[k] for cursor cursor_ids[k].  Returns (ticket, updates)."""
+        import numpy as np
+
+        ids = np.ascontiguousarray(cursor_ids, dtype=np.int32)
+        gr = np.ascontiguousarray(granules, dtype=np.uint64)
+        n = ids.size
+        ui = np.zeros(max(n, 1), np.int32)
+        up = np.zeros(max(n, 1), np.uint32)
+        ue = np.zeros(max(n, 1), np.uint32)
+        nu = ctypes.c_int32()
+        tk = ctypes.c_uint64()
+        rc = _lib.kvz_alloc_reserve_granules(self._h, ids.ctypes.data, gr.ctypes.data, n, ui.ctypes.data,
+                                             up.ctypes.data, ue.ctypes.data, ctypes.byref(nu), ctypes.byref(tk))
+        _check("kvz_alloc_reserve_granules", rc)
+        k = nu.value
+        return tk.value, list(zip(ui[:k].tolist(), up[:k].tolist(), ue[:k].tolist()))
+
+    def room(self, cursor: int) -> int:
+        r = ctypes.c_uint64()
+        _check("kvz_alloc_room", _lib.kvz_alloc_room(self._h, cursor, ctypes.byref(r)))
+        return r.value
 
     def observe(self, ticket: int, cursors_snapshot):
         import numpy as np

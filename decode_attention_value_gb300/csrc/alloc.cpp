@@ -54,20 +54,20 @@ int kvz_alloc_create(uint64_t arena_bytes, uint32_t chunk_granules, int32_t num_
 
 void kvz_alloc_destroy(kvz_alloc *a) { delete a; }
 
-int kvz_alloc_reserve(kvz_alloc *a, const int32_t *cursor_ids, const int32_t *pages, int32_t count, int32_t *upd_idx,
-                      uint32_t *upd_pos, uint32_t *upd_end, int32_t *n_upd, uint64_t *ticket)
+}  // extern "C"
+
+// Shared by both reservation calls: need_of(k) = granules cursor_ids[k] must hold.
+template <class Need>
+static int reserve_impl(kvz_alloc *a, const int32_t *cursor_ids, int32_t count, Need need_of, int32_t *upd_idx,
+                        uint32_t *upd_pos, uint32_t *upd_end, int32_t *n_upd, uint64_t *ticket)
 {
-    if (!a || count < 0 || (count > 0 && (!cursor_ids || !pages || !upd_idx || !upd_pos || !upd_end)) || !n_upd ||
-        !ticket)
-        return KVZ_ERR_INVALID_ARG;
-    const uint64_t worst_page = 2ull * 16ull * (uint64_t)a->hkv;  // two groups of at most 16 granules per head
     size_t need_chunks = 0;
     for (int32_t k = 0; k < count; ++k) {
         const int32_t c = cursor_ids[k];
-        if (c < 0 || (size_t)c >= a->cur.size() || pages[k] < 0) return KVZ_ERR_INVALID_ARG;
+        if (c < 0 || (size_t)c >= a->cur.size()) return KVZ_ERR_INVALID_ARG;
         for (int32_t m = 0; m < k; ++m)
             if (cursor_ids[m] == c) return KVZ_ERR_INVALID_ARG;
-        const uint64_t need = worst_page * (uint64_t)pages[k];
+        const uint64_t need = need_of(k);
         if (need > a->chunk) return KVZ_ERR_UNSUPPORTED;  // one call's pages must fit one chunk
         const kvz_alloc::Cursor &cu = a->cur[(size_t)c];
         if (need > 0 && (cu.chunks.empty() || cu.bound + need > cu.end)) ++need_chunks;
@@ -77,7 +77,7 @@ int kvz_alloc_reserve(kvz_alloc *a, const int32_t *cursor_ids, const int32_t *pa
     int32_t nu = 0;
     for (int32_t k = 0; k < count; ++k) {
         kvz_alloc::Cursor &cu = a->cur[(size_t)cursor_ids[k]];
-        const uint64_t need = worst_page * (uint64_t)pages[k];
+        const uint64_t need = need_of(k);
         if (need == 0) continue;
         if (cu.chunks.empty() || cu.bound + need > cu.end) {
             const uint32_t id = a->free_list.back();
@@ -96,6 +96,40 @@ int kvz_alloc_reserve(kvz_alloc *a, const int32_t *cursor_ids, const int32_t *pa
     }
     *n_upd = nu;
     *ticket = t;
+    return KVZ_OK;
+}
+
+extern "C" {
+
+int kvz_alloc_reserve(kvz_alloc *a, const int32_t *cursor_ids, const int32_t *pages, int32_t count, int32_t *upd_idx,
+                      uint32_t *upd_pos, uint32_t *upd_end, int32_t *n_upd, uint64_t *ticket)
+{
+    if (!a || count < 0 || (count > 0 && (!cursor_ids || !pages || !upd_idx || !upd_pos || !upd_end)) || !n_upd ||
+        !ticket)
+        return KVZ_ERR_INVALID_ARG;
+    for (int32_t k = 0; k < count; ++k)
+        if (pages[k] < 0) return KVZ_ERR_INVALID_ARG;
+    const uint64_t worst_page = 2ull * 16ull * (uint64_t)a->hkv;  // two groups of at most 16 granules per head
+    return reserve_impl(a, cursor_ids, count, [&](int32_t k) { return worst_page * (uint64_t)pages[k]; }, upd_idx,
+                        upd_pos, upd_end, n_upd, ticket);
+}
+
+int kvz_alloc_reserve_granules(kvz_alloc *a, const int32_t *cursor_ids, const uint64_t *granules, int32_t count,
+                               int32_t *upd_idx, uint32_t *upd_pos, uint32_t *upd_end, int32_t *n_upd,
+                               uint64_t *ticket)
+{
+    if (!a || count < 0 || (count > 0 && (!cursor_ids || !granules || !upd_idx || !upd_pos || !upd_end)) ||
+        !n_upd || !ticket)
+        return KVZ_ERR_INVALID_ARG;
+    return reserve_impl(a, cursor_ids, count, [&](int32_t k) { return granules[k]; }, upd_idx, upd_pos, upd_end,
+                        n_upd, ticket);
+}
+
+int kvz_alloc_room(const kvz_alloc *a, int32_t c, uint64_t *room)
+{
+    if (!a || !room || c < 0 || (size_t)c >= a->cur.size()) return KVZ_ERR_INVALID_ARG;
+    const kvz_alloc::Cursor &cu = a->cur[(size_t)c];
+    *room = cu.chunks.empty() ? 0 : cu.end - cu.bound;
     return KVZ_OK;
 }
 

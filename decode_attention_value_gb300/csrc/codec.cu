@@ -68,10 +68,11 @@ __global__ void __launch_bounds__(256) k_enc_validate(EncodeParams P)
     const int e = blockIdx.x * blockDim.x + threadIdx.x;
     uint32_t err = 0;
     if (e < P.n) {
-        const int s = P.src_page[e], d = P.dst_page[e], q = P.dst_seq[e];
+        // a size-only call (kvz_encode_sizes) has no destination sequences
+        const int s = P.src_page[e], d = P.dst_page[e], q = P.dst_seq ? P.dst_seq[e] : 0;
         if (s < 0 || s >= P.num_raw_pages || d < 0 || d >= P.num_meta_pages || q < 0 || q >= P.num_cursors)
             err |= KVZ_STATUS_BAD_INDEX;
-        if (e > 0 && q < P.dst_seq[e - 1]) err |= KVZ_STATUS_BAD_ORDER;
+        if (P.dst_seq && e > 0 && q < P.dst_seq[e - 1]) err |= KVZ_STATUS_BAD_ORDER;
     }
     err = __reduce_or_sync(0xffffffffu, err);
     if (err && (threadIdx.x & 31) == 0) {
@@ -367,6 +368,17 @@ cudaError_t launch_encode(const EncodeParams &P, cudaStream_t stream)
     k_enc_sizes<<<items, 256, 0, stream>>>(P, 0);
     k_enc_scan<<<1, kScanThreads, 0, stream>>>(P, 0, P.n);
     k_enc_pack<<<items, 256, 0, stream>>>(P, 0);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_encode_sizes(const EncodeParams &P, cudaStream_t stream)
+{
+    // validation, then the size pass alone: P.ws_page_size is the caller's output array
+    cudaError_t e = cudaMemsetAsync(P.ws_hdr, 0, 16, stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(P.ws_page_size, 0, (size_t)P.n * 4, stream);
+    if (e != cudaSuccess) return e;
+    k_enc_validate<<<(P.n + 255) / 256, 256, 0, stream>>>(P);
+    k_enc_sizes<<<(unsigned)((size_t)P.n * P.hkv), 256, 0, stream>>>(P, 0);
     return cudaGetLastError();
 }
 

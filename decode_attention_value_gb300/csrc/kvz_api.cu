@@ -273,6 +273,39 @@ int kvz_encode_pages(kvz_dims dims, const void *raw_pool, int64_t num_raw_pages,
     return e == cudaSuccess ? KVZ_OK : fail_cuda(e);
 }
 
+int kvz_encode_sizes(kvz_dims dims, const void *raw_pool, int64_t num_raw_pages, const int32_t *src_page, int32_t n,
+                     uint32_t *granules, void *workspace, size_t workspace_bytes, uint32_t *status,
+                     kvz_stream_t stream)
+{
+    if (!dims_ok(dims)) return dims.num_kv_heads >= 1 ? KVZ_ERR_UNSUPPORTED : KVZ_ERR_INVALID_ARG;
+    if (n < 0 || num_raw_pages < 0) return KVZ_ERR_INVALID_ARG;
+    if (n == 0) return KVZ_OK;
+    if (!raw_pool || !src_page || !granules || !workspace || !status) return KVZ_ERR_INVALID_ARG;
+    if (!aligned(raw_pool, 16) || !aligned(granules, 4) || !aligned(workspace, 16) || !aligned(status, 4))
+        return KVZ_ERR_ALIGNMENT;
+    if ((int64_t)n * dims.num_kv_heads > (int64_t)1 << 30) return KVZ_ERR_UNSUPPORTED;
+    if (workspace_bytes < kvz_encode_workspace_size(dims, n)) return KVZ_ERR_WORKSPACE;
+    EncodeParams P;
+    memset(&P, 0, sizeof P);
+    P.hkv = dims.num_kv_heads;
+    P.n = n;
+    P.raw_pool = static_cast<const uint16_t *>(raw_pool);
+    P.num_raw_pages = num_raw_pages;
+    P.src_page = src_page;
+    P.dst_page = src_page;  // only validated: no metadata is written
+    P.dst_seq = nullptr;
+    P.num_meta_pages = num_raw_pages;
+    P.num_cursors = 1;
+    P.status = status;
+    uint8_t *w = static_cast<uint8_t *>(workspace);
+    const size_t a = ((size_t)n * 4 + 15) / 16 * 16;
+    P.ws_hdr = reinterpret_cast<uint32_t *>(w);
+    P.ws_page_size = granules;
+    P.ws_pair_size = reinterpret_cast<uint32_t *>(w + 16 + 2 * a);
+    cudaError_t e = launch_encode_sizes(P, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KVZ_OK : fail_cuda(e);
+}
+
 int kvz_decode_blocks(kvz_dims dims, const uint64_t *meta, int64_t num_meta_pages, const uint8_t *arena,
                       uint64_t arena_bytes, const int32_t *page, int32_t n, void *out_pages, uint32_t *status,
                       kvz_stream_t stream)
@@ -465,6 +498,15 @@ int kvz_ga_decode_attention(kvz_dims dims, int32_t batch, int32_t num_q_heads, c
     return run_attention(FormatArgs{kFmtGa, nullptr, meta, bases}, dims, batch, num_q_heads, q, page_ids, max_pages,
                          seq_lens, tail_page, num_meta_pages, arena, arena_bytes, raw_pool, num_raw_pages, out,
                          workspace, workspace_bytes, status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kvz_selftest_bounded_wait(uint64_t limit_ns, uint32_t *status, uint64_t *out, kvz_stream_t stream)
+{
+    if (!status || !out) return KVZ_ERR_INVALID_ARG;
+    if (!aligned(status, 4) || !aligned(out, 8)) return KVZ_ERR_ALIGNMENT;
+    if (limit_ns == 0 || limit_ns > 10000000000ull) return KVZ_ERR_INVALID_ARG;  // (0, 10 s]
+    cudaError_t e = launch_wait_selftest(limit_ns, status, out, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KVZ_OK : fail_cuda(e);
 }
 
 int kvz_apply_cursor_updates(const int32_t *idx, const uint32_t *pos, const uint32_t *end, int32_t n,

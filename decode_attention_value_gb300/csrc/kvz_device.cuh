@@ -107,13 +107,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 // timeout status bit) when the limit passes; the caller then stops using the stage.
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: kernels here run for micro- to milliseconds
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *status)
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *status,
+                                          uint64_t limit_ns = kWaitLimitNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+        if ((it & 255u) == 0 && globaltimer_ns() - t0 > limit_ns) {
             atomicOr(status, KVZ_STATUS_TIMEOUT);
             return false;
         }

@@ -91,9 +91,11 @@ inline size_t attn_ws_bytes(int batch, int hkv, int grid)
 
 cudaError_t launch_encode(const EncodeParams &P, cudaStream_t stream);
 cudaError_t launch_enc_validate(const EncodeParams &P, cudaStream_t stream);
+cudaError_t launch_encode_sizes(const EncodeParams &P, cudaStream_t stream);
 cudaError_t launch_enc_scan(const EncodeParams &P, cudaStream_t stream);
 cudaError_t launch_ga_encode(const EncodeParams &P, cudaStream_t stream);
 cudaError_t launch_ga_decode(const DecodeParams &P, cudaStream_t stream);
+cudaError_t launch_wait_selftest(uint64_t limit_ns, uint32_t *status, uint64_t *out, cudaStream_t stream);
 cudaError_t launch_ga_calibrate(int hkv, const uint16_t *raw_pool, int64_t num_raw_pages, const int32_t *pages, int n,
                                 uint8_t *bases, uint32_t *status, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams &P, cudaStream_t stream);

@@ -120,6 +120,16 @@ int kvz_encode_pages(kvz_dims dims, const void *raw_pool, int64_t num_raw_pages,
                      void *workspace, size_t workspace_bytes, uint32_t *status,
                      kvz_stream_t stream);
 
+/* kvz_encode_sizes -- the encoder's size pass alone: granules[i] (device uint32) = the
+ * 256-byte granules page src_page[i] will take in the arena (all KV heads, K and V: each
+ * group 12..16), exactly what kvz_encode_pages will place for it.  Lets the caller
+ * reserve exact space (kvz_alloc_reserve_granules) instead of the worst case.  Same
+ * validation as kvz_encode_pages for src_page (KVZ_STATUS_BAD_INDEX: nothing written);
+ * workspace: kvz_encode_workspace_size(dims, n). */
+int kvz_encode_sizes(kvz_dims dims, const void *raw_pool, int64_t num_raw_pages, const int32_t *src_page,
+                     int32_t n, uint32_t *granules, void *workspace, size_t workspace_bytes, uint32_t *status,
+                     kvz_stream_t stream);
+
 /* ---------------------------------------------------------------------------------
  * kvz_decode_blocks -- standalone bit-exact decompression (ZipFusion "How it works"
  * step 4), used to check the format and to time decoding on its own.
@@ -298,6 +308,15 @@ void kvz_alloc_destroy(kvz_alloc *a);
 int kvz_alloc_reserve(kvz_alloc *a, const int32_t *cursor_ids, const int32_t *pages, int32_t count,
                       int32_t *upd_idx, uint32_t *upd_pos, uint32_t *upd_end, int32_t *n_upd,
                       uint64_t *ticket);
+/* Like kvz_alloc_reserve with exact sizes: granules[k] granules for cursor cursor_ids[k]
+ * (e.g. the totals kvz_encode_sizes reports for the pages about to be encoded there).
+ * With exact sizes the bound equals the device cursor after the encode, so no
+ * observation is needed, and a chunk is left only when the next pages do not fit it. */
+int kvz_alloc_reserve_granules(kvz_alloc *a, const int32_t *cursor_ids, const uint64_t *granules, int32_t count,
+                               int32_t *upd_idx, uint32_t *upd_pos, uint32_t *upd_end, int32_t *n_upd,
+                               uint64_t *ticket);
+/* Granules left in cursor c's current chunk by the allocator's bound (0 without a chunk). */
+int kvz_alloc_room(const kvz_alloc *a, int32_t cursor_id, uint64_t *room);
 /* cursors_snapshot: host copy of the device cursors [num_cursors][2] taken after the
  * encode that used reservation `ticket` completed. */
 int kvz_alloc_observe(kvz_alloc *a, uint64_t ticket, const uint32_t *cursors_snapshot);
@@ -311,6 +330,14 @@ int kvz_alloc_stats(const kvz_alloc *a, uint64_t *held_bytes, uint64_t *free_byt
 int kvz_apply_cursor_updates(const int32_t *idx, const uint32_t *pos, const uint32_t *end,
                              int32_t n, uint32_t *cursors, int32_t num_cursors,
                              kvz_stream_t stream);
+
+/* kvz_selftest_bounded_wait -- diagnostic with no counterpart on the pages: runs, on the
+ * device, the bounded barrier wait that every kernel here uses for its pipeline.  One wait
+ * targets an already complete phase (must return at once); one targets a phase no thread
+ * ever completes (must give up after limit_ns, OR KVZ_STATUS_TIMEOUT into *status and
+ * return).  out: device uint64[3] = {ns of the first wait, ns of the second,
+ * bit 0 = first wait succeeded, bit 1 = second wait succeeded}.  limit_ns in (0, 10 s]. */
+int kvz_selftest_bounded_wait(uint64_t limit_ns, uint32_t *status, uint64_t *out, kvz_stream_t stream);
 
 /* Text for a KVZ_ERR_* code. */
 const char *kvz_strerror(int code);

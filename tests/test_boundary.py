@@ -146,6 +146,55 @@ def test_allocator_observe_tightens_bound(kvz):
     assert up == [(0, chunk, 2 * chunk)]
 
 
+def test_allocator_exact_reservation_and_room(kvz, oracle):
+    """Exact reservations (the sizes the encoder will place) fill a chunk to the granule:
+    the oracle encodes pages into the cursor the allocator hands out, page runs split at
+    the chunk's room, and the device cursor equals the allocator's bound after each run."""
+    cfg = kvgen.KVConfig("alloc-exact", 1, 2, 8, 2, 20, seed=23, block_outlier_frac=0.3)
+    hkv = cfg.hkv
+    pool = kvgen.bits(kvgen.gen_pages(cfg, 20))
+    chunk = 256  # 4..5 pages of 52..64 granules
+    a = kvz.Allocator(arena_bytes=chunk * 256 * 16, chunk_granules=chunk, num_cursors=1, num_kv_heads=hkv)
+    assert a.room(0) == 0
+    # exact sizes of each page from the oracle's own encode (12 or 16 granules per group)
+    sizes = []
+    for p in range(20):
+        g = 0
+        for h in range(hkv):
+            for kv in range(2):
+                for j in range(4):
+                    g += 3 if oracle.encode_block(pool[p, h, kv], bool(kv), j)[1] != 0xFF else 4
+        sizes.append(g)
+    meta = np.zeros((20, hkv, 2), np.uint64)
+    arena = np.zeros(chunk * 256 * 16, np.uint8)
+    cur = np.zeros((1, 2), np.uint32)
+    p, runs = 0, 0
+    while p < 20:
+        room = a.room(0)
+        q, tot = p, 0
+        while q < 20 and tot + sizes[q] <= room:
+            tot += sizes[q]
+            q += 1
+        if q == p:  # nothing fits the current chunk: the run opens a fresh one
+            while q < 20 and tot + sizes[q] <= chunk:
+                tot += sizes[q]
+                q += 1
+        t, up = a.reserve_granules([0], [tot])
+        for c, pos, end in up:
+            cur[c] = (pos, end)
+        src = np.arange(p, q, dtype=np.int32)
+        assert oracle.encode_pages(pool, src, src, np.zeros(q - p, np.int32), meta, arena, cur, hkv) == 0
+        assert int(cur[0, 1]) - int(cur[0, 0]) == a.room(0)  # allocator bound == device cursor
+        p, runs = q, runs + 1
+    # every chunk but the last is left only when the next page no longer fits it
+    held = a.stats()["chunks_held"]
+    assert held * chunk - sum(sizes) < held * max(sizes) + chunk
+    out, st = oracle.decode_pages(meta, arena, np.arange(20, dtype=np.int32), hkv)
+    assert st == 0 and np.array_equal(out, pool)
+    with pytest.raises(kvz.KvzError):
+        a.reserve_granules([0], [chunk + 1])  # more than a chunk
+
+
 def test_allocator_with_oracle_stream(kvz, oracle):
     """Streaming page completions for several sequences, the oracle encoding into the
     cursors the allocator hands out: no group ever overflows, chunks are recycled."""
