@@ -34,7 +34,7 @@ HEAD_DIM = 128
 
 def build(force: bool = False) -> str:
     """Compile oref.c into liboref.so next to it (plain gcc, no CUDA)."""
-    srcs = [os.path.join(_HERE, f) for f in ("oref.c", "oga.c")]
+    srcs = [os.path.join(_HERE, f) for f in ("oref.c", "oga.c", "of8.c")]
     if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= max(
         os.path.getmtime(f) for f in srcs + [os.path.join(_HERE, "oref.h")]
     ):
@@ -81,6 +81,19 @@ def _load():
             ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int, P, P, P, i64, P, u64, P, P,
             i64, P, ctypes.c_int,
         ]
+        ci = ctypes.c_int
+        lib.of8_value.argtypes = [ci, ctypes.c_uint8]
+        lib.of8_value.restype = ctypes.c_double
+        lib.of8_from_bf16.argtypes = [ci, ctypes.c_uint16]
+        lib.of8_from_bf16.restype = ctypes.c_uint8
+        lib.of8_tile_bytes.argtypes = [ci]
+        lib.of8_calibrate.argtypes = [ci, P, i64, P, P]
+        lib.of8_encode_tile.argtypes = [ci, P, ci, P, P, P]
+        lib.of8_decode_tile.argtypes = [ci, P, ci, ci, P, P, P]
+        lib.of8_quantize.argtypes = [ci, P, i64, P]
+        lib.of8_encode_pages.argtypes = [ci, ci, P, i64, P, P, P, P, i32, P, i64, P, u64, P, i32]
+        lib.of8_decode_pages.argtypes = [ci, ci, P, i64, P, u64, P, P, i32, P]
+        lib.oref_f8_decode_attention.argtypes = [ci, ci, ci, ci, P, P, ci, P, P, P, i64, P, u64, P, P, i64, P, ci]
         lib.oref_bf16_exponent.argtypes = [ctypes.c_uint16]
         lib.oref_bf16_exponent.restype = ctypes.c_uint
         _lib = lib
@@ -282,6 +295,109 @@ def ga_decode_attention(q, page_ids, seq_lens, tail_page, meta, arena, bases, ra
     out = np.zeros((B, hq, HEAD_DIM), np.float64)
     st = _load().oref_ga_decode_attention(
         hkv, B, hq, _ptr(q), _ptr(page_ids), page_ids.shape[1], _ptr(seq_lens), _ptr(tail_page),
+        _ptr(meta), meta.size // (hkv * 2), _ptr(arena), arena.size, _ptr(bases), _ptr(raw_pool),
+        raw_pool.size // (hkv * 2 * PAGE * HEAD_DIM), _ptr(out), nthreads,
+    )
+    return out, st
+
+
+# ---------------------------------------------------------------------------------
+# FP8 pages with group-adaptive exponent coding (of8.c)
+# ---------------------------------------------------------------------------------
+E4M3 = 1
+E5M2 = 2
+F8_RAW_TILE = 2048
+
+
+def f8_value(fmt: int, b: int) -> float:
+    return _load().of8_value(fmt, int(b) & 0xFF)
+
+
+def f8_from_bf16(fmt: int, w: int) -> int:
+    return int(_load().of8_from_bf16(fmt, int(w) & 0xFFFF))
+
+
+def f8_quantize(fmt: int, words) -> np.ndarray:
+    """BF16 words (uint16 array) -> FP8 bytes of the same shape."""
+    a = _c(words, np.uint16)
+    out = np.zeros(a.shape, np.uint8)
+    _load().of8_quantize(fmt, _ptr(a), a.size, _ptr(out))
+    return out
+
+
+def f8_tile_bytes(fmt: int) -> int:
+    return int(_load().of8_tile_bytes(fmt))
+
+
+def f8_calibrate(fmt: int, pages) -> tuple[np.ndarray, np.ndarray]:
+    """Bases from FP8 pages uint8 [n][16][128] of one (head, K|V) -> (b3, b4)."""
+    pages = _c(pages, np.uint8).reshape(-1, PAGE, HEAD_DIM)
+    b3, b4 = np.zeros(HEAD_DIM, np.uint8), np.zeros(HEAD_DIM, np.uint8)
+    _load().of8_calibrate(fmt, _ptr(pages), pages.shape[0], _ptr(b3), _ptr(b4))
+    return b3, b4
+
+
+def f8_calibrate_pool(fmt: int, raw_pool, pages, hkv: int) -> np.ndarray:
+    """Bases [hkv][2][2][128] from the FP8 conversion of the listed BF16 raw pages."""
+    pool = _c(raw_pool, np.uint16).reshape(-1, hkv, 2, PAGE, HEAD_DIM)
+    sel = f8_quantize(fmt, pool[_c(pages, np.int64)])
+    out = np.zeros((hkv, 2, 2, HEAD_DIM), np.uint8)
+    for h in range(hkv):
+        for kv in range(2):
+            out[h, kv, 0], out[h, kv, 1] = f8_calibrate(fmt, np.ascontiguousarray(sel[:, h, kv]))
+    return out
+
+
+def f8_encode_tile(fmt: int, page, is_v: bool, b3, b4) -> bytes:
+    page = _c(page, np.uint8).reshape(PAGE, HEAD_DIM)
+    b3, b4 = _c(b3, np.uint8), _c(b4, np.uint8)
+    out = np.zeros(F8_RAW_TILE, np.uint8)
+    n = _load().of8_encode_tile(fmt, _ptr(page), int(is_v), _ptr(b3), _ptr(b4), _ptr(out))
+    return out[:n].tobytes()
+
+
+def f8_decode_tile(fmt: int, data: bytes, is_v: bool, b3, b4) -> np.ndarray:
+    assert len(data) in (f8_tile_bytes(fmt), F8_RAW_TILE)
+    buf = np.frombuffer(bytes(data), np.uint8).copy()
+    b3, b4 = _c(b3, np.uint8), _c(b4, np.uint8)
+    page = np.zeros((PAGE, HEAD_DIM), np.uint8)
+    _load().of8_decode_tile(fmt, _ptr(buf), int(len(data) == F8_RAW_TILE), int(is_v), _ptr(b3), _ptr(b4),
+                            _ptr(page))
+    return page
+
+
+def f8_encode_pages(fmt, raw_pool, bases, src_page, dst_page, dst_seq, meta, arena, cursors, hkv: int) -> int:
+    raw_pool, bases = _c(raw_pool, np.uint16), _c(bases, np.uint8)
+    src, dst, seq = _c(src_page, np.int32), _c(dst_page, np.int32), _c(dst_seq, np.int32)
+    for a, dt in ((meta, np.uint32), (arena, np.uint8), (cursors, np.uint32)):
+        assert a.dtype == dt and a.flags["C_CONTIGUOUS"]
+    num_raw = raw_pool.size // (hkv * 2 * PAGE * HEAD_DIM)
+    return _load().of8_encode_pages(
+        fmt, hkv, _ptr(raw_pool), num_raw, _ptr(bases), _ptr(src), _ptr(dst), _ptr(seq), src.size, _ptr(meta),
+        meta.size // (hkv * 2), _ptr(arena), arena.size, _ptr(cursors), cursors.size // 2,
+    )
+
+
+def f8_decode_pages(fmt, meta, arena, bases, pages, hkv: int) -> tuple[np.ndarray, int]:
+    meta, arena, bases = _c(meta, np.uint32), _c(arena, np.uint8), _c(bases, np.uint8)
+    pages = _c(pages, np.int32)
+    out = np.zeros((pages.size, hkv, 2, PAGE, HEAD_DIM), np.uint8)
+    st = _load().of8_decode_pages(fmt, hkv, _ptr(meta), meta.size // (hkv * 2), _ptr(arena), arena.size,
+                                  _ptr(bases), _ptr(pages), pages.size, _ptr(out))
+    return out, st
+
+
+def f8_decode_attention(fmt, q, page_ids, seq_lens, tail_page, meta, arena, bases, raw_pool, hkv: int,
+                        nthreads: int = 1):
+    q = _c(q, np.uint16)
+    B, hq = q.shape[0], q.shape[1]
+    page_ids = _c(page_ids, np.int32).reshape(B, -1)
+    seq_lens, tail_page = _c(seq_lens, np.int32), _c(tail_page, np.int32)
+    meta, arena, raw_pool = _c(meta, np.uint32), _c(arena, np.uint8), _c(raw_pool, np.uint16)
+    bases = _c(bases, np.uint8)
+    out = np.zeros((B, hq, HEAD_DIM), np.float64)
+    st = _load().oref_f8_decode_attention(
+        fmt, hkv, B, hq, _ptr(q), _ptr(page_ids), page_ids.shape[1], _ptr(seq_lens), _ptr(tail_page),
         _ptr(meta), meta.size // (hkv * 2), _ptr(arena), arena.size, _ptr(bases), _ptr(raw_pool),
         raw_pool.size // (hkv * 2 * PAGE * HEAD_DIM), _ptr(out), nthreads,
     )

@@ -339,13 +339,23 @@ static double bf16_to_double(uint16_t w)
 
 double oref_bf16_value(uint16_t w) { return bf16_to_double(w); }
 
+/* the BF16 word of a value that BF16 represents exactly (FP8 values) */
+static uint16_t bf16_of_double(double v)
+{
+    const float f = (float)v;
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
 typedef struct {
     int hkv, batch, hq, max_pages, compressed; /* compressed: 0 raw, 1 12-bit blocks, 2 GA tiles */
     const uint16_t *q;
     const int32_t *page_ids, *seq_lens, *tail_page;
     const uint64_t *meta;
-    const uint32_t *meta32; /* GA tile entries */
-    const uint8_t *bases;   /* GA bases [hkv][2][2][128] */
+    const uint32_t *meta32; /* GA / FP8 tile entries */
+    const uint8_t *bases;   /* GA / FP8 bases [hkv][2][2][128] */
+    int f8fmt;              /* compressed == 3: OF8_E4M3 or OF8_E5M2 */
     int64_t num_meta_pages;
     const uint8_t *arena;
     uint64_t arena_bytes;
@@ -381,7 +391,19 @@ static int attend_unit(attn_job *J, int unit)
                 ok = 0;
             } else {
                 int st;
-                if (J->compressed == 2) {
+                if (J->compressed == 3) {
+                    /* FP8 tiles: decode to FP8 bytes, then to the BF16 word of the same value
+                       (every FP8 value is a BF16 value) */
+                    const uint32_t *m = J->meta32 + ((int64_t)pid * J->hkv + kvh) * 2;
+                    const uint8_t *bb = J->bases + (size_t)kvh * 2 * 256;
+                    uint8_t k8[2048], v8[2048];
+                    st = of8_decode_entry(J->f8fmt, m[0], J->arena, J->arena_bytes, 0, bb, k8);
+                    st |= of8_decode_entry(J->f8fmt, m[1], J->arena, J->arena_bytes, 1, bb + 256, v8);
+                    for (int k = 0; k < 2048; k++) {
+                        kp[k] = bf16_of_double(of8_value(J->f8fmt, k8[k]));
+                        vp[k] = bf16_of_double(of8_value(J->f8fmt, v8[k]));
+                    }
+                } else if (J->compressed == 2) {
                     const uint32_t *m = J->meta32 + ((int64_t)pid * J->hkv + kvh) * 2;
                     const uint8_t *bb = J->bases + (size_t)kvh * 2 * 256;
                     st = oga_decode_entry(m[0], J->arena, J->arena_bytes, 0, bb, kp);
@@ -544,6 +566,36 @@ int oref_ga_decode_attention(int hkv, int batch, int hq, const uint16_t *q, cons
     J.hq = hq;
     J.max_pages = max_pages;
     J.compressed = 2;
+    J.q = q;
+    J.page_ids = page_ids;
+    J.seq_lens = seq_lens;
+    J.tail_page = tail_page;
+    J.meta32 = meta;
+    J.bases = bases;
+    J.num_meta_pages = num_meta_pages;
+    J.arena = arena;
+    J.arena_bytes = arena_bytes;
+    J.raw_pool = raw_pool;
+    J.num_raw_pages = num_raw_pages;
+    J.out = out;
+    return run_attention(&J, nthreads);
+}
+
+/* Attention over FP8 tiles (completed pages, converted to FP8 and coded) + BF16 tail. */
+int oref_f8_decode_attention(int fmt, int hkv, int batch, int hq, const uint16_t *q, const int32_t *page_ids,
+                             int max_pages, const int32_t *seq_lens, const int32_t *tail_page,
+                             const uint32_t *meta, int64_t num_meta_pages, const uint8_t *arena,
+                             uint64_t arena_bytes, const uint8_t *bases, const uint16_t *raw_pool,
+                             int64_t num_raw_pages, double *out, int nthreads)
+{
+    attn_job J;
+    memset(&J, 0, sizeof J);
+    J.hkv = hkv;
+    J.batch = batch;
+    J.hq = hq;
+    J.max_pages = max_pages;
+    J.compressed = 3;
+    J.f8fmt = fmt;
     J.q = q;
     J.page_ids = page_ids;
     J.seq_lens = seq_lens;
