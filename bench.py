@@ -407,8 +407,9 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="encode / standalone-decode throughput over 64 MB .. 4 GB of pages (exponent-spread KV)")
     ap.add_argument("--copies", type=int, default=3)
-    ap.add_argument("--format", default="zf", choices=["zf", "ga"],
-                    help="ga: group-adaptive additive tiles instead of 12-bit block groups (c1, c2, c4)")
+    ap.add_argument("--format", default="zf", choices=["zf", "ga", "f8e4", "f8e5"],
+                    help="ga: group-adaptive additive tiles; f8e4 / f8e5: completed pages converted to FP8 "
+                         "E4M3 / E5M2 and coded; instead of 12-bit block groups (c1, c2, c4)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-steps", type=int, default=256, help="decode steps of the c3 streaming run")
@@ -430,7 +431,7 @@ def main():
 
     if args.impl == "reference":
         return run_reference(args, cfg, dist, rank, world)
-    if args.format == "ga":
+    if args.format != "zf":
         return run_ga(args, cfg, dist, rank, world, local)
 
     torch.cuda.set_device(local)
@@ -612,26 +613,32 @@ def main():
 
 
 class GaCopies:
-    """The workload's pages as group-adaptive tiles: bases calibrated on the GPU from
-    every 8th encoded page of the layer, then one tile copy per KV copy."""
+    """The workload's pages as tiles of one of the tile formats: "ga" (group-adaptive BF16
+    tiles), "f8e4" / "f8e5" (pages converted to FP8 E4M3 / E5M2, then coded).  Bases are
+    calibrated on the GPU from every 8th encoded page of the layer, then one tile copy is
+    encoded per KV copy."""
 
-    def __init__(self, W: Workload, sample_step: int = 8):
+    def __init__(self, W: Workload, kind: str = "ga", sample_step: int = 8):
         kvz, cfg, dev = W.kvz, W.cfg, W.full.device
         B, hkv = cfg.batch, cfg.hkv
-        self.W = W
+        self.W, self.kind = W, kind
+        self.fmt = {"f8e4": kvz.F8_E4M3, "f8e5": kvz.F8_E5M2}.get(kind)
+        self.comp_bytes = kvz.GA_TILE_BYTES if kind == "ga" else kvz.F8_TILE_BYTES[self.fmt]
+        self.raw_bytes = kvz.GA_RAW_TILE_BYTES if kind == "ga" else kvz.F8_RAW_TILE_BYTES
         self.bases = torch.zeros((hkv, 2, 2, 128), dtype=torch.uint8, device=dev)
         self.sample = W.src[::sample_step].contiguous()
-        kvz.ga_calibrate(W.pools[0], self.sample, self.bases, W.status)
-        per = max(cfg.full_pages, 1) * hkv * 2 * (4096 // kvz.GA_GRANULE)  # granules: worst case per sequence
+        if kind == "ga":
+            kvz.ga_calibrate(W.pools[0], self.sample, self.bases, W.status)
+        else:
+            kvz.f8_calibrate(self.fmt, W.pools[0], self.sample, self.bases, W.status)
+        per = max(cfg.full_pages, 1) * hkv * 2 * (self.raw_bytes // kvz.GA_GRANULE)  # granules: worst case
         self.arena_bytes = B * per * kvz.GA_GRANULE
         self.cursor0 = torch.tensor([[b * per, (b + 1) * per] for b in range(B)], dtype=torch.int32, device=dev)
         self.metas, self.arenas = [], []
         for c in range(W.copies):
             meta = torch.zeros((cfg.num_pages, hkv, 2), dtype=torch.int32, device=dev)
             arena = torch.zeros(self.arena_bytes, dtype=torch.uint8, device=dev)
-            cur = self.cursor0.clone()
-            kvz.ga_encode_pages(W.pools[c], self.bases, W.src, W.src, W.dseq, meta, arena, cur, W.status,
-                                workspace=W.enc_ws)
+            self.encode(c, meta, arena, self.cursor0.clone())
             self.metas.append(meta)
             self.arenas.append(arena)
         self.out = torch.empty_like(W.out)
@@ -642,30 +649,50 @@ class GaCopies:
         raw = ((e.view(torch.int32) < 0) & (e != -1)).sum().item()  # bit 31 set: raw tile
         self.tiles = e.numel()
         self.raw_tiles = int(raw)
-        self.tile_bytes = (self.tiles - self.raw_tiles) * 3008 + self.raw_tiles * 4096
+        self.tile_bytes = (self.tiles - self.raw_tiles) * self.comp_bytes + self.raw_tiles * self.raw_bytes
         G = cfg.hq // hkv
         segs = B * hkv + W.grid_c() - 1
         part_bytes = 2 * segs * G * 130 * 4
         self.alg_bytes = (self.tile_bytes + W.pages_c * hkv * 8 + W.pages_c * hkv * 4 + hkv * 512 + W.tail_bytes +
                           B * cfg.hq * 128 * 2 + B * cfg.hq * 128 * 4 + part_bytes)
 
+    def encode(self, c, meta, arena, cur):
+        W, kvz = self.W, self.W.kvz
+        if self.kind == "ga":
+            kvz.ga_encode_pages(W.pools[c], self.bases, W.src, W.src, W.dseq, meta, arena, cur, W.status,
+                                workspace=W.enc_ws)
+        else:
+            kvz.f8_encode_pages(self.fmt, W.pools[c], self.bases, W.src, W.src, W.dseq, meta, arena, cur, W.status,
+                                workspace=W.enc_ws)
+
+    def decode(self, c, out):
+        W, kvz = self.W, self.W.kvz
+        if self.kind == "ga":
+            kvz.ga_decode_blocks(self.metas[c], self.arenas[c], self.bases, W.src, out, W.status)
+        else:
+            kvz.f8_decode_blocks(self.fmt, self.metas[c], self.arenas[c], self.bases, W.src, out, W.status)
+
     def step(self, k: int):
         W = self.W
         c = k % W.copies
-        W.kvz.ga_decode_attention(W.q, W.full, W.seq_lens, W.tail, self.metas[c], self.arenas[c], self.bases,
-                                  W.pools[c], self.out, W.status, workspace=W.ws_c)
+        if self.kind == "ga":
+            W.kvz.ga_decode_attention(W.q, W.full, W.seq_lens, W.tail, self.metas[c], self.arenas[c], self.bases,
+                                      W.pools[c], self.out, W.status, workspace=W.ws_c)
+        else:
+            W.kvz.f8_decode_attention(self.fmt, W.q, W.full, W.seq_lens, W.tail, self.metas[c], self.arenas[c],
+                                      self.bases, W.pools[c], self.out, W.status, workspace=W.ws_c)
 
 
 def run_ga(args, cfg, dist, rank, world, local):
-    """The workload through the group-adaptive tile format, timed beside the 12-bit
-    format and the raw kernel on the same pages."""
+    """The workload through one of the tile formats (group-adaptive BF16 tiles or FP8
+    tiles), timed beside the 12-bit format and the raw kernel on the same pages."""
     torch.cuda.set_device(local)
     import decode_attention_value_gb300 as kvz
 
     dev = torch.device("cuda", local)
     peak, peak_kind = measured_peaks()
     W = Workload(cfg, args.copies, layer=rank, dev=dev)
-    GA = GaCopies(W)
+    GA = GaCopies(W, args.format)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     for k in range(args.warmup):
         GA.step(k)
@@ -674,7 +701,7 @@ def run_ga(args, cfg, dist, rank, world, local):
     torch.cuda.synchronize()
     if int(W.status.item()) != 0:
         raise RuntimeError(f"attention status {int(W.status.item())}")
-    identical = bool(torch.equal(GA.out, W.out_raw))
+    identical = bool(torch.equal(GA.out, W.out_raw))  # FP8 formats change the values: not expected
     K = args.steps
     g_g, g_c, g_r = graph_of(GA.step, K), graph_of(W.step_c, K), graph_of(W.step_r, K)
     for g in (g_g, g_c, g_r):
@@ -703,21 +730,22 @@ def run_ga(args, cfg, dist, rank, world, local):
 
     def enc(k):
         enc_cur.copy_(GA.cursor0)
-        kvz.ga_encode_pages(W.pools[k % W.copies], GA.bases, W.src, W.src, W.dseq, enc_meta, enc_arena, enc_cur,
-                            W.status, workspace=W.enc_ws)
+        GA.encode(k % W.copies, enc_meta, enc_arena, enc_cur)
 
     enc_ms = per_launch_ms(enc, 10, flush)
     enc_in = W.src.numel() * cfg.hkv * 2 * 16 * 128 * 2
-    dec_out = torch.empty((W.src.numel(), cfg.hkv, 2, 16, 128), dtype=torch.bfloat16, device=dev)
+    dec_out = torch.empty((W.src.numel(), cfg.hkv, 2, 16, 128),
+                          dtype=torch.bfloat16 if args.format == "ga" else torch.uint8, device=dev)
 
     def dec(k):
-        kvz.ga_decode_blocks(GA.metas[k % W.copies], GA.arenas[k % W.copies], GA.bases, W.src, dec_out, W.status)
+        GA.decode(k % W.copies, dec_out)
 
     dec_ms = per_launch_ms(dec, 10, flush)
     torch.cuda.synchronize()
     if int(W.status.item()) != 0:
         raise RuntimeError(f"status {int(W.status.item())}")
-    if not torch.equal(dec_out.view(torch.int16), W.pools[(10 - 1) % W.copies][W.src.long()].view(torch.int16)):
+    if args.format == "ga" and not torch.equal(dec_out.view(torch.int16),
+                                               W.pools[(10 - 1) % W.copies][W.src.long()].view(torch.int16)):
         raise RuntimeError("tile decode differs from the input pages")
     line = {
         "metric": METRIC,
@@ -730,9 +758,11 @@ def run_ga(args, cfg, dist, rank, world, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "bf16" if args.format == "ga" else args.format.replace("f8", "fp8-"),
         "data": "synthetic",
-        "config": {"workload": cfg.name, "format": "group-adaptive tiles", "batch": cfg.batch, "q_heads": cfg.hq,
+        "config": {"workload": cfg.name, "format": {"ga": "group-adaptive BF16 tiles", "f8e4": "FP8 E4M3 tiles",
+                                                    "f8e5": "FP8 E5M2 tiles"}[args.format],
+                   "batch": cfg.batch, "q_heads": cfg.hq,
                    "kv_heads": cfg.hkv, "head_dim": 128, "page_tokens": 16, "context_tokens": cfg.full_pages * 16,
                    "tail_tokens": f"{cfg.tail_min}..{cfg.tail_max}", "page_order": "shuffled",
                    "calibration": "every 8th encoded page of the layer", "parallelism": f"replicas{world}",
@@ -742,14 +772,15 @@ def run_ga(args, cfg, dist, rank, world, local):
         "raw_us_per_step": round(us_r, 3),
         "speedup_vs_raw": round(us_r / us_g, 4),
         "speedup_vs_zf": round(us_c / us_g, 4),
-        "tile_bytes_ratio": round(GA.tile_bytes / (GA.tiles * 4096), 5),
+        "tile_bytes_ratio": round(GA.tile_bytes / (GA.tiles * 4096), 5),  # of BF16 bytes
         "raw_tile_fraction": round(GA.raw_tiles / GA.tiles, 5),
         "zf_bytes_ratio": round(W.block_bytes / (W.blocks * 1024), 5),
-        "bit_identical_tiles_vs_raw": identical,
+        "bit_identical_tiles_vs_raw": identical if args.format == "ga" else None,
         "encode_GBps": round(enc_in / (enc_ms * 1e-3) / 1e9, 2),
         "decode_GBps": round(enc_in / (dec_ms * 1e-3) / 1e9, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(args.workload, "tiles"),
+                     "frac": round(achieved / peak, 4),
+                     "traffic": profiled_traffic(args.workload, "tiles") if args.format == "ga" else None,
                      "peak_kind": peak_kind, "kernel": "k_attn<tiles> + k_attn_merge", "launch_us": round(us_g, 3),
                      "cold_single_launch_us": round(launch_ms * 1e3, 3),
                      "algorithmic_bytes_per_launch": GA.alg_bytes},

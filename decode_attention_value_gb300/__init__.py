@@ -34,6 +34,10 @@ GA_TILE_BYTES = 3008
 GA_RAW_TILE_BYTES = 4096
 GA_ENTRY_RAW = 0x80000000
 GA_ENTRY_INVALID = 0xFFFFFFFF
+F8_E4M3 = 1
+F8_E5M2 = 2
+F8_TILE_BYTES = {F8_E4M3: 1920, F8_E5M2: 1664}
+F8_RAW_TILE_BYTES = 2048
 
 EXPORTS = (
     "kvz_encode_workspace_size", "kvz_encode_pages", "kvz_decode_blocks", "kvz_attention_workspace_size",
@@ -42,6 +46,7 @@ EXPORTS = (
     "kvz_apply_cursor_updates", "kvz_strerror", "kvz_last_cuda_error", "kvz_device_sm_count",
     "kvz_ga_calibrate", "kvz_ga_encode_pages", "kvz_ga_decode_blocks", "kvz_ga_decode_attention",
     "kvz_selftest_bounded_wait", "kvz_encode_sizes", "kvz_alloc_reserve_granules", "kvz_alloc_room",
+    "kvz_f8_calibrate", "kvz_f8_encode_pages", "kvz_f8_decode_blocks", "kvz_f8_decode_attention",
 )
 
 
@@ -88,6 +93,12 @@ def _load() -> ctypes.CDLL:
         "kvz_encode_sizes": (ctypes.c_int, [Dims, P, i64, P, i32, P, P, sz, P, P]),
         "kvz_alloc_reserve_granules": (ctypes.c_int, [P, P, P, i32, P, P, P, P, P]),
         "kvz_alloc_room": (ctypes.c_int, [P, i32, P]),
+        "kvz_f8_calibrate": (ctypes.c_int, [Dims, i32, P, i64, P, i32, P, P, P]),
+        "kvz_f8_encode_pages": (ctypes.c_int, [Dims, i32, P, i64, P, P, P, P, i32, P, i64, P, u64, P, i32, P, sz, P,
+                                               P]),
+        "kvz_f8_decode_blocks": (ctypes.c_int, [Dims, i32, P, i64, P, u64, P, P, i32, P, P, P]),
+        "kvz_f8_decode_attention": (ctypes.c_int, [Dims, i32, i32, i32, P, P, i32, P, P, P, i64, P, u64, P, P, i64, P,
+                                                   P, sz, P, P]),
         "kvz_strerror": (ctypes.c_char_p, [ctypes.c_int]),
         "kvz_last_cuda_error": (ctypes.c_int, []),
         "kvz_device_sm_count": (ctypes.c_int, []),
@@ -322,6 +333,64 @@ def ga_decode_attention(q, page_ids, seq_lens, tail_page, meta, arena, bases, ra
         _ptr(status, _U32, "status"), _stream(stream),
     )
     _check("kvz_ga_decode_attention", rc)
+
+
+# ------------------------------------------------------------------------------------
+# FP8 tiles (format: F8_E4M3 or F8_E5M2)
+# ------------------------------------------------------------------------------------
+def f8_calibrate(fmt: int, raw_pool, pages, bases, status, stream=None):
+    hkv = raw_pool.shape[1]
+    rc = _lib.kvz_f8_calibrate(
+        _dims(hkv), fmt, _ptr(raw_pool, _BF16, "raw_pool"), _pages_of(raw_pool), _ptr(pages, torch.int32, "pages"),
+        pages.numel(), _ptr(bases, _U8, "bases"), _ptr(status, _U32, "status"), _stream(stream),
+    )
+    _check("kvz_f8_calibrate", rc)
+
+
+def f8_encode_pages(fmt: int, raw_pool, bases, src_page, dst_page, dst_seq, meta, arena, cursors, status,
+                    workspace=None, stream=None):
+    hkv = raw_pool.shape[1]
+    n = src_page.numel()
+    if workspace is None:
+        workspace = torch.empty(encode_workspace_size(hkv, n), dtype=torch.uint8, device=raw_pool.device)
+    rc = _lib.kvz_f8_encode_pages(
+        _dims(hkv), fmt, _ptr(raw_pool, _BF16, "raw_pool"), _pages_of(raw_pool), _ptr(bases, _U8, "bases"),
+        _ptr(src_page, torch.int32, "src_page"), _ptr(dst_page, torch.int32, "dst_page"),
+        _ptr(dst_seq, torch.int32, "dst_seq"), n, _ptr(meta, _U32, "meta"), meta.numel() // (hkv * 2),
+        _ptr(arena, _U8, "arena"), arena.numel(), _ptr(cursors, _U32, "cursors"), cursors.numel() // 2,
+        _ptr(workspace, _U8, "workspace"), workspace.numel(), _ptr(status, _U32, "status"), _stream(stream),
+    )
+    _check("kvz_f8_encode_pages", rc)
+
+
+def f8_decode_blocks(fmt: int, meta, arena, bases, pages, out, status, stream=None):
+    """Decode to FP8 bytes: out uint8 [n][Hkv][2][16][128]."""
+    hkv = out.shape[1]
+    rc = _lib.kvz_f8_decode_blocks(
+        _dims(hkv), fmt, _ptr(meta, _U32, "meta"), meta.numel() // (hkv * 2), _ptr(arena, _U8, "arena"),
+        arena.numel(), _ptr(bases, _U8, "bases"), _ptr(pages, torch.int32, "pages"), pages.numel(),
+        _ptr(out, _U8, "out"), _ptr(status, _U32, "status"), _stream(stream),
+    )
+    _check("kvz_f8_decode_blocks", rc)
+
+
+def f8_decode_attention(fmt: int, q, page_ids, seq_lens, tail_page, meta, arena, bases, raw_pool, out, status,
+                        workspace=None, stream=None):
+    B, hq = q.shape[0], q.shape[1]
+    hkv = meta.shape[1] if meta.dim() >= 2 else raw_pool.shape[1]
+    max_pages = page_ids.shape[1] if page_ids.dim() == 2 else 0
+    if workspace is None:
+        workspace = torch.empty(attention_workspace_size(hkv, B, hq, max_pages + 1), dtype=torch.uint8,
+                                device=q.device)
+    rc = _lib.kvz_f8_decode_attention(
+        _dims(hkv), fmt, B, hq, _ptr(q, _BF16, "q"), _ptr(page_ids, torch.int32, "page_ids"), max_pages,
+        _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(tail_page, torch.int32, "tail_page"),
+        _ptr(meta, _U32, "meta"), meta.numel() // (hkv * 2), _ptr(arena, _U8, "arena"), arena.numel(),
+        _ptr(bases, _U8, "bases"), _ptr(raw_pool, _BF16, "raw_pool"), _pages_of(raw_pool),
+        _ptr(out, torch.float32, "out"), _ptr(workspace, _U8, "workspace"), workspace.numel(),
+        _ptr(status, _U32, "status"), _stream(stream),
+    )
+    _check("kvz_f8_decode_attention", rc)
 
 
 def selftest_bounded_wait(limit_ns: int, status, out, stream=None):

@@ -27,6 +27,7 @@
 
 #include <cstring>
 
+#include "f8.cuh"
 #include "ga.cuh"
 #include "kvz_internal.h"
 
@@ -155,6 +156,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
 {
     constexpr bool kCompressed = kFmt != kFmtRaw;
     constexpr bool kGa = kFmt == kFmtGa;
+    constexpr bool kF8 = kFmt == kFmtF8E4 || kFmt == kFmtF8E5;
+    constexpr bool kE5 = kFmt == kFmtF8E5;
+    constexpr bool kTiles = kGa || kF8;  // 4-byte tile entries (K, V) per (page, head)
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_addr(smem);
     if (sbase & 1023u) {  // the swizzled TMA destinations need 1024-byte alignment
@@ -248,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
         auto load_meta = [&](const Pre &r, uint64_t &m0, uint64_t &m1) {  // metadata (global load)
             m0 = m1 = 0;
             if (is_compressed(r) && r.pid >= 0 && r.pid < P.num_meta_pages) {
-                if (kGa)  // the K and V tile entries
+                if (kTiles)  // the K and V tile entries
                     m0 = ld_keep_u64(reinterpret_cast<const uint64_t *>(P.meta32 + ((int64_t)r.pid * hkv + r.L.kvh) * 2),
                                      keep);
                 else
@@ -269,14 +273,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
             uint32_t d_kind = kKindSkip, d_valid = 0, d_bad = 0, d_tK = 0, d_tV = 0, d_bytes = 0;
             uint64_t d_srcK = 0, d_srcV = 0;
             if (base + lane < npage) {
-                if (kGa && is_compressed(cur)) {
+                if (kTiles && is_compressed(cur)) {
                     const uint32_t eK = (uint32_t)cm0, eV = (uint32_t)(cm0 >> 32);
                     const uint64_t oK = eK & kGaOffsetMask, oV = eV & kGaOffsetMask;
+                    const uint32_t bK = kGa ? ga_entry_bytes(eK) : f8_entry_bytes(kE5 ? kF8E5M2 : kF8E4M3, eK);
+                    const uint32_t bV = kGa ? ga_entry_bytes(eV) : f8_entry_bytes(kE5 ? kF8E5M2 : kF8E4M3, eV);
                     if (cur.pid < 0 || cur.pid >= P.num_meta_pages) {
                         d_bad = KVZ_STATUS_BAD_INDEX;
                     } else if (eK == kGaEntryInvalid || eV == kGaEntryInvalid ||
-                               oK * kGaGranule + ga_entry_bytes(eK) > P.arena_bytes ||
-                               oV * kGaGranule + ga_entry_bytes(eV) > P.arena_bytes) {
+                               oK * kGaGranule + bK > P.arena_bytes || oV * kGaGranule + bV > P.arena_bytes) {
                         d_bad = KVZ_STATUS_BAD_META;
                     } else {
                         d_kind = kKindPair;
@@ -285,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                         d_tV = eV >> 31;
                         d_srcK = oK * kGaGranule;
                         d_srcV = oV * kGaGranule;
-                        d_bytes = ga_entry_bytes(eK) | (ga_entry_bytes(eV) << 16);
+                        d_bytes = bK | (bV << 16);
                     }
                 } else if (is_compressed(cur)) {
                     const uint32_t offK = (uint32_t)cm0, offV = (uint32_t)cm1;
@@ -407,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
         const PageLoc L = locate(pref, B, hkv, x);
         const int64_t send = min(hi, unit_end(pref, hkv, L));
         const int64_t cnt = send - x;
-        const uint8_t *ga_row = kGa ? P.ga_bases + (size_t)L.kvh * 512 : nullptr;  // K b3 row; V at +256
+        const uint8_t *ga_row = kTiles ? P.ga_bases + (size_t)L.kvh * 512 : nullptr;  // K b3 row; V at +256
 
         // queries of this segment: B operand of QK^T, column n = head n % 4 (zero if >= G)
         uint32_t qf[8][2];
@@ -457,6 +462,27 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                         mma_bf16_16816(sc, a0, qf[2 * j][0], qf[2 * j][1]);
                         mma_bf16_16816(sc, a1, qf[2 * j + 1][0], qf[2 * j + 1][1]);
                     }
+                } else if (kF8 && inf.kind == kKindPair && !inf.tagsK) {
+                    F8Lane<kE5> fs = f8_lane_load<kE5>(st, lane);
+                    const bool any2 = kE5 && __any_sync(0xffffffffu, fs.modes & 0xAAAAu);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t fb[4], a0[4], a1[4];
+                        f8_block_bytes<kE5, false>(st, ga_row, fs, any2, lane, j, fb);
+                        f8_frags<kE5>(fb, a0, a1);
+                        mma_bf16_16816(sc, a0, qf[2 * j][0], qf[2 * j][1]);
+                        mma_bf16_16816(sc, a1, qf[2 * j + 1][0], qf[2 * j + 1][1]);
+                    }
+                } else if (kF8 && inf.kind == kKindPair) {  // raw FP8 tile
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(st + 512 * j + 16 * lane);
+                        const uint32_t fb[4] = {v.x, v.y, v.z, v.w};
+                        uint32_t a0[4], a1[4];
+                        f8_frags<kE5>(fb, a0, a1);
+                        mma_bf16_16816(sc, a0, qf[2 * j][0], qf[2 * j][1]);
+                        mma_bf16_16816(sc, a1, qf[2 * j + 1][0], qf[2 * j + 1][1]);
+                    }
                 } else if (kGa && inf.kind == kKindPair) {  // raw tile: 4 raw 1024-byte blocks
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -465,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                         mma_bf16_16816(sc, a0, qf[2 * j][0], qf[2 * j][1]);
                         mma_bf16_16816(sc, a1, qf[2 * j + 1][0], qf[2 * j + 1][1]);
                     }
-                } else if (!kGa && kCompressed && inf.kind == kKindPair) {
+                } else if (!kTiles && kCompressed && inf.kind == kKindPair) {
                     uint32_t off = 0;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -544,6 +570,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                         mma_bf16_16816(o[2 * j], a0, pb0, pb1);
                         mma_bf16_16816(o[2 * j + 1], a1, pb0, pb1);
                     }
+                } else if (kF8 && inf.kind == kKindPair && !inf.tagsV) {
+                    const uint8_t *tv = st + 4096;
+                    F8Lane<kE5> fs = f8_lane_load<kE5>(tv, lane);
+                    const bool any2 = kE5 && __any_sync(0xffffffffu, fs.modes & 0xAAAAu);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        uint32_t fb[4], a0[4], a1[4];
+                        f8_block_bytes<kE5, true>(tv, ga_row + 256, fs, any2, lane, j, fb);
+                        f8_frags<kE5>(fb, a0, a1);
+                        mma_bf16_16816(o[2 * j], a0, pb0, pb1);
+                        mma_bf16_16816(o[2 * j + 1], a1, pb0, pb1);
+                    }
+                } else if (kF8 && inf.kind == kKindPair) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(st + 4096 + 512 * j + 16 * lane);
+                        const uint32_t fb[4] = {v.x, v.y, v.z, v.w};
+                        uint32_t a0[4], a1[4];
+                        f8_frags<kE5>(fb, a0, a1);
+                        mma_bf16_16816(o[2 * j], a0, pb0, pb1);
+                        mma_bf16_16816(o[2 * j + 1], a1, pb0, pb1);
+                    }
                 } else if (kGa && inf.kind == kKindPair) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -552,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                         mma_bf16_16816(o[2 * j], a0, pb0, pb1);
                         mma_bf16_16816(o[2 * j + 1], a1, pb0, pb1);
                     }
-                } else if (!kGa && kCompressed && inf.kind == kKindPair) {
+                } else if (!kTiles && kCompressed && inf.kind == kKindPair) {
                     uint32_t off = 4096;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -736,17 +784,21 @@ static cudaError_t configure(int dev)
 
 cudaError_t attn_ctas_per_sm(int batch, int *out)
 {
-    // the same split for every format: the smallest occupancy of the three kernels
+    // the same split for every format: the smallest occupancy of the kernels
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = configure<kFmtRaw>(dev);
     if (e == cudaSuccess) e = configure<kFmtZf>(dev);
     if (e == cudaSuccess) e = configure<kFmtGa>(dev);
-    int a = 0, b = 0, c = 0;
+    if (e == cudaSuccess) e = configure<kFmtF8E4>(dev);
+    if (e == cudaSuccess) e = configure<kFmtF8E5>(dev);
+    int a = 0, b = 0, c = 0, d = 0, f = 0;
     if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, k_attn<kFmtRaw>, kThreads, Smem::bytes(batch));
     if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_attn<kFmtZf>, kThreads, Smem::bytes(batch));
     if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, k_attn<kFmtGa>, kThreads, Smem::bytes(batch));
-    *out = e == cudaSuccess ? min(a, min(b, c)) : 0;
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d, k_attn<kFmtF8E4>, kThreads, Smem::bytes(batch));
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&f, k_attn<kFmtF8E5>, kThreads, Smem::bytes(batch));
+    *out = e == cudaSuccess ? min(min(a, min(b, c)), min(d, f)) : 0;
     return e;
 }
 
@@ -772,6 +824,8 @@ cudaError_t launch_attention(const AttnParams &P, int format, const void *tmap, 
     case kFmtRaw: return launch_impl<kFmtRaw>(P, tmap, stream);
     case kFmtZf: return launch_impl<kFmtZf>(P, tmap, stream);
     case kFmtGa: return launch_impl<kFmtGa>(P, tmap, stream);
+    case kFmtF8E4: return launch_impl<kFmtF8E4>(P, tmap, stream);
+    case kFmtF8E5: return launch_impl<kFmtF8E5>(P, tmap, stream);
     default: return cudaErrorInvalidValue;
     }
 }

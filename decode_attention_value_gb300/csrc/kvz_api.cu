@@ -509,6 +509,119 @@ int kvz_selftest_bounded_wait(uint64_t limit_ns, uint32_t *status, uint64_t *out
     return e == cudaSuccess ? KVZ_OK : fail_cuda(e);
 }
 
+// ---------------------------------------------------------------------------------
+// FP8 tiles
+// ---------------------------------------------------------------------------------
+static bool f8_format_ok(int32_t f) { return f == KVZ_F8_E4M3 || f == KVZ_F8_E5M2; }
+
+int kvz_f8_calibrate(kvz_dims dims, int32_t format, const void *raw_pool, int64_t num_raw_pages, const int32_t *pages,
+                     int32_t n, uint8_t *bases, uint32_t *status, kvz_stream_t stream)
+{
+    if (!f8_format_ok(format)) return KVZ_ERR_INVALID_ARG;
+    if (!dims_ok(dims)) return dims.num_kv_heads >= 1 ? KVZ_ERR_UNSUPPORTED : KVZ_ERR_INVALID_ARG;
+    if (n < 0 || num_raw_pages < 0) return KVZ_ERR_INVALID_ARG;
+    if (!bases || !status || (n > 0 && (!raw_pool || !pages))) return KVZ_ERR_INVALID_ARG;
+    if (!aligned(raw_pool, 16) || !aligned(pages, 4) || !aligned(status, 4)) return KVZ_ERR_ALIGNMENT;
+    if (dims.num_kv_heads > (1 << 20)) return KVZ_ERR_UNSUPPORTED;
+    cudaError_t e = launch_f8_calibrate(format, dims.num_kv_heads, static_cast<const uint16_t *>(raw_pool),
+                                        num_raw_pages, pages, n, bases, status, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KVZ_OK : fail_cuda(e);
+}
+
+int kvz_f8_encode_pages(kvz_dims dims, int32_t format, const void *raw_pool, int64_t num_raw_pages,
+                        const uint8_t *bases, const int32_t *src_page, const int32_t *dst_page, const int32_t *dst_seq,
+                        int32_t n, uint32_t *meta, int64_t num_meta_pages, uint8_t *arena, uint64_t arena_bytes,
+                        uint32_t *cursors, int32_t num_cursors, void *workspace, size_t workspace_bytes,
+                        uint32_t *status, kvz_stream_t stream)
+{
+    if (!f8_format_ok(format)) return KVZ_ERR_INVALID_ARG;
+    if (!dims_ok(dims)) return dims.num_kv_heads >= 1 ? KVZ_ERR_UNSUPPORTED : KVZ_ERR_INVALID_ARG;
+    if (n < 0 || num_raw_pages < 0 || num_meta_pages < 0 || num_cursors < 0) return KVZ_ERR_INVALID_ARG;
+    if (n == 0) return KVZ_OK;
+    if (!raw_pool || !bases || !src_page || !dst_page || !dst_seq || !meta || !arena || !cursors || !workspace ||
+        !status)
+        return KVZ_ERR_INVALID_ARG;
+    if (!aligned(raw_pool, 16) || !aligned(bases, 16) || !aligned(meta, 8) || !aligned(arena, 64) ||
+        !aligned(cursors, 8) || !aligned(workspace, 16) || !aligned(status, 4))
+        return KVZ_ERR_ALIGNMENT;
+    if ((int64_t)n * dims.num_kv_heads > (int64_t)1 << 30) return KVZ_ERR_UNSUPPORTED;
+    if (workspace_bytes < kvz_encode_workspace_size(dims, n)) return KVZ_ERR_WORKSPACE;
+    EncodeParams P;
+    memset(&P, 0, sizeof P);
+    P.hkv = dims.num_kv_heads;
+    P.n = n;
+    P.raw_pool = static_cast<const uint16_t *>(raw_pool);
+    P.num_raw_pages = num_raw_pages;
+    P.src_page = src_page;
+    P.dst_page = dst_page;
+    P.dst_seq = dst_seq;
+    P.meta32 = meta;
+    P.ga_bases = bases;
+    P.num_meta_pages = num_meta_pages;
+    P.arena = arena;
+    P.arena_bytes = arena_bytes;
+    P.cursors = cursors;
+    P.num_cursors = num_cursors;
+    P.status = status;
+    uint8_t *w = static_cast<uint8_t *>(workspace);
+    const size_t a = ((size_t)n * 4 + 15) / 16 * 16;
+    P.ws_hdr = reinterpret_cast<uint32_t *>(w);
+    P.ws_page_size = reinterpret_cast<uint32_t *>(w + 16);
+    P.ws_page_base = reinterpret_cast<uint32_t *>(w + 16 + a);
+    P.ws_pair_size = reinterpret_cast<uint32_t *>(w + 16 + 2 * a);
+    cudaError_t e = launch_f8_encode(format, P, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KVZ_OK : fail_cuda(e);
+}
+
+int kvz_f8_decode_blocks(kvz_dims dims, int32_t format, const uint32_t *meta, int64_t num_meta_pages,
+                         const uint8_t *arena, uint64_t arena_bytes, const uint8_t *bases, const int32_t *page,
+                         int32_t n, void *out_pages, uint32_t *status, kvz_stream_t stream)
+{
+    if (!f8_format_ok(format)) return KVZ_ERR_INVALID_ARG;
+    if (!dims_ok(dims)) return dims.num_kv_heads >= 1 ? KVZ_ERR_UNSUPPORTED : KVZ_ERR_INVALID_ARG;
+    if (n < 0 || num_meta_pages < 0) return KVZ_ERR_INVALID_ARG;
+    if (n == 0) return KVZ_OK;
+    if (!meta || !arena || !bases || !page || !out_pages || !status) return KVZ_ERR_INVALID_ARG;
+    if (!aligned(meta, 4) || !aligned(arena, 64) || !aligned(out_pages, 16) || !aligned(status, 4) ||
+        !aligned(bases, 2))
+        return KVZ_ERR_ALIGNMENT;
+    if ((int64_t)n * dims.num_kv_heads > (int64_t)1 << 30) return KVZ_ERR_UNSUPPORTED;
+    DecodeParams P;
+    memset(&P, 0, sizeof P);
+    P.hkv = dims.num_kv_heads;
+    P.n = n;
+    P.meta32 = meta;
+    P.ga_bases = bases;
+    P.num_meta_pages = num_meta_pages;
+    P.arena = arena;
+    P.arena_bytes = arena_bytes;
+    P.page = page;
+    P.out = static_cast<uint16_t *>(out_pages);
+    P.status = status;
+    cudaError_t e = launch_f8_decode(format, P, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KVZ_OK : fail_cuda(e);
+}
+
+int kvz_f8_decode_attention(kvz_dims dims, int32_t format, int32_t batch, int32_t num_q_heads, const void *q,
+                            const int32_t *page_ids, int32_t max_pages, const int32_t *seq_lens,
+                            const int32_t *tail_page, const uint32_t *meta, int64_t num_meta_pages,
+                            const uint8_t *arena, uint64_t arena_bytes, const uint8_t *bases, const void *raw_pool,
+                            int64_t num_raw_pages, float *out, void *workspace, size_t workspace_bytes,
+                            uint32_t *status, kvz_stream_t stream)
+{
+    if (!f8_format_ok(format)) return KVZ_ERR_INVALID_ARG;
+    int rc = check_attention_common(dims, batch, num_q_heads, q, seq_lens, raw_pool, num_raw_pages, out, workspace,
+                                    status, max_pages, page_ids);
+    if (rc || batch == 0) return rc;
+    if (!tail_page || !meta || !arena || !bases || num_meta_pages < 0) return KVZ_ERR_INVALID_ARG;
+    if (!aligned(meta, 8) || !aligned(arena, 64) || !aligned(tail_page, 4) || !aligned(bases, 2))
+        return KVZ_ERR_ALIGNMENT;
+    const int fmt = format == KVZ_F8_E4M3 ? kFmtF8E4 : kFmtF8E5;
+    return run_attention(FormatArgs{fmt, nullptr, meta, bases}, dims, batch, num_q_heads, q, page_ids, max_pages,
+                         seq_lens, tail_page, num_meta_pages, arena, arena_bytes, raw_pool, num_raw_pages, out,
+                         workspace, workspace_bytes, status, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int kvz_apply_cursor_updates(const int32_t *idx, const uint32_t *pos, const uint32_t *end, int32_t n,
                              uint32_t *cursors, int32_t num_cursors, kvz_stream_t stream)
 {

@@ -96,6 +96,10 @@ cudaError_t launch_enc_scan(const EncodeParams &P, cudaStream_t stream);
 cudaError_t launch_ga_encode(const EncodeParams &P, cudaStream_t stream);
 cudaError_t launch_ga_decode(const DecodeParams &P, cudaStream_t stream);
 cudaError_t launch_wait_selftest(uint64_t limit_ns, uint32_t *status, uint64_t *out, cudaStream_t stream);
+cudaError_t launch_f8_calibrate(int fmt, int hkv, const uint16_t *raw_pool, int64_t num_raw_pages,
+                                const int32_t *pages, int n, uint8_t *bases, uint32_t *status, cudaStream_t stream);
+cudaError_t launch_f8_encode(int fmt, const EncodeParams &P, cudaStream_t stream);
+cudaError_t launch_f8_decode(int fmt, const DecodeParams &P, cudaStream_t stream);
 cudaError_t launch_ga_calibrate(int hkv, const uint16_t *raw_pool, int64_t num_raw_pages, const int32_t *pages, int n,
                                 uint8_t *bases, uint32_t *status, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeParams &P, cudaStream_t stream);
@@ -103,8 +107,9 @@ cudaError_t launch_apply_cursor_updates(const int32_t *idx, const uint32_t *pos,
                                         uint32_t *cursors, int num_cursors, cudaStream_t stream);
 // tmap: a CUtensorMap (128-byte object) over the raw pool viewed as
 // [num_raw_pages*Hkv*32 rows][128 BF16], box 64 x 32, 128-byte swizzle.
-// format: 0 plain BF16 pages, 1 12-bit block groups, 2 group-adaptive tiles
-enum AttnFormat : int { kFmtRaw = 0, kFmtZf = 1, kFmtGa = 2 };
+// format: 0 plain BF16 pages, 1 12-bit block groups, 2 group-adaptive tiles,
+// 3 / 4 FP8 E4M3 / E5M2 tiles (completed pages; the tail stays BF16)
+enum AttnFormat : int { kFmtRaw = 0, kFmtZf = 1, kFmtGa = 2, kFmtF8E4 = 3, kFmtF8E5 = 4 };
 cudaError_t launch_attention(const AttnParams &P, int format, const void *tmap, cudaStream_t stream);
 int attn_smem_bytes(int batch);
 // CTAs per SM both attention kernels can hold at this batch size (the smaller of the two)

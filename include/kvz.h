@@ -281,6 +281,52 @@ int kvz_ga_decode_attention(kvz_dims dims, int32_t batch, int32_t num_q_heads, c
                             size_t workspace_bytes, uint32_t *status, kvz_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
+ * FP8 pages: completed pages converted to FP8 and coded losslessly with the
+ * group-adaptive scheme above (GAAC, "Relation to FP8 KV": the codec on KV converted to
+ * FP8, Table 7).  The page gives results only; the format carries the BF16 tile over:
+ *  conversion  BF16 -> FP8 when a page completes: nearest value, ties to even, saturating
+ *              to the largest finite value (infinities included); NaN -> sign | 0x7F.
+ *              E4M3: bias 7, no infinities, max 448; E5M2: bias 15, max 57344.
+ *  tile        2048 FP8 values in storage order, group q = 8L + 2j + f.  With M mantissa
+ *              bits and S = 1 + M (E5M2 3, E4M3 4):
+ *                [0, 256 S)      sign/mantissa fields s << M | m, group q at S*q, element i
+ *                                at bits S*i (little-endian)
+ *                [+0, +768)      3-bit exponent codes, group q at 3q
+ *                [+768, +832)    2-bit modes, group q at byte q/4, bits 2(q%4)
+ *                [+832, +896)    escapes: mode 1 one byte (bit 3 of code i at bit i);
+ *                                mode 2 (E5M2 only) two bytes (bits 3..4 of code i at 2i)
+ *              modes on the exponent field e: 0 if all e - b3 in [0,8), 1 if all e - b4 in
+ *              [0,16), else 2 (code = e); E4M3 has b4 = 0.  E5M2 tile 1664 B (26 granules
+ *              of 64), E4M3 1920 B (30); more than 64 escape bytes: raw tile of 2048 FP8
+ *              bytes, element (L, f, i) of block j at 512j + 16L + 8f + i.
+ *  entries, bases, arena, cursors: as the group-adaptive tiles.  The tail page stays BF16.
+ * --------------------------------------------------------------------------------- */
+#define KVZ_F8_E4M3 1
+#define KVZ_F8_E5M2 2
+
+/* Bases [Hkv][2][2][128] over the FP8 exponent fields of the converted sample pages. */
+int kvz_f8_calibrate(kvz_dims dims, int32_t format, const void *raw_pool, int64_t num_raw_pages,
+                     const int32_t *pages, int32_t n, uint8_t *bases, uint32_t *status, kvz_stream_t stream);
+/* kvz_ga_encode_pages for FP8: converts each completed BF16 page, then codes it. */
+int kvz_f8_encode_pages(kvz_dims dims, int32_t format, const void *raw_pool, int64_t num_raw_pages,
+                        const uint8_t *bases, const int32_t *src_page, const int32_t *dst_page,
+                        const int32_t *dst_seq, int32_t n, uint32_t *meta, int64_t num_meta_pages,
+                        uint8_t *arena, uint64_t arena_bytes, uint32_t *cursors, int32_t num_cursors,
+                        void *workspace, size_t workspace_bytes, uint32_t *status, kvz_stream_t stream);
+/* Decode to the stored FP8 bytes: out uint8 [n][Hkv][2][16][128] (16-B aligned). */
+int kvz_f8_decode_blocks(kvz_dims dims, int32_t format, const uint32_t *meta, int64_t num_meta_pages,
+                         const uint8_t *arena, uint64_t arena_bytes, const uint8_t *bases, const int32_t *page,
+                         int32_t n, void *out_pages, uint32_t *status, kvz_stream_t stream);
+/* kvz_decode_attention over FP8 tiles (values widened exactly to BF16 in registers) plus
+ * the BF16 tail; same workspace, split and determinism. */
+int kvz_f8_decode_attention(kvz_dims dims, int32_t format, int32_t batch, int32_t num_q_heads, const void *q,
+                            const int32_t *page_ids, int32_t max_pages, const int32_t *seq_lens,
+                            const int32_t *tail_page, const uint32_t *meta, int64_t num_meta_pages,
+                            const uint8_t *arena, uint64_t arena_bytes, const uint8_t *bases,
+                            const void *raw_pool, int64_t num_raw_pages, float *out, void *workspace,
+                            size_t workspace_bytes, uint32_t *status, kvz_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
  * Host-side chunk allocator for the arena (GAAC "Block-Wise Compression Scheduling":
  * two fixed storage classes, 768-byte and 1024-byte block slots; ZipFusion: the memory
  * manager tracks the space left, hands chunks freed by one layer or sequence to

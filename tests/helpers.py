@@ -177,3 +177,58 @@ class GaLayer:
         return oracle.ga_decode_attention(kvgen.bits(base.q), base.full.numpy(), base.seq_lens.numpy(),
                                           base.tail.numpy(), self.o_meta if meta is None else meta, self.o_arena,
                                           self.o_bases, self.o_pool, self.cfg.hkv, nthreads=nthreads)
+
+
+class F8Layer:
+    """The same layer with its completed pages converted to FP8 and coded: bases from a
+    sample of the encoded pages, tiles encoded by the GPU and, independently, the oracle."""
+
+    def __init__(self, base: Layer, fmt: int, oracle=None, sample_step: int = 2):
+        kvz, cfg = base.kvz, base.cfg
+        self.base, self.kvz, self.cfg, self.fmt = base, kvz, cfg, fmt
+        hkv = cfg.hkv
+        self.sample = base.src[::sample_step].contiguous() if base.src.numel() else torch.zeros(0, dtype=torch.int32)
+        per_seq = max(cfg.full_pages, 1) * hkv * 2 * 32  # 64-byte granules: worst case (raw 2048 B tiles)
+        self.arena_bytes = cfg.batch * per_seq * 64
+        self.cursors0 = np.array([[b * per_seq, (b + 1) * per_seq] for b in range(cfg.batch)], np.uint32)
+        self.bases = torch.zeros((hkv, 2, 2, 128), dtype=torch.uint8, device="cuda")
+        self.meta = torch.zeros((cfg.num_pages, hkv, 2), dtype=torch.int32, device="cuda")
+        self.arena = torch.zeros(self.arena_bytes, dtype=torch.uint8, device="cuda")
+        self.cursors = torch.from_numpy(self.cursors0.view(np.int32).copy()).cuda()
+        self.status = kvz.new_status()
+        kvz.f8_calibrate(fmt, base.g_pool, self.sample.cuda(), self.bases, self.status)
+        if base.src.numel():
+            s = base.src.cuda()
+            kvz.f8_encode_pages(fmt, base.g_pool, self.bases, s, s, base.dseq.cuda(), self.meta, self.arena,
+                                self.cursors, self.status)
+        torch.cuda.synchronize()
+        assert int(self.status.item()) == 0
+        if oracle is not None and base.pool is not None:
+            self.encode_oracle(oracle)
+
+    def encode_oracle(self, oracle):
+        cfg, base = self.cfg, self.base
+        self.o_pool = kvgen.bits(base.pool)
+        self.o_bases = oracle.f8_calibrate_pool(self.fmt, self.o_pool, self.sample.numpy(), cfg.hkv)
+        self.o_meta = np.zeros((cfg.num_pages, cfg.hkv, 2), np.uint32)
+        self.o_arena = np.zeros(self.arena_bytes, np.uint8)
+        self.o_cursors = self.cursors0.copy()
+        src = base.src.numpy()
+        st = oracle.f8_encode_pages(self.fmt, self.o_pool, self.o_bases, src, src, base.dseq.numpy(), self.o_meta,
+                                    self.o_arena, self.o_cursors, cfg.hkv)
+        assert st == 0
+
+    def run(self, out=None, meta=None, status=None):
+        base = self.base
+        out = torch.empty((self.cfg.batch, self.cfg.hq, 128), dtype=torch.float32, device="cuda") if out is None else out
+        st = self.status if status is None else status
+        self.kvz.f8_decode_attention(self.fmt, base.g_q, base.full.cuda(), base.seq_lens.cuda(), base.tail.cuda(),
+                                     self.meta if meta is None else meta, self.arena, self.bases, base.g_pool, out,
+                                     st, workspace=base.workspace(False))
+        return out
+
+    def oracle_attention(self, oracle, nthreads=8, meta=None):
+        base = self.base
+        return oracle.f8_decode_attention(self.fmt, kvgen.bits(base.q), base.full.numpy(), base.seq_lens.numpy(),
+                                          base.tail.numpy(), self.o_meta if meta is None else meta, self.o_arena,
+                                          self.o_bases, self.o_pool, self.cfg.hkv, nthreads=nthreads)

@@ -1,0 +1,135 @@
+"""GPU parity of the FP8 pages (GAAC "Relation to FP8 KV" with the group-adaptive codec):
+the BF16 -> FP8 conversion over every BF16 word, bases, tile bytes, entries and cursors
+bit-exact against the CPU oracle, bit-exact decode, and attention within the tolerance of
+the fp64 oracle and bit-identical to the raw BF16 kernel over the same (FP8) values."""
+import numpy as np
+import pytest
+import torch
+
+import kvgen
+from helpers import F8Layer, Layer, check_attention
+
+pytestmark = pytest.mark.gpu
+
+FMTS = [1, 2]  # E4M3, E5M2
+
+CASES = [
+    kvgen.C0,
+    kvgen.C0_TAIL,
+    kvgen.KVConfig("ragged-b6", 1, 6, 16, 4, 9, tail_min=1, tail_max=15, k_log2_sigma=(-4, 3),
+                   v_log2_sigma=(-3, 1), k_outlier_channels=4, k_outlier_scale=32.0, block_outlier_frac=0.05,
+                   block_outlier_log2=14, seed=31),
+    kvgen.KVConfig("gqa1", 1, 3, 4, 4, 7, tail_min=3, tail_max=9, seed=32),
+    kvgen.KVConfig("spread", 1, 2, 32, 8, 12, tail_min=1, tail_max=15, spread=(6, 12), seed=34),
+    kvgen.KVConfig("llama-b4", 1, 4, 32, 8, 20, tail_min=1, tail_max=15, k_log2_sigma=(-4, 3),
+                   v_log2_sigma=(-3, 1), k_outlier_channels=4, k_outlier_scale=32.0, seed=35),
+]
+
+
+def _u32(t):
+    return t.cpu().numpy().view(np.uint32)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_conversion_of_every_bf16_word(oracle, fmt):
+    """All 65,536 BF16 words as one pool (16 pages, 1 KV head), encoded and decoded."""
+    import decode_attention_value_gb300 as kvz
+
+    words = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16).reshape(16, 1, 2, 16, 128)
+    pool = torch.from_numpy(words.view(np.int16).copy()).cuda().view(torch.bfloat16)
+    src = torch.arange(16, dtype=torch.int32, device="cuda")
+    bases = torch.zeros((1, 2, 2, 128), dtype=torch.uint8, device="cuda")
+    st = kvz.new_status()
+    kvz.f8_calibrate(fmt, pool, src, bases, st)
+    meta = torch.zeros((16, 1, 2), dtype=torch.int32, device="cuda")
+    arena = torch.zeros(16 * 2 * 2048, dtype=torch.uint8, device="cuda")
+    cur = torch.tensor([[0, 16 * 2 * 32]], dtype=torch.int32, device="cuda")
+    kvz.f8_encode_pages(fmt, pool, bases, src, src, torch.zeros(16, dtype=torch.int32, device="cuda"), meta, arena,
+                        cur, st)
+    out = torch.empty((16, 1, 2, 16, 128), dtype=torch.uint8, device="cuda")
+    kvz.f8_decode_blocks(fmt, meta, arena, bases, src, out, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    want = oracle.f8_quantize(fmt, words)
+    got = out.cpu().numpy()
+    bad = np.flatnonzero(got.reshape(-1) != want.reshape(-1))
+    assert bad.size == 0, [(hex(int(words.reshape(-1)[i])), hex(int(got.reshape(-1)[i])),
+                            hex(int(want.reshape(-1)[i]))) for i in bad[:8]]
+    # the oracle places the same tiles (same bases)
+    o_meta = np.zeros((16, 1, 2), np.uint32)
+    o_arena = np.zeros(arena.numel(), np.uint8)
+    o_cur = np.array([[0, 16 * 2 * 32]], np.uint32)
+    assert oracle.f8_encode_pages(fmt, words, bases.cpu().numpy(), np.arange(16, dtype=np.int32),
+                                  np.arange(16, dtype=np.int32), np.zeros(16, np.int32), o_meta, o_arena, o_cur,
+                                  1) == 0
+    assert np.array_equal(_u32(meta), o_meta) and np.array_equal(arena.cpu().numpy(), o_arena)
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("cfg", CASES, ids=lambda c: c.name)
+def test_codec_and_attention(kvz_lib, oracle, fmt, cfg):
+    kvz = kvz_lib
+    base = Layer(cfg, None)
+    f8 = F8Layer(base, fmt, oracle)
+    assert np.array_equal(f8.bases.cpu().numpy(), f8.o_bases), "bases"
+    assert np.array_equal(_u32(f8.meta), f8.o_meta), "entries"
+    assert np.array_equal(f8.arena.cpu().numpy(), f8.o_arena), "tile bytes"
+    assert np.array_equal(_u32(f8.cursors), f8.o_cursors), "cursors"
+    if base.src.numel():
+        out = torch.empty((base.src.numel(), cfg.hkv, 2, 16, 128), dtype=torch.uint8, device="cuda")
+        st = kvz.new_status()
+        kvz.f8_decode_blocks(fmt, f8.meta, f8.arena, f8.bases, base.src.cuda(), out, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        assert np.array_equal(out.cpu().numpy(), oracle.f8_quantize(fmt, kvgen.bits(base.pool)[base.src.numpy()]))
+    got = f8.run()
+    torch.cuda.synchronize()
+    assert int(f8.status.item()) == 0
+    ref, st = f8.oracle_attention(oracle)
+    assert st == 0
+    check_attention(got, ref, f"{cfg.name} fp8 {fmt}")
+    # the raw BF16 kernel over a pool whose completed pages hold the same FP8 values
+    pool = kvgen.bits(base.pool).copy()
+    src = base.src.numpy()
+    if src.size:
+        q8 = oracle.f8_quantize(fmt, pool[src])
+        vals = np.vectorize(lambda b: oracle.f8_value(fmt, b), otypes=[np.float32])(q8)
+        pool[src] = (vals.view(np.uint32) >> 16).astype(np.uint16)
+    g_pool = torch.from_numpy(pool.view(np.int16)).cuda().view(torch.bfloat16)
+    out_r = torch.empty_like(got)
+    st = kvz.new_status()
+    kvz.decode_attention_raw(base.g_q, base.raw_table().cuda(), base.seq_lens.cuda(), g_pool, out_r, st,
+                             workspace=base.workspace(True))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(got, out_r)
+
+
+@pytest.fixture(scope="module")
+def kvz_lib():
+    from decode_attention_value_gb300 import _build
+
+    _build.build()
+    import decode_attention_value_gb300 as m
+
+    return m
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+def test_bad_entry_flagged(kvz_lib, oracle, fmt):
+    kvz = kvz_lib
+    cfg = kvgen.KVConfig("bad-entry", 1, 3, 8, 2, 5, tail_min=2, tail_max=9, seed=51)
+    base = Layer(cfg, None)
+    f8 = F8Layer(base, fmt, oracle)
+    pid = int(base.full[1, 2])
+    meta = f8.meta.clone()
+    meta[pid, 0, 1] = -1
+    o_meta = f8.o_meta.copy()
+    o_meta[pid, 0, 1] = 0xFFFFFFFF
+    st = kvz.new_status()
+    out = f8.run(meta=meta, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & kvz.STATUS_BAD_META
+    ref, ost = f8.oracle_attention(oracle, meta=o_meta)
+    assert ost & 8
+    check_attention(out, ref, "bad entry")
