@@ -29,35 +29,42 @@ __device__ __forceinline__ void exponent_range(const uint32_t (&w)[8], uint32_t 
 }
 
 // ---------------------------------------------------------------------------------
-// launch 1: group sizes.  One CTA per (entry, head); warp w = block (kv = w/4, j = w%4)
-// reads its 16 x 32 slab (row = lane/2, 32 B per lane) and reduces the exponent range.
+// launch 1: group sizes
 // ---------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_enc_sizes(EncodeParams P, int e0)
+// Warp-per-item size pass: each warp takes whole (entry, head) items in a grid-stride
+// loop, issues all sixteen 16-byte loads of the item's 8 KB at once (lane = row pair of a
+// 16 x 32 slab per block) and reduces the eight blocks itself: no shared memory, no
+// block-wide barrier, many slices in flight per SM.
+__global__ void __launch_bounds__(256, 3) k_enc_sizes_w(EncodeParams P)
 {
-    if (P.ws_hdr[0] != 0) return;  // the call failed validation: nothing is read or written
-    const int entry = e0 + (int)(blockIdx.x / P.hkv), head = (int)(blockIdx.x % P.hkv);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kv = warp >> 2, j = warp & 3;
-    __shared__ uint32_t gran[8];
-    const int src = P.src_page[entry];
-    uint32_t g = 0;
-    {
-        const uint16_t *slab = P.raw_pool + (((int64_t)src * P.hkv + head) * 2 + kv) * kPage * kDim;
-        const uint4 *p = reinterpret_cast<const uint4 *>(slab + (lane >> 1) * kDim + 32 * j + 16 * (lane & 1));
-        uint4 a = p[0], b = p[1];
-        uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        uint32_t mn, mx;
-        exponent_range(w, mn, mx);
-        const uint32_t base = mn & ~1u;
-        g = (mx <= base + 15) ? 3u : 4u;
-    }
-    if (lane == 0) gran[warp] = g;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        uint32_t s = 0;
-        for (int k = 0; k < 8; ++k) s += gran[k];
-        P.ws_pair_size[(int64_t)entry * P.hkv + head] = s;
-        atomicAdd(P.ws_page_size + entry, s);  // integer sum: the same whatever the order
+    if (P.ws_hdr[0] != 0) return;
+    const int lane = threadIdx.x & 31;
+    const int64_t items = (int64_t)P.n * P.hkv;
+    const int64_t stride = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t it = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items; it += stride) {
+        const int entry = (int)(it / P.hkv), head = (int)(it % P.hkv);
+        const uint16_t *slice = P.raw_pool + ((int64_t)P.src_page[entry] * P.hkv + head) * 2 * kPage * kDim;
+        uint4 v[16];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {  // block (kv = b/4, j = b%4)
+            const uint4 *p = reinterpret_cast<const uint4 *>(slice + (b >> 2) * kPage * kDim + (lane >> 1) * kDim +
+                                                             32 * (b & 3) + 16 * (lane & 1));
+            v[2 * b] = p[0];
+            v[2 * b + 1] = p[1];
+        }
+        uint32_t g = 0;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            uint32_t w[8] = {v[2 * b].x, v[2 * b].y, v[2 * b].z, v[2 * b].w,
+                             v[2 * b + 1].x, v[2 * b + 1].y, v[2 * b + 1].z, v[2 * b + 1].w};
+            uint32_t mn, mx;
+            exponent_range(w, mn, mx);
+            g += (mx <= (mn & ~1u) + 15) ? 3u : 4u;
+        }
+        if (lane == 0) {
+            P.ws_pair_size[it] = g;
+            atomicAdd(P.ws_page_size + entry, g);  // integer sum: the same whatever the order
+        }
     }
 }
 
@@ -191,85 +198,104 @@ __global__ void __launch_bounds__(kScanThreads) k_enc_scan(EncodeParams P, int e
 }
 
 // ---------------------------------------------------------------------------------
-// launch 3: pack.  One CTA per (entry, head): stage the K+V slice, each warp gathers
-// its block in storage order, recomputes the tag and writes 768 or 1024 bytes at its
-// place in the group; warps 0 and 4 write the two metadata words.
+// launch 3: pack
 // ---------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_enc_pack(EncodeParams P, int e0)
+// Warp-per-item pack: each warp stages one (entry, head) slice in its own shared-memory
+// buffer, computes the eight tags, places the K and V groups and writes them; items come
+// in a grid-stride loop, so an SM keeps many slices in flight without block-wide barriers.
+constexpr int kPackWarps = 8;
+
+__global__ void __launch_bounds__(kPackWarps * 32, 2) k_enc_pack_w(EncodeParams P)
 {
-    __shared__ __align__(16) uint8_t stage[32 * kStagePitch];
-    __shared__ uint32_t tags[8];
+    extern __shared__ __align__(16) uint8_t pack_smem[];
     if (P.ws_hdr[0] != 0) return;
-    const int entry = e0 + (int)(blockIdx.x / P.hkv), head = (int)(blockIdx.x % P.hkv);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kv = warp >> 2, j = warp & 3;
-    const int src = P.src_page[entry], dst = P.dst_page[entry], seq = P.dst_seq[entry];
-    const uint16_t *slice = P.raw_pool + ((int64_t)src * P.hkv + head) * 2 * kPage * kDim;
-    load_slice_to_stage(slice, stage, threadIdx.x, blockDim.x);
-    __syncthreads();
-
-    uint32_t w[8];
-    gather_block(stage, kv, j, lane, w);
-    uint32_t mn, mx;
-    exponent_range(w, mn, mx);
-    const uint32_t b = mn & ~1u;
-    const bool eligible = mx <= b + 15;
-    const uint32_t tag = eligible ? (b >> 1) : 0xFFu;
-    if (lane == 0) tags[warp] = tag;
-    __syncthreads();
-
-    uint32_t group_tags = 0, before = 0, gsize = 0;
+    uint8_t *stage = pack_smem + warp * (32 * kStagePitch);
+    const int64_t items = (int64_t)P.n * P.hkv;
+    const int64_t stride = (int64_t)gridDim.x * kPackWarps;
+    for (int64_t it = (int64_t)blockIdx.x * kPackWarps + warp; it < items; it += stride) {
+        const int entry = (int)(it / P.hkv), head = (int)(it % P.hkv);
+        const int src = P.src_page[entry], dst = P.dst_page[entry], seq = P.dst_seq[entry];
+        // the heads before this one in the page: one load per lane, then a warp sum
+        const uint32_t ps = lane < head ? P.ws_pair_size[(int64_t)entry * P.hkv + lane] : 0u;
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(P.raw_pool + ((int64_t)src * P.hkv + head) * 2 * kPage * kDim);
+        uint4 v[16];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const uint32_t t = tags[kv * 4 + k];
-        group_tags |= t << (8 * k);
-        if (k < j) before += tag_granules(t);
-        gsize += tag_granules(t);
-    }
-    uint32_t k_size = 0;
+        for (int k = 0; k < 16; ++k) v[k] = s4[lane + 32 * k];
+        uint32_t before_heads = __reduce_add_sync(0xffffffffu, ps);
+        for (int h = 32; h < head; ++h) before_heads += P.ws_pair_size[(int64_t)entry * P.hkv + h];
+        __syncwarp();  // the previous item's gathers are done with the buffer
 #pragma unroll
-    for (int k = 0; k < 4; ++k) k_size += tag_granules(tags[k]);
-    uint64_t pair_base = P.ws_page_base[entry];  // the page's position, then the heads before this one
-    for (int h = 0; h < head; ++h) pair_base += P.ws_pair_size[(int64_t)entry * P.hkv + h];
-    const uint64_t offset0 = pair_base + (kv ? k_size : 0);
-    const uint64_t end = min((uint64_t)P.cursors[2 * seq + 1], P.arena_bytes / kGranule);
-    const bool fits = offset0 + gsize <= end;
-
-    if (fits) {
-        uint8_t *blk = P.arena + (offset0 + before) * kGranule;
-        if (eligible) {
-            uint32_t low[4], code[2];
+        for (int k = 0; k < 16; ++k) {
+            const int q = lane + 32 * k;  // 16-byte chunk q -> row q/16, byte (q%16)*16
+            *reinterpret_cast<uint4 *>(stage + (q >> 4) * kStagePitch + (q & 15) * 16) = v[k];
+        }
+        __syncwarp();
+        uint32_t tagsK = 0, tagsV = 0;  // one tag byte per block
+#pragma unroll 1
+        for (int b = 0; b < 8; ++b) {
+            uint32_t w[8];
+            gather_block(stage, b >> 2, b & 3, lane, w);
+            uint32_t mn, mx;
+            exponent_range(w, mn, mx);
+            const uint32_t base = mn & ~1u;
+            const uint32_t tag = mx <= base + 15 ? (base >> 1) : 0xFFu;
+            if (b < 4) tagsK |= tag << (8 * b);
+            else tagsV |= tag << (8 * (b - 4));
+        }
+        const uint32_t gK = group_granules(tagsK), gV = group_granules(tagsV);
+        const uint64_t pair_base = (uint64_t)P.ws_page_base[entry] + before_heads;
+        const uint64_t end = min((uint64_t)P.cursors[2 * seq + 1], P.arena_bytes / kGranule);
+#pragma unroll 1
+        for (int kv = 0; kv < 2; ++kv) {
+            const uint64_t offset0 = pair_base + (kv ? gK : 0);
+            const uint32_t group_tags = kv ? tagsV : tagsK;
+            const bool fits = offset0 + (kv ? gV : gK) <= end;
+            uint32_t before = 0;
+#pragma unroll 1
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t tag = (group_tags >> (8 * j)) & 0xFFu;
+                if (fits) {
+                    uint32_t w[8];
+                    gather_block(stage, kv, j, lane, w);
+                    uint8_t *blk = P.arena + (offset0 + before) * kGranule;
+                    if (tag != 0xFFu) {
+                        const uint32_t b = tag << 1;
+                        uint32_t low[4], code[2];
 #pragma unroll
-            for (int f = 0; f < 2; ++f) {
-                uint32_t lo03 = 0, lo47 = 0, cw = 0;
+                        for (int f = 0; f < 2; ++f) {
+                            uint32_t lo03 = 0, lo47 = 0, cw = 0;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t v = (w[f * 4 + i / 2] >> (16 * (i & 1))) & 0xFFFFu;
-                    const uint32_t s = v >> 15, e = (v >> 7) & 0xFFu, d = (e - b) >> 1;
-                    const uint32_t lowbyte = v & 0xFFu;
-                    if (i < 4) {
-                        lo03 |= lowbyte << (8 * i);
-                        cw |= ((s << 7) | d) << (8 * i);
+                            for (int i = 0; i < 8; ++i) {
+                                const uint32_t x = (w[f * 4 + i / 2] >> (16 * (i & 1))) & 0xFFFFu;
+                                const uint32_t sg = x >> 15, e = (x >> 7) & 0xFFu, d = (e - b) >> 1;
+                                if (i < 4) {
+                                    lo03 |= (x & 0xFFu) << (8 * i);
+                                    cw |= ((sg << 7) | d) << (8 * i);
+                                } else {
+                                    lo47 |= (x & 0xFFu) << (8 * (i - 4));
+                                    cw |= ((sg << 3) | (d << 4)) << (8 * (i - 4));
+                                }
+                            }
+                            low[2 * f] = lo03;
+                            low[2 * f + 1] = lo47;
+                            code[f] = cw;
+                        }
+                        *reinterpret_cast<uint4 *>(blk + 16 * lane) = make_uint4(low[0], low[1], low[2], low[3]);
+                        *reinterpret_cast<uint2 *>(blk + 512 + 8 * lane) = make_uint2(code[0], code[1]);
                     } else {
-                        lo47 |= lowbyte << (8 * (i - 4));
-                        cw |= ((s << 3) | (d << 4)) << (8 * (i - 4));
+                        *reinterpret_cast<uint4 *>(blk + 32 * lane) = make_uint4(w[0], w[1], w[2], w[3]);
+                        *reinterpret_cast<uint4 *>(blk + 32 * lane + 16) = make_uint4(w[4], w[5], w[6], w[7]);
                     }
                 }
-                low[2 * f] = lo03;
-                low[2 * f + 1] = lo47;
-                code[f] = cw;
+                before += tag_granules(tag);
             }
-            *reinterpret_cast<uint4 *>(blk + 16 * lane) = make_uint4(low[0], low[1], low[2], low[3]);
-            *reinterpret_cast<uint2 *>(blk + 512 + 8 * lane) = make_uint2(code[0], code[1]);
-        } else {
-            *reinterpret_cast<uint4 *>(blk + 32 * lane) = make_uint4(w[0], w[1], w[2], w[3]);
-            *reinterpret_cast<uint4 *>(blk + 32 * lane + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+            if (lane == 0) {
+                const uint64_t off_word = fits ? offset0 : (uint64_t)KVZ_OFFSET_INVALID;
+                P.meta[((int64_t)dst * P.hkv + head) * 2 + kv] = off_word | ((uint64_t)group_tags << 32);
+                if (!fits) atomicOr(P.status, KVZ_STATUS_ARENA_FULL);
+            }
         }
-    }
-    if (lane == 0 && j == 0) {
-        const uint64_t off_word = fits ? offset0 : (uint64_t)KVZ_OFFSET_INVALID;
-        P.meta[((int64_t)dst * P.hkv + head) * 2 + kv] = off_word | ((uint64_t)group_tags << 32);
-        if (!fits) atomicOr(P.status, KVZ_STATUS_ARENA_FULL);
     }
 }
 
@@ -359,15 +385,43 @@ __global__ void k_apply_cursor_updates(const int32_t *idx, const uint32_t *pos, 
 // ---------------------------------------------------------------------------------
 // host launchers
 // ---------------------------------------------------------------------------------
+constexpr int kPackSmem = kPackWarps * 32 * kStagePitch;  // 68 KB: one slice buffer per warp
+
+// SM count of the current device, and the pack kernel's shared-memory opt-in (once per
+// device and process)
+static cudaError_t encode_grid(int *sms)
+{
+    static unsigned long long done = 0;  // bit per device ordinal < 64
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess && !(dev < 64 && ((__atomic_load_n(&done, __ATOMIC_ACQUIRE) >> dev) & 1ull))) {
+        e = cudaFuncSetAttribute(k_enc_pack_w, cudaFuncAttributeMaxDynamicSharedMemorySize, kPackSmem);
+        if (e == cudaSuccess && dev < 64) __atomic_fetch_or(&done, 1ull << dev, __ATOMIC_ACQ_REL);
+    }
+    return e;
+}
+
+// one wave of `per_sm` CTAs per SM, fewer when there are fewer items than warps
+static unsigned grid_for(size_t items, int sms, int per_sm)
+{
+    const size_t want = (items + 7) / 8;
+    const size_t wave = (size_t)(sms > 0 ? sms : 1) * per_sm;
+    return (unsigned)(want < wave ? (want > 0 ? want : 1) : wave);
+}
+
 cudaError_t launch_encode(const EncodeParams &P, cudaStream_t stream)
 {
     cudaError_t e = cudaMemsetAsync(P.ws_hdr, 0, 16 + (size_t)P.n * 4, stream);  // header + page sizes
     if (e != cudaSuccess) return e;
     k_enc_validate<<<(P.n + 255) / 256, 256, 0, stream>>>(P);
-    const unsigned items = (unsigned)((size_t)P.n * P.hkv);
-    k_enc_sizes<<<items, 256, 0, stream>>>(P, 0);
+    const size_t items = (size_t)P.n * P.hkv;
+    int sms = 0;
+    e = encode_grid(&sms);
+    if (e != cudaSuccess) return e;
+    k_enc_sizes_w<<<grid_for(items, sms, 3), 256, 0, stream>>>(P);
     k_enc_scan<<<1, kScanThreads, 0, stream>>>(P, 0, P.n);
-    k_enc_pack<<<items, 256, 0, stream>>>(P, 0);
+    k_enc_pack_w<<<grid_for(items, sms, 2), kPackWarps * 32, kPackSmem, stream>>>(P);
     return cudaGetLastError();
 }
 
@@ -378,7 +432,10 @@ cudaError_t launch_encode_sizes(const EncodeParams &P, cudaStream_t stream)
     if (e == cudaSuccess) e = cudaMemsetAsync(P.ws_page_size, 0, (size_t)P.n * 4, stream);
     if (e != cudaSuccess) return e;
     k_enc_validate<<<(P.n + 255) / 256, 256, 0, stream>>>(P);
-    k_enc_sizes<<<(unsigned)((size_t)P.n * P.hkv), 256, 0, stream>>>(P, 0);
+    int sms = 0;
+    e = encode_grid(&sms);
+    if (e != cudaSuccess) return e;
+    k_enc_sizes_w<<<grid_for((size_t)P.n * P.hkv, sms, 3), 256, 0, stream>>>(P);
     return cudaGetLastError();
 }
 

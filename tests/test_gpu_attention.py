@@ -120,3 +120,23 @@ def test_full_size_layer_sampled(kvz, oracle):
     assert st == 0
     check_attention(out_c[pick], ref, "C1 sample")
     del sub
+
+
+def test_largest_batch_and_beyond(kvz, oracle):
+    """The largest batch the kernel takes (1024 sequences: its per-sequence tables in shared
+    memory lower occupancy to fewer CTAs per SM), ragged lengths with empty sequences;
+    one more sequence is refused on the host."""
+    cfg = kvgen.KVConfig("max-batch", 1, 1024, 8, 2, 2, tail_min=1, tail_max=15, seed=61)
+    rng = np.random.default_rng(61)
+    lens = rng.integers(0, 2 * 16 + 16, 1024)
+    lens[::97] = 0
+    layer = Layer(cfg, oracle, seq_lens=lens.astype(np.int32))
+    run_and_check(layer, oracle, "batch 1024")
+    q = torch.zeros((1025, 8, 128), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((1025, 8, 128), dtype=torch.float32, device="cuda")
+    ids = torch.zeros((1025, 1), dtype=torch.int32, device="cuda")
+    lens1 = torch.zeros(1025, dtype=torch.int32, device="cuda")
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kvz.KvzError) as e:
+        kvz.decode_attention_raw(q, ids, lens1, layer.g_pool, out, kvz.new_status(), workspace=ws)
+    assert e.value.code == -2  # KVZ_ERR_UNSUPPORTED
