@@ -55,8 +55,8 @@ struct Smem {
     static constexpr int info = qempty + 2 * 8;
     static constexpr int q = info + kStages * 16;
     static constexpr int mm = q + 2 * 4 * 256;
-    static constexpr int ml = mm + kConsumers * 4 * 4;
-    static constexpr int mo = ml + kConsumers * 4 * 4;
+    static constexpr int ml = mm + kConsumers * 8 * 4;  // per warp: (max, sum) of up to 8 heads
+    static constexpr int mo = ml + kConsumers * 8 * 4;
     static constexpr int pref = mo + kConsumers * 4 * 128 * 4;
     __host__ __device__ static int tail(int batch) { return pref + (batch + 1) * 4; }
     __host__ __device__ static int bytes(int batch) { return tail(batch) + ((batch + 15) & ~15); }
@@ -151,7 +151,7 @@ __device__ __forceinline__ void mask_v_frag(uint32_t (&a)[4], int lane, int vali
 // ---------------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------------
-template <int kFmt>
+template <int kFmt, bool kG8>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams P, const __grid_constant__ CUtensorMap tmap)
 {
     constexpr bool kCompressed = kFmt != kFmtRaw;
@@ -170,6 +170,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
     uint8_t *tail_len = smem + Smem::tail(P.batch);  // tokens in each sequence's last page if partial, else 0
     StageInfo *info = reinterpret_cast<StageInfo *>(smem + Smem::info);
     const int B = P.batch, hkv = P.hkv, G = P.G;
+    constexpr bool G8 = kG8;  // G = 8: every MMA column is a head, no spare columns
 
     // ---- barriers, and the per-sequence page-count prefix ----
     if (tid == 0) {
@@ -342,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                 if (x == seg_end) {  // new (sequence, KV head) segment: stage its queries
                     const PageLoc L = locate(pref, B, hkv, x);
                     seg_end = min(hi, unit_end(pref, hkv, L));
-                    if (lane == 0 && ok) {
+                    if (lane == 0 && ok && G <= 4) {  // G = 8: the consumers read Q from global memory
                         const int qb = seg & 1, use = seg >> 1;
                         ok = mbar_wait(sbase + Smem::qempty + 8 * qb, (use & 1) ^ 1, P.status);
                         if (ok) {
@@ -391,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                 const int64_t last = (npage - 1 - s) / kStages;
                 mbar_wait(sbase + Smem::full + 8 * s, (uint32_t)(last & 1), P.status);
             }
-            for (int qb = 0; qb < 2 && qb < seg; ++qb) {
+            for (int qb = 0; qb < 2 && qb < seg && G <= 4; ++qb) {
                 const int last = (seg - 1 - qb) / 2;
                 mbar_wait(sbase + Smem::qfull + 8 * qb, (uint32_t)(last & 1), P.status);
             }
@@ -414,9 +415,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
         const int64_t cnt = send - x;
         const uint8_t *ga_row = kTiles ? P.ga_bases + (size_t)L.kvh * 512 : nullptr;  // K b3 row; V at +256
 
-        // queries of this segment: B operand of QK^T, column n = head n % 4 (zero if >= G)
+        // queries of this segment: B operand of QK^T.  G <= 4: column n = head n % 4 (zero if
+        // >= G), staged by the producer; G = 8: column n = head n, read from global memory.
         uint32_t qf[8][2];
-        {
+        if (G8) {
+            const uint32_t *qg = reinterpret_cast<const uint32_t *>(
+                P.q + ((int64_t)L.b * hkv * G + (int64_t)L.kvh * G + g) * kDim);
+#pragma unroll
+            for (int kt = 0; kt < 8; ++kt) {
+                qf[kt][0] = __ldg(qg + 8 * kt + t);
+                qf[kt][1] = __ldg(qg + 8 * kt + t + 4);
+            }
+        } else {
             const int qb = seg & 1, use = seg >> 1;
             if (ok) ok = mbar_wait(sbase + Smem::qfull + 8 * qb, (uint32_t)(use & 1), P.status);
             const int head = g & 3;
@@ -548,16 +558,29 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                 const float p2 = exp2f(sc[2] - u0), p3 = exp2f(sc[3] - u1);
                 l0 += p0 + p2;
                 l1 += p1 + p3;
-                // P split: columns 0..3 (t < 2) carry bf16(p), columns 4..7 carry bf16(p - bf16(p))
+                // P split.  G <= 4: columns 0..3 (t < 2) carry bf16(p), columns 4..7 carry
+                // bf16(p - bf16(p)), one MMA per tile.  G = 8: bf16(p) and the remainder go
+                // through two MMAs into the same accumulator.
                 float v0 = p0, v1 = p1, v2 = p2, v3 = p3;
-                if (t >= 2) {
-                    v0 = p0 - bf16_round(p0);
-                    v1 = p1 - bf16_round(p1);
-                    v2 = p2 - bf16_round(p2);
-                    v3 = p3 - bf16_round(p3);
+                const float r0 = p0 - bf16_round(p0), r1 = p1 - bf16_round(p1);
+                const float r2 = p2 - bf16_round(p2), r3 = p3 - bf16_round(p3);
+                if (!G8 && t >= 2) {  // (the remainders are computed by these lanes only)
+                    v0 = r0;
+                    v1 = r1;
+                    v2 = r2;
+                    v3 = r3;
                 }
                 const uint32_t pb0 = movmatrix_trans(pack_bf16x2(v0, v1));  // tokens 0..7
                 const uint32_t pb1 = movmatrix_trans(pack_bf16x2(v2, v3));  // tokens 8..15
+                uint32_t pl0 = 0, pl1 = 0;
+                if (G8) {
+                    pl0 = movmatrix_trans(pack_bf16x2(r0, r1));
+                    pl1 = movmatrix_trans(pack_bf16x2(r2, r3));
+                }
+                auto pv = [&](float (&acc)[4], const uint32_t (&a)[4]) {
+                    mma_bf16_16816(acc, a, pb0, pb1);
+                    if (G8) mma_bf16_16816(acc, a, pl0, pl1);
+                };
                 // ---- O^T += V^T P^T ----
                 if (kGa && inf.kind == kKindPair && !inf.tagsV) {
                     const uint8_t *tv = st + 4096;
@@ -567,8 +590,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                     for (int j = 0; j < 4; ++j) {
                         uint32_t a0[4], a1[4];
                         ga_block_frags<true>(tv, ga_row + 256, gs, any2, lane, j, a0, a1);
-                        mma_bf16_16816(o[2 * j], a0, pb0, pb1);
-                        mma_bf16_16816(o[2 * j + 1], a1, pb0, pb1);
+                        pv(o[2 * j], a0);
+                        pv(o[2 * j + 1], a1);
                     }
                 } else if (kF8 && inf.kind == kKindPair && !inf.tagsV) {
                     const uint8_t *tv = st + 4096;
@@ -579,8 +602,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                         uint32_t fb[4], a0[4], a1[4];
                         f8_block_bytes<kE5, true>(tv, ga_row + 256, fs, any2, lane, j, fb);
                         f8_frags<kE5>(fb, a0, a1);
-                        mma_bf16_16816(o[2 * j], a0, pb0, pb1);
-                        mma_bf16_16816(o[2 * j + 1], a1, pb0, pb1);
+                        pv(o[2 * j], a0);
+                        pv(o[2 * j + 1], a1);
                     }
                 } else if (kF8 && inf.kind == kKindPair) {
 #pragma unroll
@@ -589,16 +612,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                         const uint32_t fb[4] = {v.x, v.y, v.z, v.w};
                         uint32_t a0[4], a1[4];
                         f8_frags<kE5>(fb, a0, a1);
-                        mma_bf16_16816(o[2 * j], a0, pb0, pb1);
-                        mma_bf16_16816(o[2 * j + 1], a1, pb0, pb1);
+                        pv(o[2 * j], a0);
+                        pv(o[2 * j + 1], a1);
                     }
                 } else if (kGa && inf.kind == kKindPair) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         uint32_t a0[4], a1[4];
                         block_frags(st + 4096 + 1024 * j, 0xFFu, lane, a0, a1);
-                        mma_bf16_16816(o[2 * j], a0, pb0, pb1);
-                        mma_bf16_16816(o[2 * j + 1], a1, pb0, pb1);
+                        pv(o[2 * j], a0);
+                        pv(o[2 * j + 1], a1);
                     }
                 } else if (!kTiles && kCompressed && inf.kind == kKindPair) {
                     uint32_t off = 4096;
@@ -607,8 +630,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                         const uint32_t tag = (inf.tagsV >> (8 * j)) & 0xFFu;
                         uint32_t a0[4], a1[4];
                         block_frags(st + off, tag, lane, a0, a1);
-                        mma_bf16_16816(o[2 * j], a0, pb0, pb1);
-                        mma_bf16_16816(o[2 * j + 1], a1, pb0, pb1);
+                        pv(o[2 * j], a0);
+                        pv(o[2 * j + 1], a1);
                         off += tag_granules(tag) * kGranule;
                     }
                 } else {
@@ -621,8 +644,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                             mask_v_frag(a0, lane, valid);
                             mask_v_frag(a1, lane, valid);
                         }
-                        mma_bf16_16816(o[2 * j], a0, pb0, pb1);
-                        mma_bf16_16816(o[2 * j + 1], a1, pb0, pb1);
+                        pv(o[2 * j], a0);
+                        pv(o[2 * j + 1], a1);
                     }
                 }
             }
@@ -630,59 +653,68 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
             if (lane == 0) mbar_arrive(sbase + Smem::empty + 8 * s);
         }
 
-        // ---- warp state -> shared memory (columns h and h+4 summed) ----
+        // ---- warp state -> shared memory, then the four warps merged (fixed order) into this
+        // segment's partial.  G <= 4: columns h and h+4 summed (hi and lo parts of P), one
+        // pass.  G = 8: heads 0..3 (lanes t < 2) then heads 4..7 (t >= 2), two passes through
+        // the same buffer. ----
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
             l0 += __shfl_xor_sync(0xffffffffu, l0, off);
             l1 += __shfl_xor_sync(0xffffffffu, l1, off);
         }
+        if (!G8) {
 #pragma unroll
-        for (int a = 0; a < 8; ++a)
+            for (int a = 0; a < 8; ++a)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o[a][e] += __shfl_xor_sync(0xffffffffu, o[a][e], 2);
-        if (t < 2) {
-            const int h0 = 2 * t, h1 = 2 * t + 1;
-            if (g == 0) {
-                mm[warp * 4 + h0] = m0;
-                mm[warp * 4 + h1] = m1;
-                mlv[warp * 4 + h0] = l0;
-                mlv[warp * 4 + h1] = l1;
-            }
-#pragma unroll
-            for (int a = 0; a < 8; ++a) {
-                const int d0 = 16 * a + g, d1 = 16 * a + g + 8;
-                mo[(warp * 4 + h0) * 128 + d0] = o[a][0];
-                mo[(warp * 4 + h1) * 128 + d0] = o[a][1];
-                mo[(warp * 4 + h0) * 128 + d1] = o[a][2];
-                mo[(warp * 4 + h1) * 128 + d1] = o[a][3];
-            }
+                for (int e = 0; e < 4; ++e) o[a][e] += __shfl_xor_sync(0xffffffffu, o[a][e], 2);
         }
-        asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");
-        {
-            // ---- merge the four warps (fixed order) and write this segment's partial ----
-            const int d = tid;  // 0..127
-            const int64_t slot = (int64_t)(L.b * hkv + L.kvh) + c;
-            for (int h = 0; h < G; ++h) {
-                float M = NEG_INF;
+        const int64_t slot = (int64_t)(L.b * hkv + L.kvh) + c;
+        const int gs = G8 ? 8 : 4;  // heads per partial slot
+        for (int pass = 0; pass < (G8 ? 2 : 1); ++pass) {
+            if ((t >> 1) == pass) {
+                const int h0 = 2 * t, h1 = 2 * t + 1;  // heads; buffer rows h - 4 * pass
+                if (g == 0) {
+                    mm[warp * 8 + h0] = m0;
+                    mm[warp * 8 + h1] = m1;
+                    mlv[warp * 8 + h0] = l0;
+                    mlv[warp * 8 + h1] = l1;
+                }
 #pragma unroll
-                for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, mm[w * 4 + h]);
-                float Lsum = 0.f, Osum = 0.f;
-                if (M != NEG_INF) {
+                for (int a = 0; a < 8; ++a) {
+                    const int d0 = 16 * a + g, d1 = 16 * a + g + 8;
+                    const int r0 = warp * 4 + h0 - 4 * pass, r1 = warp * 4 + h1 - 4 * pass;
+                    mo[r0 * 128 + d0] = o[a][0];
+                    mo[r1 * 128 + d0] = o[a][1];
+                    mo[r0 * 128 + d1] = o[a][2];
+                    mo[r1 * 128 + d1] = o[a][3];
+                }
+            }
+            asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");
+            {
+                const int d = tid;  // 0..127
+                const int hend = min(G, 4 * pass + 4);
+                for (int h = 4 * pass; h < hend; ++h) {
+                    float M = NEG_INF;
 #pragma unroll
-                    for (int w = 0; w < kConsumers; ++w) {
-                        const float sw = exp2f(mm[w * 4 + h] - M);
-                        Lsum += sw * mlv[w * 4 + h];
-                        Osum += sw * mo[(w * 4 + h) * 128 + d];
+                    for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, mm[w * 8 + h]);
+                    float Lsum = 0.f, Osum = 0.f;
+                    if (M != NEG_INF) {
+#pragma unroll
+                        for (int w = 0; w < kConsumers; ++w) {
+                            const float sw = exp2f(mm[w * 8 + h] - M);
+                            Lsum += sw * mlv[w * 8 + h];
+                            Osum += sw * mo[(w * 4 + h - 4 * pass) * 128 + d];
+                        }
+                    }
+                    P.part_o[(slot * gs + h) * 128 + d] = Osum;
+                    if (d == 0) {
+                        P.part_ml[(slot * gs + h) * 2 + 0] = M;
+                        P.part_ml[(slot * gs + h) * 2 + 1] = Lsum;
                     }
                 }
-                P.part_o[(slot * 4 + h) * 128 + d] = Osum;
-                if (d == 0) {
-                    P.part_ml[(slot * 4 + h) * 2 + 0] = M;
-                    P.part_ml[(slot * 4 + h) * 2 + 1] = Lsum;
-                }
             }
+            asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");
         }
-        asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");
         x = send;
         ibase += cnt;
         ++seg;
@@ -711,56 +743,60 @@ __global__ void __launch_bounds__(128) k_attn_merge(const AttnParams P)
     // CTAs between the first and last owner with an empty range (T < C) wrote nothing.
     const int64_t S = (int64_t)hkv * pb + (int64_t)kvh * n, E = S + n;
     const int64_t c0 = (S * C) / T, c1 = ((E - 1) * C) / T;
-    float M[4], Ls[4], Os[4];
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-        M[h] = -INFINITY;
-        Ls[h] = 0.f;
-        Os[h] = 0.f;
-    }
-    // running merge over chunks of slots; within a chunk every load is independent
-    for (int64_t cb = c0; cb <= c1; cb += kMergeChunk) {
-        float mv[kMergeChunk][4], lv[kMergeChunk][4], ov[kMergeChunk][4];
-#pragma unroll
-        for (int k = 0; k < kMergeChunk; ++k) {
-            const int64_t c = cb + k;
-            const bool w = c <= c1 && (c * T + C - 1) / C < ((c + 1) * T + C - 1) / C;
-            const int64_t slot = u + c;
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                mv[k][h] = -INFINITY;
-                lv[k][h] = 0.f;
-                ov[k][h] = 0.f;
-                if (w && h < G) {
-                    const float2 ml = *reinterpret_cast<const float2 *>(P.part_ml + (slot * 4 + h) * 2);
-                    mv[k][h] = ml.x;
-                    lv[k][h] = ml.y;
-                    ov[k][h] = P.part_o[(slot * 4 + h) * 128 + d];
-                }
-            }
-        }
+    const int gs = G == 8 ? 8 : 4;  // heads per partial slot
+    // heads in blocks of four (two blocks for G = 8)
+    for (int hb = 0; hb < G; hb += 4) {
+        float M[4], Ls[4], Os[4];
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-            float m = M[h];
-#pragma unroll
-            for (int k = 0; k < kMergeChunk; ++k) m = fmaxf(m, mv[k][h]);
-            if (m == -INFINITY) continue;
-            const float r = exp2f(M[h] - m);  // M[h] = -inf -> 0
-            float l = Ls[h] * r, o = Os[h] * r;
+            M[h] = -INFINITY;
+            Ls[h] = 0.f;
+            Os[h] = 0.f;
+        }
+        // running merge over chunks of slots; within a chunk every load is independent
+        for (int64_t cb = c0; cb <= c1; cb += kMergeChunk) {
+            float mv[kMergeChunk][4], lv[kMergeChunk][4], ov[kMergeChunk][4];
 #pragma unroll
             for (int k = 0; k < kMergeChunk; ++k) {
-                const float wgt = exp2f(mv[k][h] - m);
-                l += wgt * lv[k][h];
-                o += wgt * ov[k][h];
-            }
-            M[h] = m;
-            Ls[h] = l;
-            Os[h] = o;
-        }
-    }
+                const int64_t c = cb + k;
+                const bool w = c <= c1 && (c * T + C - 1) / C < ((c + 1) * T + C - 1) / C;
+                const int64_t slot = u + c;
 #pragma unroll
-    for (int h = 0; h < 4; ++h)
-        if (h < G) out[h * kDim + d] = Ls[h] > 0.f ? Os[h] / Ls[h] : 0.f;
+                for (int h = 0; h < 4; ++h) {
+                    mv[k][h] = -INFINITY;
+                    lv[k][h] = 0.f;
+                    ov[k][h] = 0.f;
+                    if (w && hb + h < G) {
+                        const float2 ml = *reinterpret_cast<const float2 *>(P.part_ml + (slot * gs + hb + h) * 2);
+                        mv[k][h] = ml.x;
+                        lv[k][h] = ml.y;
+                        ov[k][h] = P.part_o[(slot * gs + hb + h) * 128 + d];
+                    }
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                float m = M[h];
+#pragma unroll
+                for (int k = 0; k < kMergeChunk; ++k) m = fmaxf(m, mv[k][h]);
+                if (m == -INFINITY) continue;
+                const float r = exp2f(M[h] - m);  // M[h] = -inf -> 0
+                float l = Ls[h] * r, o = Os[h] * r;
+#pragma unroll
+                for (int k = 0; k < kMergeChunk; ++k) {
+                    const float wgt = exp2f(mv[k][h] - m);
+                    l += wgt * lv[k][h];
+                    o += wgt * ov[k][h];
+                }
+                M[h] = m;
+                Ls[h] = l;
+                Os[h] = o;
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+            if (hb + h < G) out[(hb + h) * kDim + d] = Ls[h] > 0.f ? Os[h] / Ls[h] : 0.f;
+    }
 }
 
 // ---------------------------------------------------------------------------------
@@ -768,66 +804,83 @@ __global__ void __launch_bounds__(128) k_attn_merge(const AttnParams P)
 // ---------------------------------------------------------------------------------
 int attn_smem_bytes(int batch) { return Smem::bytes(batch); }
 
-template <int kFmt>
+template <int kFmt, bool kG8>
 static cudaError_t configure(int dev)
 {
     // per process and device: allow the full shared-memory carve-out (attributes are per function)
     static unsigned long long done = 0;  // bit per device ordinal < 64
     if (dev < 64 && (__atomic_load_n(&done, __ATOMIC_ACQUIRE) >> dev) & 1ull) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(k_attn<kFmt>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn<kFmt>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    cudaError_t e = cudaFuncSetAttribute(k_attn<kFmt, kG8>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_attn<kFmt, kG8>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     // the merge runs between attention launches: same carve-out, no reconfiguration
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn_merge, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e == cudaSuccess && dev < 64) __atomic_fetch_or(&done, 1ull << dev, __ATOMIC_ACQ_REL);
     return e;
 }
 
-cudaError_t attn_ctas_per_sm(int batch, int *out)
+template <int kFmt, bool kG8>
+static cudaError_t occupancy(int dev, int batch, int *n)
 {
-    // the same split for every format: the smallest occupancy of the kernels
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = configure<kFmtRaw>(dev);
-    if (e == cudaSuccess) e = configure<kFmtZf>(dev);
-    if (e == cudaSuccess) e = configure<kFmtGa>(dev);
-    if (e == cudaSuccess) e = configure<kFmtF8E4>(dev);
-    if (e == cudaSuccess) e = configure<kFmtF8E5>(dev);
-    int a = 0, b = 0, c = 0, d = 0, f = 0;
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, k_attn<kFmtRaw>, kThreads, Smem::bytes(batch));
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_attn<kFmtZf>, kThreads, Smem::bytes(batch));
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c, k_attn<kFmtGa>, kThreads, Smem::bytes(batch));
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&d, k_attn<kFmtF8E4>, kThreads, Smem::bytes(batch));
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&f, k_attn<kFmtF8E5>, kThreads, Smem::bytes(batch));
-    *out = e == cudaSuccess ? min(min(a, min(b, c)), min(d, f)) : 0;
+    cudaError_t e = configure<kFmt, kG8>(dev);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, k_attn<kFmt, kG8>, kThreads, Smem::bytes(batch));
     return e;
 }
 
-template <int kFmt>
+cudaError_t attn_ctas_per_sm(int batch, int *out)
+{
+    // the same split for every format and group size: the smallest occupancy of the kernels
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    int n[10] = {0};
+    if (e == cudaSuccess) e = occupancy<kFmtRaw, false>(dev, batch, &n[0]);
+    if (e == cudaSuccess) e = occupancy<kFmtZf, false>(dev, batch, &n[1]);
+    if (e == cudaSuccess) e = occupancy<kFmtGa, false>(dev, batch, &n[2]);
+    if (e == cudaSuccess) e = occupancy<kFmtF8E4, false>(dev, batch, &n[3]);
+    if (e == cudaSuccess) e = occupancy<kFmtF8E5, false>(dev, batch, &n[4]);
+    if (e == cudaSuccess) e = occupancy<kFmtRaw, true>(dev, batch, &n[5]);
+    if (e == cudaSuccess) e = occupancy<kFmtZf, true>(dev, batch, &n[6]);
+    if (e == cudaSuccess) e = occupancy<kFmtGa, true>(dev, batch, &n[7]);
+    if (e == cudaSuccess) e = occupancy<kFmtF8E4, true>(dev, batch, &n[8]);
+    if (e == cudaSuccess) e = occupancy<kFmtF8E5, true>(dev, batch, &n[9]);
+    int m = n[0];
+    for (int k = 1; k < 10; ++k) m = min(m, n[k]);
+    *out = e == cudaSuccess ? m : 0;
+    return e;
+}
+
+template <int kFmt, bool kG8>
 static cudaError_t launch_impl(const AttnParams &P, const void *tmap, cudaStream_t stream)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = configure<kFmt>(dev);
+    if (e == cudaSuccess) e = configure<kFmt, kG8>(dev);
     if (e != cudaSuccess) return e;
     CUtensorMap map;
     memcpy(&map, tmap, sizeof(map));
-    k_attn<kFmt><<<P.grid, kThreads, Smem::bytes(P.batch), stream>>>(P, map);
+    k_attn<kFmt, kG8><<<P.grid, kThreads, Smem::bytes(P.batch), stream>>>(P, map);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     k_attn_merge<<<P.batch * P.hkv, 128, 0, stream>>>(P);
     return cudaGetLastError();
 }
 
-cudaError_t launch_attention(const AttnParams &P, int format, const void *tmap, cudaStream_t stream)
+template <bool kG8>
+static cudaError_t launch_format(const AttnParams &P, int format, const void *tmap, cudaStream_t stream)
 {
     switch (format) {
-    case kFmtRaw: return launch_impl<kFmtRaw>(P, tmap, stream);
-    case kFmtZf: return launch_impl<kFmtZf>(P, tmap, stream);
-    case kFmtGa: return launch_impl<kFmtGa>(P, tmap, stream);
-    case kFmtF8E4: return launch_impl<kFmtF8E4>(P, tmap, stream);
-    case kFmtF8E5: return launch_impl<kFmtF8E5>(P, tmap, stream);
+    case kFmtRaw: return launch_impl<kFmtRaw, kG8>(P, tmap, stream);
+    case kFmtZf: return launch_impl<kFmtZf, kG8>(P, tmap, stream);
+    case kFmtGa: return launch_impl<kFmtGa, kG8>(P, tmap, stream);
+    case kFmtF8E4: return launch_impl<kFmtF8E4, kG8>(P, tmap, stream);
+    case kFmtF8E5: return launch_impl<kFmtF8E5, kG8>(P, tmap, stream);
     default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_attention(const AttnParams &P, int format, const void *tmap, cudaStream_t stream)
+{
+    return P.G == 8 ? launch_format<true>(P, format, tmap, stream) : launch_format<false>(P, format, tmap, stream);
 }
 
 }  // namespace kvz

@@ -106,7 +106,7 @@ int check_attention_common(const kvz_dims &d, int batch, int hq, const void *q, 
     if (batch < 0 || hq < 1 || max_pages < 0 || num_raw_pages < 0) return KVZ_ERR_INVALID_ARG;
     if (hq % d.num_kv_heads != 0) return KVZ_ERR_INVALID_ARG;
     const int G = hq / d.num_kv_heads;
-    if (G != 1 && G != 2 && G != 4) return KVZ_ERR_UNSUPPORTED;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return KVZ_ERR_UNSUPPORTED;
     if (batch > kMaxBatch) return KVZ_ERR_UNSUPPORTED;
     if (batch == 0) return KVZ_OK;
     if (!q || !seq_lens || !out || !ws || !status || (max_pages > 0 && !page_ids)) return KVZ_ERR_INVALID_ARG;
@@ -135,7 +135,7 @@ int run_attention(const FormatArgs &F, const kvz_dims &d, int batch, int hq, con
     int grid = 0;
     int rc = attention_grid(batch, hkv, table_pages, &grid);
     if (rc) return rc;
-    if (attn_ws_bytes(batch, hkv, grid) > ws_bytes) return KVZ_ERR_WORKSPACE;
+    if (attn_ws_bytes(batch, hkv, grid, hq / hkv) > ws_bytes) return KVZ_ERR_WORKSPACE;
     CUtensorMap map;
     // a pool with no pages still needs a valid map object; it is never dereferenced
     rc = raw_tensor_map(raw_pool ? raw_pool : ws, num_raw_pages > 0 ? num_raw_pages : 1, hkv, &map);
@@ -164,7 +164,7 @@ int run_attention(const FormatArgs &F, const kvz_dims &d, int batch, int hq, con
     w += attn_ws_prefix_bytes(batch);
     const size_t slots = attn_slots(batch, hkv, grid);
     P.part_o = reinterpret_cast<float *>(w);
-    w += slots * 4 * 128 * 4;
+    w += slots * attn_slot_heads(hq / hkv) * 128 * 4;
     P.part_ml = reinterpret_cast<float *>(w);
     P.status = status;
     P.scale_log2 = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e) / sqrt(128)
@@ -338,7 +338,7 @@ size_t kvz_attention_workspace_size(kvz_dims dims, int32_t batch, int32_t num_q_
     if (batch == 0) return 16;
     int grid = 0;
     if (attention_grid(batch, dims.num_kv_heads, table_pages, &grid) != KVZ_OK) return 0;
-    return attn_ws_bytes(batch, dims.num_kv_heads, grid);
+    return attn_ws_bytes(batch, dims.num_kv_heads, grid, num_q_heads / dims.num_kv_heads);
 }
 
 int kvz_decode_attention(kvz_dims dims, int32_t batch, int32_t num_q_heads, const void *q, const int32_t *page_ids,
@@ -389,7 +389,8 @@ int kvz_decode_attention_noalloc(kvz_dims dims, int32_t batch, int32_t num_q_hea
     int grid = 0;
     rc = attention_grid(batch, dims.num_kv_heads, max_pages + 1, &grid);
     if (rc) return rc;
-    if (attn_ws_bytes(batch, dims.num_kv_heads, grid) > (size_t)KVZ_NOALLOC_SCRATCH_BYTES) return KVZ_ERR_NOALLOC_LIMIT;
+    if (attn_ws_bytes(batch, dims.num_kv_heads, grid, num_q_heads / dims.num_kv_heads) > (size_t)KVZ_NOALLOC_SCRATCH_BYTES)
+        return KVZ_ERR_NOALLOC_LIMIT;
     return run_attention(FormatArgs{kFmtZf, meta, nullptr, nullptr}, dims, batch, num_q_heads, q, page_ids,
                          max_pages, seq_lens, tail_page, num_meta_pages, arena, arena_bytes, raw_pool, num_raw_pages,
                          out, scratch, KVZ_NOALLOC_SCRATCH_BYTES, status, reinterpret_cast<cudaStream_t>(stream));

@@ -88,10 +88,10 @@ def test_host_rejects_bad_arguments(kvz):
     # decode: misaligned output
     assert lib.kvz_decode_blocks(_dims(kvz), fake, 1, fake, 1 << 20, fake, 1, fake + 2, fake, None) == E["align"]
     assert lib.kvz_decode_blocks(_dims(kvz), None, 0, None, 0, None, 0, None, None, None) == 0
-    # attention: GQA group must divide and be 1, 2 or 4
+    # attention: GQA group must divide and be 1, 2, 4 or 8
     assert lib.kvz_decode_attention(_dims(kvz), 2, 12, fake, fake, 4, fake, fake, fake, 1, fake, 1 << 20, fake, 1,
                                     fake, fake, 1 << 20, fake, None) == E["inval"]
-    assert lib.kvz_decode_attention(_dims(kvz), 2, 64, fake, fake, 4, fake, fake, fake, 1, fake, 1 << 20, fake, 1,
+    assert lib.kvz_decode_attention(_dims(kvz), 2, 128, fake, fake, 4, fake, fake, fake, 1, fake, 1 << 20, fake, 1,
                                     fake, fake, 1 << 20, fake, None) == E["unsup"]
     assert lib.kvz_decode_attention_raw(_dims(kvz), 2, 32, fake + 8, fake, 4, fake, fake, 1, fake, fake, 1 << 20,
                                         fake, None) == E["align"]

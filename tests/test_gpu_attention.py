@@ -42,6 +42,11 @@ CASES = [
                    block_outlier_log2=14, seed=31),
     kvgen.KVConfig("gqa1", 1, 3, 4, 4, 7, tail_min=3, tail_max=9, seed=32),
     kvgen.KVConfig("gqa2", 1, 3, 8, 4, 7, tail_min=3, tail_max=9, seed=33),
+    # G = 8 (e.g. 64 query heads over 8 KV heads): every MMA column a head
+    kvgen.KVConfig("gqa8", 1, 5, 16, 2, 11, tail_min=1, tail_max=15, k_log2_sigma=(-4, 3), v_log2_sigma=(-3, 1),
+                   k_outlier_channels=4, k_outlier_scale=32.0, block_outlier_frac=0.05, seed=36),
+    kvgen.KVConfig("gqa8-llama70b-shape", 1, 4, 64, 8, 40, tail_min=1, tail_max=15, k_log2_sigma=(-4, 3),
+                   v_log2_sigma=(-3, 1), k_outlier_channels=4, k_outlier_scale=32.0, seed=37),
     kvgen.KVConfig("spread", 1, 2, 32, 8, 12, tail_min=1, tail_max=15, spread=(8, 20), seed=34),
 ]
 

@@ -20,6 +20,7 @@ CASES = [
                    v_log2_sigma=(-3, 1), k_outlier_channels=4, k_outlier_scale=32.0, block_outlier_frac=0.05,
                    block_outlier_log2=14, seed=31),
     kvgen.KVConfig("gqa1", 1, 3, 4, 4, 7, tail_min=3, tail_max=9, seed=32),
+    kvgen.KVConfig("gqa8", 1, 5, 16, 2, 11, tail_min=1, tail_max=15, seed=36),
     kvgen.KVConfig("spread", 1, 2, 32, 8, 12, tail_min=1, tail_max=15, spread=(6, 12), seed=34),
     kvgen.KVConfig("llama-b4", 1, 4, 32, 8, 20, tail_min=1, tail_max=15, k_log2_sigma=(-4, 3),
                    v_log2_sigma=(-3, 1), k_outlier_channels=4, k_outlier_scale=32.0, seed=35),

@@ -31,6 +31,8 @@ CASES = [
                    block_outlier_log2=14, seed=31),
     kvgen.KVConfig("gqa1", 1, 3, 4, 4, 7, tail_min=3, tail_max=9, seed=32),
     kvgen.KVConfig("gqa2", 1, 3, 8, 4, 7, tail_min=3, tail_max=9, seed=33),
+    kvgen.KVConfig("gqa8", 1, 5, 16, 2, 11, tail_min=1, tail_max=15, k_log2_sigma=(-4, 3), v_log2_sigma=(-3, 1),
+                   seed=36),
     # wide exponent spreads: many 4-bit and raw groups, some tiles fall back to raw
     kvgen.KVConfig("spread", 1, 2, 32, 8, 12, tail_min=1, tail_max=15, spread=(6, 12), seed=34),
     kvgen.KVConfig("llama-b4", 1, 4, 32, 8, 20, tail_min=1, tail_max=15, k_log2_sigma=(-4, 3),
@@ -88,10 +90,11 @@ def _tile_modes(ga):
 def test_mode_mix_is_exercised(kvz, oracle):
     """The cases above hold every group mode inside compressed tiles and both tile
     classes: wide spreads overflow the escape slot, injected outliers need raw groups."""
-    raw, modes = _tile_modes(GaLayer(Layer(CASES[5], None), None))
+    by_name = {c.name: c for c in CASES}
+    raw, modes = _tile_modes(GaLayer(Layer(by_name["spread"], None), None))
     assert raw.any() and (~raw).any()
     assert modes[0] > 0 and modes[1] > 0
-    raw, modes = _tile_modes(GaLayer(Layer(CASES[2], None), None))
+    raw, modes = _tile_modes(GaLayer(Layer(by_name["ragged-b6"], None), None))
     assert modes[0] > 0 and modes[1] > 0 and modes[2] > 0 and modes[3] == 0, modes
 
 
