@@ -145,3 +145,36 @@ def test_largest_batch_and_beyond(kvz, oracle):
     with pytest.raises(kvz.KvzError) as e:
         kvz.decode_attention_raw(q, ids, lens1, layer.g_pool, out, kvz.new_status(), workspace=ws)
     assert e.value.code == -2  # KVZ_ERR_UNSUPPORTED
+
+
+def test_corrupt_metadata_fuzz(kvz, oracle):
+    """Random unusable metadata words (invalid tag bytes, offsets past the arena, the
+    unwritten-group marker) on random pages: every one is flagged, no page is read from
+    outside the arena, and the output equals the oracle's with the same pages left out."""
+    cfg = kvgen.KVConfig("fuzz", 1, 6, 16, 4, 8, tail_min=1, tail_max=15, seed=71)
+    layer = Layer(cfg, oracle)
+    rng = np.random.default_rng(71)
+    meta = layer.meta.clone()
+    o_meta = layer.o_meta.copy()
+    pages = rng.choice(layer.src.numpy(), 10, replace=False)
+    arena_granules = layer.arena_bytes // 256
+    for k, p in enumerate(pages):
+        h, kv = int(rng.integers(0, cfg.hkv)), int(rng.integers(0, 2))
+        word = int(o_meta[p, h, kv])
+        kind = k % 3
+        if kind == 0:  # a tag byte between 0x80 and 0xFE
+            j = int(rng.integers(0, 4))
+            word = (word & ~(0xFF << (32 + 8 * j))) | (int(rng.integers(0x80, 0xFF)) << (32 + 8 * j))
+        elif kind == 1:  # a group that would end past the arena
+            word = (word & ~0xFFFFFFFF) | int(rng.integers(arena_granules - 8, 0xFFFFFFF0))
+        else:  # the unwritten-group marker
+            word = (word & ~0xFFFFFFFF) | 0xFFFFFFFF
+        o_meta[p, h, kv] = np.uint64(word)
+        meta[p, h, kv] = int(np.uint64(word).view(np.int64))
+    st = kvz.new_status()
+    out = layer.run_compressed(meta=meta, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == kvz.STATUS_BAD_META
+    ref, ost = layer.oracle_attention(oracle, meta=o_meta)
+    assert ost == 8
+    check_attention(out, ref, "fuzzed metadata")
