@@ -345,7 +345,26 @@ def per_launch_ms(fn, iters: int, flush: torch.Tensor) -> float:
 # --------------------------------------------------------------------------------------
 # CPU oracle (cpu_baseline and the reference arm)
 # --------------------------------------------------------------------------------------
-def oracle_sample(cfg: kvgen.KVConfig, budget_s: float, seqs_max: int | None = None):
+def oracle_encode_rate(cfg: kvgen.KVConfig, mib: int = 64) -> float:
+    """The CPU oracle's encoder (scalar, one thread) on `mib` MiB of the workload's pages:
+    BF16 GB/s in."""
+    import oracle
+
+    oracle.build()
+    n = max(1, (mib << 20) // (cfg.hkv * 8192))
+    pool = kvgen.bits(kvgen.gen_pages(cfg, n))
+    src = np.arange(n, dtype=np.int32)
+    meta = np.zeros((n, cfg.hkv, 2), np.uint64)
+    arena = np.zeros(n * cfg.hkv * 8192, np.uint8)
+    cur = np.array([[0, arena.size // 256]], np.uint32)
+    t0 = time.perf_counter()
+    st = oracle.encode_pages(pool, src, src, np.zeros(n, np.int32), meta, arena, cur, cfg.hkv)
+    dt = time.perf_counter() - t0
+    assert st == 0
+    return pool.nbytes / dt / 1e9
+
+
+def oracle_sample(cfg: kvgen.KVConfig, budget_s: float, seqs_max: int | None = None, threads: int | None = None):
     """Time the CPU oracle's decode attention (decode of the compressed pages + fp64
     attention) on the workload's sequences, on all host cores: as many sequences as the
     budget allows, repeated until about `budget_s` seconds of work have been timed.
@@ -357,7 +376,7 @@ def oracle_sample(cfg: kvgen.KVConfig, budget_s: float, seqs_max: int | None = N
     table, seq_lens = lay["table"].numpy(), lay["seq_lens"].numpy()
     pool = kvgen.bits(kvgen.gen_pages(cfg, cfg.num_pages))
     q = kvgen.bits(kvgen.gen_q(cfg))
-    threads = os.cpu_count() or 1
+    threads = threads or os.cpu_count() or 1
 
     def prepare(sel):
         full = table[sel, : cfg.full_pages]
@@ -406,6 +425,9 @@ def main():
                     help="c2: one step = all layers of the stack, each with its own KV (else one layer per step)")
     ap.add_argument("--sweep", action="store_true",
                     help="encode / standalone-decode throughput over 64 MB .. 4 GB of pages (exponent-spread KV)")
+    ap.add_argument("--spread-sweep", action="store_true",
+                    help="long-context layer (B=2, 131072 tokens) with the per-block exponent spread fixed at each "
+                         "of 8..20: compressed fraction and attention time, compressed vs raw")
     ap.add_argument("--copies", type=int, default=3)
     ap.add_argument("--format", default="zf", choices=["zf", "ga", "f8e4", "f8e5"],
                     help="ga: group-adaptive additive tiles; f8e4 / f8e5: completed pages converted to FP8 "
@@ -422,6 +444,8 @@ def main():
     dist, rank, world, local = dist_setup()
     if args.sweep:
         return run_sweep(args, dist, rank, local)
+    if args.spread_sweep:
+        return run_spread_sweep(args, dist, rank, local)
     if args.workload == "c3":
         return run_stream(args, cfg, dist, rank, world, local)
     if args.workload == "serve":
@@ -564,6 +588,11 @@ def main():
         cpu = {"value": round(gbps, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": f"{nseq} of {cfg.batch} sequences x {cfg.hkv} KV heads of the same layer "
                          f"(decode of compressed pages + fp64 attention), {passes} passes, {secs:.1f} s"}
+        g1, s1, n1, p1, _ = oracle_sample(cfg, min(4.0, args.cpu_budget / 3), threads=1)
+        cpu["extra"] = {"attention_1core_GBps": round(g1, 3),
+                        "attention_1core_sample": f"{n1} sequences, {p1} passes, {s1:.1f} s",
+                        "encode_1core_GBps": round(oracle_encode_rate(cfg), 3),
+                        "encode_sample": "64 MiB of the layer's pages, scalar oracle encoder, one thread"}
 
     traffic = profiled_traffic(args.workload)
     line = {
@@ -1198,6 +1227,46 @@ def run_stream(args, cfg, dist, rank, world, local):
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def run_spread_sweep(args, dist, rank, local):
+    """The C4 shape (B=2, 8192 full pages + tail, 32/8 heads) with every block's exponent
+    spread fixed at S = 8..20, which moves the compressed fraction from 1 to 0 (eligible
+    iff S <= 14, or S = 15 with an even lowest exponent).  Per S: compressed fraction,
+    bytes ratio, µs per step compressed and raw (graph replays over 3 rotating copies)."""
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    rows = []
+    for S in range(8, 21):
+        cfg = kvgen.KVConfig(f"long-ctx-spread{S}", 1, 2, 32, 8, 8192, tail_min=1, tail_max=15, spread=(S, S),
+                             seed=400 + S)
+        W = Workload(cfg, 3, dev=dev)
+        for k in range(3):
+            W.step_c(k)
+            W.step_r(k)
+        torch.cuda.synchronize()
+        if int(W.status.item()) != 0 or not torch.equal(W.out, W.out_raw):
+            raise RuntimeError(f"S={S}: status {int(W.status.item())} or outputs differ")
+        K = max(10, min(args.steps, 30))
+        g_c, g_r = graph_of(W.step_c, K), graph_of(W.step_r, K)
+        g_c.replay()
+        g_r.replay()
+        ms_c, ms_r = time_graph(g_c), time_graph(g_r)
+        ms_c, ms_r = max_over_ranks(dist, [ms_c, ms_r], device=dev)
+        ratio = W.block_bytes / (W.blocks * 1024)
+        rows.append({"spread": S, "compressed_fraction": round(W.compressed_fraction, 4),
+                     "bytes_ratio": round(ratio, 4), "us_compressed": round(ms_c * 1e3 / K, 2),
+                     "us_raw": round(ms_r * 1e3 / K, 2), "speedup": round(ms_r / ms_c, 4),
+                     "byte_speedup_bound": round(1.0 / ratio, 4)})
+        del W, g_c, g_r
+        torch.cuda.empty_cache()
+    if rank == 0:
+        print(json.dumps({"metric": "attention µs/step vs compressed fraction (fixed exponent spread)",
+                          "config": {"batch": 2, "context_tokens": 131072, "q_heads": 32, "kv_heads": 8,
+                                     "tail_tokens": "1..15"}, "rows": rows, "data": "synthetic"}), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
 
 
 def run_sweep(args, dist, rank, local):
