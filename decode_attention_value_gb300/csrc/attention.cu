@@ -14,11 +14,14 @@
 //  * per CTA one producer warp and four consumer warps; the producer resolves page
 //    ids and metadata 32-64 pages ahead and streams each page into an 8-stage shared
 //    memory ring with TMA: two 1-D bulk copies (the K and V groups, 3-4 KB each) for a
-//    compressed page, two 2-D tensor copies with 128-byte swizzle for a raw page;
+//    compressed page, two 2-D tensor copies with 128-byte swizzle for a raw page.
+//    Eight lanes issue at once, one per stage, each as soon as its stage is free, so
+//    no serial per-page chain of one thread paces the stream;
 //  * each consumer warp takes whole pages: per 512-value block one 16-byte and one
 //    8-byte shared load per lane, an integer restore into bf16x2 fragments, and
 //    mma.sync m16n8k16 with K (QK^T, tokens x dims) and V^T (PV, dims x tokens) as the
-//    A operand and the G query heads in the N columns.  G <= 4 leaves four spare N
+//    A operand and the G query heads in the N columns (Q read from global memory once
+//    per segment, as the B fragments).  G <= 4 leaves four spare N
 //    columns: Q is duplicated there for QK^T, and for PV they carry the low part of
 //    P = hi + lo (both bf16), so the PV product keeps ~16 bits of P for free;
 //  * warps merge their online-softmax states per (sequence, KV head) segment, and a
@@ -50,11 +53,8 @@ struct Smem {
     static constexpr int stage = 0;
     static constexpr int full = stage + kStages * kStageBytes;
     static constexpr int empty = full + kStages * 8;
-    static constexpr int qfull = empty + kStages * 8;
-    static constexpr int qempty = qfull + 2 * 8;
-    static constexpr int info = qempty + 2 * 8;
-    static constexpr int q = info + kStages * 16;
-    static constexpr int mm = q + 2 * 4 * 256;
+    static constexpr int info = empty + kStages * 8;
+    static constexpr int mm = info + kStages * 16;
     static constexpr int ml = mm + kConsumers * 8 * 4;  // per warp: (max, sum) of up to 8 heads
     static constexpr int mo = ml + kConsumers * 8 * 4;
     static constexpr int pref = mo + kConsumers * 4 * 128 * 4;
@@ -178,10 +178,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
             mbar_init(sbase + Smem::full + 8 * s, 1);
             mbar_init(sbase + Smem::empty + 8 * s, 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(sbase + Smem::qfull + 8 * s, 1);
-            mbar_init(sbase + Smem::qempty + 8 * s, kConsumers);
-        }
         fence_barrier_init();
     }
     if (warp == 0) {
@@ -223,8 +219,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
         // =============================== producer ===============================
         // Page ids and metadata are fetched for 32 pages at a time, one page per lane,
         // a batch ahead of use (warp-wide loads, so no lane waits on another's load).
-        // For each page the lane derives the stage descriptor; lane 0 then issues the
-        // copies page by page into the ring as stages free up.
+        // Each lane derives its page's stage descriptor; then in four rounds eight lanes
+        // (one per stage) wait for their stages and issue their pages' copies.
         prefetch_tensormap(&tmap);
         const int64_t npage = hi - lo;
         // the KV stream is read once per step; the tables each step starts from stay in L2
@@ -266,9 +262,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
         prep(lo + 32 + lane, nxt);
         load_meta(cur, cm0, cm1);
 
-        int64_t seg_end = lo;
-        int seg = 0;
         bool ok = true;
+        static_assert(kStages == 8, "a round is eight lanes, one per stage");
         for (int64_t base = 0; base < npage; base += 32) {
             // ---- this lane's page descriptor: kind | valid << 8 | status << 16, source, sizes, tags ----
             uint32_t d_kind = kKindSkip, d_valid = 0, d_bad = 0, d_tK = 0, d_tV = 0, d_bytes = 0;
@@ -323,64 +318,52 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                 }
                 if (d_bad) atomicOr(P.status, d_bad);
             }
-            const uint32_t d_word = d_kind | (d_valid << 8);
             // ---- next batches: metadata of batch +1 (its page ids arrived a batch ago), ids of batch +2 ----
             uint64_t nm0 = 0, nm1 = 0;
             load_meta(nxt, nm0, nm1);
             Pre nn;
             prep(lo + base + 64 + lane, nn);
 
+            // base is a multiple of 32, so lane L's page base + L goes to stage L % 8; round r
+            // is lanes 8r..8r+7, after round r - 1 issued the previous fill of each stage
             const int cnt = (int)(npage - base < 32 ? npage - base : 32);
-            for (int j = 0; j < cnt; ++j) {
-                const int64_t i = base + j;
-                const int64_t x = lo + i;
-                const uint32_t w = __shfl_sync(0xffffffffu, d_word, j);
-                const uint64_t sK = __shfl_sync(0xffffffffu, d_srcK, j);
-                const uint64_t sV = __shfl_sync(0xffffffffu, d_srcV, j);
-                const uint32_t tK = __shfl_sync(0xffffffffu, d_tK, j);
-                const uint32_t tV = __shfl_sync(0xffffffffu, d_tV, j);
-                const uint32_t nb = __shfl_sync(0xffffffffu, d_bytes, j);
-                if (x == seg_end) {  // new (sequence, KV head) segment: stage its queries
-                    const PageLoc L = locate(pref, B, hkv, x);
-                    seg_end = min(hi, unit_end(pref, hkv, L));
-                    if (lane == 0 && ok && G <= 4) {  // G = 8: the consumers read Q from global memory
-                        const int qb = seg & 1, use = seg >> 1;
-                        ok = mbar_wait(sbase + Smem::qempty + 8 * qb, (use & 1) ^ 1, P.status);
-                        if (ok) {
-                            const uint32_t bytes = (uint32_t)G * kDim * 2;
-                            mbar_arrive_expect_tx(sbase + Smem::qfull + 8 * qb, bytes);
-                            bulk_copy_g2s(sbase + Smem::q + qb * 1024,
-                                          P.q + ((int64_t)L.b * hkv * G + (int64_t)L.kvh * G) * kDim, bytes,
-                                          sbase + Smem::qfull + 8 * qb);
-                        }
-                    }
-                    ++seg;
-                }
-                if (lane == 0 && ok) {
-                    const int s = (int)(i % kStages);
-                    const int64_t fill = i / kStages;
-                    ok = mbar_wait(sbase + Smem::empty + 8 * s, (uint32_t)((fill & 1) ^ 1), P.status);
-                    if (ok) {
-                        const uint32_t kind = w & 0xFFu;
-                        info[s] = StageInfo{kind, (w >> 8) & 0xFFu, tK, tV};
-                        const uint32_t fullbar = sbase + Smem::full + 8 * s;
+            const int s = lane & (kStages - 1);
+            const uint32_t parity = (uint32_t)((((base + lane) / kStages) & 1) ^ 1);
+            const uint32_t emptybar = sbase + Smem::empty + 8 * s, fullbar = sbase + Smem::full + 8 * s;
+            for (int r = 0; r < 4 && 8 * r < cnt && ok; ++r) {
+                bool pending = (lane >> 3) == r && lane < cnt, mine_ok = true;
+                uint32_t it = 0;
+                uint64_t t0 = 0;
+                while (__any_sync(0xffffffffu, pending)) {
+                    if (!pending) continue;
+                    if (mbar_test_wait(emptybar, parity)) {
+                        pending = false;
+                        info[s] = StageInfo{d_kind, d_valid, d_tK, d_tV};
                         const uint32_t dst = sbase + Smem::stage + s * kStageBytes;
-                        if (kind == kKindPair) {
-                            const uint32_t bK = nb & 0xFFFFu, bV = nb >> 16;
+                        if (d_kind == kKindPair) {
+                            const uint32_t bK = d_bytes & 0xFFFFu, bV = d_bytes >> 16;
                             mbar_arrive_expect_tx(fullbar, bK + bV);
-                            bulk_copy_g2s_hint(dst, P.arena + sK, bK, fullbar, stream_once);
-                            bulk_copy_g2s_hint(dst + 4096, P.arena + sV, bV, fullbar, stream_once);
-                        } else if (kind == kKindRaw) {
+                            bulk_copy_g2s_hint(dst, P.arena + d_srcK, bK, fullbar, stream_once);
+                            bulk_copy_g2s_hint(dst + 4096, P.arena + d_srcV, bV, fullbar, stream_once);
+                        } else if (d_kind == kKindRaw) {
                             mbar_arrive_expect_tx(fullbar, kStageBytes);
-                            tensor_copy_2d_g2s_hint(dst, &tmap, 0, (int32_t)sK, fullbar, stream_once);
-                            tensor_copy_2d_g2s_hint(dst + 4096, &tmap, 64, (int32_t)sK, fullbar, stream_once);
+                            tensor_copy_2d_g2s_hint(dst, &tmap, 0, (int32_t)d_srcK, fullbar, stream_once);
+                            tensor_copy_2d_g2s_hint(dst + 4096, &tmap, 64, (int32_t)d_srcK, fullbar, stream_once);
                         } else {
                             mbar_arrive(fullbar);
                         }
+                    } else if ((++it & 255u) == 0) {  // bounded: give up after kWaitLimitNs
+                        const uint64_t now = globaltimer_ns();
+                        if (t0 == 0) {
+                            t0 = now;
+                        } else if (now - t0 > kWaitLimitNs) {
+                            atomicOr(P.status, KVZ_STATUS_TIMEOUT);
+                            pending = mine_ok = false;
+                        }
                     }
                 }
+                ok = __all_sync(0xffffffffu, mine_ok);
             }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
             cur = nxt;
             cm0 = nm0;
             cm1 = nm1;
@@ -391,10 +374,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
             for (int s = 0; s < kStages && s < npage; ++s) {
                 const int64_t last = (npage - 1 - s) / kStages;
                 mbar_wait(sbase + Smem::full + 8 * s, (uint32_t)(last & 1), P.status);
-            }
-            for (int qb = 0; qb < 2 && qb < seg && G <= 4; ++qb) {
-                const int last = (seg - 1 - qb) / 2;
-                mbar_wait(sbase + Smem::qfull + 8 * qb, (uint32_t)(last & 1), P.status);
             }
         }
         return;
@@ -408,41 +387,25 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
     float *mo = reinterpret_cast<float *>(smem + Smem::mo);
     bool ok = true;
     int64_t x = lo, ibase = 0;
-    int seg = 0;
     while (x < hi) {
         const PageLoc L = locate(pref, B, hkv, x);
         const int64_t send = min(hi, unit_end(pref, hkv, L));
         const int64_t cnt = send - x;
         const uint8_t *ga_row = kTiles ? P.ga_bases + (size_t)L.kvh * 512 : nullptr;  // K b3 row; V at +256
 
-        // queries of this segment: B operand of QK^T.  G <= 4: column n = head n % 4 (zero if
-        // >= G), staged by the producer; G = 8: column n = head n, read from global memory.
+        // queries of this segment: B operand of QK^T, read from global memory.  G <= 4:
+        // column n = head n % 4 (zero if >= G); G = 8: column n = head n.
         uint32_t qf[8][2];
-        if (G8) {
+        {
+            const int head = G8 ? g : (g & 3);
+            const bool has = head < G;
             const uint32_t *qg = reinterpret_cast<const uint32_t *>(
-                P.q + ((int64_t)L.b * hkv * G + (int64_t)L.kvh * G + g) * kDim);
+                P.q + ((int64_t)L.b * hkv * G + (int64_t)L.kvh * G + (has ? head : 0)) * kDim);
 #pragma unroll
             for (int kt = 0; kt < 8; ++kt) {
-                qf[kt][0] = __ldg(qg + 8 * kt + t);
-                qf[kt][1] = __ldg(qg + 8 * kt + t + 4);
+                qf[kt][0] = has ? __ldg(qg + 8 * kt + t) : 0u;
+                qf[kt][1] = has ? __ldg(qg + 8 * kt + t + 4) : 0u;
             }
-        } else {
-            const int qb = seg & 1, use = seg >> 1;
-            if (ok) ok = mbar_wait(sbase + Smem::qfull + 8 * qb, (uint32_t)(use & 1), P.status);
-            const int head = g & 3;
-            const uint8_t *qs = smem + Smem::q + qb * 1024 + head * 256;
-#pragma unroll
-            for (int kt = 0; kt < 8; ++kt) {
-                uint32_t b0 = 0, b1 = 0;
-                if (ok && head < G) {
-                    b0 = *reinterpret_cast<const uint32_t *>(qs + (16 * kt + 2 * t) * 2);
-                    b1 = *reinterpret_cast<const uint32_t *>(qs + (16 * kt + 2 * t + 8) * 2);
-                }
-                qf[kt][0] = b0;
-                qf[kt][1] = b1;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(sbase + Smem::qempty + 8 * qb);
         }
 
         float o[8][4];
@@ -717,7 +680,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
         }
         x = send;
         ibase += cnt;
-        ++seg;
     }
 }
 

@@ -103,6 +103,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test for the phase of `parity` (the thread is never suspended, so the
+// lanes of a warp can poll different barriers together).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase of `parity` with a time limit.  Returns false (and sets the
 // timeout status bit) when the limit passes; the caller then stops using the stage.
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: kernels here run for micro- to milliseconds
