@@ -15,8 +15,8 @@
 //    ids and metadata 32-64 pages ahead and streams each page into an 8-stage shared
 //    memory ring with TMA: two 1-D bulk copies (the K and V groups, 3-4 KB each) for a
 //    compressed page, two 2-D tensor copies with 128-byte swizzle for a raw page.
-//    Eight lanes issue at once, one per stage, each as soon as its stage is free, so
-//    no serial per-page chain of one thread paces the stream;
+//    One lane per stage issues at once, each as soon as its stage is free, so no
+//    serial per-page chain of one thread paces the stream;
 //  * each consumer warp takes whole pages: per 512-value block one 16-byte and one
 //    8-byte shared load per lane, an integer restore into bf16x2 fragments, and
 //    mma.sync m16n8k16 with K (QK^T, tokens x dims) and V^T (PV, dims x tokens) as the
@@ -263,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
         load_meta(cur, cm0, cm1);
 
         bool ok = true;
-        static_assert(kStages == 8, "a round is eight lanes, one per stage");
+        static_assert(kStages <= 32, "a round is kStages lanes, one per stage");
         for (int64_t base = 0; base < npage; base += 32) {
             // ---- this lane's page descriptor: kind | valid << 8 | status << 16, source, sizes, tags ----
             uint32_t d_kind = kKindSkip, d_valid = 0, d_bad = 0, d_tK = 0, d_tV = 0, d_bytes = 0;
@@ -324,14 +324,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
             Pre nn;
             prep(lo + base + 64 + lane, nn);
 
-            // base is a multiple of 32, so lane L's page base + L goes to stage L % 8; round r
-            // is lanes 8r..8r+7, after round r - 1 issued the previous fill of each stage
+            // lane L's page base + L goes to stage (base + L) % kStages; round r is lanes
+            // [r kStages, (r + 1) kStages): the previous fill of each of their stages was issued
+            // by round r - 1 or by the previous batch (base is a multiple of 32)
             const int cnt = (int)(npage - base < 32 ? npage - base : 32);
-            const int s = lane & (kStages - 1);
+            const int s = (int)((base + lane) % kStages);
             const uint32_t parity = (uint32_t)((((base + lane) / kStages) & 1) ^ 1);
             const uint32_t emptybar = sbase + Smem::empty + 8 * s, fullbar = sbase + Smem::full + 8 * s;
-            for (int r = 0; r < 4 && 8 * r < cnt && ok; ++r) {
-                bool pending = (lane >> 3) == r && lane < cnt, mine_ok = true;
+            for (int r = 0; kStages * r < cnt && ok; ++r) {
+                bool pending = lane / kStages == r && lane < cnt, mine_ok = true;
                 uint32_t it = 0;
                 uint64_t t0 = 0;
                 while (__any_sync(0xffffffffu, pending)) {
@@ -721,7 +722,8 @@ __global__ void __launch_bounds__(128) k_attn_merge(const AttnParams P)
 #pragma unroll
             for (int k = 0; k < kMergeChunk; ++k) {
                 const int64_t c = cb + k;
-                const bool w = c <= c1 && (c * T + C - 1) / C < ((c + 1) * T + C - 1) / C;
+                // (64-bit divisions only when some CTA ranges are empty)
+                const bool w = c <= c1 && (T >= C || (c * T + C - 1) / C < ((c + 1) * T + C - 1) / C);
                 const int64_t slot = u + c;
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
