@@ -687,79 +687,132 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
 // ---------------------------------------------------------------------------------
 // merge the per-segment partials of each (sequence, KV head): fixed order over CTAs
 // ---------------------------------------------------------------------------------
-constexpr int kMergeChunk = 8;  // slots whose partials one thread keeps in flight at once
+constexpr int kMergeChunk = 8;   // slots whose partials one thread keeps in flight at once
+constexpr int kMergeGroups = 4;  // slot ranges merged side by side, then combined in order,
+                                 // when units span many CTAs
 
-__global__ void __launch_bounds__(128) k_attn_merge(const AttnParams P)
+// Running merge of slots [c0, c1] of one unit (head block hb, dimension d) into M, Ls, Os.
+__device__ __forceinline__ void merge_slots(const AttnParams &P, int64_t u, int64_t c0, int64_t c1, int64_t T,
+                                            int64_t C, int gs, int hb, int d, float (&M)[4], float (&Ls)[4],
+                                            float (&Os)[4])
 {
+    const int G = P.G;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        M[h] = -INFINITY;
+        Ls[h] = 0.f;
+        Os[h] = 0.f;
+    }
+    // within a chunk every load is independent
+    for (int64_t cb = c0; cb <= c1; cb += kMergeChunk) {
+        float mv[kMergeChunk][4], lv[kMergeChunk][4], ov[kMergeChunk][4];
+#pragma unroll
+        for (int k = 0; k < kMergeChunk; ++k) {
+            const int64_t c = cb + k;
+            // (64-bit divisions only when some CTA ranges are empty)
+            const bool w = c <= c1 && (T >= C || (c * T + C - 1) / C < ((c + 1) * T + C - 1) / C);
+            const int64_t slot = u + c;
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                mv[k][h] = -INFINITY;
+                lv[k][h] = 0.f;
+                ov[k][h] = 0.f;
+                if (w && hb + h < G) {
+                    const float2 ml = *reinterpret_cast<const float2 *>(P.part_ml + (slot * gs + hb + h) * 2);
+                    mv[k][h] = ml.x;
+                    lv[k][h] = ml.y;
+                    ov[k][h] = P.part_o[(slot * gs + hb + h) * 128 + d];
+                }
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            float m = M[h];
+#pragma unroll
+            for (int k = 0; k < kMergeChunk; ++k) m = fmaxf(m, mv[k][h]);
+            if (m == -INFINITY) continue;
+            const float r = exp2f(M[h] - m);  // M[h] = -inf -> 0
+            float l = Ls[h] * r, o = Os[h] * r;
+#pragma unroll
+            for (int k = 0; k < kMergeChunk; ++k) {
+                const float wgt = exp2f(mv[k][h] - m);
+                l += wgt * lv[k][h];
+                o += wgt * ov[k][h];
+            }
+            M[h] = m;
+            Ls[h] = l;
+            Os[h] = o;
+        }
+    }
+}
+
+// One block per (sequence, KV head), kGroups x 128 threads.  The unit's slots are cut into
+// kGroups ranges of at least kMergeChunk slots; each group of 128 threads merges its range,
+// and group 0 combines the group results in group order.  A unit with at most kMergeChunk
+// slots is merged by group 0 alone (the same arithmetic for every kGroups).
+template <int kGroups>
+__global__ void __launch_bounds__(128 * kGroups) k_attn_merge(const AttnParams P)
+{
+    __shared__ float gm[kGroups][4], gl[kGroups][4], go[kGroups][4][128];
     const int u = blockIdx.x, hkv = P.hkv, G = P.G;
-    const int b = u / hkv, kvh = u % hkv, d = threadIdx.x;
+    const int b = u / hkv, kvh = u % hkv, d = threadIdx.x & 127, grp = threadIdx.x >> 7;
     const int32_t pb = P.prefix[b], pb1 = P.prefix[b + 1], pB = P.prefix[P.batch];
     const int64_t n = pb1 - pb;
     const int64_t T = (int64_t)hkv * pB;
     const int64_t C = P.grid;
     float *out = P.out + ((int64_t)b * hkv * G + (int64_t)kvh * G) * kDim;
     if (n == 0) {
-        for (int h = 0; h < G; ++h) out[h * kDim + d] = 0.f;
+        if (grp == 0)
+            for (int h = 0; h < G; ++h) out[h * kDim + d] = 0.f;
         return;
     }
     // CTA c covers pages [ceil(cT/C), ceil((c+1)T/C)); page x belongs to CTA floor(xC/T).
     // CTAs between the first and last owner with an empty range (T < C) wrote nothing.
     const int64_t S = (int64_t)hkv * pb + (int64_t)kvh * n, E = S + n;
     const int64_t c0 = (S * C) / T, c1 = ((E - 1) * C) / T;
+    const int64_t ns = c1 - c0 + 1, per = max((int64_t)kMergeChunk, (ns + kGroups - 1) / kGroups);
+    const int64_t g0 = c0 + grp * per, g1 = min(c1, g0 + per - 1);  // empty when g0 > c1
     const int gs = G == 8 ? 8 : 4;  // heads per partial slot
     // heads in blocks of four (two blocks for G = 8)
     for (int hb = 0; hb < G; hb += 4) {
         float M[4], Ls[4], Os[4];
+        merge_slots(P, u, g0, g1, T, C, gs, hb, d, M, Ls, Os);
+        if (kGroups == 1 || ns <= kMergeChunk) {  // group 0 holds every slot
+            if (grp == 0) {
+#pragma unroll
+                for (int h = 0; h < 4; ++h)
+                    if (hb + h < G) out[(hb + h) * kDim + d] = Ls[h] > 0.f ? Os[h] / Ls[h] : 0.f;
+            }
+            continue;
+        }
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-            M[h] = -INFINITY;
-            Ls[h] = 0.f;
-            Os[h] = 0.f;
-        }
-        // running merge over chunks of slots; within a chunk every load is independent
-        for (int64_t cb = c0; cb <= c1; cb += kMergeChunk) {
-            float mv[kMergeChunk][4], lv[kMergeChunk][4], ov[kMergeChunk][4];
-#pragma unroll
-            for (int k = 0; k < kMergeChunk; ++k) {
-                const int64_t c = cb + k;
-                // (64-bit divisions only when some CTA ranges are empty)
-                const bool w = c <= c1 && (T >= C || (c * T + C - 1) / C < ((c + 1) * T + C - 1) / C);
-                const int64_t slot = u + c;
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    mv[k][h] = -INFINITY;
-                    lv[k][h] = 0.f;
-                    ov[k][h] = 0.f;
-                    if (w && hb + h < G) {
-                        const float2 ml = *reinterpret_cast<const float2 *>(P.part_ml + (slot * gs + hb + h) * 2);
-                        mv[k][h] = ml.x;
-                        lv[k][h] = ml.y;
-                        ov[k][h] = P.part_o[(slot * gs + hb + h) * 128 + d];
-                    }
-                }
+            if (d == 0) {
+                gm[grp][h] = M[h];
+                gl[grp][h] = Ls[h];
             }
+            go[grp][h][d] = Os[h];
+        }
+        __syncthreads();
+        if (grp == 0) {
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-                float m = M[h];
+                float m = -INFINITY;
 #pragma unroll
-                for (int k = 0; k < kMergeChunk; ++k) m = fmaxf(m, mv[k][h]);
-                if (m == -INFINITY) continue;
-                const float r = exp2f(M[h] - m);  // M[h] = -inf -> 0
-                float l = Ls[h] * r, o = Os[h] * r;
+                for (int k = 0; k < kGroups; ++k) m = fmaxf(m, gm[k][h]);
+                float l = 0.f, o = 0.f;
+                if (m != -INFINITY) {
 #pragma unroll
-                for (int k = 0; k < kMergeChunk; ++k) {
-                    const float wgt = exp2f(mv[k][h] - m);
-                    l += wgt * lv[k][h];
-                    o += wgt * ov[k][h];
+                    for (int k = 0; k < kGroups; ++k) {
+                        const float wgt = exp2f(gm[k][h] - m);  // empty group: -inf -> 0
+                        l += wgt * gl[k][h];
+                        o += wgt * go[k][h][d];
+                    }
                 }
-                M[h] = m;
-                Ls[h] = l;
-                Os[h] = o;
+                if (hb + h < G) out[(hb + h) * kDim + d] = l > 0.f ? o / l : 0.f;
             }
         }
-#pragma unroll
-        for (int h = 0; h < 4; ++h)
-            if (hb + h < G) out[(hb + h) * kDim + d] = Ls[h] > 0.f ? Os[h] / Ls[h] : 0.f;
+        __syncthreads();
     }
 }
 
@@ -778,7 +831,9 @@ static cudaError_t configure(int dev)
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k_attn<kFmt, kG8>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     // the merge runs between attention launches: same carve-out, no reconfiguration
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn_merge, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_attn_merge<1>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_attn_merge<kMergeGroups>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e == cudaSuccess && dev < 64) __atomic_fetch_or(&done, 1ull << dev, __ATOMIC_ACQ_REL);
     return e;
 }
@@ -825,7 +880,12 @@ static cudaError_t launch_impl(const AttnParams &P, const void *tmap, cudaStream
     k_attn<kFmt, kG8><<<P.grid, kThreads, Smem::bytes(P.batch), stream>>>(P, map);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    k_attn_merge<<<P.batch * P.hkv, 128, 0, stream>>>(P);
+    // slot groups only when the average unit spans more than a chunk of CTAs
+    const int64_t units = (int64_t)P.batch * P.hkv;
+    if ((int64_t)P.grid > (int64_t)kMergeChunk * units)
+        k_attn_merge<kMergeGroups><<<P.batch * P.hkv, 128 * kMergeGroups, 0, stream>>>(P);
+    else
+        k_attn_merge<1><<<P.batch * P.hkv, 128, 0, stream>>>(P);
     return cudaGetLastError();
 }
 
