@@ -68,13 +68,18 @@ __global__ void __launch_bounds__(256, 3) k_enc_sizes_w(EncodeParams P)
     }
 }
 
-// Validation before anything is written: an index out of range or a decreasing
-// dst_seq makes the whole call a no-op.
-__global__ void __launch_bounds__(256) k_enc_validate(EncodeParams P)
+// Validation before anything is written (an index out of range or a decreasing dst_seq
+// makes the whole call a no-op), and the per-call reset of the page-size sums: one block
+// walks the entries, so the header word is stored whole and nothing has to be zeroed
+// before the call (a memset node costs several microseconds inside a CUDA graph).
+constexpr int kPrepThreads = 1024;
+
+__global__ void __launch_bounds__(kPrepThreads) k_enc_prepare(EncodeParams P)
 {
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    __shared__ uint32_t s_err[kPrepThreads / 32];
     uint32_t err = 0;
-    if (e < P.n) {
+    for (int e = threadIdx.x; e < P.n; e += kPrepThreads) {
+        P.ws_page_size[e] = 0;
         // a size-only call (kvz_encode_sizes) has no destination sequences
         const int s = P.src_page[e], d = P.dst_page[e], q = P.dst_seq ? P.dst_seq[e] : 0;
         if (s < 0 || s >= P.num_raw_pages || d < 0 || d >= P.num_meta_pages || q < 0 || q >= P.num_cursors)
@@ -82,9 +87,13 @@ __global__ void __launch_bounds__(256) k_enc_validate(EncodeParams P)
         if (P.dst_seq && e > 0 && q < P.dst_seq[e - 1]) err |= KVZ_STATUS_BAD_ORDER;
     }
     err = __reduce_or_sync(0xffffffffu, err);
-    if (err && (threadIdx.x & 31) == 0) {
-        atomicOr(P.ws_hdr, err);
-        atomicOr(P.status, err);
+    if ((threadIdx.x & 31) == 0) s_err[threadIdx.x >> 5] = err;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint32_t all = 0;
+        for (int w = 0; w < kPrepThreads / 32; ++w) all |= s_err[w];
+        P.ws_hdr[0] = all;
+        if (all) atomicOr(P.status, all);
     }
 }
 
@@ -412,12 +421,10 @@ static unsigned grid_for(size_t items, int sms, int per_sm)
 
 cudaError_t launch_encode(const EncodeParams &P, cudaStream_t stream)
 {
-    cudaError_t e = cudaMemsetAsync(P.ws_hdr, 0, 16 + (size_t)P.n * 4, stream);  // header + page sizes
-    if (e != cudaSuccess) return e;
-    k_enc_validate<<<(P.n + 255) / 256, 256, 0, stream>>>(P);
+    k_enc_prepare<<<1, kPrepThreads, 0, stream>>>(P);
     const size_t items = (size_t)P.n * P.hkv;
     int sms = 0;
-    e = encode_grid(&sms);
+    cudaError_t e = encode_grid(&sms);
     if (e != cudaSuccess) return e;
     k_enc_sizes_w<<<grid_for(items, sms, 3), 256, 0, stream>>>(P);
     k_enc_scan<<<1, kScanThreads, 0, stream>>>(P, 0, P.n);
@@ -428,20 +435,17 @@ cudaError_t launch_encode(const EncodeParams &P, cudaStream_t stream)
 cudaError_t launch_encode_sizes(const EncodeParams &P, cudaStream_t stream)
 {
     // validation, then the size pass alone: P.ws_page_size is the caller's output array
-    cudaError_t e = cudaMemsetAsync(P.ws_hdr, 0, 16, stream);
-    if (e == cudaSuccess) e = cudaMemsetAsync(P.ws_page_size, 0, (size_t)P.n * 4, stream);
-    if (e != cudaSuccess) return e;
-    k_enc_validate<<<(P.n + 255) / 256, 256, 0, stream>>>(P);
+    k_enc_prepare<<<1, kPrepThreads, 0, stream>>>(P);
     int sms = 0;
-    e = encode_grid(&sms);
+    cudaError_t e = encode_grid(&sms);
     if (e != cudaSuccess) return e;
     k_enc_sizes_w<<<grid_for((size_t)P.n * P.hkv, sms, 3), 256, 0, stream>>>(P);
     return cudaGetLastError();
 }
 
-cudaError_t launch_enc_validate(const EncodeParams &P, cudaStream_t stream)
+cudaError_t launch_enc_prepare(const EncodeParams &P, cudaStream_t stream)
 {
-    k_enc_validate<<<(P.n + 255) / 256, 256, 0, stream>>>(P);
+    k_enc_prepare<<<1, kPrepThreads, 0, stream>>>(P);
     return cudaGetLastError();
 }
 

@@ -309,8 +309,7 @@ cudaError_t launch_f8_calibrate(int fmt, int hkv, const uint16_t *raw_pool, int6
 
 cudaError_t launch_f8_encode(int fmt, const EncodeParams &P, cudaStream_t stream)
 {
-    cudaError_t e = cudaMemsetAsync(P.ws_hdr, 0, 16 + (size_t)P.n * 4, stream);  // header + page sizes
-    if (e == cudaSuccess) e = launch_enc_validate(P, stream);
+    cudaError_t e = launch_enc_prepare(P, stream);  // validation and page-size reset
     if (e != cudaSuccess) return e;
     const unsigned items = (unsigned)((size_t)P.n * P.hkv);
     if (fmt == kF8E5M2) k_f8_sizes<true><<<items, 256, 0, stream>>>(P);

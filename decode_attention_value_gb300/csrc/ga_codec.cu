@@ -354,8 +354,7 @@ cudaError_t launch_ga_calibrate(int hkv, const uint16_t *raw_pool, int64_t num_r
 
 cudaError_t launch_ga_encode(const EncodeParams &P, cudaStream_t stream)
 {
-    cudaError_t e = cudaMemsetAsync(P.ws_hdr, 0, 16 + (size_t)P.n * 4, stream);  // header + page sizes
-    if (e == cudaSuccess) e = launch_enc_validate(P, stream);
+    cudaError_t e = launch_enc_prepare(P, stream);  // validation and page-size reset
     if (e != cudaSuccess) return e;
     const unsigned items = (unsigned)((size_t)P.n * P.hkv);
     k_ga_sizes<<<items, 256, 0, stream>>>(P);

@@ -266,7 +266,7 @@ int kvz_encode_pages(kvz_dims dims, const void *raw_pool, int64_t num_raw_pages,
     uint8_t *w = static_cast<uint8_t *>(workspace);
     const size_t a = ((size_t)n * 4 + 15) / 16 * 16;
     P.ws_hdr = reinterpret_cast<uint32_t *>(w);
-    P.ws_page_size = reinterpret_cast<uint32_t *>(w + 16);  // contiguous with the header: one memset
+    P.ws_page_size = reinterpret_cast<uint32_t *>(w + 16);  // page-size sums after the header
     P.ws_page_base = reinterpret_cast<uint32_t *>(w + 16 + a);
     P.ws_pair_size = reinterpret_cast<uint32_t *>(w + 16 + 2 * a);
     cudaError_t e = launch_encode(P, reinterpret_cast<cudaStream_t>(stream));

@@ -26,7 +26,7 @@ struct EncodeParams {
     uint32_t *meta32;
     const uint8_t *ga_bases;
     // workspace
-    uint32_t *ws_hdr;        // [4]: validation failure bits (zeroed each call)
+    uint32_t *ws_hdr;        // [4]: validation failure bits (stored by the prepare kernel each call)
     uint32_t *ws_page_size;  // [n] granules per page, summed over heads (zeroed each call)
     uint32_t *ws_page_base;  // [n] granule position of each page's first group
     uint32_t *ws_pair_size;  // [n*hkv] granules per (page, head) K+V pair
@@ -93,7 +93,7 @@ inline size_t attn_ws_bytes(int batch, int hkv, int grid, int G = 4)
 }
 
 cudaError_t launch_encode(const EncodeParams &P, cudaStream_t stream);
-cudaError_t launch_enc_validate(const EncodeParams &P, cudaStream_t stream);
+cudaError_t launch_enc_prepare(const EncodeParams &P, cudaStream_t stream);
 cudaError_t launch_encode_sizes(const EncodeParams &P, cudaStream_t stream);
 cudaError_t launch_enc_scan(const EncodeParams &P, cudaStream_t stream);
 cudaError_t launch_ga_encode(const EncodeParams &P, cudaStream_t stream);
