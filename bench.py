@@ -345,23 +345,31 @@ def per_launch_ms(fn, iters: int, flush: torch.Tensor) -> float:
 # --------------------------------------------------------------------------------------
 # CPU oracle (cpu_baseline and the reference arm)
 # --------------------------------------------------------------------------------------
-def oracle_encode_rate(cfg: kvgen.KVConfig, mib: int = 64) -> float:
-    """The CPU oracle's encoder (scalar, one thread) on `mib` MiB of the workload's pages:
-    BF16 GB/s in."""
+def oracle_encode_rate(cfg: kvgen.KVConfig, mib: int = 64, threads: int = 1) -> float:
+    """The CPU oracle's encoder (scalar) on `mib` MiB of the workload's pages per thread:
+    BF16 GB/s in over all threads (each thread encodes the same pages into its own
+    arena; the oracle's C calls release the GIL)."""
+    from concurrent.futures import ThreadPoolExecutor
+
     import oracle
 
     oracle.build()
     n = max(1, (mib << 20) // (cfg.hkv * 8192))
     pool = kvgen.bits(kvgen.gen_pages(cfg, n))
     src = np.arange(n, dtype=np.int32)
-    meta = np.zeros((n, cfg.hkv, 2), np.uint64)
-    arena = np.zeros(n * cfg.hkv * 8192, np.uint8)
-    cur = np.array([[0, arena.size // 256]], np.uint32)
+    outs = [(np.zeros((n, cfg.hkv, 2), np.uint64), np.zeros(n * cfg.hkv * 8192, np.uint8)) for _ in range(threads)]
+
+    def work(k):
+        meta, arena = outs[k]
+        cur = np.array([[0, arena.size // 256]], np.uint32)
+        return oracle.encode_pages(pool, src, src, np.zeros(n, np.int32), meta, arena, cur, cfg.hkv)
+
     t0 = time.perf_counter()
-    st = oracle.encode_pages(pool, src, src, np.zeros(n, np.int32), meta, arena, cur, cfg.hkv)
+    with ThreadPoolExecutor(threads) as ex:
+        sts = list(ex.map(work, range(threads)))
     dt = time.perf_counter() - t0
-    assert st == 0
-    return pool.nbytes / dt / 1e9
+    assert all(st == 0 for st in sts)
+    return threads * pool.nbytes / dt / 1e9
 
 
 def oracle_sample(cfg: kvgen.KVConfig, budget_s: float, seqs_max: int | None = None, threads: int | None = None):
@@ -498,6 +506,10 @@ def main():
             dist.barrier()
         ms_r = time_graph(g_r)
         ms_df = time_graph(g_df)
+        # four more timed runs of each graph, after the one the line reports: the spread
+        # of the per-run step times
+        reps_c = [ms_c] + [time_graph(g_c) for _ in range(4)]
+        reps_r = [ms_r] + [time_graph(g_r) for _ in range(4)]
         soak_until = time.time() + 0.4
         while time.time() < soak_until:
             g_c.replay()
@@ -645,7 +657,9 @@ def main():
         cpu["extra"] = {"attention_1core_GBps": round(g1, 3),
                         "attention_1core_sample": f"{n1} sequences, {p1} passes, {s1:.1f} s",
                         "encode_1core_GBps": round(oracle_encode_rate(cfg), 3),
-                        "encode_sample": "64 MiB of the layer's pages, scalar oracle encoder, one thread"}
+                        "encode_sample": "64 MiB of the layer's pages, scalar oracle encoder, one thread",
+                        "encode_allcores_GBps": round(oracle_encode_rate(cfg, 32, threads), 3),
+                        "encode_allcores_sample": f"{threads} threads x 32 MiB of the layer's pages"}
 
     traffic = profiled_traffic(args.workload)
     line = {
@@ -684,6 +698,11 @@ def main():
                      "kernel": "k_attn<compressed> + k_attn_merge",
                      "launch_us": round(us_step, 3), "cold_single_launch_us": round(launch_ms * 1e3, 3),
                      "algorithmic_bytes_per_launch": W.alg_bytes_c},
+        "runs": {"n": 5, "us_per_step_mean": round(float(np.mean(reps_c)) * 1e3 / K, 3),
+                 "us_per_step_std": round(float(np.std(reps_c)) * 1e3 / K, 3),
+                 "raw_us_per_step_mean": round(float(np.mean(reps_r)) * 1e3 / K, 3),
+                 "raw_us_per_step_std": round(float(np.std(reps_r)) * 1e3 / K, 3),
+                 "how": f"5 timed runs of the {K}-step graphs (the first is the one reported); per-rank, rank 0"},
         "roofline_raw": {"achieved": round(achieved_raw, 1), "frac": round(achieved_raw / peak, 4),
                          "launch_us": round(us_raw, 3), "cold_single_launch_us": round(launch_ms_raw * 1e3, 3),
                          "algorithmic_bytes_per_launch": W.alg_bytes_r},
