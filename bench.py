@@ -423,7 +423,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="kvz", choices=["kvz", "reference"])
     ap.add_argument("--workload", default="c1", choices=["c1", "c2", "c3", "c4", "serve"])
     ap.add_argument("--serve-budget-gb", type=float, default=4.0, help="serve: KV budget of both caches (1e9 B)")
@@ -1144,6 +1144,16 @@ def run_stack(args, cfg, dist, rank, world, local):
                      "frac": round(alg / (us_c * 1e-6) / 1e9 / peak, 4), "traffic": None, "peak_kind": peak_kind},
         "clocks": clocks, "gpu_launches": 2 * cfg.layers * K,
     }
+    if rank == 0 and not args.no_cpu_baseline:
+        # the oracle on a sample of one layer (every layer has the same shape), scaled to
+        # the full stack: µs per step = layers x layer logical bytes / oracle rate
+        gbps, secs, nseq, passes, threads = oracle_sample(cfg, args.cpu_budget)
+        line["cpu_baseline"] = {
+            "value": round(gbps, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "us_per_step": round(logical / (gbps * 1e9) * 1e6, 1),
+            "sample": f"{nseq} of {cfg.batch} sequences x {cfg.hkv} KV heads of one layer (decode of compressed "
+                      f"pages + fp64 attention), {passes} passes, {secs:.1f} s; us_per_step scales the rate to "
+                      f"the {cfg.layers}-layer step"}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
