@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
     uint8_t *tail_len = smem + Smem::tail(P.batch);  // tokens in each sequence's last page if partial, else 0
     StageInfo *info = reinterpret_cast<StageInfo *>(smem + Smem::info);
     const int B = P.batch, hkv = P.hkv, G = P.G;
-    constexpr bool G8 = kG8;  // G = 8: every MMA column is a head, no spare columns
+    constexpr bool G8 = kG8;  // G = 5..8: every MMA column is a head (zero for heads >= G), no spare columns
 
     // ---- barriers, and the per-sequence page-count prefix ----
     if (tid == 0) {
@@ -395,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
         const uint8_t *ga_row = kTiles ? P.ga_bases + (size_t)L.kvh * 512 : nullptr;  // K b3 row; V at +256
 
         // queries of this segment: B operand of QK^T, read from global memory.  G <= 4:
-        // column n = head n % 4 (zero if >= G); G = 8: column n = head n.
+        // column n = head n % 4 (zero if >= G); G = 5..8: column n = head n (zero if >= G).
         uint32_t qf[8][2];
         {
             const int head = G8 ? g : (g & 3);
@@ -523,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                 l0 += p0 + p2;
                 l1 += p1 + p3;
                 // P split.  G <= 4: columns 0..3 (t < 2) carry bf16(p), columns 4..7 carry
-                // bf16(p - bf16(p)), one MMA per tile.  G = 8: bf16(p) and the remainder go
+                // bf16(p - bf16(p)), one MMA per tile.  G > 4: bf16(p) and the remainder go
                 // through two MMAs into the same accumulator.
                 float v0 = p0, v1 = p1, v2 = p2, v3 = p3;
                 const float r0 = p0 - bf16_round(p0), r1 = p1 - bf16_round(p1);
@@ -619,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
 
         // ---- warp state -> shared memory, then the four warps merged (fixed order) into this
         // segment's partial.  G <= 4: columns h and h+4 summed (hi and lo parts of P), one
-        // pass.  G = 8: heads 0..3 (lanes t < 2) then heads 4..7 (t >= 2), two passes through
+        // pass.  G > 4: heads 0..3 (lanes t < 2) then heads 4..7 (t >= 2), two passes through
         // the same buffer. ----
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -772,8 +772,8 @@ __global__ void __launch_bounds__(128 * kGroups) k_attn_merge(const AttnParams P
     const int64_t c0 = (S * C) / T, c1 = ((E - 1) * C) / T;
     const int64_t ns = c1 - c0 + 1, per = max((int64_t)kMergeChunk, (ns + kGroups - 1) / kGroups);
     const int64_t g0 = c0 + grp * per, g1 = min(c1, g0 + per - 1);  // empty when g0 > c1
-    const int gs = G == 8 ? 8 : 4;  // heads per partial slot
-    // heads in blocks of four (two blocks for G = 8)
+    const int gs = G > 4 ? 8 : 4;  // heads per partial slot
+    // heads in blocks of four (two blocks for G = 5..8)
     for (int hb = 0; hb < G; hb += 4) {
         float M[4], Ls[4], Os[4];
         merge_slots(P, u, g0, g1, T, C, gs, hb, d, M, Ls, Os);
@@ -904,7 +904,7 @@ static cudaError_t launch_format(const AttnParams &P, int format, const void *tm
 
 cudaError_t launch_attention(const AttnParams &P, int format, const void *tmap, cudaStream_t stream)
 {
-    return P.G == 8 ? launch_format<true>(P, format, tmap, stream) : launch_format<false>(P, format, tmap, stream);
+    return P.G > 4 ? launch_format<true>(P, format, tmap, stream) : launch_format<false>(P, format, tmap, stream);
 }
 
 }  // namespace kvz

@@ -106,7 +106,7 @@ int check_attention_common(const kvz_dims &d, int batch, int hq, const void *q, 
     if (batch < 0 || hq < 1 || max_pages < 0 || num_raw_pages < 0) return KVZ_ERR_INVALID_ARG;
     if (hq % d.num_kv_heads != 0) return KVZ_ERR_INVALID_ARG;
     const int G = hq / d.num_kv_heads;
-    if (G != 1 && G != 2 && G != 4 && G != 8) return KVZ_ERR_UNSUPPORTED;
+    if (G < 1 || G > 8) return KVZ_ERR_UNSUPPORTED;
     if (batch > kMaxBatch) return KVZ_ERR_UNSUPPORTED;
     if (batch == 0) return KVZ_OK;
     if (!q || !seq_lens || !out || !ws || !status || (max_pages > 0 && !page_ids)) return KVZ_ERR_INVALID_ARG;

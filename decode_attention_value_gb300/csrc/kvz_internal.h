@@ -79,8 +79,8 @@ struct AttnParams {
 };
 
 inline size_t attn_slots(int batch, int hkv, int grid) { return (size_t)batch * hkv + grid - 1; }
-// heads per partial slot: 4 for G <= 4, 8 for G = 8
-inline int attn_slot_heads(int G) { return G == 8 ? 8 : 4; }
+// heads per partial slot: 4 for G <= 4, 8 for G = 5..8
+inline int attn_slot_heads(int G) { return G > 4 ? 8 : 4; }
 
 // workspace layout: prefix (batch+1 int32, rounded to 16 B), part_o, part_ml
 inline size_t attn_ws_prefix_bytes(int batch) { return ((size_t)(batch + 1) * 4 + 15) / 16 * 16; }

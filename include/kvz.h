@@ -148,7 +148,7 @@ int kvz_decode_blocks(kvz_dims dims, const uint64_t *meta, int64_t num_meta_page
  * and PV, no decompressed copy in memory).
  *
  *  q            BF16 [batch][num_q_heads][128]; query head h reads KV head h/G,
- *               G = num_q_heads / num_kv_heads (G in {1, 2, 4, 8})
+ *               G = num_q_heads / num_kv_heads (an integer, 1 <= G <= 8)
  *  page_ids     int32 [batch][max_pages] meta page ids of each sequence's completed pages
  *  seq_lens     int32 [batch] tokens in context; the first seq_lens/16 pages come from
  *               page_ids, the last seq_lens%16 tokens from raw page tail_page[b]

@@ -48,6 +48,12 @@ CASES = [
     kvgen.KVConfig("gqa8-llama70b-shape", 1, 4, 64, 8, 40, tail_min=1, tail_max=15, k_log2_sigma=(-4, 3),
                    v_log2_sigma=(-3, 1), k_outlier_channels=4, k_outlier_scale=32.0, seed=37),
     kvgen.KVConfig("spread", 1, 2, 32, 8, 12, tail_min=1, tail_max=15, spread=(8, 20), seed=34),
+    # group sizes that are not powers of two: G = 3 takes the spare-column kernel with one
+    # zero head column, G = 5, 6, 7 the all-heads kernel with zero columns
+    kvgen.KVConfig("gqa3", 1, 3, 6, 2, 7, tail_min=1, tail_max=15, k_log2_sigma=(-4, 3), seed=38),
+    kvgen.KVConfig("gqa5", 1, 2, 20, 4, 6, tail_min=2, tail_max=13, seed=39),
+    kvgen.KVConfig("gqa6", 1, 3, 12, 2, 9, tail_min=1, tail_max=15, v_log2_sigma=(-3, 1), seed=40),
+    kvgen.KVConfig("gqa7", 1, 2, 14, 2, 5, tail_min=3, tail_max=9, seed=43),
 ]
 
 

@@ -35,6 +35,8 @@ CASES = [
                    seed=36),
     # wide exponent spreads: many 4-bit and raw groups, some tiles fall back to raw
     kvgen.KVConfig("spread", 1, 2, 32, 8, 12, tail_min=1, tail_max=15, spread=(6, 12), seed=34),
+    kvgen.KVConfig("gqa3", 1, 3, 6, 2, 7, tail_min=1, tail_max=15, k_log2_sigma=(-4, 3), seed=38),
+    kvgen.KVConfig("gqa6", 1, 3, 12, 2, 9, tail_min=1, tail_max=15, v_log2_sigma=(-3, 1), seed=40),
     kvgen.KVConfig("llama-b4", 1, 4, 32, 8, 20, tail_min=1, tail_max=15, k_log2_sigma=(-4, 3),
                    v_log2_sigma=(-3, 1), k_outlier_channels=4, k_outlier_scale=32.0, seed=35),
 ]
