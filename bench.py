@@ -1308,8 +1308,9 @@ def run_stream(args, cfg, dist, rank, world, local):
                      "compressed_seqs": int(budget // (used_per_seq + meta_per_seq)),
                      "compressed_seqs_chunk_granular": int(budget // (held_per_seq + meta_per_seq))},
         "clocks": clocks,
-        # attention + merge per layer per step, plus 3 encode launches per layer at each page completion
-        "gpu_launches": T * L * 2 + len(enc_steps) * L * 3,
+        # attention + merge per layer per step, plus 4 encode launches (prepare, sizes, scan,
+        # pack) per layer at each page completion
+        "gpu_launches": T * L * 2 + len(enc_steps) * L * 4,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
