@@ -396,16 +396,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
 
         // queries of this segment: B operand of QK^T, read from global memory.  G <= 4:
         // column n = head n % 4 (zero if >= G); G = 5..8: column n = head n (zero if >= G).
+        // FP8 pages multiply in f16 (every FP8 value is an f16 value, so the K and V
+        // operands need no further widening): Q is converted once per segment and reloaded
+        // in BF16 for a raw BF16 tail page.
         uint32_t qf[8][2];
-        {
-            const int head = G8 ? g : (g & 3);
-            const bool has = head < G;
-            const uint32_t *qg = reinterpret_cast<const uint32_t *>(
-                P.q + ((int64_t)L.b * hkv * G + (int64_t)L.kvh * G + (has ? head : 0)) * kDim);
+        const int qhead = G8 ? g : (g & 3);
+        const bool qhas = qhead < G;
+        const uint32_t *qg = reinterpret_cast<const uint32_t *>(
+            P.q + ((int64_t)L.b * hkv * G + (int64_t)L.kvh * G + (qhas ? qhead : 0)) * kDim);
 #pragma unroll
-            for (int kt = 0; kt < 8; ++kt) {
-                qf[kt][0] = has ? __ldg(qg + 8 * kt + t) : 0u;
-                qf[kt][1] = has ? __ldg(qg + 8 * kt + t + 4) : 0u;
+        for (int kt = 0; kt < 8; ++kt) {
+            qf[kt][0] = qhas ? __ldg(qg + 8 * kt + t) : 0u;
+            qf[kt][1] = qhas ? __ldg(qg + 8 * kt + t + 4) : 0u;
+            if constexpr (kF8) {
+                qf[kt][0] = bf16x2_to_f16x2(qf[kt][0]);
+                qf[kt][1] = bf16x2_to_f16x2(qf[kt][1]);
             }
         }
 
@@ -443,9 +448,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                     for (int j = 0; j < 4; ++j) {
                         uint32_t fb[4], a0[4], a1[4];
                         f8_block_bytes<kE5, false>(st, ga_row, fs, any2, lane, j, fb);
-                        f8_frags<kE5>(fb, a0, a1);
-                        mma_bf16_16816(sc, a0, qf[2 * j][0], qf[2 * j][1]);
-                        mma_bf16_16816(sc, a1, qf[2 * j + 1][0], qf[2 * j + 1][1]);
+                        f8_frags_f16<kE5>(fb, a0, a1);
+                        mma_f16_16816(sc, a0, qf[2 * j][0], qf[2 * j][1]);
+                        mma_f16_16816(sc, a1, qf[2 * j + 1][0], qf[2 * j + 1][1]);
                     }
                 } else if (kF8 && inf.kind == kKindPair) {  // raw FP8 tile
 #pragma unroll
@@ -453,9 +458,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                         const uint4 v = *reinterpret_cast<const uint4 *>(st + 512 * j + 16 * lane);
                         const uint32_t fb[4] = {v.x, v.y, v.z, v.w};
                         uint32_t a0[4], a1[4];
-                        f8_frags<kE5>(fb, a0, a1);
-                        mma_bf16_16816(sc, a0, qf[2 * j][0], qf[2 * j][1]);
-                        mma_bf16_16816(sc, a1, qf[2 * j + 1][0], qf[2 * j + 1][1]);
+                        f8_frags_f16<kE5>(fb, a0, a1);
+                        mma_f16_16816(sc, a0, qf[2 * j][0], qf[2 * j][1]);
+                        mma_f16_16816(sc, a1, qf[2 * j + 1][0], qf[2 * j + 1][1]);
                     }
                 } else if (kGa && inf.kind == kKindPair) {  // raw tile: 4 raw 1024-byte blocks
 #pragma unroll
@@ -482,8 +487,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                         uint32_t a0[4], a1[4];
                         raw_k_frag(sta, j, 0, lane, a0);
                         raw_k_frag(sta, j, 1, lane, a1);
-                        mma_bf16_16816(sc, a0, qf[2 * j][0], qf[2 * j][1]);
-                        mma_bf16_16816(sc, a1, qf[2 * j + 1][0], qf[2 * j + 1][1]);
+                        if constexpr (kF8) {  // BF16 page: BF16 queries again
+                            const int k0 = 2 * j, k1 = 2 * j + 1;
+                            const uint32_t q00 = qhas ? __ldg(qg + 8 * k0 + t) : 0u;
+                            const uint32_t q01 = qhas ? __ldg(qg + 8 * k0 + t + 4) : 0u;
+                            const uint32_t q10 = qhas ? __ldg(qg + 8 * k1 + t) : 0u;
+                            const uint32_t q11 = qhas ? __ldg(qg + 8 * k1 + t + 4) : 0u;
+                            mma_bf16_16816(sc, a0, q00, q01);
+                            mma_bf16_16816(sc, a1, q10, q11);
+                        } else {
+                            mma_bf16_16816(sc, a0, qf[2 * j][0], qf[2 * j][1]);
+                            mma_bf16_16816(sc, a1, qf[2 * j + 1][0], qf[2 * j + 1][1]);
+                        }
                     }
                 }
                 // sc: (token g, col 2t), (token g, col 2t+1), (token g+8, col 2t), (token g+8, col 2t+1)
@@ -525,25 +540,33 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                 // P split.  G <= 4: columns 0..3 (t < 2) carry bf16(p), columns 4..7 carry
                 // bf16(p - bf16(p)), one MMA per tile.  G > 4: bf16(p) and the remainder go
                 // through two MMAs into the same accumulator.
+                // (FP8 tiles: the same split in f16, for the f16 PV product)
+                const bool pf16 = kF8 && inf.kind == kKindPair;
+                auto rnd = [&](float x) { return pf16 ? f16_round(x) : bf16_round(x); };
+                auto pack = [&](float a, float b) { return pf16 ? pack_f16x2(a, b) : pack_bf16x2(a, b); };
                 float v0 = p0, v1 = p1, v2 = p2, v3 = p3;
-                const float r0 = p0 - bf16_round(p0), r1 = p1 - bf16_round(p1);
-                const float r2 = p2 - bf16_round(p2), r3 = p3 - bf16_round(p3);
+                const float r0 = p0 - rnd(p0), r1 = p1 - rnd(p1);
+                const float r2 = p2 - rnd(p2), r3 = p3 - rnd(p3);
                 if (!G8 && t >= 2) {  // (the remainders are computed by these lanes only)
                     v0 = r0;
                     v1 = r1;
                     v2 = r2;
                     v3 = r3;
                 }
-                const uint32_t pb0 = movmatrix_trans(pack_bf16x2(v0, v1));  // tokens 0..7
-                const uint32_t pb1 = movmatrix_trans(pack_bf16x2(v2, v3));  // tokens 8..15
+                const uint32_t pb0 = movmatrix_trans(pack(v0, v1));  // tokens 0..7
+                const uint32_t pb1 = movmatrix_trans(pack(v2, v3));  // tokens 8..15
                 uint32_t pl0 = 0, pl1 = 0;
                 if (G8) {
-                    pl0 = movmatrix_trans(pack_bf16x2(r0, r1));
-                    pl1 = movmatrix_trans(pack_bf16x2(r2, r3));
+                    pl0 = movmatrix_trans(pack(r0, r1));
+                    pl1 = movmatrix_trans(pack(r2, r3));
                 }
                 auto pv = [&](float (&acc)[4], const uint32_t (&a)[4]) {
                     mma_bf16_16816(acc, a, pb0, pb1);
                     if (G8) mma_bf16_16816(acc, a, pl0, pl1);
+                };
+                auto pv16 = [&](float (&acc)[4], const uint32_t (&a)[4]) {
+                    mma_f16_16816(acc, a, pb0, pb1);
+                    if (G8) mma_f16_16816(acc, a, pl0, pl1);
                 };
                 // ---- O^T += V^T P^T ----
                 if (kGa && inf.kind == kKindPair && !inf.tagsV) {
@@ -565,9 +588,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                     for (int j = 0; j < 4; ++j) {
                         uint32_t fb[4], a0[4], a1[4];
                         f8_block_bytes<kE5, true>(tv, ga_row + 256, fs, any2, lane, j, fb);
-                        f8_frags<kE5>(fb, a0, a1);
-                        pv(o[2 * j], a0);
-                        pv(o[2 * j + 1], a1);
+                        f8_frags_f16<kE5>(fb, a0, a1);
+                        pv16(o[2 * j], a0);
+                        pv16(o[2 * j + 1], a1);
                     }
                 } else if (kF8 && inf.kind == kKindPair) {
 #pragma unroll
@@ -575,9 +598,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                         const uint4 v = *reinterpret_cast<const uint4 *>(st + 4096 + 512 * j + 16 * lane);
                         const uint32_t fb[4] = {v.x, v.y, v.z, v.w};
                         uint32_t a0[4], a1[4];
-                        f8_frags<kE5>(fb, a0, a1);
-                        pv(o[2 * j], a0);
-                        pv(o[2 * j + 1], a1);
+                        f8_frags_f16<kE5>(fb, a0, a1);
+                        pv16(o[2 * j], a0);
+                        pv16(o[2 * j + 1], a1);
                     }
                 } else if (kGa && inf.kind == kKindPair) {
 #pragma unroll
@@ -785,34 +808,36 @@ __global__ void __launch_bounds__(128 * kGroups) k_attn_merge(const AttnParams P
             }
             continue;
         }
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            if (d == 0) {
-                gm[grp][h] = M[h];
-                gl[grp][h] = Ls[h];
-            }
-            go[grp][h][d] = Os[h];
-        }
-        __syncthreads();
-        if (grp == 0) {
+        if constexpr (kGroups > 1) {
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-                float m = -INFINITY;
-#pragma unroll
-                for (int k = 0; k < kGroups; ++k) m = fmaxf(m, gm[k][h]);
-                float l = 0.f, o = 0.f;
-                if (m != -INFINITY) {
-#pragma unroll
-                    for (int k = 0; k < kGroups; ++k) {
-                        const float wgt = exp2f(gm[k][h] - m);  // empty group: -inf -> 0
-                        l += wgt * gl[k][h];
-                        o += wgt * go[k][h][d];
-                    }
+                if (d == 0) {
+                    gm[grp][h] = M[h];
+                    gl[grp][h] = Ls[h];
                 }
-                if (hb + h < G) out[(hb + h) * kDim + d] = l > 0.f ? o / l : 0.f;
+                go[grp][h][d] = Os[h];
             }
+            __syncthreads();
+            if (grp == 0) {
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    float m = -INFINITY;
+#pragma unroll
+                    for (int k = 0; k < kGroups; ++k) m = fmaxf(m, gm[k][h]);
+                    float l = 0.f, o = 0.f;
+                    if (m != -INFINITY) {
+#pragma unroll
+                        for (int k = 0; k < kGroups; ++k) {
+                            const float wgt = exp2f(gm[k][h] - m);  // empty group: -inf -> 0
+                            l += wgt * gl[k][h];
+                            o += wgt * go[k][h][d];
+                        }
+                    }
+                    if (hb + h < G) out[(hb + h) * kDim + d] = l > 0.f ? o / l : 0.f;
+                }
+            }
+            __syncthreads();
         }
-        __syncthreads();
     }
 }
 

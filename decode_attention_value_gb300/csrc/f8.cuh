@@ -58,32 +58,6 @@ __device__ __forceinline__ uint32_t f8_from_bf16x2(uint32_t w2)
     return out;
 }
 
-// Two FP8 bytes (bits 0..15 of x, low byte first) -> bf16x2 holding the same values.
-template <bool kE5>
-__device__ __forceinline__ uint32_t f8x2_to_bf16x2(uint32_t x)
-{
-    uint32_t h2;  // f16x2: every FP8 value is an f16 value
-    if (kE5) {
-        h2 = __byte_perm(x, 0, 0x1404);  // E5M2 is the high byte of an f16
-    } else {
-        const uint16_t a = (uint16_t)x;
-        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(a));
-    }
-    float f0, f1;
-    asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
-        : "=f"(f0), "=f"(f1) : "r"(h2));
-    // every such value is a BF16 value: the upper halves of the two floats are exact
-    return __byte_perm(__float_as_uint(f0), __float_as_uint(f1), 0x7632);
-}
-
-// Four FP8 bytes of elements (k, k+1, k+2, k+3) -> two bf16x2 registers.
-template <bool kE5>
-__device__ __forceinline__ void f8x4_to_bf16(uint32_t b4, uint32_t &p01, uint32_t &p23)
-{
-    p01 = f8x2_to_bf16x2<kE5>(b4 & 0xFFFFu);
-    p23 = f8x2_to_bf16x2<kE5>(b4 >> 16);
-}
-
 // Sign/mantissa field of a group -> per-element values s << M | m in bytes (elements 0..3,
 // 4..7).  E5M2: 24-bit field of 3-bit values; E4M3: 32-bit field of nibbles.
 template <bool kE5>
@@ -228,14 +202,30 @@ __device__ __forceinline__ void f8_block_bytes(const uint8_t *tile, const uint8_
                               row, lane, j, 1, fb[2], fb[3]);
 }
 
-// 16 FP8 bytes of a lane (fragment 0: fb[0..1], fragment 1: fb[2..3]) -> A fragments.
+// 16 FP8 bytes of a lane (fragment 0: fb[0..1], fragment 1: fb[2..3]) -> the two f16 A
+// fragments (every FP8 value is an f16 value: E5M2 is the high byte of an f16, E4M3 widens
+// exactly in hardware).
 template <bool kE5>
-__device__ __forceinline__ void f8_frags(const uint32_t (&fb)[4], uint32_t (&a0)[4], uint32_t (&a1)[4])
+__device__ __forceinline__ uint32_t f8x2_to_f16x2(uint32_t x)
 {
-    f8x4_to_bf16<kE5>(fb[0], a0[0], a0[1]);
-    f8x4_to_bf16<kE5>(fb[1], a0[2], a0[3]);
-    f8x4_to_bf16<kE5>(fb[2], a1[0], a1[1]);
-    f8x4_to_bf16<kE5>(fb[3], a1[2], a1[3]);
+    if (kE5) return __byte_perm(x, 0, 0x1404);
+    uint32_t h2;
+    const uint16_t a = (uint16_t)x;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(a));
+    return h2;
+}
+
+template <bool kE5>
+__device__ __forceinline__ void f8_frags_f16(const uint32_t (&fb)[4], uint32_t (&a0)[4], uint32_t (&a1)[4])
+{
+    a0[0] = f8x2_to_f16x2<kE5>(fb[0] & 0xFFFFu);
+    a0[1] = f8x2_to_f16x2<kE5>(fb[0] >> 16);
+    a0[2] = f8x2_to_f16x2<kE5>(fb[1] & 0xFFFFu);
+    a0[3] = f8x2_to_f16x2<kE5>(fb[1] >> 16);
+    a1[0] = f8x2_to_f16x2<kE5>(fb[2] & 0xFFFFu);
+    a1[1] = f8x2_to_f16x2<kE5>(fb[2] >> 16);
+    a1[2] = f8x2_to_f16x2<kE5>(fb[3] & 0xFFFFu);
+    a1[3] = f8x2_to_f16x2<kE5>(fb[3] >> 16);
 }
 
 }  // namespace kvz

@@ -271,4 +271,35 @@ __device__ __forceinline__ float bf16_round(float x)
     return __uint_as_float(r << 16);
 }
 
+// D = A(16x16, f16, row) * B(16x8, f16, col) + D, fp32 accumulate.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// f16x2 pack, round to nearest even: low half = lo, high half = hi.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ float f16_round(float x)
+{
+    float r;
+    asm("{\n\t.reg .f16 h;\n\tcvt.rn.f16.f32 h, %1;\n\tcvt.f32.f16 %0, h;\n\t}" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// bf16x2 -> f16x2, round to nearest even (exact for values in the f16 normal range).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w)
+{
+    return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
 }  // namespace kvz

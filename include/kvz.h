@@ -317,8 +317,11 @@ int kvz_f8_encode_pages(kvz_dims dims, int32_t format, const void *raw_pool, int
 int kvz_f8_decode_blocks(kvz_dims dims, int32_t format, const uint32_t *meta, int64_t num_meta_pages,
                          const uint8_t *arena, uint64_t arena_bytes, const uint8_t *bases, const int32_t *page,
                          int32_t n, void *out_pages, uint32_t *status, kvz_stream_t stream);
-/* kvz_decode_attention over FP8 tiles (values widened exactly to BF16 in registers) plus
- * the BF16 tail; same workspace, split and determinism. */
+/* kvz_decode_attention over FP8 tiles plus the BF16 tail; same workspace, split and
+ * determinism.  FP8 pages are multiplied in f16 (every FP8 value is an f16 value): the
+ * queries are rounded to f16 for them, which is exact for |q| in [2^-17, 65504]; larger
+ * queries overflow, so q must stay below 65504 in magnitude.  The tail page is multiplied
+ * in BF16 with the BF16 queries. */
 int kvz_f8_decode_attention(kvz_dims dims, int32_t format, int32_t batch, int32_t num_q_heads, const void *q,
                             const int32_t *page_ids, int32_t max_pages, const int32_t *seq_lens,
                             const int32_t *tail_page, const uint32_t *meta, int64_t num_meta_pages,

@@ -105,7 +105,11 @@ def test_codec_and_attention(kvz_lib, oracle, fmt, cfg):
                              workspace=base.workspace(True))
     torch.cuda.synchronize()
     assert int(st.item()) == 0
-    assert torch.equal(got, out_r)
+    # FP8 pages are multiplied in f16, the raw kernel's pages in BF16: the K and V values
+    # are the same, and so are the queries (exact in f16 here); P = hi + lo keeps ~22 bits
+    # in f16 against ~16 in BF16, so the outputs agree to ~1e-5 of their scale
+    scale = float(out_r.float().pow(2).mean().sqrt())
+    assert float((got - out_r).abs().max()) <= 2e-4 * max(scale, 1e-30)
 
 
 @pytest.fixture(scope="module")
