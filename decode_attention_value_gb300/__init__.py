@@ -26,6 +26,7 @@ STATUS_BAD_ORDER = 4
 STATUS_BAD_META = 8
 STATUS_TIMEOUT = 16
 STATUS_BAD_TAIL = 32
+STATUS_Q_RANGE = 64
 
 ERR_OUT_OF_SPACE = -7
 

@@ -404,15 +404,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
         const bool qhas = qhead < G;
         const uint32_t *qg = reinterpret_cast<const uint32_t *>(
             P.q + ((int64_t)L.b * hkv * G + (int64_t)L.kvh * G + (qhas ? qhead : 0)) * kDim);
+        uint32_t qbad = 0;  // FP8: a finite query that overflows f16
 #pragma unroll
         for (int kt = 0; kt < 8; ++kt) {
             qf[kt][0] = qhas ? __ldg(qg + 8 * kt + t) : 0u;
             qf[kt][1] = qhas ? __ldg(qg + 8 * kt + t + 4) : 0u;
             if constexpr (kF8) {
-                qf[kt][0] = bf16x2_to_f16x2(qf[kt][0]);
-                qf[kt][1] = bf16x2_to_f16x2(qf[kt][1]);
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    const uint32_t b = qf[kt][w], h = bf16x2_to_f16x2(b);
+                    // per half: f16 exponent all ones while the BF16 exponent is not
+                    const uint32_t hinf = ~h & 0x7C007C00u, binf = ~b & 0x7F807F80u;
+                    qbad |= ((hinf & 0x7C00u) == 0 && (binf & 0x7F80u) != 0) ||
+                            ((hinf & 0x7C000000u) == 0 && (binf & 0x7F800000u) != 0);
+                    qf[kt][w] = h;
+                }
             }
         }
+        if (kF8 && __any_sync(0xffffffffu, qbad) && lane == 0) atomicOr(P.status, KVZ_STATUS_Q_RANGE);
 
         float o[8][4];
 #pragma unroll

@@ -81,6 +81,7 @@ extern "C" {
 #define KVZ_STATUS_BAD_META 8u
 #define KVZ_STATUS_TIMEOUT 16u
 #define KVZ_STATUS_BAD_TAIL 32u
+#define KVZ_STATUS_Q_RANGE 64u /* FP8 attention: a query beyond the f16 range (|q| >= 65520) */
 
 /* A CUDA stream (same object as cudaStream_t / CUstream); NULL = legacy stream. */
 typedef struct CUstream_st *kvz_stream_t;
@@ -320,8 +321,9 @@ int kvz_f8_decode_blocks(kvz_dims dims, int32_t format, const uint32_t *meta, in
 /* kvz_decode_attention over FP8 tiles plus the BF16 tail; same workspace, split and
  * determinism.  FP8 pages are multiplied in f16 (every FP8 value is an f16 value): the
  * queries are rounded to f16 for them, which is exact for |q| in [2^-17, 65504]; larger
- * queries overflow, so q must stay below 65504 in magnitude.  The tail page is multiplied
- * in BF16 with the BF16 queries. */
+ * queries overflow (flagged as KVZ_STATUS_Q_RANGE; that output is not usable), so q must
+ * stay below 65504 in magnitude.  The tail page is multiplied in BF16 with the BF16
+ * queries. */
 int kvz_f8_decode_attention(kvz_dims dims, int32_t format, int32_t batch, int32_t num_q_heads, const void *q,
                             const int32_t *page_ids, int32_t max_pages, const int32_t *seq_lens,
                             const int32_t *tail_page, const uint32_t *meta, int64_t num_meta_pages,

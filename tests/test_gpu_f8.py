@@ -140,3 +140,22 @@ def test_bad_entry_flagged(kvz_lib, oracle, fmt):
     ref, ost = f8.oracle_attention(oracle, meta=o_meta)
     assert ost & 8
     check_attention(out, ref, "bad entry")
+
+
+@pytest.mark.parametrize("fmt", [1, 2], ids=["e4m3", "e5m2"])
+def test_query_beyond_f16_range_is_flagged(kvz_lib, oracle, fmt):
+    """FP8 pages are multiplied in f16: a finite BF16 query element beyond the f16 range
+    sets KVZ_STATUS_Q_RANGE (queries inside the range leave the status clear)."""
+    kvz = kvz_lib
+    cfg = kvgen.KVConfig("q-range", 1, 2, 8, 2, 4, tail_min=1, tail_max=9, seed=61)
+    base = Layer(cfg, None)
+    f8 = F8Layer(base, fmt, oracle)
+    st = kvz.new_status()
+    f8.run(status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    base.g_q[1, 5, 17] = 1.0e5  # BF16 99840: finite, above 65504
+    st = kvz.new_status()
+    f8.run(status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == kvz.STATUS_Q_RANGE
