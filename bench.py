@@ -323,17 +323,23 @@ def flush_l2(buf: torch.Tensor):
     buf.view(torch.int64).sum()
 
 
-def per_launch_ms(fn, iters: int, flush: torch.Tensor) -> float:
-    """Average duration of one call, CUDA events around it, L2 flushed before each call
-    (the flush also keeps the stream busy so the events bracket only the call)."""
+def per_launch_ms(fn, iters: int, flush: torch.Tensor, period: int = 1, prep=None) -> float:
+    """Average duration of one call, CUDA events around it, L2 flushed before each call.
+    Each call is replayed from a CUDA graph (one per k % period), so the events bracket
+    the call's GPU work and not the host's launch overhead; prep(k), if given, runs
+    between the flush and the first event (untimed set-up such as a cursor reset)."""
+    graphs = [graph_of(lambda _k, p=p: fn(p), 1) for p in range(period)]
+    torch.cuda.synchronize()
     st = torch.cuda.current_stream()
     ts = []
     evs = []
     for k in range(iters):
         flush_l2(flush)
+        if prep is not None:
+            prep(k)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(st)
-        fn(k)
+        graphs[k % period].replay()
         e1.record(st)
         evs.append((e0, e1))
     torch.cuda.synchronize()
@@ -528,8 +534,8 @@ def main():
     # (L2 flushed, nothing before or after it) is reported beside it
     achieved = W.alg_bytes_c / (us_step * 1e-6) / 1e9
     achieved_raw = W.alg_bytes_r / (us_raw * 1e-6) / 1e9
-    launch_ms = per_launch_ms(W.step_c, max(10, min(K, 40)), flush)
-    launch_ms_raw = per_launch_ms(W.step_r, max(10, min(K, 40)), flush)
+    launch_ms = per_launch_ms(W.step_c, max(10, min(K, 40)), flush, period=W.copies)
+    launch_ms_raw = per_launch_ms(W.step_r, max(10, min(K, 40)), flush, period=W.copies)
 
     # encode and standalone decode throughput (C1 full pages, cold inputs)
     enc_meta = torch.zeros_like(W.metas[0])
@@ -537,18 +543,17 @@ def main():
     enc_cur = W.cursor0.clone()
 
     def enc(k):
-        enc_cur.copy_(W.cursor0)
         kvz.encode_pages(W.pools[k % W.copies], W.src, W.src, W.dseq, enc_meta, enc_arena, enc_cur, W.status,
                          workspace=W.enc_ws)
 
-    enc_ms = per_launch_ms(enc, 10, flush)
+    enc_ms = per_launch_ms(enc, 10, flush, period=W.copies, prep=lambda k: enc_cur.copy_(W.cursor0))
     enc_in = W.src.numel() * cfg.hkv * 2 * 16 * 128 * 2
     dec_out = torch.empty((W.src.numel(), cfg.hkv, 2, 16, 128), dtype=torch.bfloat16, device=dev)
 
     def dec(k):
         kvz.decode_blocks(W.metas[k % W.copies], W.arenas[k % W.copies], W.src, dec_out, W.status)
 
-    dec_ms = per_launch_ms(dec, 10, flush)
+    dec_ms = per_launch_ms(dec, 10, flush, period=W.copies)
     torch.cuda.synchronize()
     if int(W.status.item()) != 0:
         raise RuntimeError(f"status {int(W.status.item())}")
@@ -834,17 +839,16 @@ def run_ga(args, cfg, dist, rank, world, local):
     us_g, us_c, us_r = (m * 1e3 / K for m in (ms_g, ms_c, ms_r))
     value = job_throughput(world, W.logical_bytes, K, ms_g)
     achieved = GA.alg_bytes / (us_g * 1e-6) / 1e9
-    launch_ms = per_launch_ms(GA.step, max(10, min(K, 40)), flush)
+    launch_ms = per_launch_ms(GA.step, max(10, min(K, 40)), flush, period=W.copies)
 
     enc_meta = torch.zeros_like(GA.metas[0])
     enc_arena = torch.zeros_like(GA.arenas[0])
     enc_cur = GA.cursor0.clone()
 
     def enc(k):
-        enc_cur.copy_(GA.cursor0)
         GA.encode(k % W.copies, enc_meta, enc_arena, enc_cur)
 
-    enc_ms = per_launch_ms(enc, 10, flush)
+    enc_ms = per_launch_ms(enc, 10, flush, period=W.copies, prep=lambda k: enc_cur.copy_(GA.cursor0))
     enc_in = W.src.numel() * cfg.hkv * 2 * 16 * 128 * 2
     dec_out = torch.empty((W.src.numel(), cfg.hkv, 2, 16, 128),
                           dtype=torch.bfloat16 if args.format == "ga" else torch.uint8, device=dev)
@@ -852,7 +856,7 @@ def run_ga(args, cfg, dist, rank, world, local):
     def dec(k):
         GA.decode(k % W.copies, dec_out)
 
-    dec_ms = per_launch_ms(dec, 10, flush)
+    dec_ms = per_launch_ms(dec, 10, flush, period=W.copies)
     torch.cuda.synchronize()
     if int(W.status.item()) != 0:
         raise RuntimeError(f"status {int(W.status.item())}")
@@ -1383,18 +1387,18 @@ def run_sweep(args, dist, rank, local):
         out = torch.empty_like(pool)
 
         def enc(k):
-            cur.copy_(cur0)
             kvz.encode_pages(pool, src, src, seq, meta, arena, cur, st, workspace=ws)
 
         def dec(k):
             kvz.decode_blocks(meta, arena, src, out, st)
 
+        cur.copy_(cur0)
         enc(0)
         dec(0)
         torch.cuda.synchronize()
         assert int(st.item()) == 0 and torch.equal(out.view(torch.int16), pool.view(torch.int16))
         reps = 5 if mb <= 1024 else 3
-        e_ms = per_launch_ms(enc, reps, flush)
+        e_ms = per_launch_ms(enc, reps, flush, prep=lambda k: cur.copy_(cur0))
         d_ms = per_launch_ms(dec, reps, flush)
         nbytes = pool.numel() * 2
         tags = (meta >> 32) & 0xFFFFFFFF

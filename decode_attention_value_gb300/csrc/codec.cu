@@ -309,75 +309,111 @@ __global__ void __launch_bounds__(kPackWarps * 32, 2) k_enc_pack_w(EncodeParams 
 }
 
 // ---------------------------------------------------------------------------------
-// standalone decode: one CTA per (entry, head); warp w restores block (w/4, w%4) with
-// the same register restore the attention kernel uses, scatters it to a staged page
-// slice, and the CTA writes the 8 KB slice back in the plain page layout.
+// standalone decode: warp per (entry, head) item in a grid-stride loop.  The warp loads
+// the item's two group words, issues the loads of a group's four blocks together,
+// restores each lane's fragments with the same register restore the attention kernel
+// uses, scatters them into its own staged page slice, and writes the 8 KB slice back in
+// the plain page layout with 16-byte stores.  Many items per SM stay in flight (a CTA
+// per item with a warp per block kept too few in flight to cover the three dependent
+// loads of page id, group words and blocks).
 // ---------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_decode(DecodeParams P)
+constexpr int kDecWarps = 8;
+
+__global__ void __launch_bounds__(kDecWarps * 32, 3) k_decode_w(DecodeParams P)
 {
-    __shared__ __align__(16) uint8_t stage[32 * kStagePitch];
-    const int entry = blockIdx.x / P.hkv, head = blockIdx.x % P.hkv;
+    extern __shared__ __align__(16) uint8_t dec_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kv = warp >> 2, j = warp & 3;
-    const int page = P.page[entry];
-    uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    uint32_t bad = 0;
-    if (page < 0 || page >= P.num_meta_pages) {
-        bad = KVZ_STATUS_BAD_INDEX;
-    } else {
-        const uint64_t word = P.meta[((int64_t)page * P.hkv + head) * 2 + kv];
-        const uint32_t offset0 = (uint32_t)word, tags = (uint32_t)(word >> 32);
-        if (!tags_valid(tags) || offset0 == KVZ_OFFSET_INVALID ||
-            ((uint64_t)offset0 + group_granules(tags)) * kGranule > P.arena_bytes) {
-            bad = KVZ_STATUS_BAD_META;
+    uint8_t *stage = dec_smem + warp * (32 * kStagePitch);
+    const int64_t items = (int64_t)P.n * P.hkv;
+    const int64_t stride = (int64_t)gridDim.x * kDecWarps;
+    for (int64_t it = (int64_t)blockIdx.x * kDecWarps + warp; it < items; it += stride) {
+        const int entry = (int)(it / P.hkv), head = (int)(it % P.hkv);
+        const int page = P.page[entry];
+        uint32_t bad = 0;
+        uint64_t words[2] = {0, 0};
+        if (page < 0 || page >= P.num_meta_pages) {
+            bad = KVZ_STATUS_BAD_INDEX;
         } else {
-            uint32_t before = 0;
-            for (int k = 0; k < j; ++k) before += tag_granules((tags >> (8 * k)) & 0xFFu);
-            const uint32_t tag = (tags >> (8 * j)) & 0xFFu;
-            const uint8_t *blk = P.arena + ((uint64_t)offset0 + before) * kGranule;
-            if (tag == 0xFFu) {
-                uint4 a = *reinterpret_cast<const uint4 *>(blk + 32 * lane);
-                uint4 c = *reinterpret_cast<const uint4 *>(blk + 32 * lane + 16);
-                w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-                w[4] = c.x; w[5] = c.y; w[6] = c.z; w[7] = c.w;
-            } else {
-                const uint4 low = *reinterpret_cast<const uint4 *>(blk + 16 * lane);
-                const uint2 code = *reinterpret_cast<const uint2 *>(blk + 512 + 8 * lane);
-                const uint32_t bb = tag * 0x01010101u;
-                uint32_t f0[4], f1[4];
-                restore_fragment(low.x, low.y, code.x, bb, f0);
-                restore_fragment(low.z, low.w, code.y, bb, f1);
-                w[0] = f0[0]; w[1] = f0[1]; w[2] = f0[2]; w[3] = f0[3];
-                w[4] = f1[0]; w[5] = f1[1]; w[6] = f1[2]; w[7] = f1[3];
+            const uint64_t *m = P.meta + ((int64_t)page * P.hkv + head) * 2;
+            words[0] = m[0];
+            words[1] = m[1];
+        }
+        __syncwarp();  // the previous item's stores are done with the buffer
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
+            const uint32_t offset0 = (uint32_t)words[kv], tags = (uint32_t)(words[kv] >> 32);
+            bool use = !(bad & KVZ_STATUS_BAD_INDEX);  // a bad K word leaves the V group usable
+            if (use && (!tags_valid(tags) || offset0 == KVZ_OFFSET_INVALID ||
+                        ((uint64_t)offset0 + group_granules(tags)) * kGranule > P.arena_bytes)) {
+                bad |= KVZ_STATUS_BAD_META;
+                use = false;
             }
+            // the group's four blocks: loads first, then the restores
+            uint4 x[4], y[4];
+            uint32_t before = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t tag = (tags >> (8 * j)) & 0xFFu;
+                x[j] = make_uint4(0, 0, 0, 0);
+                y[j] = make_uint4(0, 0, 0, 0);
+                if (use) {
+                    const uint8_t *blk = P.arena + ((uint64_t)offset0 + before) * kGranule;
+                    if (tag == 0xFFu) {
+                        x[j] = *reinterpret_cast<const uint4 *>(blk + 32 * lane);
+                        y[j] = *reinterpret_cast<const uint4 *>(blk + 32 * lane + 16);
+                    } else {
+                        x[j] = *reinterpret_cast<const uint4 *>(blk + 16 * lane);
+                        const uint2 code = *reinterpret_cast<const uint2 *>(blk + 512 + 8 * lane);
+                        y[j].x = code.x;
+                        y[j].y = code.y;
+                    }
+                }
+                before += tag_granules(tag);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t tag = (tags >> (8 * j)) & 0xFFu;
+                uint32_t w[8];
+                if (!use || tag == 0xFFu) {
+                    w[0] = x[j].x; w[1] = x[j].y; w[2] = x[j].z; w[3] = x[j].w;
+                    w[4] = y[j].x; w[5] = y[j].y; w[6] = y[j].z; w[7] = y[j].w;
+                } else {
+                    const uint32_t bb = tag * 0x01010101u;
+                    uint32_t f0[4], f1[4];
+                    restore_fragment(x[j].x, x[j].y, y[j].x, bb, f0);
+                    restore_fragment(x[j].z, x[j].w, y[j].y, bb, f1);
+                    w[0] = f0[0]; w[1] = f0[1]; w[2] = f0[2]; w[3] = f0[3];
+                    w[4] = f1[0]; w[5] = f1[1]; w[6] = f1[2]; w[7] = f1[3];
+                }
+                // scatter to the staged slice (inverse of gather_block)
+#pragma unroll
+                for (int f = 0; f < 2; ++f)
+#pragma unroll
+                    for (int i = 0; i < 8; i += 2) {
+                        const int r = frag_row(lane, i), c = frag_col(lane, i);
+                        const int dim0 = 32 * j + 16 * f;
+                        const uint32_t v = w[f * 4 + i / 2];
+                        if (kv == 0) {
+                            *reinterpret_cast<uint32_t *>(stage + r * kStagePitch + (dim0 + c) * 2) = v;
+                        } else {
+                            uint8_t *base = stage + (16 + c) * kStagePitch + (dim0 + r) * 2;
+                            *reinterpret_cast<uint16_t *>(base) = (uint16_t)(v & 0xFFFFu);
+                            *reinterpret_cast<uint16_t *>(base + kStagePitch) = (uint16_t)(v >> 16);
+                        }
+                    }
+            }
+        }
+        if (bad && lane == 0) atomicOr(P.status, bad);
+        __syncwarp();
+        uint4 *out = reinterpret_cast<uint4 *>(P.out + ((int64_t)entry * P.hkv + head) * 2 * kPage * kDim);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int q = lane + 32 * k;  // 16-byte chunk q -> row q/16, byte (q%16)*16
+            out[q] = *reinterpret_cast<const uint4 *>(stage + (q >> 4) * kStagePitch + (q & 15) * 16);
         }
     }
-    if (bad && lane == 0) atomicOr(P.status, bad);
-    // scatter to the staged slice (inverse of gather_block)
-#pragma unroll
-    for (int f = 0; f < 2; ++f)
-#pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-            const int r = frag_row(lane, i), c = frag_col(lane, i);
-            const int dim0 = 32 * j + 16 * f;
-            const uint32_t v = w[f * 4 + i / 2];
-            if (kv == 0) {
-                *reinterpret_cast<uint32_t *>(stage + r * kStagePitch + (dim0 + c) * 2) = v;
-            } else {
-                uint8_t *base = stage + (16 + c) * kStagePitch + (dim0 + r) * 2;
-                *reinterpret_cast<uint16_t *>(base) = (uint16_t)(v & 0xFFFFu);
-                *reinterpret_cast<uint16_t *>(base + kStagePitch) = (uint16_t)(v >> 16);
-            }
-        }
-    __syncthreads();
-    uint4 *out = reinterpret_cast<uint4 *>(P.out + ((int64_t)entry * P.hkv + head) * 2 * kPage * kDim);
-    for (int q = threadIdx.x; q < 512; q += blockDim.x)
-        out[q] = *reinterpret_cast<const uint4 *>(stage + (q >> 4) * kStagePitch + (q & 15) * 16);
 }
 
-// ---------------------------------------------------------------------------------
-// cursor updates from the host allocator
-// ---------------------------------------------------------------------------------
 __global__ void k_apply_cursor_updates(const int32_t *idx, const uint32_t *pos, const uint32_t *end, int n,
                                        uint32_t *cursors, int num_cursors)
 {
@@ -395,6 +431,7 @@ __global__ void k_apply_cursor_updates(const int32_t *idx, const uint32_t *pos, 
 // host launchers
 // ---------------------------------------------------------------------------------
 constexpr int kPackSmem = kPackWarps * 32 * kStagePitch;  // 68 KB: one slice buffer per warp
+constexpr int kDecSmem = kDecWarps * 32 * kStagePitch;    // the same for the decoder
 
 // SM count of the current device, and the pack kernel's shared-memory opt-in (once per
 // device and process)
@@ -406,6 +443,8 @@ static cudaError_t encode_grid(int *sms)
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess && !(dev < 64 && ((__atomic_load_n(&done, __ATOMIC_ACQUIRE) >> dev) & 1ull))) {
         e = cudaFuncSetAttribute(k_enc_pack_w, cudaFuncAttributeMaxDynamicSharedMemorySize, kPackSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_decode_w, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
         if (e == cudaSuccess && dev < 64) __atomic_fetch_or(&done, 1ull << dev, __ATOMIC_ACQ_REL);
     }
     return e;
@@ -457,7 +496,10 @@ cudaError_t launch_enc_scan(const EncodeParams &P, cudaStream_t stream)
 
 cudaError_t launch_decode(const DecodeParams &P, cudaStream_t stream)
 {
-    k_decode<<<P.n * P.hkv, 256, 0, stream>>>(P);
+    int sms = 0;
+    cudaError_t e = encode_grid(&sms);
+    if (e != cudaSuccess) return e;
+    k_decode_w<<<grid_for((size_t)P.n * P.hkv, sms, 3), kDecWarps * 32, kDecSmem, stream>>>(P);
     return cudaGetLastError();
 }
 
