@@ -244,56 +244,77 @@ __global__ void __launch_bounds__(256) k_f8_pack(EncodeParams P)
 }
 
 // ---------------------------------------------------------------------------------
-// standalone decode to FP8 bytes: out uint8 [n][hkv][2][16][128]
+// standalone decode to FP8 bytes: out uint8 [n][hkv][2][16][128].  Warp per (entry, head)
+// item in a grid-stride loop: per tile the lane state is loaded once and the four blocks
+// are restored with the attention kernel's register path into the warp's 4 KB page buffer.
 // ---------------------------------------------------------------------------------
+constexpr int kF8DecWarps = 8;
+constexpr int kF8DecSmem = kF8DecWarps * 2 * kPage * kDim;  // 32 KB
+
 template <bool kE5>
-__global__ void __launch_bounds__(256) k_f8_decode(DecodeParams P)
+__global__ void __launch_bounds__(kF8DecWarps * 32) k_f8_decode_w(DecodeParams P)
 {
-    using Lt = F8Layout<kE5>;
-    __shared__ __align__(16) uint8_t page[2][kPage * kDim];
-    const int entry = blockIdx.x / P.hkv, head = blockIdx.x % P.hkv;
+    extern __shared__ __align__(16) uint8_t f8_dec_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kv = warp >> 2, j = warp & 3;
-    const int pid = P.page[entry];
-    uint32_t fb[4] = {0, 0, 0, 0};
-    uint32_t bad = 0;
-    if (pid < 0 || pid >= P.num_meta_pages) {
-        bad = KVZ_STATUS_BAD_INDEX;
-    } else {
-        const uint32_t word = P.meta32[((int64_t)pid * P.hkv + head) * 2 + kv];
-        const uint64_t off = word & kGaOffsetMask;
-        if (word == kGaEntryInvalid || off * kGaGranule + f8_entry_bytes(kE5 ? kF8E5M2 : kF8E4M3, word) > P.arena_bytes) {
-            bad = KVZ_STATUS_BAD_META;
-        } else if (word & kGaEntryRaw) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(P.arena + off * kGaGranule + 512 * j + 16 * lane);
-            fb[0] = v.x; fb[1] = v.y; fb[2] = v.z; fb[3] = v.w;
-        } else {
+    uint8_t *page = f8_dec_smem + warp * (2 * kPage * kDim);
+    const int64_t items = (int64_t)P.n * P.hkv;
+    const int64_t stride = (int64_t)gridDim.x * kF8DecWarps;
+    for (int64_t it = (int64_t)blockIdx.x * kF8DecWarps + warp; it < items; it += stride) {
+        const int entry = (int)(it / P.hkv), head = (int)(it % P.hkv);
+        const int pid = P.page[entry];
+        const bool page_ok = pid >= 0 && pid < P.num_meta_pages;
+        uint32_t bad = page_ok ? 0u : KVZ_STATUS_BAD_INDEX;
+        uint2 words = make_uint2(kGaEntryInvalid, kGaEntryInvalid);
+        if (page_ok) words = *reinterpret_cast<const uint2 *>(P.meta32 + ((int64_t)pid * P.hkv + head) * 2);
+        __syncwarp();  // the previous item's stores are done with the buffer
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
+            const uint32_t word = kv ? words.y : words.x;
+            const uint64_t off = word & kGaOffsetMask;
+            bool use = page_ok;
+            if (use && (word == kGaEntryInvalid ||
+                        off * kGaGranule + f8_entry_bytes(kE5 ? kF8E5M2 : kF8E4M3, word) > P.arena_bytes)) {
+                bad |= KVZ_STATUS_BAD_META;
+                use = false;
+            }
             const uint8_t *tile = P.arena + off * kGaGranule;
             const uint8_t *row = P.ga_bases + ((size_t)head * 2 + kv) * 256;
-            F8Lane<kE5> s = f8_lane_load<kE5>(tile, lane);
-            const uint32_t mask = (1u << (4 * j)) - 1u;  // groups k < 2j of this lane
-            s.off += __popc(s.modes & 0x5555u & mask) + Lt::kEscRaw * __popc(s.modes & 0xAAAAu & mask);
-            const bool any2 = __any_sync(0xffffffffu, s.modes & 0xAAAAu);
-            if (kv == 0) f8_block_bytes<kE5, false>(tile, row, s, any2, lane, j, fb);
-            else f8_block_bytes<kE5, true>(tile, row, s, any2, lane, j, fb);
+            const bool raw = use && (word & kGaEntryRaw);
+            F8Lane<kE5> s;
+            bool any2 = false;
+            if (use && !raw) {  // warp-uniform
+                s = f8_lane_load<kE5>(tile, lane);
+                any2 = __any_sync(0xffffffffu, s.modes & 0xAAAAu);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t fb[4] = {0, 0, 0, 0};
+                if (raw) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(tile + 512 * j + 16 * lane);
+                    fb[0] = v.x; fb[1] = v.y; fb[2] = v.z; fb[3] = v.w;
+                } else if (use) {
+                    if (kv == 0) f8_block_bytes<kE5, false>(tile, row, s, any2, lane, j, fb);
+                    else f8_block_bytes<kE5, true>(tile, row, s, any2, lane, j, fb);
+                }
+#pragma unroll
+                for (int f = 0; f < 2; ++f)
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int r = frag_row(lane, i), c = frag_col(lane, i);
+                        const int dim0 = 32 * j + 16 * f;
+                        const uint8_t b = (uint8_t)(fb[2 * f + i / 4] >> (8 * (i & 3)));
+                        if (kv == 0) page[r * kDim + dim0 + c] = b;                      // K: token r, dim c
+                        else page[kPage * kDim + c * kDim + dim0 + r] = b;                // V: token c, dim r
+                    }
+            }
         }
+        if (bad && lane == 0) atomicOr(P.status, bad);
+        __syncwarp();
+        uint4 *out = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(P.out) +
+                                               ((int64_t)entry * P.hkv + head) * 2 * kPage * kDim);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) out[lane + 32 * k] = reinterpret_cast<const uint4 *>(page)[lane + 32 * k];
     }
-    if (bad && lane == 0) atomicOr(P.status, bad);
-#pragma unroll
-    for (int f = 0; f < 2; ++f)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int r = frag_row(lane, i), c = frag_col(lane, i);
-            const int dim0 = 32 * j + 16 * f;
-            const uint8_t b = (uint8_t)(fb[2 * f + i / 4] >> (8 * (i & 3)));
-            if (kv == 0) page[0][r * kDim + dim0 + c] = b;  // K: token r, dim c
-            else page[1][c * kDim + dim0 + r] = b;          // V: token c, dim r
-        }
-    __syncthreads();
-    uint4 *out = reinterpret_cast<uint4 *>(reinterpret_cast<uint8_t *>(P.out) +
-                                           ((int64_t)entry * P.hkv + head) * 2 * kPage * kDim);
-    for (int q = threadIdx.x; q < 2 * kPage * kDim / 16; q += blockDim.x)
-        out[q] = reinterpret_cast<const uint4 *>(&page[0][0])[q];
 }
 
 // ---------------------------------------------------------------------------------
@@ -323,8 +344,22 @@ cudaError_t launch_f8_encode(int fmt, const EncodeParams &P, cudaStream_t stream
 
 cudaError_t launch_f8_decode(int fmt, const DecodeParams &P, cudaStream_t stream)
 {
-    if (fmt == kF8E5M2) k_f8_decode<true><<<P.n * P.hkv, 256, 0, stream>>>(P);
-    else k_f8_decode<false><<<P.n * P.hkv, 256, 0, stream>>>(P);
+    static unsigned long long done = 0;  // bit per device ordinal < 64: shared-memory opt-in
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess && !(dev < 64 && ((__atomic_load_n(&done, __ATOMIC_ACQUIRE) >> dev) & 1ull))) {
+        e = cudaFuncSetAttribute(k_f8_decode_w<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kF8DecSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_f8_decode_w<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kF8DecSmem);
+        if (e == cudaSuccess && dev < 64) __atomic_fetch_or(&done, 1ull << dev, __ATOMIC_ACQ_REL);
+    }
+    if (e != cudaSuccess) return e;
+    const int64_t items = (int64_t)P.n * P.hkv, want = (items + kF8DecWarps - 1) / kF8DecWarps;
+    const int64_t wave = (int64_t)(sms > 0 ? sms : 1) * 4;
+    const unsigned grid = (unsigned)(want < wave ? (want > 0 ? want : 1) : wave);
+    if (fmt == kF8E5M2) k_f8_decode_w<true><<<grid, kF8DecWarps * 32, kF8DecSmem, stream>>>(P);
+    else k_f8_decode_w<false><<<grid, kF8DecWarps * 32, kF8DecSmem, stream>>>(P);
     return cudaGetLastError();
 }
 

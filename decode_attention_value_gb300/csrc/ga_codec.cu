@@ -277,69 +277,87 @@ __global__ void __launch_bounds__(256) k_ga_pack(EncodeParams P)
 }
 
 // ---------------------------------------------------------------------------------
-// standalone decode: one CTA per (entry, head); warp (kv, j) restores block j of its
-// tile with the attention kernel's register restore, reading the tile in place.
+// standalone decode: warp per (entry, head) item in a grid-stride loop; per tile the
+// lane state (modes, escape offset, codes) is loaded once and the four blocks are
+// restored with the attention kernel's register path, scattered into the warp's staged
+// page slice and written back in the plain page layout.
 // ---------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_ga_decode(DecodeParams P)
+constexpr int kGaDecWarps = 8;
+
+__global__ void __launch_bounds__(kGaDecWarps * 32, 3) k_ga_decode_w(DecodeParams P)
 {
-    __shared__ __align__(16) uint8_t stage[32 * kStagePitch];
-    const int entry = blockIdx.x / P.hkv, head = blockIdx.x % P.hkv;
+    extern __shared__ __align__(16) uint8_t ga_dec_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kv = warp >> 2, j = warp & 3;
-    const int page = P.page[entry];
-    uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    uint32_t bad = 0;
-    if (page < 0 || page >= P.num_meta_pages) {
-        bad = KVZ_STATUS_BAD_INDEX;
-    } else {
-        const uint32_t entry_word = P.meta32[((int64_t)page * P.hkv + head) * 2 + kv];
-        const uint64_t off = entry_word & kGaOffsetMask;
-        if (entry_word == kGaEntryInvalid || off * kGaGranule + ga_entry_bytes(entry_word) > P.arena_bytes) {
-            bad = KVZ_STATUS_BAD_META;
-        } else if (entry_word & kGaEntryRaw) {
-            const uint8_t *blk = P.arena + off * kGaGranule + 1024 * j;
-            const uint4 a = *reinterpret_cast<const uint4 *>(blk + 32 * lane);
-            const uint4 c = *reinterpret_cast<const uint4 *>(blk + 32 * lane + 16);
-            w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-            w[4] = c.x; w[5] = c.y; w[6] = c.z; w[7] = c.w;
-        } else {
+    uint8_t *stage = ga_dec_smem + warp * (32 * kStagePitch);
+    const int64_t items = (int64_t)P.n * P.hkv;
+    const int64_t stride = (int64_t)gridDim.x * kGaDecWarps;
+    for (int64_t it = (int64_t)blockIdx.x * kGaDecWarps + warp; it < items; it += stride) {
+        const int entry = (int)(it / P.hkv), head = (int)(it % P.hkv);
+        const int page = P.page[entry];
+        const bool page_ok = page >= 0 && page < P.num_meta_pages;
+        uint32_t bad = page_ok ? 0u : KVZ_STATUS_BAD_INDEX;
+        uint2 words = make_uint2(kGaEntryInvalid, kGaEntryInvalid);
+        if (page_ok) words = *reinterpret_cast<const uint2 *>(P.meta32 + ((int64_t)page * P.hkv + head) * 2);
+        __syncwarp();  // the previous item's stores are done with the buffer
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
+            const uint32_t ew = kv ? words.y : words.x;
+            const uint64_t off = ew & kGaOffsetMask;
+            bool use = page_ok;
+            if (use && (ew == kGaEntryInvalid || off * kGaGranule + ga_entry_bytes(ew) > P.arena_bytes)) {
+                bad |= KVZ_STATUS_BAD_META;
+                use = false;
+            }
             const uint8_t *tile = P.arena + off * kGaGranule;
             const uint8_t *row = P.ga_bases + ((size_t)head * 2 + kv) * 256;
-            GaLane s = ga_lane_load(tile, lane);
-            const uint32_t mask = (1u << (4 * j)) - 1u;  // groups k < 2j of this lane
-            s.off += __popc(s.modes & 0x5555u & mask) + 5u * __popc(s.modes & 0xAAAAu & mask);
-            uint32_t f0[4], f1[4];
-            if (kv == 0) {
-                ga_group_frag_any<false>(tile, row, s.modes, s.off, lane, 2 * j, f0);
-                ga_group_frag_any<false>(tile, row, s.modes, s.off, lane, 2 * j + 1, f1);
-            } else {
-                ga_group_frag_any<true>(tile, row, s.modes, s.off, lane, 2 * j, f0);
-                ga_group_frag_any<true>(tile, row, s.modes, s.off, lane, 2 * j + 1, f1);
+            const bool raw = use && (ew & kGaEntryRaw);
+            GaLane gs;
+            bool any2 = false;
+            if (use && !raw) {  // warp-uniform
+                gs = ga_lane_load(tile, lane);
+                any2 = ga_tile_any_raw_groups(gs);
             }
-            w[0] = f0[0]; w[1] = f0[1]; w[2] = f0[2]; w[3] = f0[3];
-            w[4] = f1[0]; w[5] = f1[1]; w[6] = f1[2]; w[7] = f1[3];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                if (raw) {
+                    const uint4 a = *reinterpret_cast<const uint4 *>(tile + 1024 * j + 32 * lane);
+                    const uint4 c = *reinterpret_cast<const uint4 *>(tile + 1024 * j + 32 * lane + 16);
+                    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+                    w[4] = c.x; w[5] = c.y; w[6] = c.z; w[7] = c.w;
+                } else if (use) {
+                    uint32_t a0[4], a1[4];
+                    if (kv == 0) ga_block_frags<false>(tile, row, gs, any2, lane, j, a0, a1);
+                    else ga_block_frags<true>(tile, row, gs, any2, lane, j, a0, a1);
+                    w[0] = a0[0]; w[1] = a0[1]; w[2] = a0[2]; w[3] = a0[3];
+                    w[4] = a1[0]; w[5] = a1[1]; w[6] = a1[2]; w[7] = a1[3];
+                }
+#pragma unroll
+                for (int f = 0; f < 2; ++f)
+#pragma unroll
+                    for (int i = 0; i < 8; i += 2) {
+                        const int r = frag_row(lane, i), c = frag_col(lane, i);
+                        const int dim0 = 32 * j + 16 * f;
+                        const uint32_t v = w[f * 4 + i / 2];
+                        if (kv == 0) {
+                            *reinterpret_cast<uint32_t *>(stage + r * kStagePitch + (dim0 + c) * 2) = v;
+                        } else {
+                            uint8_t *base = stage + (16 + c) * kStagePitch + (dim0 + r) * 2;
+                            *reinterpret_cast<uint16_t *>(base) = (uint16_t)(v & 0xFFFFu);
+                            *reinterpret_cast<uint16_t *>(base + kStagePitch) = (uint16_t)(v >> 16);
+                        }
+                    }
+            }
+        }
+        if (bad && lane == 0) atomicOr(P.status, bad);
+        __syncwarp();
+        uint4 *out = reinterpret_cast<uint4 *>(P.out + ((int64_t)entry * P.hkv + head) * 2 * kPage * kDim);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int q = lane + 32 * k;
+            out[q] = *reinterpret_cast<const uint4 *>(stage + (q >> 4) * kStagePitch + (q & 15) * 16);
         }
     }
-    if (bad && lane == 0) atomicOr(P.status, bad);
-#pragma unroll
-    for (int f = 0; f < 2; ++f)
-#pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-            const int r = frag_row(lane, i), c = frag_col(lane, i);
-            const int dim0 = 32 * j + 16 * f;
-            const uint32_t v = w[f * 4 + i / 2];
-            if (kv == 0) {
-                *reinterpret_cast<uint32_t *>(stage + r * kStagePitch + (dim0 + c) * 2) = v;
-            } else {
-                uint8_t *base = stage + (16 + c) * kStagePitch + (dim0 + r) * 2;
-                *reinterpret_cast<uint16_t *>(base) = (uint16_t)(v & 0xFFFFu);
-                *reinterpret_cast<uint16_t *>(base + kStagePitch) = (uint16_t)(v >> 16);
-            }
-        }
-    __syncthreads();
-    uint4 *out = reinterpret_cast<uint4 *>(P.out + ((int64_t)entry * P.hkv + head) * 2 * kPage * kDim);
-    for (int q = threadIdx.x; q < 512; q += blockDim.x)
-        out[q] = *reinterpret_cast<const uint4 *>(stage + (q >> 4) * kStagePitch + (q & 15) * 16);
 }
 
 // ---------------------------------------------------------------------------------
@@ -366,7 +384,19 @@ cudaError_t launch_ga_encode(const EncodeParams &P, cudaStream_t stream)
 
 cudaError_t launch_ga_decode(const DecodeParams &P, cudaStream_t stream)
 {
-    k_ga_decode<<<P.n * P.hkv, 256, 0, stream>>>(P);
+    constexpr int smem = kGaDecWarps * 32 * kStagePitch;
+    static unsigned long long done = 0;  // bit per device ordinal < 64: shared-memory opt-in
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess && !(dev < 64 && ((__atomic_load_n(&done, __ATOMIC_ACQUIRE) >> dev) & 1ull))) {
+        e = cudaFuncSetAttribute(k_ga_decode_w, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess && dev < 64) __atomic_fetch_or(&done, 1ull << dev, __ATOMIC_ACQ_REL);
+    }
+    if (e != cudaSuccess) return e;
+    const int64_t items = (int64_t)P.n * P.hkv, want = (items + kGaDecWarps - 1) / kGaDecWarps;
+    const int64_t wave = (int64_t)(sms > 0 ? sms : 1) * 3;
+    k_ga_decode_w<<<(unsigned)(want < wave ? (want > 0 ? want : 1) : wave), kGaDecWarps * 32, smem, stream>>>(P);
     return cudaGetLastError();
 }
 
