@@ -246,3 +246,58 @@ def test_allocator_with_oracle_stream(kvz, oracle):
     assert all(spans[k][1] <= spans[k + 1][0] for k in range(len(spans) - 1))
     st = a.stats()
     assert st["chunks_held"] + st["chunks_free"] == nchunks
+
+
+def test_allocator_random_exact_reservations_model(kvz):
+    """Random exact reservations and releases over a small arena, against a model of the
+    device cursors: every granted region lies in one chunk owned by its cursor, regions of
+    live cursors never overlap, the allocator's room equals the model cursor's room, a
+    refused reservation changes nothing, and releasing every cursor frees every chunk."""
+    rng = np.random.default_rng(7)
+    chunk, nchunks, ncur = 64, 12, 6
+    a = kvz.Allocator(arena_bytes=chunk * 256 * nchunks, chunk_granules=chunk, num_cursors=ncur, num_kv_heads=2)
+    cur = {}  # cursor -> [pos, end] in granules (the device cursor after the updates)
+    regions = {c: [] for c in range(ncur)}
+    refused = 0
+    for _ in range(3000):
+        if rng.random() < 0.12:
+            c = int(rng.integers(ncur))
+            a.release(c)
+            regions[c] = []
+            cur.pop(c, None)
+            assert a.room(c) == 0
+        else:
+            ids = rng.choice(ncur, size=int(rng.integers(1, 4)), replace=False).astype(np.int32)
+            gr = rng.integers(1, chunk + 1, size=ids.size).astype(np.uint64)
+            before = a.stats()
+            try:
+                _, ups = a.reserve_granules(ids, gr)
+            except kvz.KvzError as e:
+                assert e.code == kvz.ERR_OUT_OF_SPACE
+                assert a.stats() == before
+                refused += 1
+                continue
+            for c, pos, end in ups:
+                cur[c] = [pos, end]
+            for c, g in zip(ids.tolist(), gr.tolist()):
+                pos, end = cur[c]
+                assert pos + g <= end and end - pos <= chunk
+                assert pos // chunk == (pos + g - 1) // chunk  # inside one chunk
+                regions[c].append((pos, pos + g))
+                cur[c][0] = pos + g
+        st = a.stats()
+        assert st["chunks_held"] + st["chunks_free"] == nchunks
+        assert st["held_bytes"] == st["chunks_held"] * chunk * 256
+        for c in range(ncur):
+            assert a.room(c) == (cur[c][1] - cur[c][0] if c in cur else 0)
+        live = sorted((r, c) for c in range(ncur) for r in regions[c])
+        for (r0, c0), (r1, c1) in zip(live, live[1:]):
+            assert r0[1] <= r1[0], (r0, c0, r1, c1)
+        chunks_of = {c: {r[0] // chunk for r in regions[c]} for c in range(ncur)}
+        for c0 in range(ncur):
+            for c1 in range(c0 + 1, ncur):
+                assert not (chunks_of[c0] & chunks_of[c1])  # a chunk belongs to one cursor
+    assert refused > 0  # the arena did run out along the way
+    for c in range(ncur):
+        a.release(c)
+    assert a.stats()["chunks_free"] == nchunks
