@@ -1201,7 +1201,13 @@ def run_stream(args, cfg, dist, rank, world, local):
     arena = torch.zeros(nchunks * chunk * 256, dtype=torch.uint8, device=dev)
     alloc = kvz.Allocator(arena.numel(), chunk, B, hkv)
     cursors = torch.zeros((B, 2), dtype=torch.int32, device=dev)
-    enc_ws = torch.empty(kvz.encode_workspace_size(hkv, B * 16), dtype=torch.uint8, device=dev)
+    enc_ws = torch.empty(kvz.encode_workspace_size(hkv, B * max(16, L)), dtype=torch.uint8, device=dev)
+    # every layer's pages as one pool and one metadata array, so a page completion encodes
+    # all layers in one call (entries ordered by sequence, then layer: each sequence's
+    # groups land in its chunk in layer order, as with one call per layer)
+    raw_all = raw.view((L * P,) + tuple(raw.shape[2:]))
+    meta_all = meta.view((L * P,) + tuple(meta.shape[2:]))
+    lay_off = torch.arange(L, device=dev, dtype=torch.int32) * P
     seqs = np.arange(B, dtype=np.int32)
 
     def apply(updates):
@@ -1243,11 +1249,10 @@ def run_stream(args, cfg, dist, rank, world, local):
                 pending = None
             ticket, ups = alloc.reserve(seqs, [L] * B)
             apply(ups)
-            page = (ids + prompt_pages + t // 16).contiguous()
-            dseq = torch.arange(B, device=dev, dtype=torch.int32)
-            for layer in range(L):
-                kvz.encode_pages(raw[layer], page, page, dseq, meta[layer], arena, cursors, status,
-                                 workspace=enc_ws)
+            page = ids + prompt_pages + t // 16
+            src = (page[:, None] + lay_off[None, :]).reshape(-1).contiguous()  # [B][L]
+            dseq = torch.arange(B, device=dev, dtype=torch.int32).repeat_interleave(L)
+            kvz.encode_pages(raw_all, src, src, dseq, meta_all, arena, cursors, status, workspace=enc_ws)
             pin_cur.copy_(cursors, non_blocking=True)
             ev = torch.cuda.Event()
             ev.record()
@@ -1313,8 +1318,8 @@ def run_stream(args, cfg, dist, rank, world, local):
                      "compressed_seqs_chunk_granular": int(budget // (held_per_seq + meta_per_seq))},
         "clocks": clocks,
         # attention + merge per layer per step, plus 4 encode launches (prepare, sizes, scan,
-        # pack) per layer at each page completion
-        "gpu_launches": T * L * 2 + len(enc_steps) * L * 4,
+        # pack) for all layers at each page completion
+        "gpu_launches": T * L * 2 + len(enc_steps) * 4,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
