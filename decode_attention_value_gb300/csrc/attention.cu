@@ -59,7 +59,9 @@ struct Smem {
     static constexpr int mo = ml + kConsumers * 8 * 4;
     static constexpr int pref = mo + kConsumers * 4 * 128 * 4;
     __host__ __device__ static int tail(int batch) { return pref + (batch + 1) * 4; }
-    __host__ __device__ static int bytes(int batch) { return tail(batch) + ((batch + 15) & ~15); }
+    // tile formats: the segment's KV-head base table (256 words)
+    __host__ __device__ static int bases(int batch) { return (tail(batch) + batch + 15) & ~15; }
+    __host__ __device__ static int bytes(int batch, bool tiles) { return bases(batch) + (tiles ? 1024 : 0); }
 };
 
 __device__ __forceinline__ uint32_t swz128(int row, int col)
@@ -392,7 +394,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
         const PageLoc L = locate(pref, B, hkv, x);
         const int64_t send = min(hi, unit_end(pref, hkv, L));
         const int64_t cnt = send - x;
-        const uint8_t *ga_row = kTiles ? P.ga_bases + (size_t)L.kvh * 512 : nullptr;  // K b3 row; V at +256
+        // tile formats: this KV head's base vectors as a shared-memory table (the previous
+        // segment's readers have passed its closing barrier)
+        uint32_t *btbl = reinterpret_cast<uint32_t *>(smem + Smem::bases(B));
+        if constexpr (kTiles) {
+            ga_fill_bases_table(P.ga_bases + (size_t)L.kvh * 512, btbl, tid);
+            asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");
+        }
 
         // queries of this segment: B operand of QK^T, read from global memory.  G <= 4:
         // column n = head n % 4 (zero if >= G); G = 5..8: column n = head n (zero if >= G).
@@ -446,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         uint32_t a0[4], a1[4];
-                        ga_block_frags<false>(st, ga_row, gs, any2, lane, j, a0, a1);
+                        ga_block_frags<false>(st, btbl, gs, any2, lane, j, a0, a1);
                         mma_bf16_16816(sc, a0, qf[2 * j][0], qf[2 * j][1]);
                         mma_bf16_16816(sc, a1, qf[2 * j + 1][0], qf[2 * j + 1][1]);
                     }
@@ -456,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         uint32_t fb[4], a0[4], a1[4];
-                        f8_block_bytes<kE5, false>(st, ga_row, fs, any2, lane, j, fb);
+                        f8_block_bytes<kE5, false>(st, btbl, fs, any2, lane, j, fb);
                         f8_frags_f16<kE5>(fb, a0, a1);
                         mma_f16_16816(sc, a0, qf[2 * j][0], qf[2 * j][1]);
                         mma_f16_16816(sc, a1, qf[2 * j + 1][0], qf[2 * j + 1][1]);
@@ -585,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         uint32_t a0[4], a1[4];
-                        ga_block_frags<true>(tv, ga_row + 256, gs, any2, lane, j, a0, a1);
+                        ga_block_frags<true>(tv, btbl, gs, any2, lane, j, a0, a1);
                         pv(o[2 * j], a0);
                         pv(o[2 * j + 1], a1);
                     }
@@ -596,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         uint32_t fb[4], a0[4], a1[4];
-                        f8_block_bytes<kE5, true>(tv, ga_row + 256, fs, any2, lane, j, fb);
+                        f8_block_bytes<kE5, true>(tv, btbl, fs, any2, lane, j, fb);
                         f8_frags_f16<kE5>(fb, a0, a1);
                         pv16(o[2 * j], a0);
                         pv16(o[2 * j + 1], a1);
@@ -853,8 +861,6 @@ __global__ void __launch_bounds__(128 * kGroups) k_attn_merge(const AttnParams P
 // ---------------------------------------------------------------------------------
 // launcher
 // ---------------------------------------------------------------------------------
-int attn_smem_bytes(int batch) { return Smem::bytes(batch); }
-
 template <int kFmt, bool kG8>
 static cudaError_t configure(int dev)
 {
@@ -876,7 +882,8 @@ template <int kFmt, bool kG8>
 static cudaError_t occupancy(int dev, int batch, int *n)
 {
     cudaError_t e = configure<kFmt, kG8>(dev);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, k_attn<kFmt, kG8>, kThreads, Smem::bytes(batch));
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(n, k_attn<kFmt, kG8>, kThreads,
+                                                                     Smem::bytes(batch, kFmt >= kFmtGa));
     return e;
 }
 
@@ -911,7 +918,7 @@ static cudaError_t launch_impl(const AttnParams &P, const void *tmap, cudaStream
     if (e != cudaSuccess) return e;
     CUtensorMap map;
     memcpy(&map, tmap, sizeof(map));
-    k_attn<kFmt, kG8><<<P.grid, kThreads, Smem::bytes(P.batch), stream>>>(P, map);
+    k_attn<kFmt, kG8><<<P.grid, kThreads, Smem::bytes(P.batch, kFmt >= kFmtGa), stream>>>(P, map);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // slot groups only when the average unit spans more than a chunk of CTAs

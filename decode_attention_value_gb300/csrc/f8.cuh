@@ -89,9 +89,9 @@ __device__ __forceinline__ uint32_t f8_assemble(uint32_t sm, uint32_t e)
 // One group of a compressed tile -> its 8 FP8 bytes (f0: elements 0..3, f1: 4..7).
 // Modes 0 and 1 take no branch; raw-exponent groups (E5M2 mode 2) are handled in a
 // branch that only tiles holding them enter (any2, warp-uniform).
-template <bool kE5, bool kV>
+template <bool kE5, bool kV, typename Row>
 __device__ __forceinline__ void f8_restore_group(uint32_t smfield, uint32_t code, uint32_t mode, bool any2,
-                                                 const uint8_t *esc, uint32_t &off, const uint8_t *row, int lane,
+                                                 const uint8_t *esc, uint32_t &off, const Row *row, int lane,
                                                  int j, int f, uint32_t &f0, uint32_t &f1)
 {
     using Lt = F8Layout<kE5>;
@@ -190,8 +190,8 @@ __device__ __forceinline__ uint32_t f8_sm_field(const F8Lane<kE5> &s, int k)
 }
 
 // FP8 bytes of block j (both f) of a compressed tile: f[0..1] fragment 0, f[2..3] fragment 1.
-template <bool kE5, bool kV>
-__device__ __forceinline__ void f8_block_bytes(const uint8_t *tile, const uint8_t *row, F8Lane<kE5> &s, bool any2,
+template <bool kE5, bool kV, typename Row>
+__device__ __forceinline__ void f8_block_bytes(const uint8_t *tile, const Row *row, F8Lane<kE5> &s, bool any2,
                                                int lane, int j, uint32_t (&fb)[4])
 {
     const uint8_t *esc = tile + F8Layout<kE5>::kEscOff;

@@ -85,6 +85,41 @@ __device__ __forceinline__ void ga_bases(const uint8_t *row, uint32_t w, int lan
     }
 }
 
+// The same base vectors from a per-KV-head table in shared memory, built once per
+// attention segment by ga_fill_bases_table: K words [((2j + f) * 2 + w) * 4 + t] as
+// (b0, b1) pairs at 2x, V words at 128 + ((2j + f) * 2 + w) * 8 + g (b0 = b1).
+template <bool kV>
+__device__ __forceinline__ void ga_bases(const uint32_t *tbl, uint32_t w, int lane, int j, int f, uint32_t &b0,
+                                         uint32_t &b1)
+{
+    if (!kV) {
+        const uint2 v = *reinterpret_cast<const uint2 *>(tbl + 2 * (((2 * j + f) * 2 + (int)w) * 4 + (lane & 3)));
+        b0 = v.x;
+        b1 = v.y;
+    } else {
+        b0 = b1 = tbl[128 + ((2 * j + f) * 2 + (int)w) * 8 + (lane >> 2)];
+    }
+}
+
+// Build the table above for one KV head (row: its 512 bytes of bases, K b3 | K b4 | V b3 |
+// V b4), 128 threads (tid 0..127): the same words ga_bases computes from the row.
+__device__ __forceinline__ void ga_fill_bases_table(const uint8_t *row, uint32_t *tbl, int tid)
+{
+    if (tid < 64) {  // K pair: (2j + f, w, t)
+        const int t = tid & 3, w = (tid >> 2) & 1, jf = tid >> 3;
+        uint32_t b0, b1;
+        ga_bases<false>(row, (uint32_t)w, t, jf >> 1, jf & 1, b0, b1);
+        tbl[2 * tid] = b0;
+        tbl[2 * tid + 1] = b1;
+    }
+    {  // V word: (2j + f, w, g)
+        const int g = tid & 7, w = (tid >> 3) & 1, jf = tid >> 4;
+        uint32_t b0, b1;
+        ga_bases<true>(row + 256, (uint32_t)w, g << 2, jf >> 1, jf & 1, b0, b1);
+        tbl[128 + tid] = b0;
+    }
+}
+
 // Exponent bytes + sign/fraction bytes -> the four bf16x2 fragment registers.
 __device__ __forceinline__ void ga_assemble(uint32_t sf0, uint32_t sf1, uint32_t e0, uint32_t e1, uint32_t (&a)[4])
 {
@@ -104,10 +139,10 @@ __device__ __forceinline__ void ga_assemble(uint32_t sf0, uint32_t sf1, uint32_t
 // holding such groups enter (any2, warp-uniform).  sf0/sf1: sign/fraction bytes of
 // elements 0..3 / 4..7; code: 24-bit field; esc: the tile's escape area; off: running
 // offset of this lane's next escape byte.
-template <bool kV>
+template <bool kV, typename Row>
 __device__ __forceinline__ void ga_restore_group_fast(uint32_t sf0, uint32_t sf1, uint32_t code, uint32_t mode,
                                                       bool any2, const uint8_t *esc, uint32_t &off,
-                                                      const uint8_t *row, int lane, int j, int f, uint32_t (&a)[4])
+                                                      const Row *row, int lane, int j, int f, uint32_t (&a)[4])
 {
     const uint32_t m1 = mode & 1u;
     uint32_t h = 0;
@@ -129,31 +164,6 @@ __device__ __forceinline__ void ga_restore_group_fast(uint32_t sf0, uint32_t sf1
         }
     }
     ga_assemble(sf0, sf1, c0 + b0, c1 + b1, a);  // byte adds never carry (every e <= 255)
-}
-
-// Restore one group of any mode (tiles holding raw-exponent groups).
-template <bool kV>
-__device__ __forceinline__ void ga_restore_group(uint32_t sf0, uint32_t sf1, uint32_t code, uint32_t mode,
-                                                 const uint8_t *esc, uint32_t &off, const uint8_t *row, int lane,
-                                                 int j, int f, uint32_t (&a)[4])
-{
-    uint32_t c0 = ga_spread3(code & 0xFFFu), c1 = ga_spread3((code >> 12) & 0xFFFu);
-    uint32_t b0 = 0, b1 = 0;
-    if (mode == 1) {
-        const uint32_t h = esc[min(off, kGaEscCap - 1)];
-        c0 |= ga_spread1_hi(h);
-        c1 |= ga_spread1_hi(h >> 4);
-        off += 1;
-    } else if (mode >= 2) {
-        const uint8_t *p = esc + min(off, kGaEscCap - 5);
-        const uint32_t lo = (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
-        const uint32_t hi8 = p[4];
-        c0 |= ga_spread5_hi(lo & 0xFFFFFu);
-        c1 |= ga_spread5_hi((lo >> 20) | (hi8 << 12));
-        off += 5;
-    }
-    if (mode < 2) ga_bases<kV>(row, mode, lane, j, f, b0, b1);
-    ga_assemble(sf0, sf1, c0 + b0, c1 + b1, a);
 }
 
 // This lane's 24 code bytes (groups 8L..8L+7) as six words; group k's field.
@@ -187,8 +197,8 @@ __device__ __forceinline__ GaLane ga_lane_load(const uint8_t *tile, int lane)
 
 // Fragments of block j (both f) of a compressed tile; row = this head's b3 row;
 // any2: some lane's group of this tile has mode 2 (warp-uniform).
-template <bool kV>
-__device__ __forceinline__ void ga_block_frags(const uint8_t *tile, const uint8_t *row, GaLane &s, bool any2, int lane,
+template <bool kV, typename Row>
+__device__ __forceinline__ void ga_block_frags(const uint8_t *tile, const Row *row, GaLane &s, bool any2, int lane,
                                                int j, uint32_t (&a0)[4], uint32_t (&a1)[4])
 {
     const uint4 sf = *reinterpret_cast<const uint4 *>(tile + 512 * j + 16 * lane);
@@ -196,19 +206,6 @@ __device__ __forceinline__ void ga_block_frags(const uint8_t *tile, const uint8_
     const uint32_t m0 = (s.modes >> (4 * j)) & 3u, m1 = (s.modes >> (4 * j + 2)) & 3u;
     ga_restore_group_fast<kV>(sf.x, sf.y, ga_code_field(s.code, 2 * j), m0, any2, esc, s.off, row, lane, j, 0, a0);
     ga_restore_group_fast<kV>(sf.z, sf.w, ga_code_field(s.code, 2 * j + 1), m1, any2, esc, s.off, row, lane, j, 1, a1);
-}
-
-// Fragment of group k = 2j + f (any mode) with run-time k, reading the code field from
-// the tile: the compact path for tiles that hold raw-exponent groups.
-template <bool kV>
-__device__ __forceinline__ void ga_group_frag_any(const uint8_t *tile, const uint8_t *row, uint32_t modes,
-                                                  uint32_t &off, int lane, int k, uint32_t (&a)[4])
-{
-    const int j = k >> 1, f = k & 1;
-    const uint2 sf = *reinterpret_cast<const uint2 *>(tile + 512 * j + 16 * lane + 8 * f);
-    const uint8_t *c = tile + kGaCodeOff + 24 * lane + 3 * k;
-    const uint32_t code = (uint32_t)c[0] | ((uint32_t)c[1] << 8) | ((uint32_t)c[2] << 16);
-    ga_restore_group<kV>(sf.x, sf.y, code, (modes >> (2 * k)) & 3u, tile + kGaEscOff, off, row, lane, j, f, a);
 }
 
 // Whether any lane's groups of this tile use the raw-exponent mode.  Warp-collective.

@@ -114,7 +114,6 @@ cudaError_t launch_apply_cursor_updates(const int32_t *idx, const uint32_t *pos,
 // 3 / 4 FP8 E4M3 / E5M2 tiles (completed pages; the tail stays BF16)
 enum AttnFormat : int { kFmtRaw = 0, kFmtZf = 1, kFmtGa = 2, kFmtF8E4 = 3, kFmtF8E5 = 4 };
 cudaError_t launch_attention(const AttnParams &P, int format, const void *tmap, cudaStream_t stream);
-int attn_smem_bytes(int batch);
 // CTAs per SM both attention kernels can hold at this batch size (the smaller of the two)
 cudaError_t attn_ctas_per_sm(int batch, int *out);
 
