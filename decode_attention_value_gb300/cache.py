@@ -156,30 +156,53 @@ class CompressedKVCache:
         self.lens[slots] += 1
 
     def _finalize(self, done):
-        """Encode the filled tail pages of `done` in every layer, each layer's pages placed
-        by exact reservation (all-or-nothing check first, so OutOfSpace changes nothing)."""
+        """Encode the filled tail pages of `done` in every layer, placed by exact
+        reservation (all-or-nothing check first, so OutOfSpace changes nothing).  All
+        layers go through at most two encode calls: first, for every sequence, the layers
+        that still fit its current chunk (in layer order); then the rest, each sequence's
+        remainder in a fresh chunk.  The layers' tail pages and metadata are viewed as one
+        pool and one array, entries ordered by sequence and then layer."""
         dev = self.device
         src = torch.as_tensor(done, dtype=torch.int32, device=dev)
-        dst = torch.as_tensor([s * self.max_pages + int(self.lens[s]) // PAGE for s in done], dtype=torch.int32,
-                              device=dev)
         sizes = self._sizes(self.tails, src)  # [layers][n]
         chunk = self.chunk_bytes // 256
-        # chunks the whole step needs, counted before anything is reserved
-        need = 0
+        L, n = self.layers, len(done)
+        # per sequence: how many leading layers fit the current chunk's room
+        split = []
         for i, s in enumerate(done):
-            room, fresh = self.alloc.room(s), False
-            for layer in range(self.layers):
-                if sizes[layer, i] > room:
-                    need += 1
-                    room, fresh = chunk, True
-                room -= sizes[layer, i]
+            room, k = self.alloc.room(s), 0
+            while k < L and sizes[k, i] <= room:
+                room -= sizes[k, i]
+                k += 1
+            if k < L and int(sizes[k:, i].sum()) > chunk:
+                raise ValueError("one page completion of every layer is larger than a chunk")
+            split.append(k)
+        need = sum(1 for k in split if k < L)
         if need > self.alloc.stats()["chunks_free"]:
             raise OutOfSpace("no free arena chunk")
-        for layer in range(self.layers):
-            self._reserve(done, sizes[layer].tolist())
-            encode_pages(self.tails[layer], src, dst, src, self.meta[layer], self.arena, self.cursors, self.status,
-                         workspace=self._ws(len(done)))
-        self.pages_encoded += len(done) * self.layers
+        pages_per_layer = self.max_seqs * self.max_pages
+        pool = self.tails.view((L * self.max_seqs,) + tuple(self.tails.shape[2:]))
+        meta = self.meta.view((L * pages_per_layer,) + tuple(self.meta.shape[2:]))
+        for phase in range(2):
+            seqs, grans, ent_src, ent_dst, ent_seq = [], [], [], [], []
+            for i, s in enumerate(done):
+                layers = range(split[i]) if phase == 0 else range(split[i], L)
+                if not len(layers):
+                    continue
+                seqs.append(s)
+                grans.append(int(sum(sizes[l, i] for l in layers)))
+                page = int(self.lens[s]) // PAGE
+                for l in layers:
+                    ent_src.append(l * self.max_seqs + s)
+                    ent_dst.append(l * pages_per_layer + s * self.max_pages + page)
+                    ent_seq.append(s)
+            if not seqs:
+                continue
+            self._reserve(seqs, grans)
+            t = lambda a: torch.as_tensor(a, dtype=torch.int32, device=dev)
+            encode_pages(pool, t(ent_src), t(ent_dst), t(ent_seq), meta, self.arena, self.cursors, self.status,
+                         workspace=self._ws(len(ent_src)))
+        self.pages_encoded += n * L
         self.granules_encoded += int(sizes.sum())
 
     def release(self, slot: int):
