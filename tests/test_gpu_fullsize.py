@@ -93,3 +93,45 @@ def test_8k_layer_sampled(kvz, oracle):
     ref, pool = _oracle_attention(oracle, W, pick)
     check_attention(W.out[pick], ref, "8K layer")
     _check_blocks(kvz, oracle, W, pool)
+
+
+@pytest.mark.parametrize("kind", ["ga", "f8e4", "f8e5"])
+def test_c1_tile_formats_sampled(kvz, oracle, kind):
+    """The tile formats on the Llama-3.1-8B-shaped layer in the launch configuration
+    bench.py --format times: bases calibrated on the GPU equal the oracle's own (same
+    sample of pages), and sampled sequences' outputs match the fp64 oracle run over the
+    oracle's own tiles of those sequences."""
+    import bench
+
+    W = _layer(kvz, kvgen.C1)
+    GA = bench.GaCopies(W, kind)
+    GA.step(0)
+    torch.cuda.synchronize()
+    assert int(W.status.item()) == 0
+    cfg, hkv = W.cfg, W.cfg.hkv
+    pool = kvgen.bits(W.pools[0].cpu())
+    sample = GA.sample.cpu().numpy().astype(np.int32)
+    fmt = {"f8e4": 1, "f8e5": 2}.get(kind)
+    o_bases = (oracle.ga_calibrate_pool(pool, sample, hkv) if kind == "ga"
+               else oracle.f8_calibrate_pool(fmt, pool, sample, hkv))
+    assert np.array_equal(GA.bases.cpu().numpy(), o_bases), "bases"
+    pick = [0, 13, 31]
+    full = W.full[pick].cpu().numpy()
+    gran = (64 if kind == "ga" else 32) * hkv * 2  # worst-case 64-byte granules per page
+    per = cfg.full_pages * gran
+    o_meta = np.zeros((cfg.num_pages, hkv, 2), np.uint32)
+    o_arena = np.zeros(len(pick) * per * 64, np.uint8)
+    cur = np.array([[i * per, (i + 1) * per] for i in range(len(pick))], np.uint32)
+    src = full.reshape(-1).astype(np.int32)
+    seq = np.repeat(np.arange(len(pick), dtype=np.int32), cfg.full_pages)
+    q = kvgen.bits(W.q[pick].cpu())
+    lens, tail = W.seq_lens[pick].cpu().numpy(), W.tail[pick].cpu().numpy()
+    if kind == "ga":
+        assert oracle.ga_encode_pages(pool, o_bases, src, src, seq, o_meta, o_arena, cur, hkv) == 0
+        ref, st = oracle.ga_decode_attention(q, full, lens, tail, o_meta, o_arena, o_bases, pool, hkv, nthreads=16)
+    else:
+        assert oracle.f8_encode_pages(fmt, pool, o_bases, src, src, seq, o_meta, o_arena, cur, hkv) == 0
+        ref, st = oracle.f8_decode_attention(fmt, q, full, lens, tail, o_meta, o_arena, o_bases, pool, hkv,
+                                             nthreads=16)
+    assert st == 0
+    check_attention(GA.out[pick], ref, f"C1 {kind}")
