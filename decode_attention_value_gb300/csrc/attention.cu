@@ -1,7 +1,8 @@
 // attention.cu -- split-KV GQA paged decode attention over compressed pages plus a raw
-// BF16 tail (12-bit block groups, kFmt = kFmtZf; group-adaptive tiles, kFmt = kFmtGa),
-// and the same kernel over plain BF16 pages (kFmt = kFmtRaw, the in-run uncompressed
-// baseline).
+// BF16 tail (12-bit block groups, kFmt = kFmtZf; group-adaptive tiles, kFmt = kFmtGa;
+// FP8 tiles, kFmt = kFmtF8E4 / kFmtF8E5), and the same kernel over plain BF16 pages
+// (kFmt = kFmtRaw, the in-run uncompressed baseline).  kG8 selects the instantiation for
+// 5..8 query heads per KV head.
 //
 // GAAC ("Attention with On-the-Fly Decompression"): the kernel reads compressed tiles
 // and their metadata, rebuilds BF16 only in registers, and compressed blocks and the
@@ -23,7 +24,9 @@
 //    A operand and the G query heads in the N columns (Q read from global memory once
 //    per segment, as the B fragments).  G <= 4 leaves four spare N
 //    columns: Q is duplicated there for QK^T, and for PV they carry the low part of
-//    P = hi + lo (both bf16), so the PV product keeps ~16 bits of P for free;
+//    P = hi + lo (both bf16), so the PV product keeps ~16 bits of P for free.  FP8 tiles
+//    multiply in f16 (their values widen to f16 exactly) and the tile formats read their
+//    per-channel exponent bases from a shared-memory table built once per segment;
 //  * warps merge their online-softmax states per (sequence, KV head) segment, and a
 //    small follow-up kernel merges the segments in a fixed order.
 #include <cuda.h>
