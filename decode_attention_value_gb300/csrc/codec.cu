@@ -52,18 +52,22 @@ __global__ void __launch_bounds__(256, 3) k_enc_sizes_w(EncodeParams P)
             v[2 * b] = p[0];
             v[2 * b + 1] = p[1];
         }
-        uint32_t g = 0;
+        uint32_t g = 0, tags[2] = {0, 0};
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
             uint32_t w[8] = {v[2 * b].x, v[2 * b].y, v[2 * b].z, v[2 * b].w,
                              v[2 * b + 1].x, v[2 * b + 1].y, v[2 * b + 1].z, v[2 * b + 1].w};
             uint32_t mn, mx;
             exponent_range(w, mn, mx);
-            g += (mx <= (mn & ~1u) + 15) ? 3u : 4u;
+            const uint32_t base = mn & ~1u;
+            const bool ok = mx <= base + 15;
+            g += ok ? 3u : 4u;
+            tags[b >> 2] |= (ok ? (base >> 1) : 0xFFu) << (8 * (b & 3));
         }
         if (lane == 0) {
             P.ws_pair_size[it] = g;
             atomicAdd(P.ws_page_size + entry, g);  // integer sum: the same whatever the order
+            if (P.ws_tags) P.ws_tags[it] = tags[0] | ((uint64_t)tags[1] << 32);  // for the pack pass
         }
     }
 }
@@ -240,18 +244,9 @@ __global__ void __launch_bounds__(kPackWarps * 32, 2) k_enc_pack_w(EncodeParams 
             *reinterpret_cast<uint4 *>(stage + (q >> 4) * kStagePitch + (q & 15) * 16) = v[k];
         }
         __syncwarp();
-        uint32_t tagsK = 0, tagsV = 0;  // one tag byte per block
-#pragma unroll 1
-        for (int b = 0; b < 8; ++b) {
-            uint32_t w[8];
-            gather_block(stage, b >> 2, b & 3, lane, w);
-            uint32_t mn, mx;
-            exponent_range(w, mn, mx);
-            const uint32_t base = mn & ~1u;
-            const uint32_t tag = mx <= base + 15 ? (base >> 1) : 0xFFu;
-            if (b < 4) tagsK |= tag << (8 * b);
-            else tagsV |= tag << (8 * (b - 4));
-        }
+        // one tag byte per block, as the size pass found them
+        const uint64_t tags = P.ws_tags[it];
+        const uint32_t tagsK = (uint32_t)tags, tagsV = (uint32_t)(tags >> 32);
         const uint32_t gK = group_granules(tagsK), gV = group_granules(tagsV);
         const uint64_t pair_base = (uint64_t)P.ws_page_base[entry] + before_heads;
         const uint64_t end = min((uint64_t)P.cursors[2 * seq + 1], P.arena_bytes / kGranule);

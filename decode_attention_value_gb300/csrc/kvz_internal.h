@@ -30,9 +30,17 @@ struct EncodeParams {
     uint32_t *ws_page_size;  // [n] granules per page, summed over heads (zeroed each call)
     uint32_t *ws_page_base;  // [n] granule position of each page's first group
     uint32_t *ws_pair_size;  // [n*hkv] granules per (page, head) K+V pair
+    uint64_t *ws_tags;       // [n*hkv] 12-bit encoder: the size pass's block tags per (page, head),
+                             // K group's four tag bytes | V group's << 32 (null: not kept)
 };
 
 inline size_t encode_ws_bytes(int n, int hkv)
+{
+    const size_t a = ((size_t)n * 4 + 15) / 16 * 16;
+    return 16 + 2 * a + ((size_t)n * hkv * 4 + 15) / 16 * 16 + (size_t)n * hkv * 8;
+}
+// byte offset of ws_tags in the encoder workspace
+inline size_t encode_ws_tags_offset(int n, int hkv)
 {
     const size_t a = ((size_t)n * 4 + 15) / 16 * 16;
     return 16 + 2 * a + ((size_t)n * hkv * 4 + 15) / 16 * 16;
