@@ -1091,6 +1091,12 @@ def run_stack(args, cfg, dist, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     layers = [Workload(cfg, 1, layer=layer, dev=dev) for layer in range(cfg.layers)]
+    # one block table for every layer, as a paged KV cache keeps it (each layer has its own
+    # pools and metadata behind the same page ids)
+    for W in layers[1:]:
+        assert torch.equal(W.table, layers[0].table) and torch.equal(W.seq_lens, layers[0].seq_lens)
+        W.table, W.full, W.tail, W.raw_table = layers[0].table, layers[0].full, layers[0].tail, layers[0].raw_table
+        W.seq_lens = layers[0].seq_lens
     K = args.steps
 
     def step_c(k):
