@@ -82,7 +82,11 @@ def test_host_rejects_bad_arguments(kvz):
     assert lib.kvz_encode_pages(_dims(kvz), fake, 1, fake, fake, fake, 1, fake, 1, fake + 16, 1 << 20, fake, 1,
                                 fake, 1 << 20, fake, None) == E["align"]
     ws = kvz.encode_workspace_size(8, 10)
-    assert ws >= 10 * 8 * 4 + 2 * 10 * 4  # per-(page, head) sizes, per-page sizes and positions
+    # per-(page, head) sizes and block tags, per-page sizes and positions
+    assert ws >= 10 * 8 * (4 + 8) + 2 * 10 * 4
+    for hkv, n in ((1, 1), (2, 7), (8, 4096)):  # grows with the call, stays 16-byte granular
+        w = kvz.encode_workspace_size(hkv, n)
+        assert w % 8 == 0 and w >= n * hkv * 12 + 2 * n * 4 + 16
     assert lib.kvz_encode_pages(_dims(kvz), fake, 10, fake, fake, fake, 10, fake, 10, fake, 1 << 20, fake, 1,
                                 fake, ws - 1, fake, None) == E["ws"]
     # decode: misaligned output
