@@ -62,216 +62,335 @@ __global__ void __launch_bounds__(256) k_ga_calibrate(int hkv, const uint16_t *p
 }
 
 // ---------------------------------------------------------------------------------
-// group modes of a lane's two groups of block (kv, j), from the staged slice
+// Window tests, two values at a time.  With the exponents of a bf16x2 word spread to
+// 16-bit halves, X = (w >> 7) & 0x00FF00FF, and the bases spread the same way, each half
+// of D = X + 0x0100 - B is 256 + e - b in [1, 511] (no borrow between halves), and e lies
+// in [b, b + 8) exactly when (D & 0x1F8) == 0x100 (0x1F0 for [b, b + 16)).
 // ---------------------------------------------------------------------------------
-struct GaGroups {
-    uint32_t w[8];     // the 16 values in storage order (see gather_block)
-    uint32_t mode[2];  // per fragment f
-    uint32_t esc[2];   // escape bytes per fragment
-};
+constexpr uint32_t kGaHalfOne = 0x01000100u, kGaWin8 = 0x01F801F8u, kGaWin16 = 0x01F001F0u;
 
-// sb: this head's bases in shared memory, [2 kv][2 width][128]
-__device__ __forceinline__ void ga_modes(const uint8_t *stage, const uint8_t *sb, int kv, int j, int lane, GaGroups &G)
+__device__ __forceinline__ uint32_t ga_exp2(uint32_t w) { return (w >> 7) & 0x00FF00FFu; }
+// bytes 2s and 2s+1 of x (two bases) -> 16-bit halves
+__device__ __forceinline__ uint32_t ga_spread(uint32_t x, int s) { return __byte_perm(x, 0, s ? 0x4342 : 0x4140); }
+// nonzero half: that value is outside the window
+__device__ __forceinline__ uint32_t ga_viol(uint32_t d, uint32_t win) { return (d & win) ^ kGaHalfOne; }
+
+// ---------------------------------------------------------------------------------
+// size pass: warp per (entry, head) item in a grid-stride loop.  The page slice is read in
+// its plain layout (lane = token lane/2, channels 16*(lane%2)..+16 of each block), the
+// window tests run on bf16x2 words, and each storage-order group (lane', f) is gathered
+// from the lanes that hold it with shuffles: a K group is channels {c, c+1, c+8, c+9} of
+// tokens r and r+8 (words c/2 and c/2+4 of lanes 2r+f and 2r+f+16); a V group is channels
+// r and r+8 (one half of words r/2 and r/2+4) of tokens c, c+1, c+8, c+9 (lanes 2c+f
+// xor 0, 2, 16, 18).  It records the granules of the pair and the two tiles' escape
+// byte counts for the pack pass.
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t ga_block_flags(const uint4 &lo, const uint4 &hi, const uint8_t *row)
 {
-    gather_block(stage, kv, j, lane, G.w);
+    // row: the block's 16 channels of this lane in the b3 table; b4 is 128 bytes on
+    const uint4 b3 = __ldg(reinterpret_cast<const uint4 *>(row));
+    const uint4 b4 = __ldg(reinterpret_cast<const uint4 *>(row + 128));
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    const uint32_t s3[4] = {b3.x, b3.y, b3.z, b3.w}, s4[4] = {b4.x, b4.y, b4.z, b4.w};
+    uint32_t p3[4] = {0, 0, 0, 0}, p4[4] = {0, 0, 0, 0};
 #pragma unroll
-    for (int f = 0; f < 2; ++f) {
-        bool ok3 = true, ok4 = true;
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t x = ga_exp2(w[k]) + kGaHalfOne;
+        p3[k & 3] |= ga_viol(x - ga_spread(s3[k >> 1], k & 1), kGaWin8);
+        p4[k & 3] |= ga_viol(x - ga_spread(s4[k >> 1], k & 1), kGaWin16);
+    }
+    // per half: bit 2g (8-wide window missed) and 2g+1 (16-wide missed) for words g, g+4;
+    // halves are <= 0x1F8, so adding 0x7FFF sets bit 15 exactly when one is nonzero
+    uint32_t m = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const uint32_t v = (G.w[f * 4 + i / 2] >> (16 * (i & 1))) & 0xFFFFu;
-            const uint32_t e = (v >> 7) & 0xFFu;
-            const int dim = 32 * j + 16 * f + (kv == 0 ? frag_col(lane, i) : frag_row(lane, i));
-            const uint32_t b3 = sb[(kv * 2 + 0) * 128 + dim], b4 = sb[(kv * 2 + 1) * 128 + dim];
-            ok3 = ok3 && e >= b3 && e - b3 < 8u;
-            ok4 = ok4 && e >= b4 && e - b4 < 16u;
+    for (int g = 0; g < 4; ++g) {
+        m |= (((p3[g] + 0x7FFF7FFFu) & 0x80008000u) >> (15 - 2 * g));
+        m |= (((p4[g] + 0x7FFF7FFFu) & 0x80008000u) >> (14 - 2 * g));
+    }
+    return m;  // bits 0..7: low halves; bits 16..23: high halves
+}
+
+// escape bytes of the groups in a flag word (bit 2g: 8-wide missed, 2g+1: 16-wide missed):
+// 0 for the 3-bit mode, 1 for the 4-bit mode, 5 for raw groups
+__device__ __forceinline__ uint32_t ga_flag_escapes(uint32_t m)
+{
+    const uint32_t n3 = m & 0x55555555u, n4 = (m >> 1) & 0x55555555u;
+    return __popc(n3) + 4 * __popc(n3 & n4);
+}
+
+__global__ void __launch_bounds__(256, 3) k_ga_sizes_w(EncodeParams P)
+{
+    if (P.ws_hdr[0] != 0) return;
+    const int lane = threadIdx.x & 31;
+    const int64_t items = (int64_t)P.n * P.hkv;
+    const int64_t stride = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t it = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items; it += stride) {
+        const int entry = (int)(it / P.hkv), head = (int)(it % P.hkv);
+        const uint16_t *slice = P.raw_pool + ((int64_t)P.src_page[entry] * P.hkv + head) * 2 * kPage * kDim;
+        uint4 v[16];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {  // block (kv = b/4, j = b%4)
+            const uint4 *p = reinterpret_cast<const uint4 *>(slice + (b >> 2) * kPage * kDim + (lane >> 1) * kDim +
+                                                             32 * (b & 3) + 16 * (lane & 1));
+            v[2 * b] = p[0];
+            v[2 * b + 1] = p[1];
         }
-        G.mode[f] = ok3 ? 0u : (ok4 ? 1u : 2u);
-        G.esc[f] = ok3 ? 0u : (ok4 ? 1u : 5u);
-    }
-}
-
-__device__ __forceinline__ void ga_stage_page(const EncodeParams &P, int entry, int head, uint8_t *stage, uint8_t *sb)
-{
-    const int src = P.src_page[entry];
-    const uint16_t *slice = P.raw_pool + ((int64_t)src * P.hkv + head) * 2 * kPage * kDim;
-    load_slice_to_stage(slice, stage, threadIdx.x, blockDim.x);
-    for (int k = threadIdx.x; k < 512 / 16; k += blockDim.x)
-        reinterpret_cast<uint4 *>(sb)[k] = reinterpret_cast<const uint4 *>(P.ga_bases + (size_t)head * 512)[k];
-}
-
-// ---------------------------------------------------------------------------------
-// size pass: one CTA per (entry, head); warp w = block (kv = w/4, j = w%4)
-// ---------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_ga_sizes(EncodeParams P)
-{
-    __shared__ __align__(16) uint8_t stage[32 * kStagePitch];
-    __shared__ __align__(16) uint8_t sb[512];
-    __shared__ uint32_t esc[8];
-    if (P.ws_hdr[0] != 0) return;
-    const int entry = (int)(blockIdx.x / P.hkv), head = (int)(blockIdx.x % P.hkv);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kv = warp >> 2, j = warp & 3;
-    ga_stage_page(P, entry, head, stage, sb);
-    __syncthreads();
-    GaGroups G;
-    ga_modes(stage, sb, kv, j, lane, G);
-    const uint32_t n = __reduce_add_sync(0xffffffffu, G.esc[0] + G.esc[1]);
-    if (lane == 0) esc[warp] = n;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        const uint32_t eK = esc[0] + esc[1] + esc[2] + esc[3], eV = esc[4] + esc[5] + esc[6] + esc[7];
-        const uint32_t g = (eK <= kGaEscCap ? kGaTileBytes : kGaRawBytes) / kGaGranule +
-                           (eV <= kGaEscCap ? kGaTileBytes : kGaRawBytes) / kGaGranule;
-        P.ws_pair_size[(int64_t)entry * P.hkv + head] = g;
-        atomicAdd(P.ws_page_size + entry, g);
-    }
-}
-
-// ---------------------------------------------------------------------------------
-// pack pass: one CTA per (entry, head).  Each warp (kv, j) computes its lanes' two
-// groups, the escape offsets (lane-major group order) come from per-lane counts in
-// shared memory, compressed tiles are assembled in shared memory and copied out,
-// raw tiles are written straight from the gathered words.
-// ---------------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_ga_pack(EncodeParams P)
-{
-    __shared__ __align__(16) uint8_t stage[32 * kStagePitch];
-    __shared__ __align__(16) uint8_t sb[512];
-    __shared__ __align__(16) uint8_t tile[2][kGaTileBytes];
-    __shared__ uint8_t cnt[2][32][4];  // escape bytes of lane L's two groups of block j
-    __shared__ uint32_t total[2];
-    if (P.ws_hdr[0] != 0) return;
-    const int entry = (int)(blockIdx.x / P.hkv), head = (int)(blockIdx.x % P.hkv);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int kv = warp >> 2, j = warp & 3;
-    const int dst = P.dst_page[entry], seq = P.dst_seq[entry];
-    ga_stage_page(P, entry, head, stage, sb);
-    // modes and escape area start at zero; the other tile bytes are all written below
-    for (int k = threadIdx.x; k < 2 * 12; k += blockDim.x)  // bytes [2816, 3008) = 12 uint4 per tile
-        reinterpret_cast<uint4 *>(tile[k / 12] + kGaTagOff)[k % 12] = make_uint4(0, 0, 0, 0);
-    __syncthreads();
-    GaGroups G;
-    ga_modes(stage, sb, kv, j, lane, G);
-    cnt[kv][lane][j] = (uint8_t)(G.esc[0] + G.esc[1]);
-    __syncthreads();
-    uint32_t tot = 0, before_j = 0;
+        const uint8_t *rows = P.ga_bases + (size_t)head * 512 + 16 * (lane & 1);
+        uint32_t fk = 0, fv01 = 0, fv23 = 0;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const uint32_t c = cnt[kv][lane][k];
-        tot += c;
-        if (k < j) before_j += c;
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t mk = ga_block_flags(v[2 * j], v[2 * j + 1], rows + 32 * j);
+            fk |= ((mk | (mk >> 16)) & 0xFFu) << (8 * j);  // a K group spans both halves
+            const uint32_t mv = ga_block_flags(v[8 + 2 * j], v[9 + 2 * j], rows + 256 + 32 * j);
+            if (j < 2) fv01 |= mv << (8 * j);
+            else fv23 |= mv << (8 * (j - 2));
+        }
+        fk |= __shfl_xor_sync(0xffffffffu, fk, 16);
+        fv01 |= __shfl_xor_sync(0xffffffffu, fv01, 2);
+        fv23 |= __shfl_xor_sync(0xffffffffu, fv23, 2);
+        fv01 |= __shfl_xor_sync(0xffffffffu, fv01, 16);
+        fv23 |= __shfl_xor_sync(0xffffffffu, fv23, 16);
+        // each group counted once: K by the lanes of tokens 0..7, V by those of tokens 0, 2, 4, 6
+        const uint32_t eK = __reduce_add_sync(0xffffffffu, lane < 16 ? ga_flag_escapes(fk) : 0u);
+        const uint32_t eV =
+            __reduce_add_sync(0xffffffffu, (lane & 18) == 0 ? ga_flag_escapes(fv01) + ga_flag_escapes(fv23) : 0u);
+        if (lane == 0) {
+            const uint32_t g = (eK <= kGaEscCap ? kGaTileBytes : kGaRawBytes) / kGaGranule +
+                               (eV <= kGaEscCap ? kGaTileBytes : kGaRawBytes) / kGaGranule;
+            P.ws_pair_size[it] = g;
+            atomicAdd(P.ws_page_size + entry, g);  // integer sum: the same whatever the order
+            P.ws_tags[it] = eK | ((uint64_t)eV << 32);
+        }
     }
-    uint32_t incl = tot;
+}
+
+// ---------------------------------------------------------------------------------
+// pack pass: warp per (entry, head) item.  The warp stages the slice in its own shared
+// buffer, gathers each block in storage order, and per group (lane, f) picks the mode,
+// writes the sign/mantissa bytes straight to the arena and keeps the 3-bit codes and the
+// escape bits in registers; after a warp scan of the escape bytes (lane-major group
+// order) the code, mode and escape areas are assembled in shared memory and copied out.
+// Raw tiles are written from the gathered words.
+// ---------------------------------------------------------------------------------
+constexpr int kGaPackWarps = 8;
+constexpr int kGaAuxBytes = (int)(kGaTileBytes - kGaCodeOff);  // 960: codes, modes, escapes
+constexpr int kGaPackWarpSmem = 32 * kStagePitch + kGaAuxBytes;
+constexpr int kGaPackSmem = kGaPackWarps * kGaPackWarpSmem;
+static_assert(kGaPackWarpSmem % 16 == 0 && kGaAuxBytes % 16 == 0, "16-byte staging");
+
+// prmt with the selector used as is: a selector nibble with bit 3 set gives the sign bit of
+// the chosen byte replicated over the result byte
+__device__ __forceinline__ uint32_t prmt_b32(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// In the pack pass the window tests run on the exponents in place: with Ex = w & 0x7F807F80
+// and the bases shifted the same way (b << 7 in each half), D = Ex + 0x80008000 - B holds
+// (256 + e - b) << 7 per half, so e - b is bits 7.. of each half and e is in [b, b + 8)
+// exactly when (D & 0xFC00) == 0x8000 (0xF800 for [b, b + 16)).
+constexpr uint32_t kGaExMask = 0x7F807F80u, kGaHalfOneS = 0x80008000u;
+constexpr uint32_t kGaWin8S = 0xFC00FC00u, kGaWin16S = 0xF800F800u;
+
+// nonzero: some half of the four words lies outside its window
+__device__ __forceinline__ uint32_t ga_miss4(const uint32_t (&d)[4], uint32_t win)
+{
+    const uint32_t any = (d[0] | d[1] | d[2] | d[3]) & (win ^ kGaHalfOneS);  // a bit that must be clear
+    const uint32_t all = d[0] & d[1] & d[2] & d[3];                            // the bit that must be set
+    return any | (~all & kGaHalfOneS);
+}
+
+template <bool kV>
+__device__ __forceinline__ void ga_pack_tile(const uint8_t *stage, uint8_t *aux, const uint8_t *row, int lane,
+                                             uint8_t *tile)
+{
+    // codes: group q = 8 lane + 2 j + f at bytes 3q..3q+2, so this lane's eight 24-bit
+    // fields fill six words; escape bits per group (the fifth byte of raw groups in ehi)
+    uint32_t modes = 0, cnt = 0, cw[6] = {0, 0, 0, 0, 0, 0}, elo[8], ehi[2] = {0, 0};
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-    }
-    if (lane == 31 && j == 0) total[kv] = incl;
-    const uint32_t tile_esc = __shfl_sync(0xffffffffu, incl, 31);
-    const bool compressed = tile_esc <= kGaEscCap;
-
-    // placement: the page's position, then the heads before this one, then K before V
-    uint64_t pair_base = P.ws_page_base[entry];
-    for (int h = 0; h < head; ++h) pair_base += P.ws_pair_size[(int64_t)entry * P.hkv + h];
-    __syncthreads();  // total[] visible
-    const uint32_t gK = (total[0] <= kGaEscCap ? kGaTileBytes : kGaRawBytes) / kGaGranule;
-    const uint32_t gV = (total[1] <= kGaEscCap ? kGaTileBytes : kGaRawBytes) / kGaGranule;
-    const uint64_t gmine = kv ? gV : gK;
-    const uint64_t off0 = pair_base + (kv ? gK : 0);
-    uint64_t end = P.cursors[2 * seq + 1];
-    end = min(end, P.arena_bytes / kGaGranule);
-    end = min(end, (uint64_t)kGaOffsetMask);
-    const bool fits = off0 + gmine <= end;
-
-    if (compressed) {
-        uint8_t *t = tile[kv];
-        uint32_t sfw[4], codes[2];
+    for (int j = 0; j < 4; ++j) {
+        uint32_t w[8];
+        gather_block(stage, kV ? 1 : 0, j, lane, w);
+        uint32_t sfw[4];
 #pragma unroll
         for (int f = 0; f < 2; ++f) {
-            uint32_t sf0 = 0, sf1 = 0, field = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t v = (G.w[f * 4 + i / 2] >> (16 * (i & 1))) & 0xFFFFu;
-                const uint32_t e = (v >> 7) & 0xFFu;
-                const uint32_t sf = ((v >> 8) & 0x80u) | (v & 0x7Fu);
-                const int dim = 32 * j + 16 * f + (kv == 0 ? frag_col(lane, i) : frag_row(lane, i));
-                const uint32_t b = G.mode[f] == 0 ? sb[kv * 256 + dim] : (G.mode[f] == 1 ? sb[kv * 256 + 128 + dim] : 0u);
-                const uint32_t c = e - b;
-                if (i < 4) sf0 |= sf << (8 * i);
-                else sf1 |= sf << (8 * (i - 4));
-                field |= (c & 7u) << (3 * i);
+            const int q = 2 * j + f;
+            // bases (shifted) of words 0..3: K [A, A, C, C] (channels c, c+1 | c+8, c+9);
+            // V [A, C, A, C] (channel r | r+8, both halves)
+            uint32_t A3, C3, A4, C4;
+            if (!kV) {
+                const uint8_t *p = row + 32 * j + 16 * f + 2 * (lane & 3);
+                A3 = ga_spread(__ldg(reinterpret_cast<const uint16_t *>(p)), 0) << 7;
+                C3 = ga_spread(__ldg(reinterpret_cast<const uint16_t *>(p + 8)), 0) << 7;
+                A4 = ga_spread(__ldg(reinterpret_cast<const uint16_t *>(p + 128)), 0) << 7;
+                C4 = ga_spread(__ldg(reinterpret_cast<const uint16_t *>(p + 136)), 0) << 7;
+            } else {
+                const uint8_t *p = row + 32 * j + 16 * f + (lane >> 2);
+                A3 = __ldg(p) * 0x00800080u;
+                C3 = __ldg(p + 8) * 0x00800080u;
+                A4 = __ldg(p + 128) * 0x00800080u;
+                C4 = __ldg(p + 136) * 0x00800080u;
             }
-            sfw[2 * f] = sf0;
-            sfw[2 * f + 1] = sf1;
-            codes[f] = field;
-        }
-        *reinterpret_cast<uint4 *>(t + 512 * j + 16 * lane) = make_uint4(sfw[0], sfw[1], sfw[2], sfw[3]);
+            uint32_t Ex[4], D3[4], D4[4];
 #pragma unroll
-        for (int f = 0; f < 2; ++f) {
-            const int q = 8 * lane + 2 * j + f;
-            t[kGaCodeOff + 3 * q] = (uint8_t)codes[f];
-            t[kGaCodeOff + 3 * q + 1] = (uint8_t)(codes[f] >> 8);
-            t[kGaCodeOff + 3 * q + 2] = (uint8_t)(codes[f] >> 16);
-        }
-        // modes: this warp's two groups are bits [4(j%2), 4(j%2)+4) of byte 2L + j/2
-        const uint32_t nib = G.mode[0] | (G.mode[1] << 2);
-        const int tb = 2 * lane + (j >> 1);
-        atomicOr(reinterpret_cast<uint32_t *>(t + kGaTagOff + (tb & ~3)), nib << (8 * (tb & 3) + 4 * (j & 1)));
-        // escape bytes
-        uint32_t off = (incl - tot) + before_j;
+            for (int k = 0; k < 4; ++k) {
+                const bool second = kV ? (k & 1) : (k >> 1);
+                Ex[k] = w[4 * f + k] & kGaExMask;
+                D3[k] = Ex[k] + kGaHalfOneS - (second ? C3 : A3);
+                D4[k] = Ex[k] + kGaHalfOneS - (second ? C4 : A4);
+            }
+            const uint32_t mode = ga_miss4(D3, kGaWin8S) == 0 ? 0u : (ga_miss4(D4, kGaWin16S) == 0 ? 1u : 2u);
+            modes |= mode << (2 * q);
+            cnt += mode == 0 ? 0u : (mode == 1 ? 1u : 5u);
+            // sign | 7 mantissa bits per value: the low bytes with bit 7 from the sign-replicated high bytes
+            const uint32_t *wf = w + 4 * f;
+            sfw[2 * f] = (prmt_b32(wf[0], wf[1], 0x6420) & 0x7F7F7F7Fu) | (prmt_b32(wf[0], wf[1], 0xFDB9) & 0x80808080u);
+            sfw[2 * f + 1] = (prmt_b32(wf[2], wf[3], 0x6420) & 0x7F7F7F7Fu) | (prmt_b32(wf[2], wf[3], 0xFDB9) & 0x80808080u);
+            // codes: the low three bits of e - base (bits 7..9 of each half of the mode's D;
+            // base 0 for raw groups), value i at bits 3i of the 24-bit field
+            const uint32_t As = mode == 0 ? A3 : (mode == 1 ? A4 : 0u), Cs = mode == 0 ? C3 : (mode == 1 ? C4 : 0u);
+            uint32_t t[4];
 #pragma unroll
-        for (int f = 0; f < 2; ++f) {
-            if (G.mode[f] == 0) continue;
-            uint32_t hb_lo = 0, hb_hi = 0;  // 40-bit field for raw groups, byte for 4-bit groups
+            for (int k = 0; k < 4; ++k) {
+                const bool second = kV ? (k & 1) : (k >> 1);
+                t[k] = (Ex[k] + kGaHalfOneS - (second ? Cs : As)) & 0x03800380u;
+            }
+            // pairs of words: values 2k, 2k+2 at bits 7, 13 and 2k+1, 2k+3 at 23, 29; then
+            // the high half folded down next to the low one -> four values at bits 7..18
+            const uint32_t p01 = t[0] + t[1] * 64u, p23 = t[2] + t[3] * 64u;
+            const uint32_t u01 = (p01 | (p01 >> 13)) & 0x7FF80u, u23 = (p23 | (p23 >> 13)) & 0x7FF80u;
+            const uint32_t field = (u01 >> 7) + (u23 << 5);
+            uint32_t lo = 0, hi = 0;
+            if (mode == 1) {  // bit 3 of e - b4 of each value (bits 10 and 26 of D4)
+                const uint32_t s01 = (D4[0] & 0x04000400u) + (D4[1] & 0x04000400u) * 4u;
+                const uint32_t s23 = (D4[2] & 0x04000400u) + (D4[3] & 0x04000400u) * 4u;
+                const uint32_t v01 = (s01 | (s01 >> 15)) & 0x3C00u, v23 = (s23 | (s23 >> 15)) & 0x3C00u;
+                lo = (v01 + (v23 << 4)) >> 10;
+            } else if (mode == 2) {  // e >> 3 of each value, 5 bits each (bits 10..14 and 26..30 of Ex)
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint32_t v = (G.w[f * 4 + i / 2] >> (16 * (i & 1))) & 0xFFFFu;
-                const uint32_t e = (v >> 7) & 0xFFu;
-                const int dim = 32 * j + 16 * f + (kv == 0 ? frag_col(lane, i) : frag_row(lane, i));
-                if (G.mode[f] == 1) {
-                    hb_lo |= (((e - sb[kv * 256 + 128 + dim]) >> 3) & 1u) << i;
-                } else {
-                    const uint64_t h5 = (uint64_t)((e >> 3) & 31u) << (5 * i);
-                    hb_lo |= (uint32_t)h5;
-                    hb_hi |= (uint32_t)(h5 >> 32);
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t u = ((Ex[k] >> 10) & 0x1Fu) | ((Ex[k] >> 21) & 0x3E0u);
+                    lo |= u << (10 * k);
+                    if (k == 3) hi = u >> 2;
                 }
             }
-            uint8_t *e = t + kGaEscOff;
-            if (G.mode[f] == 1) {
-                e[off] = (uint8_t)hb_lo;
+            const int bit = 24 * q, wi = bit >> 5, sh = bit & 31;
+            cw[wi] |= field << sh;
+            if (sh > 8) cw[wi + 1] |= field >> (32 - sh);
+            elo[q] = lo;
+            ehi[q >> 2] |= hi << (8 * (q & 3));
+        }
+        *reinterpret_cast<uint4 *>(tile + 512 * j + 16 * lane) = make_uint4(sfw[0], sfw[1], sfw[2], sfw[3]);
+    }
+    // escape bytes in lane-major group order
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+    __syncwarp();  // the previous tile's copy-out is done with aux
+    uint2 *c2 = reinterpret_cast<uint2 *>(aux + 24 * lane);
+    c2[0] = make_uint2(cw[0], cw[1]);
+    c2[1] = make_uint2(cw[2], cw[3]);
+    c2[2] = make_uint2(cw[4], cw[5]);
+    *reinterpret_cast<uint16_t *>(aux + (kGaTagOff - kGaCodeOff) + 2 * lane) = (uint16_t)modes;
+    uint8_t *esc = aux + (kGaEscOff - kGaCodeOff);
+    if (lane < (int)(kGaEscCap / 16)) reinterpret_cast<uint4 *>(esc)[lane] = make_uint4(0, 0, 0, 0);
+    __syncwarp();
+    if (total <= kGaEscCap) {  // the size pass found the same total; never past the area
+        uint32_t off = incl - cnt;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const uint32_t m = (modes >> (2 * q)) & 3u;
+            if (m == 1) {
+                esc[off] = (uint8_t)elo[q];
                 off += 1;
-            } else {
-                e[off] = (uint8_t)hb_lo;
-                e[off + 1] = (uint8_t)(hb_lo >> 8);
-                e[off + 2] = (uint8_t)(hb_lo >> 16);
-                e[off + 3] = (uint8_t)(hb_lo >> 24);
-                e[off + 4] = (uint8_t)hb_hi;
+            } else if (m == 2) {
+                esc[off] = (uint8_t)elo[q];
+                esc[off + 1] = (uint8_t)(elo[q] >> 8);
+                esc[off + 2] = (uint8_t)(elo[q] >> 16);
+                esc[off + 3] = (uint8_t)(elo[q] >> 24);
+                esc[off + 4] = (uint8_t)(ehi[q >> 2] >> (8 * (q & 3)));
                 off += 5;
             }
         }
-    } else if (fits) {
-        uint8_t *blk = P.arena + off0 * kGaGranule + 1024 * j;
-        *reinterpret_cast<uint4 *>(blk + 32 * lane) = make_uint4(G.w[0], G.w[1], G.w[2], G.w[3]);
-        *reinterpret_cast<uint4 *>(blk + 32 * lane + 16) = make_uint4(G.w[4], G.w[5], G.w[6], G.w[7]);
     }
-    __syncthreads();
-    // copy the compressed tiles out (188 uint4 each)
+    __syncwarp();
+    uint4 *dst = reinterpret_cast<uint4 *>(tile + kGaCodeOff);
+    const uint4 *src = reinterpret_cast<const uint4 *>(aux);
+    for (int k = lane; k < kGaAuxBytes / 16; k += 32) dst[k] = src[k];
+}
+
+__global__ void __launch_bounds__(kGaPackWarps * 32, 2) k_ga_pack_w(EncodeParams P)
+{
+    extern __shared__ __align__(16) uint8_t ga_pack_smem[];
+    if (P.ws_hdr[0] != 0) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t *stage = ga_pack_smem + warp * kGaPackWarpSmem;
+    uint8_t *aux = stage + 32 * kStagePitch;
+    const int64_t items = (int64_t)P.n * P.hkv;
+    const int64_t stride = (int64_t)gridDim.x * kGaPackWarps;
+    for (int64_t it = (int64_t)blockIdx.x * kGaPackWarps + warp; it < items; it += stride) {
+        const int entry = (int)(it / P.hkv), head = (int)(it % P.hkv);
+        const int src = P.src_page[entry], dst = P.dst_page[entry], seq = P.dst_seq[entry];
+        // the heads before this one in the page: one load per lane, then a warp sum
+        const uint32_t ps = lane < head ? P.ws_pair_size[(int64_t)entry * P.hkv + lane] : 0u;
+        const uint4 *s4 = reinterpret_cast<const uint4 *>(P.raw_pool + ((int64_t)src * P.hkv + head) * 2 * kPage * kDim);
+        uint4 v[8];  // the slice in two halves (K rows, then V rows)
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        const bool comp = total[t] <= kGaEscCap;
-        const uint64_t o = pair_base + (t ? gK : 0);
-        const bool fit = o + (t ? gV : gK) <= end;
-        if (comp && fit) {
-            uint4 *d = reinterpret_cast<uint4 *>(P.arena + o * kGaGranule);
-            const uint4 *s = reinterpret_cast<const uint4 *>(tile[t]);
-            for (int k = threadIdx.x; k < (int)(kGaTileBytes / 16); k += blockDim.x) d[k] = s[k];
+        for (int k = 0; k < 8; ++k) v[k] = s4[lane + 32 * k];
+        uint32_t before_heads = __reduce_add_sync(0xffffffffu, ps);
+        for (int h = 32; h < head; ++h) before_heads += P.ws_pair_size[(int64_t)entry * P.hkv + h];
+        __syncwarp();  // the previous item's gathers are done with the buffer
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            if (half) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) v[k] = s4[lane + 32 * (k + 8)];
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int q = lane + 32 * (k + 8 * half);  // 16-byte chunk q -> row q/16, byte (q%16)*16
+                *reinterpret_cast<uint4 *>(stage + (q >> 4) * kStagePitch + (q & 15) * 16) = v[k];
+            }
         }
-        if (threadIdx.x == 0) {
-            const uint32_t word = fit ? ((uint32_t)o | (comp ? 0u : kGaEntryRaw)) : kGaEntryInvalid;
-            P.meta32[((int64_t)dst * P.hkv + head) * 2 + t] = word;
-            if (!fit) atomicOr(P.status, KVZ_STATUS_ARENA_FULL);
+        __syncwarp();
+        const uint64_t esc = P.ws_tags[it];
+        const bool compK = (uint32_t)esc <= kGaEscCap, compV = (uint32_t)(esc >> 32) <= kGaEscCap;
+        const uint32_t gK = (compK ? kGaTileBytes : kGaRawBytes) / kGaGranule;
+        const uint32_t gV = (compV ? kGaTileBytes : kGaRawBytes) / kGaGranule;
+        const uint64_t pair_base = (uint64_t)P.ws_page_base[entry] + before_heads;
+        uint64_t end = min((uint64_t)P.cursors[2 * seq + 1], P.arena_bytes / kGaGranule);
+        end = min(end, (uint64_t)kGaOffsetMask);
+        const uint8_t *row = P.ga_bases + (size_t)head * 512;
+#pragma unroll 1
+        for (int kv = 0; kv < 2; ++kv) {
+            const uint64_t o = pair_base + (kv ? gK : 0);
+            const bool comp = kv ? compV : compK;
+            const bool fit = o + (kv ? gV : gK) <= end;
+            uint8_t *tile = P.arena + o * kGaGranule;
+            if (fit && comp) {
+                if (kv == 0) ga_pack_tile<false>(stage, aux, row, lane, tile);
+                else ga_pack_tile<true>(stage, aux, row + 256, lane, tile);
+            } else if (fit) {
+#pragma unroll 1
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t w[8];
+                    gather_block(stage, kv, j, lane, w);
+                    uint8_t *blk = tile + 1024 * j;
+                    *reinterpret_cast<uint4 *>(blk + 32 * lane) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4 *>(blk + 32 * lane + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+                }
+            }
+            if (lane == 0) {
+                P.meta32[((int64_t)dst * P.hkv + head) * 2 + kv] =
+                    fit ? ((uint32_t)o | (comp ? 0u : kGaEntryRaw)) : kGaEntryInvalid;
+                if (!fit) atomicOr(P.status, KVZ_STATUS_ARENA_FULL);
+            }
         }
     }
 }
@@ -370,15 +489,31 @@ cudaError_t launch_ga_calibrate(int hkv, const uint16_t *raw_pool, int64_t num_r
     return cudaGetLastError();
 }
 
+// one wave of `per_sm` CTAs of 8 warps per SM, fewer when there are fewer items than warps
+static unsigned ga_grid(int64_t items, int sms, int per_sm)
+{
+    const int64_t want = (items + 7) / 8, wave = (int64_t)(sms > 0 ? sms : 1) * per_sm;
+    return (unsigned)(want < wave ? (want > 0 ? want : 1) : wave);
+}
+
 cudaError_t launch_ga_encode(const EncodeParams &P, cudaStream_t stream)
 {
-    cudaError_t e = launch_enc_prepare(P, stream);  // validation and page-size reset
+    static unsigned long long done = 0;  // bit per device ordinal < 64: shared-memory opt-in
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess && !(dev < 64 && ((__atomic_load_n(&done, __ATOMIC_ACQUIRE) >> dev) & 1ull))) {
+        e = cudaFuncSetAttribute(k_ga_pack_w, cudaFuncAttributeMaxDynamicSharedMemorySize, kGaPackSmem);
+        if (e == cudaSuccess && dev < 64) __atomic_fetch_or(&done, 1ull << dev, __ATOMIC_ACQ_REL);
+    }
     if (e != cudaSuccess) return e;
-    const unsigned items = (unsigned)((size_t)P.n * P.hkv);
-    k_ga_sizes<<<items, 256, 0, stream>>>(P);
+    e = launch_enc_prepare(P, stream);  // validation and page-size reset
+    if (e != cudaSuccess) return e;
+    const int64_t items = (int64_t)P.n * P.hkv;
+    k_ga_sizes_w<<<ga_grid(items, sms, 3), 256, 0, stream>>>(P);
     e = launch_enc_scan(P, stream);
     if (e != cudaSuccess) return e;
-    k_ga_pack<<<items, 256, 0, stream>>>(P);
+    k_ga_pack_w<<<ga_grid(items, sms, 2), kGaPackWarps * 32, kGaPackSmem, stream>>>(P);
     return cudaGetLastError();
 }
 

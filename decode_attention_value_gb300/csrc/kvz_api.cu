@@ -453,6 +453,7 @@ int kvz_ga_encode_pages(kvz_dims dims, const void *raw_pool, int64_t num_raw_pag
     P.ws_page_size = reinterpret_cast<uint32_t *>(w + 16);
     P.ws_page_base = reinterpret_cast<uint32_t *>(w + 16 + a);
     P.ws_pair_size = reinterpret_cast<uint32_t *>(w + 16 + 2 * a);
+    P.ws_tags = reinterpret_cast<uint64_t *>(w + encode_ws_tags_offset(n, dims.num_kv_heads));
     cudaError_t e = launch_ga_encode(P, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KVZ_OK : fail_cuda(e);
 }

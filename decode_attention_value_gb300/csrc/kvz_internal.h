@@ -30,8 +30,9 @@ struct EncodeParams {
     uint32_t *ws_page_size;  // [n] granules per page, summed over heads (zeroed each call)
     uint32_t *ws_page_base;  // [n] granule position of each page's first group
     uint32_t *ws_pair_size;  // [n*hkv] granules per (page, head) K+V pair
-    uint64_t *ws_tags;       // [n*hkv] 12-bit encoder: the size pass's block tags per (page, head),
-                             // K group's four tag bytes | V group's << 32 (null: not kept)
+    uint64_t *ws_tags;       // [n*hkv] the size pass's findings per (page, head) for the pack pass:
+                             // 12-bit: the K group's four tag bytes | the V group's << 32 (null:
+                             // not kept); group-adaptive: K tile escape bytes | V tile's << 32
 };
 
 inline size_t encode_ws_bytes(int n, int hkv)
