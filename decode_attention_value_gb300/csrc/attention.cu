@@ -401,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
         // segment's readers have passed its closing barrier)
         uint32_t *btbl = reinterpret_cast<uint32_t *>(smem + Smem::bases(B));
         if constexpr (kTiles) {
-            ga_fill_bases_table(P.ga_bases + (size_t)L.kvh * 512, btbl, tid);
+            ga_fill_bases_table(P.ga_bases + (size_t)L.kvh * 512, btbl, tid, kFmt == kFmtF8E4);
             asm volatile("bar.sync 1, %0;" ::"r"(kConsumers * 32) : "memory");
         }
 

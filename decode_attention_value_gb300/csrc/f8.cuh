@@ -12,7 +12,8 @@
 //   +64               2-bit modes, group q at byte q/4, bits 2(q%4)
 //   +64               escapes in q order: mode 1 one byte (bit 3 of code i at bit i),
 //                     mode 2 (E5M2) two bytes (bits 3..4 of code i at bits 2i..2i+1)
-// Mode 0: e = code + b3[ch]; mode 1: e = code + b4[ch] (E4M3: b4 = 0); mode 2: e = code.
+// Mode 0: e = code + b3[ch]; mode 1: e = code + b4[ch] (E4M3: b4 = 0, whatever the bases
+// table holds); mode 2: e = code.
 // E5M2 tile 1664 B, E4M3 1920 B; a tile needing more than 64 escape bytes stays raw:
 // 2048 FP8 bytes, element (L, f, i) of block j at 512j + 16L + 8f + i.
 #pragma once
@@ -86,6 +87,15 @@ __device__ __forceinline__ uint32_t f8_assemble(uint32_t sm, uint32_t e)
     return ((sm & smask) << (7 - M)) | (e << M) | (sm & mmask);
 }
 
+template <typename Row>
+struct RowIsBytes {
+    static constexpr bool value = false;
+};
+template <>
+struct RowIsBytes<uint8_t> {
+    static constexpr bool value = true;
+};
+
 // One group of a compressed tile -> its 8 FP8 bytes (f0: elements 0..3, f1: 4..7).
 // Modes 0 and 1 take no branch; raw-exponent groups (E5M2 mode 2) are handled in a
 // branch that only tiles holding them enter (any2, warp-uniform).
@@ -101,6 +111,9 @@ __device__ __forceinline__ void f8_restore_group(uint32_t smfield, uint32_t code
     off += m1;
     uint32_t b0, b1;
     ga_bases<kV>(row, m1, lane, j, f, b0, b1);
+    // E4M3: b4 = 0 (the 16-wide window is the whole field); a base table (uint32 words)
+    // already holds 0 there, a byte row of the bases table is not read for it
+    if (!kE5 && RowIsBytes<Row>::value && m1) b0 = b1 = 0;
     const uint32_t l0 = ga_spread3(code & 0xFFFu), l1 = ga_spread3((code >> 12) & 0xFFFu);
     uint32_t c0 = l0 | ga_spread1_hi(h), c1 = l1 | ga_spread1_hi(h >> 4);
     if (kE5 && any2) {

@@ -102,21 +102,22 @@ __device__ __forceinline__ void ga_bases(const uint32_t *tbl, uint32_t w, int la
 }
 
 // Build the table above for one KV head (row: its 512 bytes of bases, K b3 | K b4 | V b3 |
-// V b4), 128 threads (tid 0..127): the same words ga_bases computes from the row.
-__device__ __forceinline__ void ga_fill_bases_table(const uint8_t *row, uint32_t *tbl, int tid)
+// V b4), 128 threads (tid 0..127): the same words ga_bases computes from the row.  zero_b4:
+// the b4 words are 0 (FP8 E4M3, whose 16-wide window is the whole exponent field).
+__device__ __forceinline__ void ga_fill_bases_table(const uint8_t *row, uint32_t *tbl, int tid, bool zero_b4)
 {
     if (tid < 64) {  // K pair: (2j + f, w, t)
         const int t = tid & 3, w = (tid >> 2) & 1, jf = tid >> 3;
         uint32_t b0, b1;
         ga_bases<false>(row, (uint32_t)w, t, jf >> 1, jf & 1, b0, b1);
-        tbl[2 * tid] = b0;
-        tbl[2 * tid + 1] = b1;
+        tbl[2 * tid] = zero_b4 && w ? 0u : b0;
+        tbl[2 * tid + 1] = zero_b4 && w ? 0u : b1;
     }
     {  // V word: (2j + f, w, g)
         const int g = tid & 7, w = (tid >> 3) & 1, jf = tid >> 4;
         uint32_t b0, b1;
         ga_bases<true>(row + 256, (uint32_t)w, g << 2, jf >> 1, jf & 1, b0, b1);
-        tbl[128 + tid] = b0;
+        tbl[128 + tid] = zero_b4 && w ? 0u : b0;
     }
 }
 

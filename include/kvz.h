@@ -297,7 +297,8 @@ int kvz_ga_decode_attention(kvz_dims dims, int32_t batch, int32_t num_q_heads, c
  *                [+832, +896)    escapes: mode 1 one byte (bit 3 of code i at bit i);
  *                                mode 2 (E5M2 only) two bytes (bits 3..4 of code i at 2i)
  *              modes on the exponent field e: 0 if all e - b3 in [0,8), 1 if all e - b4 in
- *              [0,16), else 2 (code = e); E4M3 has b4 = 0.  E5M2 tile 1664 B (26 granules
+ *              [0,16), else 2 (code = e); E4M3 takes b4 = 0 (the table's E4M3 b4 entries
+ *              are not read), so its groups use modes 0 and 1 only.  E5M2 tile 1664 B (26 granules
  *              of 64), E4M3 1920 B (30); more than 64 escape bytes: raw tile of 2048 FP8
  *              bytes, element (L, f, i) of block j at 512j + 16L + 8f + i.
  *  entries, bases, arena, cursors: as the group-adaptive tiles.  The tail page stays BF16.

@@ -17,8 +17,10 @@
  *   - tile: one (page, KV head, K|V) slice of 2048 FP8 values in the storage order of the
  *     12-bit format; group q = 8L + 2j + f = elements (L, f, i = 0..7) of block j;
  *   - group modes (as the BF16 codec, on the exponent field e): 0 if every e - b3 is in
- *     [0,8), else 1 if every e - b4 is in [0,16), else 2 (code = e).  For E4M3 b4 = 0, so
- *     mode 1 holds the whole 4-bit field and mode 2 never occurs;
+ *     [0,8), else 1 if every e - b4 is in [0,16), else 2 (code = e).  For E4M3 the
+ *     16-wide window is the whole 4-bit field: b4 = 0 whatever the table holds (its E4M3
+ *     b4 entries are not read), so mode 1 takes every group that mode 0 does not and
+ *     mode 2 never occurs;
  *   - layout (S = 1 + M sign/mantissa bits: 3 for E5M2, 4 for E4M3):
  *       [0, 256 S)           sign/mantissa fields: group q at S*q bytes, element i at bits
  *                            S*i .. S*i+S-1 (value s << M | m), little-endian
@@ -181,7 +183,7 @@ int of8_encode_tile(int fmt, const uint8_t *page, int is_v, const uint8_t *b3c, 
                     e[i] = f8_exp(&F, b);
                     sm[i] = ((unsigned)(b >> 7) << F.mbits) | (b & ((1u << F.mbits) - 1));
                     b3[i] = b3c[dim];
-                    b4[i] = b4c[dim];
+                    b4[i] = fmt == OF8_E4M3 ? 0u : b4c[dim];
                 }
                 const int mode = oga_group_mode(e, b3, b4);
                 for (int i = 0; i < 8; i++) {
@@ -245,7 +247,8 @@ void of8_decode_tile(int fmt, const uint8_t *in, int raw, int is_v, const uint8_
                         unsigned c = get_bits(in + code_off, 24 * q + 3 * i, 3);
                         if (mode == 1) c |= ((hb >> i) & 1u) << 3;
                         if (mode == 2) c |= ((hb >> (2 * i)) & 3u) << 3;
-                        const unsigned e = c + (mode == 0 ? b3c[dim] : mode == 1 ? b4c[dim] : 0u);
+                        const unsigned b4 = fmt == OF8_E4M3 ? 0u : b4c[dim];
+                        const unsigned e = c + (mode == 0 ? b3c[dim] : mode == 1 ? b4 : 0u);
                         const unsigned sm = get_bits(in, (F.sm_bits * 8) * q + F.sm_bits * i, F.sm_bits);
                         b = (uint8_t)(((sm >> F.mbits) << 7) | ((e & ((1u << F.ebits) - 1)) << F.mbits) |
                                       (sm & ((1u << F.mbits) - 1)));

@@ -159,3 +159,45 @@ def test_query_beyond_f16_range_is_flagged(kvz_lib, oracle, fmt):
     f8.run(status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == kvz.STATUS_Q_RANGE
+
+
+def test_e4m3_ignores_b4_entries(kvz_lib, oracle):
+    """E4M3 takes b4 = 0 whatever the bases table holds: with junk b4 entries the encoder
+    writes the same tiles (and the oracle agrees), and decode and attention read them the
+    same way."""
+    kvz = kvz_lib
+    cfg = kvgen.KVConfig("e4-junk-b4", 1, 3, 8, 2, 9, tail_min=1, tail_max=15, k_log2_sigma=(-4, 3),
+                         v_log2_sigma=(-3, 1), k_outlier_channels=4, k_outlier_scale=32.0, seed=63)
+    base = Layer(cfg, None)
+    f8 = F8Layer(base, 1, oracle)
+    assert np.array_equal(f8.arena.cpu().numpy(), f8.o_arena)
+    junk = f8.bases.clone()
+    g = torch.Generator().manual_seed(5)
+    junk[:, :, 1, :] = torch.randint(1, 256, junk[:, :, 1, :].shape, generator=g, dtype=torch.uint8).cuda()
+    meta = torch.zeros_like(f8.meta)
+    arena = torch.zeros_like(f8.arena)
+    cur = torch.from_numpy(f8.cursors0.view(np.int32).copy()).cuda()
+    st = kvz.new_status()
+    s = base.src.cuda()
+    kvz.f8_encode_pages(1, base.g_pool, junk, s, s, base.dseq.cuda(), meta, arena, cur, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(meta, f8.meta) and torch.equal(arena, f8.arena)
+    o_meta = np.zeros_like(f8.o_meta)
+    o_arena = np.zeros_like(f8.o_arena)
+    o_cur = f8.cursors0.copy()
+    src = base.src.numpy()
+    assert oracle.f8_encode_pages(1, f8.o_pool, junk.cpu().numpy(), src, src, base.dseq.numpy(), o_meta, o_arena,
+                                  o_cur, cfg.hkv) == 0
+    assert np.array_equal(o_arena, f8.o_arena) and np.array_equal(o_meta, f8.o_meta)
+    out = torch.empty((s.numel(), cfg.hkv, 2, 16, 128), dtype=torch.uint8, device="cuda")
+    kvz.f8_decode_blocks(1, meta, arena, junk, s, out, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert np.array_equal(out.cpu().numpy(), oracle.f8_quantize(1, kvgen.bits(base.pool)[src]))
+    want = f8.run()
+    got = torch.empty_like(want)
+    kvz.f8_decode_attention(1, base.g_q, base.full.cuda(), base.seq_lens.cuda(), base.tail.cuda(), meta, arena,
+                            junk, base.g_pool, got, st, workspace=base.workspace(False))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and torch.equal(got, want)

@@ -170,6 +170,22 @@ def test_e4m3_never_uses_mode_2(oracle):
         assert (modes < 2).all() and (modes == 1).any()
 
 
+def test_e4m3_ignores_the_b4_table(oracle):
+    """E4M3's 16-wide window is the whole exponent field: a table with arbitrary b4 entries
+    gives the same tile as b4 = 0 (modes 0/1 only), and decodes losslessly with either."""
+    rng = np.random.default_rng(29)
+    b3 = rng.integers(0, 8, 128).astype(np.uint8)  # the filler exponent 7 is in every 8-window
+    for trial in range(4):
+        page = np.full((16, 128), 0x38, np.uint8)
+        page[trial] = rng.integers(0, 256, 128, dtype=np.uint8)
+        junk = rng.integers(0, 256, 128).astype(np.uint8)
+        for is_v in (False, True):
+            a = oracle.f8_encode_tile(E4M3, page, is_v, b3, np.zeros(128, np.uint8))
+            b = oracle.f8_encode_tile(E4M3, page, is_v, b3, junk)
+            assert a == b and len(a) == 1920
+            assert np.array_equal(oracle.f8_decode_tile(E4M3, b, is_v, b3, junk), page)
+
+
 @pytest.mark.parametrize("fmt", [E4M3, E5M2])
 def test_attention_over_fp8_tiles_equals_plain_oracle(oracle, fmt):
     hkv, hq, B = 2, 8, 3
