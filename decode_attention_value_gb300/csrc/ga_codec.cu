@@ -70,8 +70,6 @@ __global__ void __launch_bounds__(256) k_ga_calibrate(int hkv, const uint16_t *p
 constexpr uint32_t kGaHalfOne = 0x01000100u, kGaWin8 = 0x01F801F8u, kGaWin16 = 0x01F001F0u;
 
 __device__ __forceinline__ uint32_t ga_exp2(uint32_t w) { return (w >> 7) & 0x00FF00FFu; }
-// bytes 2s and 2s+1 of x (two bases) -> 16-bit halves
-__device__ __forceinline__ uint32_t ga_spread(uint32_t x, int s) { return __byte_perm(x, 0, s ? 0x4342 : 0x4140); }
 // nonzero half: that value is outside the window
 __device__ __forceinline__ uint32_t ga_viol(uint32_t d, uint32_t win) { return (d & win) ^ kGaHalfOne; }
 
@@ -96,8 +94,8 @@ __device__ __forceinline__ uint32_t ga_block_flags(const uint4 &lo, const uint4 
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const uint32_t x = ga_exp2(w[k]) + kGaHalfOne;
-        p3[k & 3] |= ga_viol(x - ga_spread(s3[k >> 1], k & 1), kGaWin8);
-        p4[k & 3] |= ga_viol(x - ga_spread(s4[k >> 1], k & 1), kGaWin16);
+        p3[k & 3] |= ga_viol(x - enc_spread2(s3[k >> 1], k & 1), kGaWin8);
+        p4[k & 3] |= ga_viol(x - enc_spread2(s4[k >> 1], k & 1), kGaWin16);
     }
     // per half: bit 2g (8-wide window missed) and 2g+1 (16-wide missed) for words g, g+4;
     // halves are <= 0x1F8, so adding 0x7FFF sets bit 15 exactly when one is nonzero
@@ -178,15 +176,6 @@ constexpr int kGaPackWarpSmem = 32 * kStagePitch + kGaAuxBytes;
 constexpr int kGaPackSmem = kGaPackWarps * kGaPackWarpSmem;
 static_assert(kGaPackWarpSmem % 16 == 0 && kGaAuxBytes % 16 == 0, "16-byte staging");
 
-// prmt with the selector used as is: a selector nibble with bit 3 set gives the sign bit of
-// the chosen byte replicated over the result byte
-__device__ __forceinline__ uint32_t prmt_b32(uint32_t a, uint32_t b, uint32_t sel)
-{
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
-}
-
 // In the pack pass the window tests run on the exponents in place: with Ex = w & 0x7F807F80
 // and the bases shifted the same way (b << 7 in each half), D = Ex + 0x80008000 - B holds
 // (256 + e - b) << 7 per half, so e - b is bits 7.. of each half and e is in [b, b + 8)
@@ -222,10 +211,10 @@ __device__ __forceinline__ void ga_pack_tile(const uint8_t *stage, uint8_t *aux,
             uint32_t A3, C3, A4, C4;
             if (!kV) {
                 const uint8_t *p = row + 32 * j + 16 * f + 2 * (lane & 3);
-                A3 = ga_spread(__ldg(reinterpret_cast<const uint16_t *>(p)), 0) << 7;
-                C3 = ga_spread(__ldg(reinterpret_cast<const uint16_t *>(p + 8)), 0) << 7;
-                A4 = ga_spread(__ldg(reinterpret_cast<const uint16_t *>(p + 128)), 0) << 7;
-                C4 = ga_spread(__ldg(reinterpret_cast<const uint16_t *>(p + 136)), 0) << 7;
+                A3 = enc_spread2(__ldg(reinterpret_cast<const uint16_t *>(p)), 0) << 7;
+                C3 = enc_spread2(__ldg(reinterpret_cast<const uint16_t *>(p + 8)), 0) << 7;
+                A4 = enc_spread2(__ldg(reinterpret_cast<const uint16_t *>(p + 128)), 0) << 7;
+                C4 = enc_spread2(__ldg(reinterpret_cast<const uint16_t *>(p + 136)), 0) << 7;
             } else {
                 const uint8_t *p = row + 32 * j + 16 * f + (lane >> 2);
                 A3 = __ldg(p) * 0x00800080u;
@@ -489,13 +478,6 @@ cudaError_t launch_ga_calibrate(int hkv, const uint16_t *raw_pool, int64_t num_r
     return cudaGetLastError();
 }
 
-// one wave of `per_sm` CTAs of 8 warps per SM, fewer when there are fewer items than warps
-static unsigned ga_grid(int64_t items, int sms, int per_sm)
-{
-    const int64_t want = (items + 7) / 8, wave = (int64_t)(sms > 0 ? sms : 1) * per_sm;
-    return (unsigned)(want < wave ? (want > 0 ? want : 1) : wave);
-}
-
 cudaError_t launch_ga_encode(const EncodeParams &P, cudaStream_t stream)
 {
     static unsigned long long done = 0;  // bit per device ordinal < 64: shared-memory opt-in
@@ -510,10 +492,10 @@ cudaError_t launch_ga_encode(const EncodeParams &P, cudaStream_t stream)
     e = launch_enc_prepare(P, stream);  // validation and page-size reset
     if (e != cudaSuccess) return e;
     const int64_t items = (int64_t)P.n * P.hkv;
-    k_ga_sizes_w<<<ga_grid(items, sms, 3), 256, 0, stream>>>(P);
+    k_ga_sizes_w<<<enc_warp_grid(items, sms, 3), 256, 0, stream>>>(P);
     e = launch_enc_scan(P, stream);
     if (e != cudaSuccess) return e;
-    k_ga_pack_w<<<ga_grid(items, sms, 2), kGaPackWarps * 32, kGaPackSmem, stream>>>(P);
+    k_ga_pack_w<<<enc_warp_grid(items, sms, 2), kGaPackWarps * 32, kGaPackSmem, stream>>>(P);
     return cudaGetLastError();
 }
 

@@ -572,6 +572,7 @@ int kvz_f8_encode_pages(kvz_dims dims, int32_t format, const void *raw_pool, int
     P.ws_page_size = reinterpret_cast<uint32_t *>(w + 16);
     P.ws_page_base = reinterpret_cast<uint32_t *>(w + 16 + a);
     P.ws_pair_size = reinterpret_cast<uint32_t *>(w + 16 + 2 * a);
+    P.ws_tags = reinterpret_cast<uint64_t *>(w + encode_ws_tags_offset(n, dims.num_kv_heads));
     cudaError_t e = launch_f8_encode(format, P, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KVZ_OK : fail_cuda(e);
 }

@@ -32,8 +32,17 @@ struct EncodeParams {
     uint32_t *ws_pair_size;  // [n*hkv] granules per (page, head) K+V pair
     uint64_t *ws_tags;       // [n*hkv] the size pass's findings per (page, head) for the pack pass:
                              // 12-bit: the K group's four tag bytes | the V group's << 32 (null:
-                             // not kept); group-adaptive: K tile escape bytes | V tile's << 32
+                             // not kept); group-adaptive and FP8 tiles: K tile escape bytes |
+                             // V tile's << 32
 };
+
+// grid of a warp-per-item encoder pass with 8-warp CTAs: one wave of `per_sm` CTAs per
+// SM, fewer when there are fewer items than warps
+inline unsigned enc_warp_grid(int64_t items, int sms, int per_sm)
+{
+    const int64_t want = (items + 7) / 8, wave = (int64_t)(sms > 0 ? sms : 1) * per_sm;
+    return (unsigned)(want < wave ? (want > 0 ? want : 1) : wave);
+}
 
 inline size_t encode_ws_bytes(int n, int hkv)
 {

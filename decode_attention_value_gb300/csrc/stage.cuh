@@ -39,6 +39,18 @@ __device__ __forceinline__ void gather_block(const uint8_t *stage, int kv, int j
         }
 }
 
+// bytes 2s and 2s+1 of x -> the low bytes of two 16-bit halves
+__device__ __forceinline__ uint32_t enc_spread2(uint32_t x, int s) { return __byte_perm(x, 0, s ? 0x4342 : 0x4140); }
+
+// prmt with the selector used as is: a selector nibble with bit 3 set gives the sign bit of
+// the chosen byte replicated over the result byte
+__device__ __forceinline__ uint32_t prmt_b32(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
 __device__ __forceinline__ void load_slice_to_stage(const uint16_t *src, uint8_t *stage, int tid, int nthreads)
 {
     // 8 KB slice: 512 chunks of 16 B; chunk q -> row q/16, byte (q%16)*16
