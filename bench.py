@@ -1092,11 +1092,13 @@ def run_stack(args, cfg, dist, rank, world, local):
     dev = torch.device("cuda", local)
     layers = [Workload(cfg, 1, layer=layer, dev=dev) for layer in range(cfg.layers)]
     # one block table for every layer, as a paged KV cache keeps it (each layer has its own
-    # pools and metadata behind the same page ids)
+    # pools and metadata behind the same page ids), and one attention workspace, the scratch
+    # buffer a serving loop hands to each layer's call in turn
     for W in layers[1:]:
         assert torch.equal(W.table, layers[0].table) and torch.equal(W.seq_lens, layers[0].seq_lens)
         W.table, W.full, W.tail, W.raw_table = layers[0].table, layers[0].full, layers[0].tail, layers[0].raw_table
         W.seq_lens = layers[0].seq_lens
+        W.ws_c, W.ws_r = layers[0].ws_c, layers[0].ws_r
     K = args.steps
 
     def step_c(k):
