@@ -18,7 +18,7 @@
  *   [EX]   "ExANS: lossless GPU compression for BF16 KV cache", section "Under the
  *          hood" (the BF16 field boundary and value formula).
  *
- * Readings of points the pages leave open (each one is listed in the design doc):
+ * Readings of points the pages leave open:
  *   - a 16-token page of one layer, one KV head and one of K/V is a 16 x 128 BF16
  *     matrix [token][dim]; block j (0..3) is dims [32j, 32j+32) x all 16 tokens;
  *   - inside a block the 512 values are stored in "storage order" n = (L*2+f)*8+i
