@@ -92,7 +92,7 @@ def test_host_rejects_bad_arguments(kvz):
     # decode: misaligned output
     assert lib.kvz_decode_blocks(_dims(kvz), fake, 1, fake, 1 << 20, fake, 1, fake + 2, fake, None) == E["align"]
     assert lib.kvz_decode_blocks(_dims(kvz), None, 0, None, 0, None, 0, None, None, None) == 0
-    # attention: GQA group must divide and be 1, 2, 4 or 8
+    # attention: the query heads must be a whole multiple (1 to 8) of the KV heads
     assert lib.kvz_decode_attention(_dims(kvz), 2, 12, fake, fake, 4, fake, fake, fake, 1, fake, 1 << 20, fake, 1,
                                     fake, fake, 1 << 20, fake, None) == E["inval"]
     assert lib.kvz_decode_attention(_dims(kvz), 2, 128, fake, fake, 4, fake, fake, fake, 1, fake, 1 << 20, fake, 1,
