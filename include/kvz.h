@@ -125,8 +125,8 @@ int kvz_encode_pages(kvz_dims dims, const void *raw_pool, int64_t num_raw_pages,
  * 256-byte granules page src_page[i] will take in the arena (all KV heads, K and V: each
  * group 12..16), exactly what kvz_encode_pages will place for it.  Lets the caller
  * reserve exact space (kvz_alloc_reserve_granules) instead of the worst case.  Same
- * validation as kvz_encode_pages for src_page (KVZ_STATUS_BAD_INDEX: nothing written);
- * workspace: kvz_encode_workspace_size(dims, n). */
+ * validation as kvz_encode_pages for src_page (KVZ_STATUS_BAD_INDEX: no page is read
+ * and every granules[i] is 0); workspace: kvz_encode_workspace_size(dims, n). */
 int kvz_encode_sizes(kvz_dims dims, const void *raw_pool, int64_t num_raw_pages, const int32_t *src_page,
                      int32_t n, uint32_t *granules, void *workspace, size_t workspace_bytes, uint32_t *status,
                      kvz_stream_t stream);

@@ -159,3 +159,46 @@ def test_decode_bit_exact_and_bad_metadata(kvz, oracle, cfg):
     torch.cuda.synchronize()
     assert int(st.item()) == o_st == (oracle.BAD_META | oracle.BAD_INDEX)
     assert np.array_equal(out.cpu().view(torch.int16).numpy().view(np.uint16), o_out)
+
+
+@pytest.mark.parametrize("cfg", [kvgen.C0, spread_cfg(8, 20, 11, hkv=8),
+                                 kvgen.KVConfig("llama-like-sizes", 1, 1, 32, 8, 40, k_log2_sigma=(-4, 3),
+                                                v_log2_sigma=(-3, 1), k_outlier_channels=4,
+                                                k_outlier_scale=32.0, seed=12)],
+                         ids=lambda c: c.name)
+def test_encode_sizes_match_the_oracle_placement(kvz, oracle, cfg):
+    """kvz_encode_sizes (the size pass alone, for exact reservations): per page the
+    granules of all its groups, each 3 or 4 per block by the oracle's own tags, and the
+    distance the oracle's cursor moves over that page; a call with an out-of-range page id
+    reads no page, reports 0 for every page and is flagged."""
+    n = cfg.num_pages
+    pool = kvgen.gen_pages(cfg, n)
+    src = np.random.default_rng(cfg.seed + 1).permutation(n).astype(np.int32)
+    g_sizes = torch.full((n,), -1, dtype=torch.int32, device="cuda")
+    st = kvz.new_status()
+    kvz.encode_sizes(pool.cuda(), torch.from_numpy(src).cuda(), g_sizes, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    got = g_sizes.cpu().numpy().astype(np.int64)
+    # oracle: encode the same pages one cursor per page, read sizes off the tags and cursors
+    o_meta = np.zeros((n, cfg.hkv, 2), np.uint64)
+    o_arena = np.zeros(n * cfg.hkv * 8192, np.uint8)
+    per = cfg.hkv * 2 * 16
+    cur = np.array([[i * per, (i + 1) * per] for i in range(n)], np.uint32)
+    start = cur[:, 0].copy()
+    assert oracle.encode_pages(kvgen.bits(pool), src, np.arange(n, dtype=np.int32), np.arange(n, dtype=np.int32),
+                               o_meta, o_arena, cur, cfg.hkv) == 0
+    tags = (o_meta >> np.uint64(32)).astype(np.uint64)
+    raw = sum(((tags >> np.uint64(8 * j)) & np.uint64(0xFF)) == 0xFF for j in range(4)).sum(axis=(1, 2))
+    from_tags = 3 * 4 * 2 * cfg.hkv + raw.astype(np.int64)
+    assert np.array_equal(from_tags, cur[:, 0].astype(np.int64) - start)
+    assert np.array_equal(got, from_tags)
+    # an out-of-range page id: no sizes, BAD_INDEX
+    bad = src.copy()
+    bad[n // 2] = n + 5
+    g_sizes.fill_(-1)
+    st = kvz.new_status()
+    kvz.encode_sizes(pool.cuda(), torch.from_numpy(bad).cuda(), g_sizes, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == kvz.STATUS_BAD_INDEX
+    assert (g_sizes.cpu() == 0).all()
