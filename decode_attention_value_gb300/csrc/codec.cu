@@ -304,79 +304,103 @@ __global__ void __launch_bounds__(kPackWarps * 32, 2) k_enc_pack_w(EncodeParams 
 }
 
 // ---------------------------------------------------------------------------------
-// standalone decode: warp per (entry, head) item in a grid-stride loop.  The warp loads
-// the item's two group words, issues the loads of a group's four blocks together,
-// restores each lane's fragments with the same register restore the attention kernel
-// uses, scatters them into its own staged page slice, and writes the 8 KB slice back in
-// the plain page layout with 16-byte stores.  Many items per SM stay in flight (a CTA
-// per item with a warp per block kept too few in flight to cover the three dependent
-// loads of page id, group words and blocks).
+// standalone decode: warp per (entry, head) item in a grid-stride loop.  The warp issues
+// the loads of all eight blocks of the item (K and V groups) together, restores each
+// lane's fragments with the same register restore the attention kernel uses, scatters
+// them into its own staged page slice, and writes the 8 KB slice back in the plain page
+// layout with 16-byte stores.  The next item's page id and group words are loaded while
+// this one is restored, so only the block loads wait on memory.  Many items per SM stay in
+// flight (a CTA per item with a warp per block kept too few in flight to cover the three
+// dependent loads of page id, group words and blocks).
 // ---------------------------------------------------------------------------------
 constexpr int kDecWarps = 8;
+constexpr int kDecCtasPerSm = 2;  // registers for both groups' loads in flight at once
 
-__global__ void __launch_bounds__(kDecWarps * 32, 3) k_decode_w(DecodeParams P)
+// Group words of (page, head); bad |= KVZ_STATUS_BAD_INDEX (words 0) for a page out of range.
+__device__ __forceinline__ void dec_words(const DecodeParams &P, int page, int head, uint64_t (&w)[2], uint32_t &bad)
+{
+    w[0] = w[1] = 0;
+    bad = 0;
+    if (page < 0 || page >= P.num_meta_pages) {
+        bad = KVZ_STATUS_BAD_INDEX;
+    } else {
+        const uint64_t *m = P.meta + ((int64_t)page * P.hkv + head) * 2;
+        w[0] = m[0];
+        w[1] = m[1];
+    }
+}
+
+__global__ void __launch_bounds__(kDecWarps * 32, kDecCtasPerSm) k_decode_w(DecodeParams P)
 {
     extern __shared__ __align__(16) uint8_t dec_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint8_t *stage = dec_smem + warp * (32 * kStagePitch);
     const int64_t items = (int64_t)P.n * P.hkv;
     const int64_t stride = (int64_t)gridDim.x * kDecWarps;
-    for (int64_t it = (int64_t)blockIdx.x * kDecWarps + warp; it < items; it += stride) {
+    int64_t it = (int64_t)blockIdx.x * kDecWarps + warp;
+    // this item's group words, and the next item's page id, loaded an iteration ahead
+    uint64_t words[2] = {0, 0};
+    uint32_t bad_idx = 0;
+    int page_next = 0;
+    if (it < items) dec_words(P, P.page[it / P.hkv], (int)(it % P.hkv), words, bad_idx);
+    if (it + stride < items) page_next = P.page[(it + stride) / P.hkv];
+    for (; it < items; it += stride) {
         const int entry = (int)(it / P.hkv), head = (int)(it % P.hkv);
-        const int page = P.page[entry];
-        uint32_t bad = 0;
-        uint64_t words[2] = {0, 0};
-        if (page < 0 || page >= P.num_meta_pages) {
-            bad = KVZ_STATUS_BAD_INDEX;
-        } else {
-            const uint64_t *m = P.meta + ((int64_t)page * P.hkv + head) * 2;
-            words[0] = m[0];
-            words[1] = m[1];
-        }
-        __syncwarp();  // the previous item's stores are done with the buffer
+        // both groups' blocks: every load first (a bad K word leaves the V group usable)
+        uint32_t bad = bad_idx, tags[2] = {0, 0}, use[2] = {0, 0};
+        uint4 x[2][4], y[2][4];
 #pragma unroll
         for (int kv = 0; kv < 2; ++kv) {
-            const uint32_t offset0 = (uint32_t)words[kv], tags = (uint32_t)(words[kv] >> 32);
-            bool use = !(bad & KVZ_STATUS_BAD_INDEX);  // a bad K word leaves the V group usable
-            if (use && (!tags_valid(tags) || offset0 == KVZ_OFFSET_INVALID ||
-                        ((uint64_t)offset0 + group_granules(tags)) * kGranule > P.arena_bytes)) {
+            const uint32_t offset0 = (uint32_t)words[kv];
+            tags[kv] = (uint32_t)(words[kv] >> 32);
+            use[kv] = !(bad_idx & KVZ_STATUS_BAD_INDEX);
+            if (use[kv] && (!tags_valid(tags[kv]) || offset0 == KVZ_OFFSET_INVALID ||
+                            ((uint64_t)offset0 + group_granules(tags[kv])) * kGranule > P.arena_bytes)) {
                 bad |= KVZ_STATUS_BAD_META;
-                use = false;
+                use[kv] = 0;
             }
-            // the group's four blocks: loads first, then the restores
-            uint4 x[4], y[4];
             uint32_t before = 0;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const uint32_t tag = (tags >> (8 * j)) & 0xFFu;
-                x[j] = make_uint4(0, 0, 0, 0);
-                y[j] = make_uint4(0, 0, 0, 0);
-                if (use) {
+                const uint32_t tag = (tags[kv] >> (8 * j)) & 0xFFu;
+                x[kv][j] = make_uint4(0, 0, 0, 0);
+                y[kv][j] = make_uint4(0, 0, 0, 0);
+                if (use[kv]) {
                     const uint8_t *blk = P.arena + ((uint64_t)offset0 + before) * kGranule;
                     if (tag == 0xFFu) {
-                        x[j] = *reinterpret_cast<const uint4 *>(blk + 32 * lane);
-                        y[j] = *reinterpret_cast<const uint4 *>(blk + 32 * lane + 16);
+                        x[kv][j] = __ldg(reinterpret_cast<const uint4 *>(blk + 32 * lane));
+                        y[kv][j] = __ldg(reinterpret_cast<const uint4 *>(blk + 32 * lane + 16));
                     } else {
-                        x[j] = *reinterpret_cast<const uint4 *>(blk + 16 * lane);
-                        const uint2 code = *reinterpret_cast<const uint2 *>(blk + 512 + 8 * lane);
-                        y[j].x = code.x;
-                        y[j].y = code.y;
+                        x[kv][j] = __ldg(reinterpret_cast<const uint4 *>(blk + 16 * lane));
+                        const uint2 code = __ldg(reinterpret_cast<const uint2 *>(blk + 512 + 8 * lane));
+                        y[kv][j].x = code.x;
+                        y[kv][j].y = code.y;
                     }
                 }
                 before += tag_granules(tag);
             }
+        }
+        // the next item's group words and the page id of the one after it
+        {
+            const int64_t nx = it + stride;
+            if (nx < items) dec_words(P, page_next, (int)(nx % P.hkv), words, bad_idx);
+            if (nx + stride < items) page_next = P.page[(nx + stride) / P.hkv];
+        }
+        __syncwarp();  // the previous item's stores are done with the buffer
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const uint32_t tag = (tags >> (8 * j)) & 0xFFu;
+                const uint32_t tag = (tags[kv] >> (8 * j)) & 0xFFu;
                 uint32_t w[8];
-                if (!use || tag == 0xFFu) {
-                    w[0] = x[j].x; w[1] = x[j].y; w[2] = x[j].z; w[3] = x[j].w;
-                    w[4] = y[j].x; w[5] = y[j].y; w[6] = y[j].z; w[7] = y[j].w;
+                if (!use[kv] || tag == 0xFFu) {
+                    w[0] = x[kv][j].x; w[1] = x[kv][j].y; w[2] = x[kv][j].z; w[3] = x[kv][j].w;
+                    w[4] = y[kv][j].x; w[5] = y[kv][j].y; w[6] = y[kv][j].z; w[7] = y[kv][j].w;
                 } else {
                     const uint32_t bb = tag * 0x01010101u;
                     uint32_t f0[4], f1[4];
-                    restore_fragment(x[j].x, x[j].y, y[j].x, bb, f0);
-                    restore_fragment(x[j].z, x[j].w, y[j].y, bb, f1);
+                    restore_fragment(x[kv][j].x, x[kv][j].y, y[kv][j].x, bb, f0);
+                    restore_fragment(x[kv][j].z, x[kv][j].w, y[kv][j].y, bb, f1);
                     w[0] = f0[0]; w[1] = f0[1]; w[2] = f0[2]; w[3] = f0[3];
                     w[4] = f1[0]; w[5] = f1[1]; w[6] = f1[2]; w[7] = f1[3];
                 }
@@ -494,7 +518,7 @@ cudaError_t launch_decode(const DecodeParams &P, cudaStream_t stream)
     int sms = 0;
     cudaError_t e = encode_grid(&sms);
     if (e != cudaSuccess) return e;
-    k_decode_w<<<grid_for((size_t)P.n * P.hkv, sms, 3), kDecWarps * 32, kDecSmem, stream>>>(P);
+    k_decode_w<<<grid_for((size_t)P.n * P.hkv, sms, kDecCtasPerSm), kDecWarps * 32, kDecSmem, stream>>>(P);
     return cudaGetLastError();
 }
 
