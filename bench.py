@@ -1,21 +1,27 @@
 """Benchmark: paged GQA decode attention over 12-bit compressed BF16 KV pages on GB300.
 
-Default workload: one Llama-3.1-8B-shaped attention layer at decode -- batch 32, 32
-query heads, 8 KV heads, head dim 128, 2048 tokens in 128 compressed 16-token pages
-per sequence (shuffled physical order) plus a raw tail of 1..15 tokens.  A step is one
-kvz_decode_attention call over the whole batch (attention + split merge).  Synthetic,
-seeded inputs (kvgen); the KV is resident in HBM before timing starts.
+Default workload: the full Llama-3.1-8B-shaped decode step at 8K context -- 32 layers,
+batch 16, 32 query heads, 8 KV heads, head dim 128, 8192 tokens in 512 compressed
+16-token pages per sequence (shuffled physical order) plus a raw tail of 1..15 tokens,
+each layer with its own seeded KV.  A step is one kvz_decode_attention call per layer,
+in layer order (attention + split merge, 64 kernel launches); every step reads all 32
+layers' caches once (14.7 GB compressed, far more than L2).  Synthetic, seeded inputs
+(kvgen); the KV is resident in HBM before timing starts.
 
-Reported: logical-KV GB/s (BF16 K+V bytes attended / time) as `value`, µs per step,
-the in-run raw-BF16 kernel on the same pages, the compressed-block fraction, encode and
-standalone-decode GB/s, the dominant kernel's HBM roofline fraction, an end-to-end
-figure through the C ABI with host buffers, one layer of the 8K-context stack (batch 16)
-compressed against raw (`at_8k_context`), and the CPU oracle timed on host cores.
+Reported: logical-KV GB/s (BF16 K+V bytes attended / time) as `value`, µs per step (the
+median of five timed runs of K steps), the in-run raw-BF16 kernel on the same pages, the
+compressed-block fraction, the dominant kernel's HBM roofline fraction, an end-to-end
+figure through the C ABI with host buffers (every layer's queries in, every layer's
+output back, each step), the CPU oracle on the host cores, and as extra keys: one C1
+layer (batch 32, 2K context) with encode / standalone decode / decompress-first, one
+layer of the 8K stack compressed against raw, the streaming Qwen3-8B-shaped step with
+page-completion encodes and the capacity count, and one 131072-token layer with the
+encode/decode throughput at 1-4 GB.
 
-Timing rules: >= 3 warm-up steps; the timed steps are one CUDA graph replay over
-rotating copies of the KV (3 copies, ~0.6 GB, > L2) so every step reads cold data;
-CUDA events on the launching stream, synchronize on both sides, max over ranks.
-`--impl reference` times the CPU oracle (the reference arm of this build).
+Timing rules: >= 3 warm-up steps; inputs larger than L2 (the stack) or rotating copies
+of the KV (single layers: 3 copies, > L2) so every step reads cold data; CUDA events on
+the launching stream, synchronize on both sides, max over ranks.  `--impl reference`
+times the CPU oracle on the same configuration (the reference arm of this build).
 """
 from __future__ import annotations
 
@@ -38,6 +44,7 @@ import kvgen  # noqa: E402
 
 METRIC = "decode-attention µs/step & logical KV GB/s; % of HBM roofline; encode GB/s"
 FALLBACK_HBM_GBS = 6800.0
+RUNS = 5  # timed runs of K steps per measurement; the median is reported
 
 
 # --------------------------------------------------------------------------------------
@@ -165,6 +172,36 @@ def profiled_traffic(workload: str, kernel: str = "compressed"):
         return None
 
 
+def layer_cfg(name: str) -> kvgen.KVConfig:
+    """Single-layer workloads: C1 as it is, one layer of the C2 and C4 stacks."""
+    base = {"c1": kvgen.C1, "c2-layer": kvgen.C2, "c4": kvgen.C4}[name]
+    return kvgen.KVConfig(**{**base.__dict__, "layers": 1})
+
+
+def config_dict(workload: str, world: int) -> dict:
+    """The `config` object of the JSON line; the same function serves both arms, so the
+    GPU line and the reference (oracle) line describe the same workload."""
+    par = f"replicas{world}"
+    if workload == "c2":
+        cfg = kvgen.C2
+        return {"workload": cfg.name + "-full-stack", "layers": cfg.layers, "batch": cfg.batch, "q_heads": cfg.hq,
+                "kv_heads": cfg.hkv, "head_dim": 128, "page_tokens": 16, "context_tokens": cfg.full_pages * 16,
+                "tail_tokens": f"{cfg.tail_min}..{cfg.tail_max}", "page_order": "shuffled",
+                "kv": "a separate seeded KV cache per layer", "parallelism": par,
+                "l2": "inputs larger than L2: each step reads all 32 layers' caches once"}
+    if workload == "c3":
+        cfg = kvgen.C3
+        return {"workload": cfg.name, "layers": cfg.layers, "batch": cfg.batch, "q_heads": cfg.hq,
+                "kv_heads": cfg.hkv, "head_dim": 128, "page_tokens": 16, "prompt_tokens": 2048,
+                "parallelism": par}
+    cfg = layer_cfg(workload)
+    return {"workload": cfg.name + ("" if workload == "c1" else "-one-layer"), "layers": 1, "batch": cfg.batch,
+            "q_heads": cfg.hq, "kv_heads": cfg.hkv, "head_dim": 128, "page_tokens": 16,
+            "context_tokens": cfg.full_pages * 16, "tail_tokens": f"{cfg.tail_min}..{cfg.tail_max}",
+            "page_order": "shuffled", "parallelism": par,
+            "l2": "inputs larger than L2: 3 rotating KV copies read in turn"}
+
+
 # --------------------------------------------------------------------------------------
 # workload
 # --------------------------------------------------------------------------------------
@@ -208,7 +245,7 @@ class Workload:
             self.arenas.append(arena)
         self.out = torch.empty((B, hq, 128), dtype=torch.float32, device=dev)
         self.out_raw = torch.empty_like(self.out)
-        self.out_df = torch.empty_like(self.out)
+        self.out_df = None
         self.ws_c = torch.empty(kvz.attention_workspace_size(hkv, B, hq, cfg.full_pages + 1), dtype=torch.uint8,
                                 device=dev)
         self.ws_r = torch.empty(kvz.attention_workspace_size(hkv, B, hq, self.raw_table.shape[1]),
@@ -238,18 +275,16 @@ class Workload:
         tail_bytes = int(self.tail_len.sum()) * hkv * 2 * 128 * 2
         q_bytes = B * hq * 128 * 2
         out_bytes = B * hq * 128 * 4
-        grid_slots = (self.ws_c.numel()) // 1  # upper bound only; partials counted below
-        del grid_slots
-        units = B * hkv
         # partials: each (unit, CTA) segment writes G x (128 + 2) floats, the merge reads them
         G = hq // hkv
-        segs = units + self.grid_c() - 1
+        segs = B * hkv + self.grid_c() - 1
         part_bytes = 2 * segs * G * 130 * 4
         self.alg_bytes_c = (self.block_bytes + pages_c * hkv * 16 + pages_c * hkv * 4 + tail_bytes + q_bytes +
                             out_bytes + part_bytes)
         raw_pages = int(((self.seq_lens + 15) // 16).sum())
         self.alg_bytes_r = (self.logical_bytes + raw_pages * hkv * 4 + q_bytes + out_bytes + part_bytes)
         self.pages_c, self.tail_bytes = pages_c, tail_bytes
+        self.bytes_ratio = self.block_bytes / (self.blocks * 1024)
 
     def grid_c(self):
         # the kernel's grid: (workspace - prefix) / (per-slot bytes) = units + C - 1 slots
@@ -276,16 +311,24 @@ class Workload:
         self.df_tail_src = self.tail.long().clamp_min(0)
         self.df_ws = torch.empty(self.kvz.attention_workspace_size(cfg.hkv, B, cfg.hq, nf + 1), dtype=torch.uint8,
                                  device=dev)
+        self.out_df = torch.empty_like(self.out)
 
-    def step_df(self, k: int):
-        """Decompress-first: decode every compressed page of the layer to BF16, put the
-        tails beside them, then run the raw kernel over the decoded pool."""
+    def step_df_decode(self, k: int):
+        """Decompress-first, first half: decode every compressed page of the layer to
+        BF16 and put the sequences' tails beside them."""
         c = k % self.copies
         B, nf = self.cfg.batch, self.cfg.full_pages
         self.kvz.decode_blocks(self.metas[c], self.arenas[c], self.src, self.df_pool[: B * nf], self.status)
         self.df_pool[B * nf:] = self.pools[c][self.df_tail_src]
+
+    def step_df_attend(self, k: int):
+        """Decompress-first, second half: the raw kernel over the decoded pool."""
         self.kvz.decode_attention_raw(self.q, self.df_table, self.seq_lens, self.df_pool, self.out_df, self.status,
                                       workspace=self.df_ws)
+
+    def step_df(self, k: int):
+        self.step_df_decode(k)
+        self.step_df_attend(k)
 
     def step_r(self, k: int):
         c = k % self.copies
@@ -316,6 +359,31 @@ def time_graph(g, reps: int = 1) -> float:
     e1.record(st)
     torch.cuda.synchronize()
     return e0.elapsed_time(e1)
+
+
+def timed_runs(g, dist=None, runs: int = RUNS) -> list[float]:
+    """ms of each of `runs` timed replays of a K-step graph (barrier before each)."""
+    out = []
+    for _ in range(runs):
+        if dist:
+            dist.barrier()
+        out.append(time_graph(g))
+    return out
+
+
+def runs_summary(ms: list[float], K: int) -> dict:
+    us = [m * 1e3 / K for m in ms]
+    return {"n": len(us), "us_per_step_median": round(statistics.median(us), 3),
+            "us_per_step_mean": round(float(np.mean(us)), 3), "us_per_step_std": round(float(np.std(us)), 3),
+            "us_per_step_runs": [round(u, 3) for u in us]}
+
+
+def soak(g, seconds: float):
+    """Replay a graph for a while so the 200 ms clock samples see the GPU under load."""
+    until = time.time() + seconds
+    while time.time() < until:
+        g.replay()
+        torch.cuda.synchronize()
 
 
 def flush_l2(buf: torch.Tensor):
@@ -426,188 +494,127 @@ def oracle_sample(cfg: kvgen.KVConfig, budget_s: float, seqs_max: int | None = N
 
 
 # --------------------------------------------------------------------------------------
-def measure_8k_layer(args, local, dev) -> dict:
-    """One layer of the 8K-context stack (batch 16, 512 compressed pages + a 1..15-token
-    tail per sequence, 32/8 heads), compressed and raw kernels timed as the headline layer
-    is (graph of K steps over 3 rotating KV copies, CUDA events): the comparison the
-    compressed format is judged on (step time against the raw kernel, in proportion to the
-    bytes it saves)."""
-    cfg = kvgen.KVConfig(**{**kvgen.C2.__dict__, "layers": 1})
-    W = Workload(cfg, args.copies, layer=0, dev=dev)
-    for k in range(3):
-        W.step_c(k)
-        W.step_r(k)
-    torch.cuda.synchronize()
-    if int(W.status.item()) != 0:
-        raise RuntimeError(f"8K layer: attention status {int(W.status.item())}")
-    identical = bool(torch.equal(W.out, W.out_raw))
-    K = args.steps
-    g_c = graph_of(W.step_c, K)
-    g_r = graph_of(W.step_r, K)
-    g_c.replay()
-    g_r.replay()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        soak_until = time.time() + 0.4  # so the 200 ms clock samples see the GPU under load
-        while time.time() < soak_until:
-            g_c.replay()
-            torch.cuda.synchronize()
-        ms_c = time_graph(g_c)
-        ms_r = time_graph(g_r)
-    us_c, us_r = ms_c * 1e3 / K, ms_r * 1e3 / K
-    ratio = W.block_bytes / (W.blocks * 1024)
-    res = {"workload": cfg.name + " (one layer)", "batch": cfg.batch, "context_tokens": cfg.full_pages * 16,
-           "us_per_step": round(us_c, 3), "raw_us_per_step": round(us_r, 3),
-           "speedup_vs_raw": round(us_r / us_c, 4), "expected_speedup_from_fraction": round(1.0 / ratio, 4),
-           "compressed_fraction": round(W.compressed_fraction, 5), "compressed_bytes_ratio": round(ratio, 5),
-           "logical_GBps": round(W.logical_bytes / (us_c * 1e-6) / 1e9, 2),
-           "bit_identical_compressed_vs_raw": identical, "clocks": clk.summary()}
-    del g_c, g_r, W
-    torch.cuda.empty_cache()
-    return res
-
-
-def main():
-    ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--impl", default="kvz", choices=["kvz", "reference"])
-    ap.add_argument("--workload", default="c1", choices=["c1", "c2", "c3", "c4", "serve"])
-    ap.add_argument("--serve-budget-gb", type=float, default=4.0, help="serve: KV budget of both caches (1e9 B)")
-    ap.add_argument("--serve-requests", type=int, default=256, help="serve: requests in the queue")
-    ap.add_argument("--budget-gb", type=float, default=60.0, help="KV budget for the c3 capacity count (1e9 B)")
-    ap.add_argument("--stack", action="store_true",
-                    help="c2: one step = all layers of the stack, each with its own KV (else one layer per step)")
-    ap.add_argument("--sweep", action="store_true",
-                    help="encode / standalone-decode throughput over 64 MB .. 4 GB of pages (exponent-spread KV)")
-    ap.add_argument("--spread-sweep", action="store_true",
-                    help="long-context layer (B=2, 131072 tokens) with the per-block exponent spread fixed at each "
-                         "of 8..20: compressed fraction and attention time, compressed vs raw")
-    ap.add_argument("--copies", type=int, default=3)
-    ap.add_argument("--format", default="zf", choices=["zf", "ga", "f8e4", "f8e5"],
-                    help="ga: group-adaptive additive tiles; f8e4 / f8e5: completed pages converted to FP8 "
-                         "E4M3 / E5M2 and coded; instead of 12-bit block groups (c1, c2, c4)")
-    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-8k", action="store_true",
-                    help="c1: skip the 8K-context layer measured beside the headline layer")
-    ap.add_argument("--decode-steps", type=int, default=256, help="decode steps of the c3 streaming run")
-    args = ap.parse_args()
-    if args.warmup < 3:
-        args.warmup = 3
-    cfg = kvgen.CONFIGS.get(args.workload, kvgen.C3)
-    if args.workload in ("c2", "c4"):
-        cfg = kvgen.KVConfig(**{**cfg.__dict__, "layers": 1})  # one layer of the 32-layer stack per step
-    dist, rank, world, local = dist_setup()
-    if args.sweep:
-        return run_sweep(args, dist, rank, local)
-    if args.spread_sweep:
-        return run_spread_sweep(args, dist, rank, local)
-    if args.workload == "c3":
-        return run_stream(args, cfg, dist, rank, world, local)
-    if args.workload == "serve":
-        return run_serve(args, dist, rank, world, local)
-    if args.stack:
-        return run_stack(args, kvgen.CONFIGS[args.workload], dist, rank, world, local)
-
-    if args.impl == "reference":
-        return run_reference(args, cfg, dist, rank, world)
-    if args.format != "zf":
-        return run_ga(args, cfg, dist, rank, world, local)
-
-    torch.cuda.set_device(local)
+# measurements
+# --------------------------------------------------------------------------------------
+def measure_layer(cfg: kvgen.KVConfig, args, dev, local, dist, world: int, rank: int, flush=None,
+                  decompress_first: bool = False, codec: bool = False) -> dict:
+    """One decode layer, compressed and raw kernels each timed as a graph of K steps over
+    rotating KV copies (median of RUNS timed runs).  Optionally the decompress-first
+    pipeline (standalone decode into a BF16 scratch pool, then the raw kernel; its two
+    legs also timed apart) and the encode / standalone-decode throughput of the layer."""
     import decode_attention_value_gb300 as kvz
 
-    dev = torch.device("cuda", local)
     peak, peak_kind = measured_peaks()
     W = Workload(cfg, args.copies, layer=rank, dev=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 256 MB > L2
-
-    # warm-up (also configures the kernels) and a bit-identity spot check
     for k in range(args.warmup):
         W.step_c(k)
         W.step_r(k)
     torch.cuda.synchronize()
     if int(W.status.item()) != 0:
-        raise RuntimeError(f"attention status {int(W.status.item())}")
+        raise RuntimeError(f"{cfg.name}: attention status {int(W.status.item())}")
     identical = bool(torch.equal(W.out, W.out_raw))
-
-    # timed region: one graph of K steps, rotating KV copies
     K = args.steps
-    g_c = graph_of(W.step_c, K)
-    g_r = graph_of(W.step_r, K)
-    W.setup_decompress_first()
-    g_df = graph_of(W.step_df, K)
-    g_c.replay()
-    g_r.replay()
-    g_df.replay()
+    g_c, g_r = graph_of(W.step_c, K), graph_of(W.step_r, K)
+    graphs = {"c": g_c, "r": g_r}
+    if decompress_first:
+        W.setup_decompress_first()
+        graphs["df"] = graph_of(W.step_df, K)
+        graphs["dfd"] = graph_of(W.step_df_decode, K)
+        graphs["dfa"] = graph_of(W.step_df_attend, K)
+    for g in graphs.values():
+        g.replay()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        soak_until = time.time() + 0.6
-        while time.time() < soak_until:
-            g_c.replay()
-            torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
-        torch.cuda.synchronize()
-        ms_c = time_graph(g_c)
-        if dist:
-            dist.barrier()
-        ms_r = time_graph(g_r)
-        ms_df = time_graph(g_df)
-        # four more timed runs of each graph, after the one the line reports: the spread
-        # of the per-run step times
-        reps_c = [ms_c] + [time_graph(g_c) for _ in range(4)]
-        reps_r = [ms_r] + [time_graph(g_r) for _ in range(4)]
-        soak_until = time.time() + 0.4
-        while time.time() < soak_until:
-            g_c.replay()
-            torch.cuda.synchronize()
+        soak(g_c, 0.5)
+        ms = {name: timed_runs(g, dist) for name, g in graphs.items()}
+        soak(g_c, 0.3)
     clocks = clk.summary()
-    ms_c, ms_r, ms_df = max_over_ranks(dist, [ms_c, ms_r, ms_df], device=dev)
-    if not torch.equal(W.out_df, W.out_raw):
-        raise RuntimeError("decompress-first output differs from the raw kernel's")
+    med = {name: statistics.median(v) for name, v in ms.items()}
+    names = list(med)
+    vals = max_over_ranks(dist, [med[n] for n in names], device=dev)
+    med = dict(zip(names, vals))
+    us_c, us_r = med["c"] * 1e3 / K, med["r"] * 1e3 / K
+    achieved = W.alg_bytes_c / (us_c * 1e-6) / 1e9
+    achieved_r = W.alg_bytes_r / (us_r * 1e-6) / 1e9
+    res = {"workload": cfg.name, "batch": cfg.batch, "context_tokens": cfg.full_pages * 16,
+           "us_per_step": round(us_c, 3), "raw_us_per_step": round(us_r, 3),
+           "speedup_vs_raw": round(us_r / us_c, 4), "expected_speedup_from_fraction": round(1.0 / W.bytes_ratio, 4),
+           "compressed_fraction": round(W.compressed_fraction, 5), "compressed_bytes_ratio": round(W.bytes_ratio, 5),
+           "logical_GBps": round(job_throughput(world, W.logical_bytes, K, med["c"]), 2),
+           "bit_identical_compressed_vs_raw": identical,
+           "roofline": {"achieved": round(achieved, 1), "frac": round(achieved / peak, 4), "peak": peak,
+                        "peak_kind": peak_kind, "algorithmic_bytes_per_launch": W.alg_bytes_c},
+           "roofline_raw": {"achieved": round(achieved_r, 1), "frac": round(achieved_r / peak, 4),
+                            "algorithmic_bytes_per_launch": W.alg_bytes_r},
+           "runs": runs_summary(ms["c"], K), "runs_raw": runs_summary(ms["r"], K), "clocks": clocks}
+    if decompress_first:
+        if not torch.equal(W.out_df, W.out_raw):
+            raise RuntimeError(f"{cfg.name}: decompress-first output differs from the raw kernel's")
+        us_df, us_dfd, us_dfa = (med[n] * 1e3 / K for n in ("df", "dfd", "dfa"))
+        res["decompress_first"] = {
+            "us_per_step": round(us_df, 3), "decode_leg_us": round(us_dfd, 3), "attention_leg_us": round(us_dfa, 3),
+            "decode_share": round(us_dfd / (us_dfd + us_dfa), 4), "fused_speedup": round(us_df / us_c, 4),
+            "how": "standalone decode of every compressed page into a BF16 scratch pool (plus a copy of the tails), "
+                   "then the raw kernel over it; each leg also timed as its own graph"}
+    if codec:
+        fl = flush if flush is not None else torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        enc_meta = torch.zeros_like(W.metas[0])
+        enc_arena = torch.zeros_like(W.arenas[0])
+        enc_cur = W.cursor0.clone()
 
-    us_step = ms_c * 1e3 / K
-    us_raw = ms_r * 1e3 / K
-    value = job_throughput(world, W.logical_bytes, K, ms_c)
+        def enc(k):
+            kvz.encode_pages(W.pools[k % W.copies], W.src, W.src, W.dseq, enc_meta, enc_arena, enc_cur, W.status,
+                             workspace=W.enc_ws)
 
-    # dominant kernel: algorithmic bytes per launch / average launch duration over the
-    # timed region (one attention launch + its merge per step); a cold single launch
-    # (L2 flushed, nothing before or after it) is reported beside it
-    achieved = W.alg_bytes_c / (us_step * 1e-6) / 1e9
-    achieved_raw = W.alg_bytes_r / (us_raw * 1e-6) / 1e9
-    launch_ms = per_launch_ms(W.step_c, max(10, min(K, 40)), flush, period=W.copies)
-    launch_ms_raw = per_launch_ms(W.step_r, max(10, min(K, 40)), flush, period=W.copies)
+        enc_ms = per_launch_ms(enc, 10, fl, period=W.copies, prep=lambda k: enc_cur.copy_(W.cursor0))
+        enc_in = W.src.numel() * cfg.hkv * 2 * 16 * 128 * 2
+        dec_out = torch.empty((W.src.numel(), cfg.hkv, 2, 16, 128), dtype=torch.bfloat16, device=dev)
 
-    # encode and standalone decode throughput (C1 full pages, cold inputs)
-    enc_meta = torch.zeros_like(W.metas[0])
-    enc_arena = torch.zeros_like(W.arenas[0])
-    enc_cur = W.cursor0.clone()
+        def dec(k):
+            kvz.decode_blocks(W.metas[k % W.copies], W.arenas[k % W.copies], W.src, dec_out, W.status)
 
-    def enc(k):
-        kvz.encode_pages(W.pools[k % W.copies], W.src, W.src, W.dseq, enc_meta, enc_arena, enc_cur, W.status,
-                         workspace=W.enc_ws)
+        dec_ms = per_launch_ms(dec, 10, fl, period=W.copies)
+        torch.cuda.synchronize()
+        if int(W.status.item()) != 0:
+            raise RuntimeError(f"{cfg.name}: codec status {int(W.status.item())}")
+        if not torch.equal(dec_out.view(torch.int16), W.pools[(10 - 1) % W.copies][W.src.long()].view(torch.int16)):
+            raise RuntimeError(f"{cfg.name}: standalone decode differs from the input pages")
+        res["encode_GBps"] = round(enc_in / (enc_ms * 1e-3) / 1e9, 2)
+        res["decode_GBps"] = round(enc_in / (dec_ms * 1e-3) / 1e9, 2)
+        res["codec_how"] = "one call per graph replay, L2 read-flushed before each; GB/s of BF16 pages in (encode) / out (decode)"
+    res["_W"] = W
+    return res
 
-    enc_ms = per_launch_ms(enc, 10, flush, period=W.copies, prep=lambda k: enc_cur.copy_(W.cursor0))
-    enc_in = W.src.numel() * cfg.hkv * 2 * 16 * 128 * 2
-    dec_out = torch.empty((W.src.numel(), cfg.hkv, 2, 16, 128), dtype=torch.bfloat16, device=dev)
 
-    def dec(k):
-        kvz.decode_blocks(W.metas[k % W.copies], W.arenas[k % W.copies], W.src, dec_out, W.status)
+def stack_layers(cfg: kvgen.KVConfig, dev) -> list:
+    """Every layer of the stack with its own seeded KV, one block table for all layers
+    (as a paged KV cache keeps it: each layer has its own pools and metadata behind the
+    same page ids) and one attention workspace, the scratch buffer a serving loop hands
+    to each layer's call in turn."""
+    one = kvgen.KVConfig(**{**cfg.__dict__, "layers": 1})
+    layers = [Workload(one, 1, layer=layer, dev=dev) for layer in range(cfg.layers)]
+    for W in layers[1:]:
+        assert torch.equal(W.table, layers[0].table) and torch.equal(W.seq_lens, layers[0].seq_lens)
+        W.table, W.full, W.tail, W.raw_table = layers[0].table, layers[0].full, layers[0].tail, layers[0].raw_table
+        W.seq_lens = layers[0].seq_lens
+        W.ws_c, W.ws_r = layers[0].ws_c, layers[0].ws_r
+    return layers
 
-    dec_ms = per_launch_ms(dec, 10, flush, period=W.copies)
-    torch.cuda.synchronize()
-    if int(W.status.item()) != 0:
-        raise RuntimeError(f"status {int(W.status.item())}")
 
-    # end to end through the C ABI with host buffers: H2D of the step's inputs, D2H of the output
-    # the step's inputs travel as one pinned buffer (q, table, lengths, tails back to back,
-    # each 16-byte aligned) and one host-to-device copy; the output comes back in one copy;
-    # the K steps (copies and the C-ABI call) are captured in one CUDA graph, as a serving
-    # engine replays its decode step
-    parts = [W.q.contiguous(), W.full.contiguous(), W.seq_lens.contiguous(), W.tail.contiguous()]
+def stack_e2e(layers, K: int, dev, dist, world: int) -> dict:
+    """The stack end to end through the C ABI with host buffers.  Per step: one
+    host-to-device copy of every layer's queries plus the block table, lengths and tail
+    ids (one pinned buffer, back to back, 16-byte aligned), the 32 kvz_decode_attention
+    calls, and one device-to-host copy of every layer's fp32 output.  Pipelined as a
+    serving engine runs it: a copy stream brings step k+1's inputs in and takes step k's
+    outputs back while the neighbouring step computes (device inputs and outputs and the
+    pinned outputs double-buffered); the K steps are one CUDA graph.  Also reported: the
+    same copies and calls back to back on one stream."""
+    kvz = layers[0].kvz
+    W0 = layers[0]
+    L = len(layers)
+    q_all = torch.stack([W.q for W in layers]).contiguous()
+    parts = [q_all, W0.full.contiguous(), W0.seq_lens.contiguous(), W0.tail.contiguous()]
     offs, total = [], 0
     for t in parts:
         offs.append(total)
@@ -616,45 +623,27 @@ def main():
     for t, o in zip(parts, offs):
         nb = t.numel() * t.element_size()
         pin_in[o: o + nb].copy_(t.cpu().contiguous().view(torch.uint8).reshape(-1))
-    d_in = torch.empty_like(pin_in, device=dev)
-    d_q, d_table, d_lens, d_tail = (d_in[o: o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
-                                    for t, o in zip(parts, offs))
-    pin_out = torch.empty(W.out.shape, dtype=torch.float32).pin_memory()
-    h2d = total
-    d2h = pin_out.numel() * 4
-
-    def e2e_step(k):
-        d_in.copy_(pin_in, non_blocking=True)
-        c = k % W.copies
-        kvz.decode_attention(d_q, d_table, d_lens, d_tail, W.metas[c], W.arenas[c], W.pools[c], W.out, W.status,
-                             workspace=W.ws_c)
-        pin_out.copy_(W.out, non_blocking=True)
-
-    for k in range(3):
-        e2e_step(k)
-    torch.cuda.synchronize()
-    g_e2e = graph_of(e2e_step, K)
-    g_e2e.replay()
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    e2e_serial_ms = max_over_ranks(dist, [time_graph(g_e2e)], device=dev)[0]
-    e2e_serial = job_throughput(world, W.logical_bytes, K, e2e_serial_ms)
-    if not torch.equal(pin_out, W.out.cpu()):
-        raise RuntimeError("end-to-end output differs from the device output")
-
-    # the same copies pipelined as a serving engine runs them: a copy stream brings step k+1's
-    # inputs in and step k's output back while step k+1 / k computes (inputs and outputs
-    # double-buffered on the device, outputs double-buffered in pinned host memory)
-    d_in2 = [d_in, torch.empty_like(d_in)]
+    d_in2 = [torch.empty_like(pin_in, device=dev) for _ in range(2)]
     views2 = [[buf[o: o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for t, o in zip(parts, offs)]
               for buf in d_in2]
-    out2 = [torch.empty_like(W.out) for _ in range(2)]
-    pin_out2 = [torch.empty(W.out.shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+    out_shape = (L,) + tuple(W0.out.shape)
+    out2 = [torch.empty(out_shape, dtype=torch.float32, device=dev) for _ in range(2)]
+    pin_out2 = [torch.empty(out_shape, dtype=torch.float32).pin_memory() for _ in range(2)]
+    status = kvz.new_status(dev)
 
-    def e2e_pipelined_graph(steps: int):
-        s = torch.cuda.Stream()
-        cs = torch.cuda.Stream()
+    def calls(views, out):
+        q_, t_, l_, tl_ = views
+        for i, W in enumerate(layers):
+            kvz.decode_attention(q_[i], t_, l_, tl_, W.metas[0], W.arenas[0], W.pools[0], out[i], status,
+                                 workspace=W0.ws_c)
+
+    def serial_step(k):
+        d_in2[0].copy_(pin_in, non_blocking=True)
+        calls(views2[0], out2[0])
+        pin_out2[0].copy_(out2[0], non_blocking=True)
+
+    def pipelined_graph(steps: int):
+        s, cs = torch.cuda.Stream(), torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(s):
@@ -668,7 +657,7 @@ def main():
                             e = torch.cuda.Event()
                             e.record(cs)
                             ev_in.append(e)
-                    if k >= 1:  # output of step k - 1
+                    if k >= 1:  # outputs of step k - 1
                         j = k - 1
                         done = torch.cuda.Event()
                         done.record(s)
@@ -677,105 +666,323 @@ def main():
                             pin_out2[j % 2].copy_(out2[j % 2], non_blocking=True)
                     if k < steps:
                         s.wait_event(ev_in[k])
-                        q_, t_, l_, tl_ = views2[k % 2]
-                        c = k % W.copies
-                        kvz.decode_attention(q_, t_, l_, tl_, W.metas[c], W.arenas[c], W.pools[c], out2[k % 2],
-                                             W.status, workspace=W.ws_c)
+                        calls(views2[k % 2], out2[k % 2])
                 s.wait_stream(cs)
         torch.cuda.current_stream().wait_stream(s)
         return g
 
-    g_pipe = e2e_pipelined_graph(K)
+    serial_step(0)
+    torch.cuda.synchronize()
+    g_ser = graph_of(serial_step, K)
+    g_pipe = pipelined_graph(K)
+    g_ser.replay()
     g_pipe.replay()
     torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    e2e_ms = max_over_ranks(dist, [time_graph(g_pipe)], device=dev)[0]
-    e2e_value = job_throughput(world, W.logical_bytes, K, e2e_ms)
-    for j in range(2):
-        if not torch.equal(pin_out2[j], W.out.cpu()):
-            raise RuntimeError("pipelined end-to-end output differs from the device output")
+    if int(status.item()) != 0:
+        raise RuntimeError(f"end-to-end status {int(status.item())}")
+    ms_pipe = statistics.median(timed_runs(g_pipe, dist))
+    ms_ser = statistics.median(timed_runs(g_ser, dist))
+    ms_pipe, ms_ser = max_over_ranks(dist, [ms_pipe, ms_ser], device=dev)
+    expect = torch.stack([W.out for W in layers]).cpu()
+    for buf in [pin_out2[0], pin_out2[1]]:
+        if not torch.equal(buf, expect):
+            raise RuntimeError("end-to-end outputs differ from the device outputs")
+    logical = sum(W.logical_bytes for W in layers)
+    return {"value": round(job_throughput(world, logical, K, ms_pipe), 2), "unit": "GB/s",
+            "h2d_bytes_per_step": total, "d2h_bytes_per_step": pin_out2[0].numel() * 4,
+            "us_per_step": round(ms_pipe * 1e3 / K, 2),
+            "how": "pinned host buffers; per step one host-to-device copy of every layer's queries, the block table, "
+                   "lengths and tail ids, the 32 C-ABI calls, one device-to-host copy of every layer's output; the "
+                   "copies run on a second stream, overlapping the neighbouring steps (inputs and outputs "
+                   "double-buffered); the K steps replayed as one CUDA graph; median of 5 timed runs",
+            "serial_value": round(job_throughput(world, logical, K, ms_ser), 2),
+            "serial_how": "the same copies and calls issued back to back on one stream"}
 
-    at_8k = None
-    if args.workload == "c1" and not args.no_8k:
-        at_8k = measure_8k_layer(args, local, dev)
 
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
-        gbps, secs, nseq, passes, threads = oracle_sample(cfg, args.cpu_budget)
-        cpu = {"value": round(gbps, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": f"{nseq} of {cfg.batch} sequences x {cfg.hkv} KV heads of the same layer "
-                         f"(decode of compressed pages + fp64 attention), {passes} passes, {secs:.1f} s"}
-        g1, s1, n1, p1, _ = oracle_sample(cfg, min(4.0, args.cpu_budget / 3), threads=1)
-        cpu["extra"] = {"attention_1core_GBps": round(g1, 3),
-                        "attention_1core_sample": f"{n1} sequences, {p1} passes, {s1:.1f} s",
-                        "encode_1core_GBps": round(oracle_encode_rate(cfg), 3),
-                        "encode_sample": "64 MiB of the layer's pages, scalar oracle encoder, one thread",
-                        "encode_allcores_GBps": round(oracle_encode_rate(cfg, 32, threads), 3),
-                        "encode_allcores_sample": f"{threads} threads x 32 MiB of the layer's pages"}
+def measure_stack(args, dev, local, dist, world: int, rank: int) -> dict:
+    """The full 32-layer 8K decode step, compressed and raw, plus its end-to-end leg."""
+    cfg = kvgen.C2
+    peak, peak_kind = measured_peaks()
+    layers = stack_layers(cfg, dev)
+    L = cfg.layers
+    K = args.steps
 
-    traffic = profiled_traffic(args.workload)
-    line = {
-        "metric": METRIC,
-        "value": round(value, 2),
-        "unit": "GB/s",
-        "n_gpus": world,
-        "steps": K,
-        "warmup": args.warmup,
-        "ms_per_step": round(us_step / 1e3, 5),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic",
-        "config": {"workload": cfg.name, "batch": cfg.batch, "q_heads": cfg.hq, "kv_heads": cfg.hkv,
-                   "head_dim": 128, "page_tokens": 16, "context_tokens": cfg.full_pages * 16,
-                   "tail_tokens": f"{cfg.tail_min}..{cfg.tail_max}", "page_order": "shuffled",
-                   "parallelism": f"replicas{world}",
-                   "l2": f"inputs larger than L2: {args.copies} rotating KV copies "
-                         f"({args.copies * (W.block_bytes + W.tail_bytes) / 1e9:.2f} GB compressed)"},
-        "us_per_step": round(us_step, 3),
-        "raw_us_per_step": round(us_raw, 3),
-        "speedup_vs_raw": round(us_raw / us_step, 4),
-        "expected_speedup_from_fraction": round(1.0 / (W.block_bytes / (W.blocks * 1024)), 4),
-        "decompress_first_us_per_step": round(ms_df * 1e3 / K, 3),
-        "decompress_first_decode_share": round(1.0 - ms_r / ms_df, 4),
-        "speedup_vs_decompress_first": round(ms_df / ms_c, 4),
-        "compressed_fraction": round(W.compressed_fraction, 5),
-        "compressed_bytes_ratio": round(W.block_bytes / (W.blocks * 1024), 5),
+    def step_c(k):
+        for W in layers:
+            W.step_c(0)
+
+    def step_r(k):
+        for W in layers:
+            W.step_r(0)
+
+    for k in range(args.warmup):
+        step_c(k)
+        step_r(k)
+    torch.cuda.synchronize()
+    for W in layers:
+        if int(W.status.item()) != 0:
+            raise RuntimeError(f"status {int(W.status.item())}")
+    identical = all(torch.equal(W.out, W.out_raw) for W in layers)
+    g_c, g_r = graph_of(step_c, K), graph_of(step_r, K)
+    g_c.replay()
+    g_r.replay()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        soak(g_c, 0.6)
+        ms_c = timed_runs(g_c, dist)
+        ms_r = timed_runs(g_r, dist)
+        soak(g_c, 0.3)
+    clocks = clk.summary()
+    med_c, med_r = max_over_ranks(dist, [statistics.median(ms_c), statistics.median(ms_r)], device=dev)
+    us_c, us_r = med_c * 1e3 / K, med_r * 1e3 / K
+    logical = sum(W.logical_bytes for W in layers)
+    alg = sum(W.alg_bytes_c for W in layers)
+    alg_r = sum(W.alg_bytes_r for W in layers)
+    blocks = sum(W.blocks for W in layers)
+    raw_blocks = sum(W.raw_blocks for W in layers)
+    block_bytes = sum(W.block_bytes for W in layers)
+    e2e = stack_e2e(layers, K, dev, dist, world)
+    launch_us = us_c / L  # one attention launch + its merge, averaged over the layers of a step
+    achieved = alg / L / (launch_us * 1e-6) / 1e9
+    achieved_r = alg_r / (us_r * 1e-6) / 1e9
+    res = {
+        "value": round(job_throughput(world, logical, K, med_c), 2), "ms_per_step": round(us_c / 1e3, 5),
+        "us_per_step": round(us_c, 2), "raw_us_per_step": round(us_r, 2), "speedup_vs_raw": round(us_r / us_c, 4),
+        "compressed_fraction": round(1 - raw_blocks / blocks, 5),
+        "compressed_bytes_ratio": round(block_bytes / (blocks * 1024), 5),
+        "expected_speedup_from_fraction": round(blocks * 1024 / block_bytes, 4),
         "bit_identical_compressed_vs_raw": identical,
-        "encode_GBps": round(enc_in / (enc_ms * 1e-3) / 1e9, 2),
-        "decode_GBps": round(enc_in / (dec_ms * 1e-3) / 1e9, 2),
+        "compressed_GB": round(block_bytes / 1e9, 3), "logical_GB_per_step": round(logical / 1e9, 3),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": "k_attn<compressed> + k_attn_merge",
-                     "launch_us": round(us_step, 3), "cold_single_launch_us": round(launch_ms * 1e3, 3),
-                     "algorithmic_bytes_per_launch": W.alg_bytes_c},
-        "runs": {"n": 5, "us_per_step_mean": round(float(np.mean(reps_c)) * 1e3 / K, 3),
-                 "us_per_step_std": round(float(np.std(reps_c)) * 1e3 / K, 3),
-                 "raw_us_per_step_mean": round(float(np.mean(reps_r)) * 1e3 / K, 3),
-                 "raw_us_per_step_std": round(float(np.std(reps_r)) * 1e3 / K, 3),
-                 "how": f"5 timed runs of the {K}-step graphs (the first is the one reported); per-rank, rank 0"},
-        "roofline_raw": {"achieved": round(achieved_raw, 1), "frac": round(achieved_raw / peak, 4),
-                         "launch_us": round(us_raw, 3), "cold_single_launch_us": round(launch_ms_raw * 1e3, 3),
-                         "algorithmic_bytes_per_launch": W.alg_bytes_r},
-        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "how": "pinned host buffers; per step one host-to-device copy of q, table, lengths and tails, the "
-                       "C-ABI call, one device-to-host copy of the output; the copies run on a second stream, "
-                       "overlapping the neighbouring steps' attention (inputs and outputs double-buffered); the "
-                       "K steps replayed as one CUDA graph",
-                "serial_value": round(e2e_serial, 2),
-                "serial_how": "the same copies and call issued back to back on one stream"},
-        "cpu_baseline": cpu,
-        "clocks": clocks,
-        "gpu_launches": 2 * K,
-        "at_8k_context": at_8k,
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic("c2"), "peak_kind": peak_kind,
+                     "kernel": "k_attn<12-bit groups> + k_attn_merge (one layer's call)",
+                     "launch_us": round(launch_us, 3), "algorithmic_bytes_per_launch": round(alg / L),
+                     "how": "algorithmic bytes of one layer's call (mean over the 32 layers) / (median step time / 32); "
+                            "traffic: dram bytes of one launch on one layer of this stack (ncu summary in profiles/)"},
+        "roofline_raw": {"achieved": round(achieved_r, 1), "frac": round(achieved_r / peak, 4),
+                         "algorithmic_bytes_per_step": alg_r},
+        "runs": {**runs_summary(ms_c, K), "how": f"{RUNS} timed runs of the {K}-step graph, median reported"},
+        "runs_raw": runs_summary(ms_r, K),
+        "e2e": e2e, "clocks": clocks, "gpu_launches": 2 * L * K,
     }
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if dist:
-        dist.barrier()
-        dist.destroy_process_group()
+    del layers, g_c, g_r
+    torch.cuda.empty_cache()
+    return res
+
+
+def measure_stream(args, dev, local, world: int) -> dict:
+    """Streaming decode, Qwen3-8B shape (36 layers, 32/8 heads, batch 64): a 2048-token
+    prompt (128 pages per sequence and layer, encoded at prefill), then `decode_steps`
+    steps that each append one token per sequence and layer and run attention in every
+    layer.  When a sequence's tail page fills (every 16th step) the page is encoded in
+    every layer before that step's attention, into chunk slots handed out by the host
+    allocator; per-step latency includes the encoding.  The same loop on raw pages gives
+    the uncompressed step time.  At the end: sequences that fit in the KV budget."""
+    import decode_attention_value_gb300 as kvz
+
+    cfg = kvgen.C3
+    B, L, hkv, hq = cfg.batch, cfg.layers, cfg.hkv, cfg.hq
+    prompt_pages = cfg.full_pages
+    T = args.decode_steps
+    dec_pages = (T + 15) // 16
+    ppseq = prompt_pages + dec_pages + 1  # raw page slots per sequence: prompt, decode pages, spare
+    P = B * ppseq
+    # raw pool of every layer; page b*ppseq + k is sequence b's k-th page (meta ids are the same)
+    raw = torch.empty((L, P, hkv, 2, 16, 128), dtype=torch.bfloat16, device=dev)
+    for layer in range(L):
+        raw[layer] = kvgen.gen_pages(cfg, P, layer=layer, device=dev)
+    new_kv = kvgen.gen_new_tokens(cfg, T, device=dev)  # [T][L][B][hkv][2][128]
+    qs = [kvgen.gen_q(cfg, layer=layer).to(dev) for layer in range(L)]
+    ids = torch.arange(B, device=dev, dtype=torch.int32) * ppseq
+    table = (ids[:, None] + torch.arange(ppseq - 1, device=dev, dtype=torch.int32)[None]).contiguous()
+    full_table = table[:, : prompt_pages + dec_pages].contiguous()
+    lens_h = [2048 + t + 1 for t in range(T)]
+    seq_lens = torch.tensor([[x] * B for x in lens_h], dtype=torch.int32, device=dev)  # [T][B]
+    tails = torch.stack([(ids + prompt_pages + t // 16) if x % 16 else torch.full_like(ids, -1)
+                         for t, x in enumerate(lens_h)]).contiguous()
+    status = kvz.new_status(dev)
+    meta = torch.zeros((L, P, hkv, 2), dtype=torch.int64, device=dev)
+    chunk = 32768  # granules (8 MiB)
+    worst_seq = L * (prompt_pages + dec_pages) * hkv * 32 * 256
+    nchunks = B * (worst_seq // (chunk * 256) + 2)
+    arena = torch.zeros(nchunks * chunk * 256, dtype=torch.uint8, device=dev)
+    alloc = kvz.Allocator(arena.numel(), chunk, B, hkv)
+    cursors = torch.zeros((B, 2), dtype=torch.int32, device=dev)
+    enc_ws = torch.empty(kvz.encode_workspace_size(hkv, B * max(16, L)), dtype=torch.uint8, device=dev)
+    # every layer's pages as one pool and one metadata array, so a page completion encodes
+    # all layers in one call (entries ordered by sequence, then layer: each sequence's
+    # groups land in its chunk in layer order, as with one call per layer)
+    raw_all = raw.view((L * P,) + tuple(raw.shape[2:]))
+    meta_all = meta.view((L * P,) + tuple(meta.shape[2:]))
+    lay_off = torch.arange(L, device=dev, dtype=torch.int32) * P
+    seqs = np.arange(B, dtype=np.int32)
+
+    def apply(updates):
+        if updates:
+            u = torch.tensor(updates, dtype=torch.int64)
+            kvz.apply_cursor_updates(u[:, 0].to(torch.int32).to(dev), u[:, 1].to(torch.int32).to(dev),
+                                     u[:, 2].to(torch.int32).to(dev), cursors)
+
+    # ---- prefill: encode every prompt page of every layer, 16 pages per sequence per call ----
+    for k0 in range(0, prompt_pages, 16):
+        n = min(16, prompt_pages - k0)
+        for layer in range(L):
+            ticket, ups = alloc.reserve(seqs, [n] * B)
+            apply(ups)
+            src = (ids[:, None] + torch.arange(k0, k0 + n, device=dev, dtype=torch.int32)[None]).reshape(-1).contiguous()
+            dseq = torch.arange(B, device=dev, dtype=torch.int32).repeat_interleave(n)
+            kvz.encode_pages(raw[layer], src, src, dseq, meta[layer], arena, cursors, status, workspace=enc_ws)
+            alloc.observe(ticket, cursors.cpu().numpy().view(np.uint32))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, int(status.item())
+
+    out_c = torch.empty((B, hq, 128), dtype=torch.float32, device=dev)
+    out_r = torch.empty_like(out_c)
+    ws_c = torch.empty(kvz.attention_workspace_size(hkv, B, hq, full_table.shape[1] + 1), dtype=torch.uint8, device=dev)
+    ws_r = torch.empty(kvz.attention_workspace_size(hkv, B, hq, table.shape[1]), dtype=torch.uint8, device=dev)
+    pin_cur = torch.empty((B, 2), dtype=torch.int32).pin_memory()
+    pending = None  # (ticket, event) of the last cursor snapshot in flight
+
+    def append(t):
+        j, pos = t // 16, t % 16
+        raw[:, (ids + prompt_pages + j).long(), :, :, pos, :] = new_kv[t]
+
+    def step_compressed(t):
+        nonlocal pending
+        append(t)
+        if lens_h[t] % 16 == 0:  # every sequence's tail page just filled: encode it in every layer
+            if pending is not None and pending[1].query():
+                alloc.observe(pending[0], pin_cur.numpy().view(np.uint32))
+                pending = None
+            ticket, ups = alloc.reserve(seqs, [L] * B)
+            apply(ups)
+            page = ids + prompt_pages + t // 16
+            src = (page[:, None] + lay_off[None, :]).reshape(-1).contiguous()  # [B][L]
+            dseq = torch.arange(B, device=dev, dtype=torch.int32).repeat_interleave(L)
+            kvz.encode_pages(raw_all, src, src, dseq, meta_all, arena, cursors, status, workspace=enc_ws)
+            pin_cur.copy_(cursors, non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record()
+            pending = (ticket, ev)
+        for layer in range(L):
+            kvz.decode_attention(qs[layer], full_table, seq_lens[t], tails[t], meta[layer], arena, raw[layer], out_c,
+                                 status, workspace=ws_c)
+
+    def step_raw(t):
+        append(t)
+        for layer in range(L):
+            kvz.decode_attention_raw(qs[layer], table, seq_lens[t], raw[layer], out_r, status, workspace=ws_r)
+
+    def run(step_fn):
+        times = []
+        for t in range(T):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            step_fn(t)
+            torch.cuda.synchronize()
+            times.append((time.perf_counter() - t0) * 1e6)
+        return times
+
+    # the raw loop re-appends the same tokens at the same places, so both loops see the same KV
+    with ClockSampler(local) as clk:
+        t_c = run(step_compressed)
+        t_r = run(step_raw)
+    clocks = clk.summary()
+    torch.cuda.synchronize()
+    st = int(status.item())
+    assert st == 0, st
+    identical = bool(torch.equal(out_c, out_r))  # last step: same pages, same split -> same bits
+    if pending is not None:
+        alloc.observe(pending[0], cursors.cpu().numpy().view(np.uint32))
+    stats = alloc.stats()
+    enc_steps = [t for t in range(T) if lens_h[t] % 16 == 0]
+    plain = [t for t in range(T) if lens_h[t] % 16 != 0]
+    meta_per_seq = L * (prompt_pages + dec_pages) * hkv * 16
+    used_per_seq = stats["used_bytes_bound"] / B
+    held_per_seq = stats["held_bytes"] / B
+    raw_per_seq = L * (2048 + T) * hkv * 2 * 128 * 2
+    budget = args.budget_gb * 1e9
+    logical = [L * B * lens_h[t] * hkv * 512 for t in range(T)]
+    med_c = statistics.median(t_c)
+    res = {
+        "workload": cfg.name, "decode_steps": T, "chunk_bytes": chunk * 256,
+        "timing": "wall time per step, synchronised (an engine reading logits every step); median over the steps",
+        "logical_GBps": round(world * statistics.mean(logical) / (med_c * 1e-6) / 1e9, 2),
+        "us_per_step": round(med_c, 1),
+        "us_per_step_mean": round(statistics.mean(t_c), 1),
+        "us_per_step_with_encode": round(statistics.median([t_c[t] for t in enc_steps]), 1),
+        "us_per_step_without_encode": round(statistics.median([t_c[t] for t in plain]), 1),
+        "raw_us_per_step": round(statistics.median(t_r), 1),
+        "raw_us_per_step_mean": round(statistics.mean(t_r), 1),
+        "speedup_vs_raw": round(statistics.mean(t_r) / statistics.mean(t_c), 4),
+        "bit_identical_last_step": identical,
+        "capacity": {"budget_bytes": budget, "raw_bytes_per_seq": raw_per_seq,
+                     "compressed_bytes_per_seq": round(used_per_seq + meta_per_seq),
+                     "compressed_bytes_per_seq_chunk_granular": round(held_per_seq + meta_per_seq),
+                     "raw_seqs": int(budget // raw_per_seq),
+                     "compressed_seqs": int(budget // (used_per_seq + meta_per_seq)),
+                     "compressed_seqs_chunk_granular": int(budget // (held_per_seq + meta_per_seq))},
+        "clocks": clocks,
+        # attention + merge per layer per step, plus 4 encode launches (prepare, sizes, scan,
+        # pack) for all layers at each page completion
+        "gpu_launches": T * L * 2 + len(enc_steps) * 4,
+    }
+    del raw, arena, meta, new_kv
+    torch.cuda.empty_cache()
+    return res
+
+
+def codec_sweep(dev, sizes_mb) -> list[dict]:
+    """Encode and standalone-decode throughput on `sizes_mb` MB of BF16 pages whose
+    per-block exponent spread is uniform in 8..20 (so about 58% of blocks qualify).
+    encode GB/s = BF16 bytes in / time; decode GB/s = BF16 bytes out / time."""
+    import decode_attention_value_gb300 as kvz
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    hkv = 8
+    rows = []
+    for mb in sizes_mb:
+        pages = mb * (1 << 20) // (hkv * 8192)
+        cfg = kvgen.KVConfig(f"spread-sweep-{mb}MB", 1, 1, 32, hkv, pages, spread=(8, 20), seed=40 + mb)
+        pool = kvgen.gen_pages(cfg, pages, device=dev)
+        src = torch.arange(pages, dtype=torch.int32, device=dev)
+        seq = torch.zeros_like(src)
+        meta = torch.zeros((pages, hkv, 2), dtype=torch.int64, device=dev)
+        arena = torch.zeros(pages * hkv * 8192, dtype=torch.uint8, device=dev)
+        cur0 = torch.tensor([[0, arena.numel() // 256]], dtype=torch.int32, device=dev)
+        cur = cur0.clone()
+        st = kvz.new_status(dev)
+        ws = torch.empty(kvz.encode_workspace_size(hkv, pages), dtype=torch.uint8, device=dev)
+        out = torch.empty_like(pool)
+
+        def enc(k):
+            kvz.encode_pages(pool, src, src, seq, meta, arena, cur, st, workspace=ws)
+
+        def dec(k):
+            kvz.decode_blocks(meta, arena, src, out, st)
+
+        cur.copy_(cur0)
+        enc(0)
+        dec(0)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0 and torch.equal(out.view(torch.int16), pool.view(torch.int16))
+        reps = 5 if mb <= 1024 else 3
+        e_ms = per_launch_ms(enc, reps, flush, prep=lambda k: cur.copy_(cur0))
+        d_ms = per_launch_ms(dec, reps, flush)
+        nbytes = pool.numel() * 2
+        tags = (meta >> 32) & 0xFFFFFFFF
+        raw = sum(int((((tags >> (8 * j)) & 0xFF) == 0xFF).sum()) for j in range(4))
+        rows.append({"MB": mb, "encode_GBps": round(nbytes / e_ms / 1e6, 1), "decode_GBps": round(nbytes / d_ms / 1e6, 1),
+                     "encode_us": round(e_ms * 1e3, 1), "decode_us": round(d_ms * 1e3, 1),
+                     "compressed_fraction": round(1 - raw / (tags.numel() * 4), 4)})
+        del pool, meta, arena, out, ws
+        torch.cuda.empty_cache()
+    return rows
+
+
+def public(d: dict) -> dict:
+    """A measurement dict without its private handles."""
+    return {k: v for k, v in d.items() if not k.startswith("_")}
 
 
 class GaCopies:
@@ -1133,255 +1340,6 @@ def run_serve(args, dist, rank, world, local):
         dist.destroy_process_group()
 
 
-def run_stack(args, cfg, dist, rank, world, local):
-    """Full-stack decode step: every layer of the configuration, each with its own seeded
-    KV (so a step reads all layers' caches once, far more than L2), attention in layer
-    order.  Reports µs per full step compressed vs raw and the compressed fraction."""
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    layers = [Workload(cfg, 1, layer=layer, dev=dev) for layer in range(cfg.layers)]
-    # one block table for every layer, as a paged KV cache keeps it (each layer has its own
-    # pools and metadata behind the same page ids), and one attention workspace, the scratch
-    # buffer a serving loop hands to each layer's call in turn
-    for W in layers[1:]:
-        assert torch.equal(W.table, layers[0].table) and torch.equal(W.seq_lens, layers[0].seq_lens)
-        W.table, W.full, W.tail, W.raw_table = layers[0].table, layers[0].full, layers[0].tail, layers[0].raw_table
-        W.seq_lens = layers[0].seq_lens
-        W.ws_c, W.ws_r = layers[0].ws_c, layers[0].ws_r
-    K = args.steps
-
-    def step_c(k):
-        for W in layers:
-            W.step_c(0)
-
-    def step_r(k):
-        for W in layers:
-            W.step_r(0)
-
-    for k in range(args.warmup):
-        step_c(k)
-        step_r(k)
-    torch.cuda.synchronize()
-    for W in layers:
-        if int(W.status.item()) != 0:
-            raise RuntimeError(f"status {int(W.status.item())}")
-    identical = all(torch.equal(W.out, W.out_raw) for W in layers)
-    g_c, g_r = graph_of(step_c, K), graph_of(step_r, K)
-    g_c.replay()
-    g_r.replay()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        soak_until = time.time() + 0.5
-        while time.time() < soak_until:
-            g_c.replay()
-            torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
-        ms_c = time_graph(g_c)
-        ms_r = time_graph(g_r)
-    clocks = clk.summary()
-    ms_c, ms_r = max_over_ranks(dist, [ms_c, ms_r], device=dev)
-    us_c, us_r = ms_c * 1e3 / K, ms_r * 1e3 / K
-    logical = sum(W.logical_bytes for W in layers)
-    alg = sum(W.alg_bytes_c for W in layers)
-    blocks = sum(W.blocks for W in layers)
-    raw_blocks = sum(W.raw_blocks for W in layers)
-    block_bytes = sum(W.block_bytes for W in layers)
-    peak, peak_kind = measured_peaks()
-    line = {
-        "metric": METRIC, "value": round(job_throughput(world, logical, K, ms_c), 2), "unit": "GB/s",
-        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(us_c / 1e3, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": cfg.name + "-full-stack", "layers": cfg.layers, "batch": cfg.batch, "q_heads": cfg.hq,
-                   "kv_heads": cfg.hkv, "head_dim": 128, "context_tokens": cfg.full_pages * 16,
-                   "tail_tokens": f"{cfg.tail_min}..{cfg.tail_max}", "parallelism": f"replicas{world}",
-                   "l2": f"inputs larger than L2: {cfg.layers} layers of separate KV ({block_bytes / 1e9:.1f} GB compressed)"},
-        "us_per_step": round(us_c, 2), "raw_us_per_step": round(us_r, 2), "speedup_vs_raw": round(us_r / us_c, 4),
-        "compressed_fraction": round(1 - raw_blocks / blocks, 5),
-        "compressed_bytes_ratio": round(block_bytes / (blocks * 1024), 5),
-        "expected_speedup_from_fraction": round(blocks * 1024 / block_bytes, 4),
-        "bit_identical_compressed_vs_raw": identical,
-        "roofline": {"bound": "hbm", "achieved": round(alg / (us_c * 1e-6) / 1e9, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(alg / (us_c * 1e-6) / 1e9 / peak, 4), "traffic": None, "peak_kind": peak_kind},
-        "clocks": clocks, "gpu_launches": 2 * cfg.layers * K,
-    }
-    if rank == 0 and not args.no_cpu_baseline:
-        # the oracle on a sample of one layer (every layer has the same shape), scaled to
-        # the full stack: µs per step = layers x layer logical bytes / oracle rate
-        gbps, secs, nseq, passes, threads = oracle_sample(cfg, args.cpu_budget)
-        line["cpu_baseline"] = {
-            "value": round(gbps, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "us_per_step": round(logical / (gbps * 1e9) * 1e6, 1),
-            "sample": f"{nseq} of {cfg.batch} sequences x {cfg.hkv} KV heads of one layer (decode of compressed "
-                      f"pages + fp64 attention), {passes} passes, {secs:.1f} s; us_per_step scales the rate to "
-                      f"the {cfg.layers}-layer step"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-
-
-def run_stream(args, cfg, dist, rank, world, local):
-    """Streaming decode, Qwen3-8B shape (36 layers, 32/8 heads, batch 64): a 2048-token
-    prompt (128 pages per sequence and layer, encoded at prefill), then `decode_steps`
-    steps that each append one token per sequence and layer and run attention in every
-    layer.  When a sequence's tail page fills (every 16th step) the page is encoded in
-    every layer before that step's attention, into chunk slots handed out by the host
-    allocator; per-step latency includes the encoding.  The same loop on raw pages gives
-    the uncompressed step time.  At the end: sequences that fit in the KV budget."""
-    torch.cuda.set_device(local)
-    import decode_attention_value_gb300 as kvz
-
-    dev = torch.device("cuda", local)
-    B, L, hkv, hq = cfg.batch, cfg.layers, cfg.hkv, cfg.hq
-    prompt_pages = cfg.full_pages
-    T = args.decode_steps
-    dec_pages = (T + 15) // 16
-    ppseq = prompt_pages + dec_pages + 1  # raw page slots per sequence: prompt, decode pages, spare
-    P = B * ppseq
-    # raw pool of every layer; page b*ppseq + k is sequence b's k-th page (meta ids are the same)
-    raw = torch.empty((L, P, hkv, 2, 16, 128), dtype=torch.bfloat16, device=dev)
-    for layer in range(L):
-        raw[layer] = kvgen.gen_pages(cfg, P, layer=layer, device=dev)
-    new_kv = kvgen.gen_new_tokens(cfg, T, device=dev)  # [T][L][B][hkv][2][128]
-    qs = [kvgen.gen_q(cfg, layer=layer).to(dev) for layer in range(L)]
-    ids = torch.arange(B, device=dev, dtype=torch.int32) * ppseq
-    table = (ids[:, None] + torch.arange(ppseq - 1, device=dev, dtype=torch.int32)[None]).contiguous()
-    full_table = table[:, : prompt_pages + dec_pages].contiguous()
-    lens_h = [2048 + t + 1 for t in range(T)]
-    seq_lens = torch.tensor([[x] * B for x in lens_h], dtype=torch.int32, device=dev)  # [T][B]
-    tails = torch.stack([(ids + prompt_pages + t // 16) if x % 16 else torch.full_like(ids, -1)
-                         for t, x in enumerate(lens_h)]).contiguous()
-    status = kvz.new_status(dev)
-    meta = torch.zeros((L, P, hkv, 2), dtype=torch.int64, device=dev)
-    chunk = 32768  # granules (8 MiB)
-    worst_seq = L * (prompt_pages + dec_pages) * hkv * 32 * 256
-    nchunks = B * (worst_seq // (chunk * 256) + 2)
-    arena = torch.zeros(nchunks * chunk * 256, dtype=torch.uint8, device=dev)
-    alloc = kvz.Allocator(arena.numel(), chunk, B, hkv)
-    cursors = torch.zeros((B, 2), dtype=torch.int32, device=dev)
-    enc_ws = torch.empty(kvz.encode_workspace_size(hkv, B * max(16, L)), dtype=torch.uint8, device=dev)
-    # every layer's pages as one pool and one metadata array, so a page completion encodes
-    # all layers in one call (entries ordered by sequence, then layer: each sequence's
-    # groups land in its chunk in layer order, as with one call per layer)
-    raw_all = raw.view((L * P,) + tuple(raw.shape[2:]))
-    meta_all = meta.view((L * P,) + tuple(meta.shape[2:]))
-    lay_off = torch.arange(L, device=dev, dtype=torch.int32) * P
-    seqs = np.arange(B, dtype=np.int32)
-
-    def apply(updates):
-        if updates:
-            u = torch.tensor(updates, dtype=torch.int64)
-            kvz.apply_cursor_updates(u[:, 0].to(torch.int32).to(dev), u[:, 1].to(torch.int32).to(dev),
-                                     u[:, 2].to(torch.int32).to(dev), cursors)
-
-    # ---- prefill: encode every prompt page of every layer, 16 pages per sequence per call ----
-    for k0 in range(0, prompt_pages, 16):
-        n = min(16, prompt_pages - k0)
-        for layer in range(L):
-            ticket, ups = alloc.reserve(seqs, [n] * B)
-            apply(ups)
-            src = (ids[:, None] + torch.arange(k0, k0 + n, device=dev, dtype=torch.int32)[None]).reshape(-1).contiguous()
-            dseq = torch.arange(B, device=dev, dtype=torch.int32).repeat_interleave(n)
-            kvz.encode_pages(raw[layer], src, src, dseq, meta[layer], arena, cursors, status, workspace=enc_ws)
-            alloc.observe(ticket, cursors.cpu().numpy().view(np.uint32))
-    torch.cuda.synchronize()
-    assert int(status.item()) == 0, int(status.item())
-
-    out_c = torch.empty((B, hq, 128), dtype=torch.float32, device=dev)
-    out_r = torch.empty_like(out_c)
-    ws_c = torch.empty(kvz.attention_workspace_size(hkv, B, hq, full_table.shape[1] + 1), dtype=torch.uint8, device=dev)
-    ws_r = torch.empty(kvz.attention_workspace_size(hkv, B, hq, table.shape[1]), dtype=torch.uint8, device=dev)
-    pin_cur = torch.empty((B, 2), dtype=torch.int32).pin_memory()
-    pending = None  # (ticket, event) of the last cursor snapshot in flight
-
-    def append(t):
-        j, pos = t // 16, t % 16
-        raw[:, (ids + prompt_pages + j).long(), :, :, pos, :] = new_kv[t]
-
-    def step_compressed(t):
-        nonlocal pending
-        append(t)
-        if lens_h[t] % 16 == 0:  # every sequence's tail page just filled: encode it in every layer
-            if pending is not None and pending[1].query():
-                alloc.observe(pending[0], pin_cur.numpy().view(np.uint32))
-                pending = None
-            ticket, ups = alloc.reserve(seqs, [L] * B)
-            apply(ups)
-            page = ids + prompt_pages + t // 16
-            src = (page[:, None] + lay_off[None, :]).reshape(-1).contiguous()  # [B][L]
-            dseq = torch.arange(B, device=dev, dtype=torch.int32).repeat_interleave(L)
-            kvz.encode_pages(raw_all, src, src, dseq, meta_all, arena, cursors, status, workspace=enc_ws)
-            pin_cur.copy_(cursors, non_blocking=True)
-            ev = torch.cuda.Event()
-            ev.record()
-            pending = (ticket, ev)
-        for layer in range(L):
-            kvz.decode_attention(qs[layer], full_table, seq_lens[t], tails[t], meta[layer], arena, raw[layer], out_c,
-                                 status, workspace=ws_c)
-
-    def step_raw(t):
-        append(t)
-        for layer in range(L):
-            kvz.decode_attention_raw(qs[layer], table, seq_lens[t], raw[layer], out_r, status, workspace=ws_r)
-
-    def run(step_fn):
-        times = []
-        for t in range(T):
-            torch.cuda.synchronize()
-            t0 = time.perf_counter()
-            step_fn(t)
-            torch.cuda.synchronize()
-            times.append((time.perf_counter() - t0) * 1e6)
-        return times
-
-    # the raw loop re-appends the same tokens at the same places, so both loops see the same KV
-    with ClockSampler(local) as clk:
-        t_c = run(step_compressed)
-        t_r = run(step_raw)
-    clocks = clk.summary()
-    torch.cuda.synchronize()
-    st = int(status.item())
-    assert st == 0, st
-    identical = bool(torch.equal(out_c, out_r))  # last step: same pages, same split -> same bits
-    if pending is not None:
-        alloc.observe(pending[0], cursors.cpu().numpy().view(np.uint32))
-    stats = alloc.stats()
-    enc_steps = [t for t in range(T) if lens_h[t] % 16 == 0]
-    plain = [t for t in range(T) if lens_h[t] % 16 != 0]
-    meta_per_seq = L * (prompt_pages + dec_pages) * hkv * 16
-    used_per_seq = stats["used_bytes_bound"] / B
-    held_per_seq = stats["held_bytes"] / B
-    raw_per_seq = L * (2048 + T) * hkv * 2 * 128 * 2
-    budget = args.budget_gb * 1e9
-    logical = [L * B * lens_h[t] * hkv * 512 for t in range(T)]
-    mean_c = statistics.mean(t_c)
-    line = {
-        "metric": METRIC, "value": round(statistics.mean(logical) / (mean_c * 1e-6) / 1e9, 2), "unit": "GB/s",
-        "n_gpus": world, "steps": T, "warmup": 0, "ms_per_step": round(mean_c / 1e3, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": cfg.name, "layers": L, "batch": B, "q_heads": hq, "kv_heads": hkv, "head_dim": 128,
-                   "prompt_tokens": 2048, "decode_steps": T, "chunk_bytes": chunk * 256,
-                   "timing": "wall time per step, synchronised (an engine reading logits every step)"},
-        "us_per_step": round(mean_c, 1),
-        "us_per_step_with_encode": round(statistics.mean([t_c[t] for t in enc_steps]), 1),
-        "us_per_step_without_encode": round(statistics.mean([t_c[t] for t in plain]), 1),
-        "raw_us_per_step": round(statistics.mean(t_r), 1),
-        "speedup_vs_raw": round(statistics.mean(t_r) / mean_c, 4),
-        "bit_identical_last_step": identical,
-        "capacity": {"budget_bytes": budget, "raw_bytes_per_seq": raw_per_seq,
-                     "compressed_bytes_per_seq": round(used_per_seq + meta_per_seq),
-                     "compressed_bytes_per_seq_chunk_granular": round(held_per_seq + meta_per_seq),
-                     "raw_seqs": int(budget // raw_per_seq),
-                     "compressed_seqs": int(budget // (used_per_seq + meta_per_seq)),
-                     "compressed_seqs_chunk_granular": int(budget // (held_per_seq + meta_per_seq))},
-        "clocks": clocks,
-        # attention + merge per layer per step, plus 4 encode launches (prepare, sizes, scan,
-        # pack) for all layers at each page completion
-        "gpu_launches": T * L * 2 + len(enc_steps) * 4,
-    }
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-
-
 def run_spread_sweep(args, dist, rank, local):
     """The C4 shape (B=2, 8192 full pages + tail, 32/8 heads) with every block's exponent
     spread fixed at S = 8..20, which moves the compressed fraction from 1 to 0 (eligible
@@ -1422,104 +1380,223 @@ def run_spread_sweep(args, dist, rank, local):
         dist.destroy_process_group()
 
 
-def run_sweep(args, dist, rank, local):
-    """Encode and standalone-decode throughput over 64 MB .. 4 GB of BF16 pages whose
-    per-block exponent spread is uniform in 8..20 (so about 58% of blocks qualify).
-    encode GB/s = BF16 bytes in / time; decode GB/s = BF16 bytes out / time."""
+def cpu_baseline_line(cfg: kvgen.KVConfig, budget: float, step_logical: int, layers: int = 1) -> dict:
+    """The oracle (decode of compressed pages + fp64 attention) on the host cores, on a
+    bounded sample of one layer of the workload, with one-core and encoder figures."""
+    gbps, secs, nseq, passes, threads = oracle_sample(cfg, budget)
+    cpu = {"value": round(gbps, 3), "unit": "GB/s", "cores": threads, "kind": "oracle",
+           "us_per_step": round(step_logical / (gbps * 1e9) * 1e6, 1),
+           "sample": f"{nseq} of {cfg.batch} sequences x {cfg.hkv} KV heads of one layer (decode of compressed pages "
+                     f"+ fp64 attention), {passes} passes, {secs:.1f} s"
+                     + (f"; us_per_step scales the rate to the {layers}-layer step" if layers > 1 else "")}
+    g1, s1, n1, p1, _ = oracle_sample(cfg, min(4.0, budget / 3), threads=1)
+    cpu["extra"] = {"attention_1core_GBps": round(g1, 3),
+                    "attention_1core_sample": f"{n1} sequences, {p1} passes, {s1:.1f} s",
+                    "encode_1core_GBps": round(oracle_encode_rate(cfg), 3),
+                    "encode_sample": "64 MiB of the layer's pages, scalar oracle encoder, one thread",
+                    "encode_allcores_GBps": round(oracle_encode_rate(cfg, 32, threads), 3),
+                    "encode_allcores_sample": f"{threads} threads x 32 MiB of the layer's pages"}
+    return cpu
+
+
+def base_line(workload: str, world: int, args, value: float, us_step: float) -> dict:
+    return {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(us_step / 1e3, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_dict(workload, world)}
+
+
+def run_default(args, dist, rank, world, local):
+    """Headline: the full 32-layer 8K decode step (C2).  Extra keys: one C1 layer, one
+    layer of the 8K stack, one 131072-token layer with the codec throughput at 1-4 GB,
+    and the streaming C3 step with page-completion encodes and the capacity count."""
     torch.cuda.set_device(local)
-    import decode_attention_value_gb300 as kvz
-
     dev = torch.device("cuda", local)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    hkv = 8
-    rows = []
-    mb = 64
-    while mb <= 4096:
-        pages = mb * (1 << 20) // (hkv * 8192)
-        cfg = kvgen.KVConfig(f"spread-sweep-{mb}MB", 1, 1, 32, hkv, pages, spread=(8, 20), seed=40 + mb)
-        pool = kvgen.gen_pages(cfg, pages, device=dev)
-        src = torch.arange(pages, dtype=torch.int32, device=dev)
-        seq = torch.zeros_like(src)
-        meta = torch.zeros((pages, hkv, 2), dtype=torch.int64, device=dev)
-        arena = torch.zeros(pages * hkv * 8192, dtype=torch.uint8, device=dev)
-        cur0 = torch.tensor([[0, arena.numel() // 256]], dtype=torch.int32, device=dev)
-        cur = cur0.clone()
-        st = kvz.new_status(dev)
-        ws = torch.empty(kvz.encode_workspace_size(hkv, pages), dtype=torch.uint8, device=dev)
-        out = torch.empty_like(pool)
-
-        def enc(k):
-            kvz.encode_pages(pool, src, src, seq, meta, arena, cur, st, workspace=ws)
-
-        def dec(k):
-            kvz.decode_blocks(meta, arena, src, out, st)
-
-        cur.copy_(cur0)
-        enc(0)
-        dec(0)
-        torch.cuda.synchronize()
-        assert int(st.item()) == 0 and torch.equal(out.view(torch.int16), pool.view(torch.int16))
-        reps = 5 if mb <= 1024 else 3
-        e_ms = per_launch_ms(enc, reps, flush, prep=lambda k: cur.copy_(cur0))
-        d_ms = per_launch_ms(dec, reps, flush)
-        nbytes = pool.numel() * 2
-        tags = (meta >> 32) & 0xFFFFFFFF
-        raw = sum(int((((tags >> (8 * j)) & 0xFF) == 0xFF).sum()) for j in range(4))
-        rows.append({"MB": mb, "encode_GBps": round(nbytes / e_ms / 1e6, 1), "decode_GBps": round(nbytes / d_ms / 1e6, 1),
-                     "encode_us": round(e_ms * 1e3, 1), "decode_us": round(d_ms * 1e3, 1),
-                     "compressed_fraction": round(1 - raw / (tags.numel() * 4), 4)})
-        del pool, meta, arena, out, ws
+    S = measure_stack(args, dev, local, dist, world, rank)
+    extras = {}
+    if not args.no_extras:
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        for key, wl, df, codec in (("at_8k_context", "c2-layer", True, True), ("c1_layer", "c1", True, True),
+                                   ("c4_layer", "c4", False, False)):
+            r = measure_layer(layer_cfg(wl), args, dev, local, dist, world, rank, flush, decompress_first=df,
+                              codec=codec)
+            r["roofline"]["traffic"] = profiled_traffic(wl)
+            del r["_W"]
+            torch.cuda.empty_cache()
+            extras[key] = public(r)
+        rows = codec_sweep(dev, [1024, 4096])
+        extras["c4_layer"]["codec_sweep"] = rows
+        extras["c4_layer"]["encode_GBps_max"] = max(r["encode_GBps"] for r in rows)
+        extras["c4_layer"]["decode_GBps_max"] = max(r["decode_GBps"] for r in rows)
+        del flush
         torch.cuda.empty_cache()
-        mb *= 2
+        extras["c3_streaming"] = measure_stream(args, dev, local, world)
+    cpu = None
+    cfg1 = kvgen.KVConfig(**{**kvgen.C2.__dict__, "layers": 1})
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_line(cfg1, args.cpu_budget, int(S["logical_GB_per_step"] * 1e9), kvgen.C2.layers)
+    line = base_line("c2", world, args, S["value"], S["us_per_step"])
+    line.update({k: v for k, v in S.items() if k not in ("value", "ms_per_step")})
+    if "at_8k_context" in extras:
+        line["encode_GBps"] = extras["at_8k_context"]["encode_GBps"]
+        line["decode_GBps"] = extras["at_8k_context"]["decode_GBps"]
+        line["codec_note"] = "encode / standalone decode of one layer of this stack (BF16 GB/s in / out)"
+    line["cpu_baseline"] = cpu
+    line.update(extras)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_layer(args, dist, rank, world, local):
+    """One layer (C1, one layer of C2, or one C4 layer) as the headline."""
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cfg = layer_cfg(args.workload)
+    r = measure_layer(cfg, args, dev, local, dist, world, rank, decompress_first=True, codec=True)
+    W = r.pop("_W")
+    e2e = stack_e2e([W], args.steps, dev, dist, world)
+    line = base_line(args.workload, world, args, r["logical_GBps"], r["us_per_step"])
+    roof = r.pop("roofline")
+    line["roofline"] = {"bound": "hbm", "achieved": roof["achieved"], "peak": roof["peak"], "unit": "GB/s",
+                        "frac": roof["frac"], "traffic": profiled_traffic(args.workload),
+                        "peak_kind": roof["peak_kind"], "kernel": "k_attn<12-bit groups> + k_attn_merge",
+                        "launch_us": r["us_per_step"],
+                        "algorithmic_bytes_per_launch": roof["algorithmic_bytes_per_launch"]}
+    line.update({k: v for k, v in r.items() if k not in ("logical_GBps",)})
+    line["e2e"] = e2e
+    line["gpu_launches"] = 2 * args.steps
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_line(cfg, args.cpu_budget, W.logical_bytes)
+    line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_stream(args, dist, rank, world, local):
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    r = measure_stream(args, dev, local, world)
+    line = base_line("c3", world, args, r["logical_GBps"], r["us_per_step"])
+    line["steps"], line["warmup"] = r["decode_steps"], 0
+    line.update({k: v for k, v in r.items() if k != "logical_GBps"})
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_sweep(args, dist, rank, local):
+    torch.cuda.set_device(local)
+    rows = codec_sweep(torch.device("cuda", local), [64 << k for k in range(7)])
     if rank == 0:
         print(json.dumps({"metric": "encode / standalone-decode GB/s sweep", "unit": "GB/s", "rows": rows,
                           "data": "synthetic", "flush": "L2 read-flushed before each call"}), flush=True)
 
 
-def run_reference(args, cfg, dist, rank, world):
-    """The CPU oracle as it stands, on the host cores: each step a bounded sample."""
+def run_reference(args, dist, rank, world):
+    """The CPU oracle as it stands, on the host cores, on the configuration the GPU arm
+    measures: each step a bounded sample of that workload (sequences of one layer; for
+    the 32-layer stack every layer has the same shape and distributions)."""
+    if args.sweep or args.spread_sweep or args.format != "zf" or args.workload in ("c3", "serve"):
+        sys.stderr.write("--impl reference times the CPU oracle on the attention workloads c2, c2-layer, c1 and c4 "
+                         "only; it has no oracle counterpart for the requested mode\n")
+        if dist:
+            dist.destroy_process_group()
+        sys.exit(2)
     if rank != 0:
         if dist:
             dist.destroy_process_group()
         return
+    wl = args.workload
+    cfg = layer_cfg("c2-layer" if wl == "c2" else wl)
     K, Wm = args.steps, args.warmup
     per_step_budget = max(0.5, min(4.0, 150.0 / max(1, K + Wm)))
-    vals = []
-    secs = []
+    vals, secs = [], []
     nseq = threads = 0
     for k in range(Wm + K):
         gbps, dt, nseq, passes, threads = oracle_sample(cfg, per_step_budget, seqs_max=cfg.batch)
         if k >= Wm:
             vals.append(gbps)
             secs.append(dt)
-    value = statistics.mean(vals)
+    value = statistics.median(vals)
+    lay = kvgen.gen_layout(cfg)
+    layer_logical = kvgen.logical_kv_bytes(cfg, lay["seq_lens"])
+    layers = kvgen.C2.layers if wl == "c2" else 1
+    full_step_ms = layers * layer_logical / (value * 1e9) * 1e3
     logical_per_seq = (cfg.full_pages * 16 + (cfg.tail_min + cfg.tail_max) / 2) * cfg.hkv * 512
     line = {
-        "impl": "reference",
-        "metric": METRIC,
-        "value": round(value, 4),
-        "unit": "GB/s",
-        "n_gpus": world,
-        "steps": K,
-        "warmup": Wm,
-        "ms_per_step": round(1e3 * statistics.mean(secs), 3),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "f64",
-        "data": "synthetic",
-        "config": {"workload": cfg.name, "batch": cfg.batch, "q_heads": cfg.hq, "kv_heads": cfg.hkv,
-                   "head_dim": 128, "page_tokens": 16, "context_tokens": cfg.full_pages * 16,
-                   "parallelism": "host"},
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": Wm, "ms_per_step": round(1e3 * statistics.median(secs), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(wl, world),
+        "full_step_equivalent_ms": round(full_step_ms, 1),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "kind": "oracle", "cores": threads,
-                         "sample": f"{nseq} sequence(s) x {cfg.hkv} KV heads per pass, repeated for "
+                         "sample": f"{nseq} sequence(s) x {cfg.hkv} KV heads of one layer per pass, repeated for "
                                    f"~{per_step_budget:.1f} s per step (~{nseq * logical_per_seq / 1e6:.0f} MB "
-                                   "logical KV per pass)"},
+                                   "logical KV per pass); value = median over the steps"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kvz", choices=["kvz", "reference"])
+    ap.add_argument("--workload", default="c2", choices=["c2", "c2-layer", "c1", "c4", "c3", "serve"],
+                    help="c2: the full 32-layer 8K step (default headline); c2-layer / c1 / c4: one layer as the "
+                         "headline; c3: streaming decode with page-completion encodes; serve: toy admission loop")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="c2: skip the extra keys (C1 layer, 8K layer, C4 layer and codec points, C3 streaming)")
+    ap.add_argument("--serve-budget-gb", type=float, default=4.0, help="serve: KV budget of both caches (1e9 B)")
+    ap.add_argument("--serve-requests", type=int, default=256, help="serve: requests in the queue")
+    ap.add_argument("--budget-gb", type=float, default=60.0, help="KV budget for the c3 capacity count (1e9 B)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="encode / standalone-decode throughput over 64 MB .. 4 GB of pages (exponent-spread KV)")
+    ap.add_argument("--spread-sweep", action="store_true",
+                    help="long-context layer (B=2, 131072 tokens) with the per-block exponent spread fixed at each "
+                         "of 8..20: compressed fraction and attention time, compressed vs raw")
+    ap.add_argument("--copies", type=int, default=3)
+    ap.add_argument("--format", default="zf", choices=["zf", "ga", "f8e4", "f8e5"],
+                    help="ga: group-adaptive additive tiles; f8e4 / f8e5: completed pages converted to FP8 "
+                         "E4M3 / E5M2 and coded; instead of 12-bit block groups (c1, c2-layer, c4)")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-steps", type=int, default=256, help="decode steps of the c3 streaming run")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    dist, rank, world, local = dist_setup()
+    # the reference arm first: no GPU mode may run under its name
+    if args.impl == "reference":
+        return run_reference(args, dist, rank, world)
+    if args.sweep:
+        return run_sweep(args, dist, rank, local)
+    if args.spread_sweep:
+        return run_spread_sweep(args, dist, rank, local)
+    if args.workload == "c3":
+        return run_stream(args, dist, rank, world, local)
+    if args.workload == "serve":
+        return run_serve(args, dist, rank, world, local)
+    if args.format != "zf":
+        if args.workload == "c2":
+            ap.error("the tile formats run on single layers: --workload c1, c2-layer or c4")
+        return run_ga(args, layer_cfg(args.workload), dist, rank, world, local)
+    if args.workload == "c2":
+        return run_default(args, dist, rank, world, local)
+    return run_layer(args, dist, rank, world, local)
 
 
 if __name__ == "__main__":

@@ -104,6 +104,102 @@ def test_host_rejects_bad_arguments(kvz):
     assert lib.kvz_apply_cursor_updates(None, None, None, 0, None, 0, None) == 0
 
 
+def test_host_rejects_bad_tile_arguments(kvz):
+    """The group-adaptive and FP8 tile calls check their arguments on the host as the
+    12-bit calls do: shapes, formats, null pointers, alignment (64-byte arena, 4/8-byte
+    entries, 16-byte bases for the encoders) and the encoder workspace, all before any
+    launch (fake pointers are never dereferenced)."""
+    lib = kvz.lib()
+    E = dict(inval=-1, unsup=-2, align=-3, ws=-4)
+    fake = 1 << 20
+    d, d64, d0 = _dims(kvz), _dims(kvz, d=64), _dims(kvz, hkv=0)
+    M = 1 << 20
+    # ---- calibration: shapes, null bases, null sample, misaligned pool / sample ----
+    assert lib.kvz_ga_calibrate(d64, fake, 1, fake, 1, fake, fake, None) == E["unsup"]
+    assert lib.kvz_ga_calibrate(d0, fake, 1, fake, 1, fake, fake, None) == E["inval"]
+    assert lib.kvz_ga_calibrate(d, fake, 1, fake, -1, fake, fake, None) == E["inval"]
+    assert lib.kvz_ga_calibrate(d, fake, 1, fake, 1, None, fake, None) == E["inval"]
+    assert lib.kvz_ga_calibrate(d, fake, 1, None, 1, fake, fake, None) == E["inval"]
+    assert lib.kvz_ga_calibrate(d, fake + 8, 1, fake, 1, fake, fake, None) == E["align"]
+    assert lib.kvz_ga_calibrate(d, fake, 1, fake + 2, 1, fake, fake, None) == E["align"]
+    for fmt in (0, 3, -1):  # only KVZ_F8_E4M3 (1) and KVZ_F8_E5M2 (2) exist
+        assert lib.kvz_f8_calibrate(d, fmt, fake, 1, fake, 1, fake, fake, None) == E["inval"]
+    assert lib.kvz_f8_calibrate(d64, 1, fake, 1, fake, 1, fake, fake, None) == E["unsup"]
+    assert lib.kvz_f8_calibrate(d, 2, fake, 1, fake, 1, None, fake, None) == E["inval"]
+    assert lib.kvz_f8_calibrate(d, 1, fake + 8, 1, fake, 1, fake, fake, None) == E["align"]
+
+    # ---- encoders: n = 0 no-op, bad n, nulls, alignment of every buffer, short workspace ----
+    def ga_enc(dims=d, pool=fake, bases=fake, src=fake, n=10, meta=fake, arena=fake, cur=fake, ws=fake,
+               ws_bytes=M, status=fake):
+        return lib.kvz_ga_encode_pages(dims, pool, 64, bases, src, src, src, n, meta, 64, arena, M, cur, 4, ws,
+                                       ws_bytes, status, None)
+
+    def f8_enc(fmt=1, dims=d, pool=fake, bases=fake, src=fake, n=10, meta=fake, arena=fake, cur=fake, ws=fake,
+               ws_bytes=M, status=fake):
+        return lib.kvz_f8_encode_pages(dims, fmt, pool, 64, bases, src, src, src, n, meta, 64, arena, M, cur, 4,
+                                       ws, ws_bytes, status, None)
+
+    for enc in (ga_enc, f8_enc):
+        assert enc(n=0, pool=None, bases=None, src=None, meta=None, arena=None, cur=None, ws=None,
+                   status=None) == 0
+        assert enc(dims=d64) == E["unsup"]
+        assert enc(dims=d0) == E["inval"]
+        assert enc(n=-1) == E["inval"]
+        for k in ("pool", "bases", "src", "meta", "arena", "cur", "ws", "status"):
+            assert enc(**{k: None}) == E["inval"], k
+        assert enc(pool=fake + 8) == E["align"]
+        assert enc(bases=fake + 8) == E["align"]   # bases: 16-byte aligned
+        assert enc(meta=fake + 4) == E["align"]    # 4-byte entries read in K/V pairs: 8-byte aligned
+        assert enc(arena=fake + 32) == E["align"]  # 64-byte granules
+        assert enc(cur=fake + 4) == E["align"]
+        assert enc(ws=fake + 8) == E["align"]
+        assert enc(ws_bytes=kvz.encode_workspace_size(8, 10) - 1) == E["ws"]
+    for fmt in (0, 3):
+        assert f8_enc(fmt=fmt) == E["inval"]
+
+    # ---- standalone decoders ----
+    def ga_dec(meta=fake, arena=fake, bases=fake, page=fake, n=4, out=fake, status=fake):
+        return lib.kvz_ga_decode_blocks(d, meta, 64, arena, M, bases, page, n, out, status, None)
+
+    def f8_dec(fmt=2, meta=fake, arena=fake, bases=fake, page=fake, n=4, out=fake, status=fake):
+        return lib.kvz_f8_decode_blocks(d, fmt, meta, 64, arena, M, bases, page, n, out, status, None)
+
+    for dec in (ga_dec, f8_dec):
+        assert dec(n=0, meta=None, arena=None, bases=None, page=None, out=None, status=None) == 0
+        assert dec(n=-1) == E["inval"]
+        for k in ("meta", "arena", "bases", "page", "out", "status"):
+            assert dec(**{k: None}) == E["inval"], k
+        assert dec(meta=fake + 2) == E["align"]
+        assert dec(arena=fake + 32) == E["align"]
+        assert dec(out=fake + 8) == E["align"]
+    assert f8_dec(bases=fake + 1) == E["align"]
+    assert f8_dec(fmt=0) == E["inval"]
+
+    # ---- attention over tiles: GQA shape, nulls, alignment ----
+    def ga_att(B=2, hq=32, q=fake, tail=fake, meta=fake, arena=fake, bases=fake, ws=fake):
+        return lib.kvz_ga_decode_attention(d, B, hq, q, fake, 4, fake, tail, meta, 64, arena, M, bases, fake, 1,
+                                           fake, ws, M, fake, None)
+
+    def f8_att(fmt=1, B=2, hq=32, q=fake, tail=fake, meta=fake, arena=fake, bases=fake, ws=fake):
+        return lib.kvz_f8_decode_attention(d, fmt, B, hq, q, fake, 4, fake, tail, meta, 64, arena, M, bases, fake,
+                                           1, fake, ws, M, fake, None)
+
+    for att in (ga_att, f8_att):
+        assert att(B=0, q=None, tail=None, meta=None, arena=None, bases=None, ws=None) == 0
+        assert att(hq=12) == E["inval"]   # not a whole multiple of the 8 KV heads
+        assert att(hq=128) == E["unsup"]  # G = 16 > 8
+        assert att(q=fake + 8) == E["align"]
+        assert att(ws=fake + 8) == E["align"]
+        for k in ("tail", "meta", "arena", "bases", "q", "ws"):
+            assert att(**{k: None}) == E["inval"], k
+        assert att(meta=fake + 4) == E["align"]
+        assert att(arena=fake + 32) == E["align"]
+        assert att(bases=fake + 1) == E["align"]
+        assert att(tail=fake + 2) == E["align"]
+    for fmt in (0, 3):
+        assert f8_att(fmt=fmt) == E["inval"]
+
+
 # --------------------------------------------------------------------------------------
 # allocator
 # --------------------------------------------------------------------------------------

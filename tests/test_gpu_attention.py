@@ -105,32 +105,68 @@ def test_missing_tail_page_is_flagged(kvz, oracle):
     assert int(st.item()) & kvz.STATUS_BAD_TAIL
 
 
-def test_full_size_layer_sampled(kvz, oracle):
+def test_full_size_layer_all_outputs(kvz, oracle):
     """The Llama-3.1-8B-shaped layer (batch 32, 32/8 heads, 2048 + tail tokens, shuffled
-    pages) in the bench's launch configuration; the fp64 oracle on a sample of sequences."""
-    cfg = kvgen.C1
-    layer = Layer(cfg, None)
+    pages) in the bench's launch configuration: every output against the fp64 oracle
+    run over the oracle's own encoding of every page."""
+    layer = Layer(kvgen.C1, oracle)
     out_c = layer.run_compressed()
     out_r = layer.run_raw()
     torch.cuda.synchronize()
     assert int(layer.status.item()) == 0
     assert torch.equal(out_c, out_r)
-    pick = [0, 7, 19, 31]
-    sub = kvgen.KVConfig(cfg.name, 1, len(pick), cfg.hq, cfg.hkv, cfg.full_pages, cfg.tail_min, cfg.tail_max)
-    pool = kvgen.bits(layer.g_pool.cpu())
-    o_meta = np.zeros((cfg.num_pages, cfg.hkv, 2), np.uint64)
-    per = (cfg.full_pages + 1) * cfg.hkv * 32
-    o_arena = np.zeros(len(pick) * per * 256, np.uint8)
-    cur = np.array([[i * per, (i + 1) * per] for i in range(len(pick))], np.uint32)
-    src = np.concatenate([layer.full[b].numpy() for b in pick]).astype(np.int32)
-    seq = np.repeat(np.arange(len(pick), dtype=np.int32), cfg.full_pages)
-    assert oracle.encode_pages(pool, src, src, seq, o_meta, o_arena, cur, cfg.hkv) == 0
-    ref, st = oracle.decode_attention(kvgen.bits(layer.q[pick]), layer.full[pick].numpy(),
-                                      layer.seq_lens[pick].numpy(), layer.tail[pick].numpy(), o_meta, o_arena,
-                                      pool, cfg.hkv, nthreads=8)
+    ref, st = layer.oracle_attention(oracle, nthreads=16)
     assert st == 0
-    check_attention(out_c[pick], ref, "C1 sample")
-    del sub
+    check_attention(out_c, ref, "C1 layer")
+
+
+def _decompress_first(kvz, layer):
+    """Decompress-first composition: kvz_decode_blocks of every compressed page into a
+    BF16 scratch pool (in table order), each sequence's raw tail page copied beside them,
+    then kvz_decode_attention_raw over the scratch pool with a table one column wider
+    than the compressed call's (the same work split)."""
+    cfg = layer.cfg
+    B, nf = cfg.batch, cfg.full_pages
+    full = layer.full.cuda()
+    scratch = torch.empty((B * nf + B, cfg.hkv, 2, 16, 128), dtype=torch.bfloat16, device="cuda")
+    st = kvz.new_status()
+    n_full = (layer.seq_lens // 16).tolist()
+    ids = torch.arange(B * nf, dtype=torch.int32).view(B, nf)
+    for b in range(B):  # only the completed pages are encoded; the rest of each row stays unused
+        if n_full[b]:
+            kvz.decode_blocks(layer.meta, layer.arena, full[b, : n_full[b]].contiguous(),
+                              scratch[b * nf: b * nf + n_full[b]], st)
+    tails = layer.tail.clamp_min(0).long().cuda()
+    scratch[B * nf:] = layer.g_pool[tails]
+    # row b: its decoded pages, then its tail at column n_full[b] (unused when the length is
+    # a whole number of pages); columns past the sequence's pages are never read
+    table = torch.full((B, nf + 1), -1, dtype=torch.int32)
+    for b in range(B):
+        table[b, : n_full[b]] = ids[b, : n_full[b]]
+        table[b, n_full[b]] = B * nf + b
+    out = torch.empty((B, cfg.hq, 128), dtype=torch.float32, device="cuda")
+    ws = torch.empty(kvz.attention_workspace_size(cfg.hkv, B, cfg.hq, nf + 1), dtype=torch.uint8, device="cuda")
+    kvz.decode_attention_raw(layer.g_q, table.contiguous().cuda(), layer.seq_lens.cuda(), scratch, out, st,
+                             workspace=ws)
+    return out, st
+
+
+@pytest.mark.parametrize("cfg", [kvgen.C0_TAIL, CASES[2], kvgen.KVConfig(
+    "df-lengths", 1, 9, 8, 2, 6, tail_min=1, tail_max=15, seed=44)], ids=lambda c: c.name)
+def test_decompress_first_matches_oracle(kvz, oracle, cfg):
+    """The decompress-first pipeline (standalone decode, then the raw kernel) gives the
+    fp64 oracle's attention within the tolerance and the fused kernel's output bit for
+    bit; with ragged lengths, including whole-page lengths with no tail."""
+    lens = [0, 16, 17, 40, 64, 65, 90, 95, 96] if cfg.name == "df-lengths" else None
+    layer = Layer(cfg, oracle, seq_lens=lens)
+    out_df, st = _decompress_first(kvz, layer)
+    out_c = layer.run_compressed()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and int(layer.status.item()) == 0
+    ref, ost = layer.oracle_attention(oracle)
+    assert ost == 0
+    check_attention(out_df, ref, cfg.name + " decompress-first")
+    assert torch.equal(out_df, out_c), "decompress-first and fused outputs differ"
 
 
 def test_largest_batch_and_beyond(kvz, oracle):

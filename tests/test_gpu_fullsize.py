@@ -1,8 +1,7 @@
 """Parity at the benchmark's full sizes, in the launch configuration bench.py times:
 the 131072-token long-context layer (every (sequence, KV head) unit split across ~29
 CTAs, ~29 partials per merge) and the 8K-context layer, against the fp64 CPU oracle on
-every output (long context) or on sampled sequences (8K), plus sampled block tags and
-bit-exact standalone decodes of sampled pages."""
+every output, plus sampled block tags and bit-exact standalone decodes of sampled pages."""
 import numpy as np
 import pytest
 import torch
@@ -81,18 +80,36 @@ def test_long_context_layer_all_outputs(kvz, oracle):
     _check_blocks(kvz, oracle, W, pool)
 
 
-def test_8k_layer_sampled(kvz, oracle):
+def test_8k_layer_all_outputs(kvz, oracle):
+    """One layer of the 8K stack (batch 16): every output against the oracle, and the
+    decompress-first pipeline as bench.py times it equal to the fused kernel."""
     cfg = kvgen.KVConfig(**{**kvgen.C2.__dict__, "layers": 1})
     W = _layer(kvz, cfg)
     W.step_c(0)
     W.step_r(0)
+    W.setup_decompress_first()
+    W.step_df(0)
     torch.cuda.synchronize()
     assert int(W.status.item()) == 0
     assert torch.equal(W.out, W.out_raw)
-    pick = [0, 9, 15]
-    ref, pool = _oracle_attention(oracle, W, pick)
-    check_attention(W.out[pick], ref, "8K layer")
+    assert torch.equal(W.out_df, W.out)
+    ref, pool = _oracle_attention(oracle, W, list(range(cfg.batch)))
+    check_attention(W.out, ref, "8K layer")
     _check_blocks(kvz, oracle, W, pool)
+
+
+def test_c1_layer_decompress_first_all_outputs(kvz, oracle):
+    """The C1 layer's decompress-first pipeline (standalone decode into a BF16 scratch
+    pool, then the raw kernel), as bench.py times it: every output against the oracle."""
+    W = _layer(kvz, kvgen.C1)
+    W.setup_decompress_first()
+    W.step_df(0)
+    W.step_c(0)
+    torch.cuda.synchronize()
+    assert int(W.status.item()) == 0
+    assert torch.equal(W.out_df, W.out)
+    ref, _ = _oracle_attention(oracle, W, list(range(W.cfg.batch)))
+    check_attention(W.out_df, ref, "C1 decompress-first")
 
 
 @pytest.mark.parametrize("kind", ["ga", "f8e4", "f8e5"])

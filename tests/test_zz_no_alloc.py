@@ -4,9 +4,10 @@ policy forbids allocation while work is recorded).  It keeps its split-KV scratc
 a fixed array inside libkvz instead of a caller workspace.
 
 Called here through the C ABI with ctypes, twice in a row (the second call finds the
-first call's leftovers in the shared array), and compared with kvz_decode_attention
-on the same inputs within the attention tolerance of the other GPU tests.  The file
-name makes pytest collect it last."""
+first call's leftovers in the shared array).  Both calls use the same work split as
+kvz_decode_attention, so their outputs must equal its output bit for bit; they are also
+checked against the fp64 CPU oracle within the attention tolerance of the other GPU
+tests.  The file name makes pytest collect it last."""
 import ctypes
 
 import numpy as np
@@ -14,7 +15,7 @@ import pytest
 import torch
 
 import kvgen
-from helpers import Layer
+from helpers import Layer, check_attention
 
 pytestmark = pytest.mark.gpu
 
@@ -41,18 +42,23 @@ def _call(kvz, fn, layer, out, status, batch=None):
               torch.cuda.current_stream().cuda_stream)
 
 
-def test_noalloc_matches_workspace_entry_point():
+def test_noalloc_matches_workspace_entry_point(oracle):
     import decode_attention_value_gb300 as kvz
 
     fn = _noalloc_fn(kvz)
     cfg = kvgen.KVConfig("noalloc-ragged", 1, 12, 32, 8, 40, tail_min=1, tail_max=15, k_log2_sigma=(-4, 3),
                          v_log2_sigma=(-3, 1), k_outlier_channels=4, k_outlier_scale=32.0, seed=77)
-    layer = Layer(cfg, None)
+    rng = np.random.default_rng(77)
+    lens = rng.integers(0, 40 * 16 + 16, cfg.batch).astype(np.int32)
+    lens[3] = 0
+    lens[5] = 16 * 7  # a whole number of pages: no tail
+    layer = Layer(cfg, oracle, seq_lens=lens)
     ref = layer.run_compressed()
     torch.cuda.synchronize()
     assert int(layer.status.item()) == 0
-    r = ref.double().cpu().numpy()
-    scale = float(np.sqrt(np.mean(r ** 2)))
+    o_ref, o_st = layer.oracle_attention(oracle)
+    assert o_st == 0
+    check_attention(ref, o_ref, "workspace entry point")
     for call in range(2):
         out = torch.full_like(ref, float("nan"))
         status = kvz.new_status()
@@ -60,9 +66,8 @@ def test_noalloc_matches_workspace_entry_point():
         assert rc == 0, kvz.lib().kvz_strerror(rc)
         torch.cuda.synchronize()
         assert int(status.item()) == 0, f"call {call}: status {int(status.item())}"
-        err = np.abs(out.double().cpu().numpy() - r)
-        assert np.isfinite(err).all()
-        assert err.max() <= 4e-3 * scale and err.mean() <= 5e-4 * scale, (call, err.max(), err.mean(), scale)
+        assert torch.equal(out, ref), f"call {call}: differs from kvz_decode_attention"
+        check_attention(out, o_ref, f"no-alloc call {call}")
 
 
 def test_noalloc_rejects_problems_beyond_its_array():
