@@ -3,10 +3,13 @@
 Default workload: the full Llama-3.1-8B-shaped decode step at 8K context -- 32 layers,
 batch 16, 32 query heads, 8 KV heads, head dim 128, 8192 tokens in 512 compressed
 16-token pages per sequence (shuffled physical order) plus a raw tail of 1..15 tokens,
-each layer with its own seeded KV.  A step is one kvz_decode_attention call per layer,
-in layer order (attention + split merge, 64 kernel launches); every step reads all 32
-layers' caches once (14.7 GB compressed, far more than L2).  Synthetic, seeded inputs
-(kvgen); the KV is resident in HBM before timing starts.
+each layer with its own seeded KV.  A step is one attention call per layer, in layer
+order (attention + split merge, 64 kernel launches): kvz_decode_attention_ex with
+KVZ_ATTN_OVERLAP_PREVIOUS, so each layer's start-up overlaps the previous layer's merge
+(the same step with plain kvz_decode_attention calls is reported beside it; outputs are
+bit-identical).  Every step reads all 32 layers' caches once (14.7 GB compressed, far
+more than L2).  Synthetic, seeded inputs (kvgen); the KV is resident in HBM before
+timing starts.
 
 Reported: logical-KV GB/s (BF16 K+V bytes attended / time) as `value`, µs per step (the
 median of five timed runs of K steps), the in-run raw-BF16 kernel on the same pages, the
@@ -43,6 +46,7 @@ sys.path.insert(0, ROOT)
 import kvgen  # noqa: E402
 
 METRIC = "decode-attention µs/step & logical KV GB/s; % of HBM roofline; encode GB/s"
+OVERLAP = 1  # KVZ_ATTN_OVERLAP_PREVIOUS
 FALLBACK_HBM_GBS = 6800.0
 RUNS = 5  # timed runs of K steps per measurement; the median is reported
 
@@ -187,7 +191,7 @@ def config_dict(workload: str, world: int) -> dict:
         return {"workload": cfg.name + "-full-stack", "layers": cfg.layers, "batch": cfg.batch, "q_heads": cfg.hq,
                 "kv_heads": cfg.hkv, "head_dim": 128, "page_tokens": 16, "context_tokens": cfg.full_pages * 16,
                 "tail_tokens": f"{cfg.tail_min}..{cfg.tail_max}", "page_order": "shuffled",
-                "kv": "a separate seeded KV cache per layer", "parallelism": par,
+                "kv": "a separate seeded KV cache per layer", "launch": "overlapped layer calls", "parallelism": par,
                 "l2": "inputs larger than L2: each step reads all 32 layers' caches once"}
     if workload == "c3":
         cfg = kvgen.C3
@@ -293,11 +297,12 @@ class Workload:
         slots = (self.ws_c.numel() - pre) // (4 * 128 * 4 + 4 * 2 * 4)
         return slots - cfg.batch * cfg.hkv + 1
 
-    def step_c(self, k: int, q=None, out=None):
+    def step_c(self, k: int, q=None, out=None, flags: int = 0):
         c = k % self.copies
+        kw = {"flags": flags} if flags else {}
         self.kvz.decode_attention(self.q if q is None else q, self.full, self.seq_lens, self.tail, self.metas[c],
                                   self.arenas[c], self.pools[c], self.out if out is None else out, self.status,
-                                  workspace=self.ws_c)
+                                  workspace=self.ws_c, **kw)
 
     def setup_decompress_first(self):
         """Scratch BF16 pool for the decompress-first pipeline: the layer's compressed pages
@@ -330,10 +335,11 @@ class Workload:
         self.step_df_decode(k)
         self.step_df_attend(k)
 
-    def step_r(self, k: int):
+    def step_r(self, k: int, flags: int = 0):
         c = k % self.copies
+        kw = {"flags": flags} if flags else {}
         self.kvz.decode_attention_raw(self.q, self.raw_table, self.seq_lens, self.pools[c], self.out_raw,
-                                      self.status, workspace=self.ws_r)
+                                      self.status, workspace=self.ws_r, **kw)
 
 
 def graph_of(fn, steps: int):
@@ -515,7 +521,9 @@ def measure_layer(cfg: kvgen.KVConfig, args, dev, local, dist, world: int, rank:
     identical = bool(torch.equal(W.out, W.out_raw))
     K = args.steps
     g_c, g_r = graph_of(W.step_c, K), graph_of(W.step_r, K)
-    graphs = {"c": g_c, "r": g_r}
+    graphs = {"c": g_c, "r": g_r,
+              "co": graph_of(lambda k: W.step_c(k, flags=OVERLAP), K),
+              "ro": graph_of(lambda k: W.step_r(k, flags=OVERLAP), K)}
     if decompress_first:
         W.setup_decompress_first()
         graphs["df"] = graph_of(W.step_df, K)
@@ -547,6 +555,14 @@ def measure_layer(cfg: kvgen.KVConfig, args, dev, local, dist, world: int, rank:
            "roofline_raw": {"achieved": round(achieved_r, 1), "frac": round(achieved_r / peak, 4),
                             "algorithmic_bytes_per_launch": W.alg_bytes_r},
            "runs": runs_summary(ms["c"], K), "runs_raw": runs_summary(ms["r"], K), "clocks": clocks}
+    us_co, us_ro = med["co"] * 1e3 / K, med["ro"] * 1e3 / K
+    res["overlapped_launches"] = {
+        "us_per_step": round(us_co, 3), "raw_us_per_step": round(us_ro, 3), "speedup_vs_raw": round(us_ro / us_co, 4),
+        "logical_GBps": round(job_throughput(world, W.logical_bytes, K, med["co"]), 2),
+        "roofline_frac": round(W.alg_bytes_c / (us_co * 1e-6) / 1e9 / peak, 4),
+        "how": "each step's call with KVZ_ATTN_OVERLAP_PREVIOUS: its start-up overlaps the previous step's merge"}
+    if not torch.equal(W.out, W.out_raw):
+        raise RuntimeError(f"{cfg.name}: overlapped calls changed the output")
     if decompress_first:
         if not torch.equal(W.out_df, W.out_raw):
             raise RuntimeError(f"{cfg.name}: decompress-first output differs from the raw kernel's")
@@ -601,7 +617,7 @@ def stack_layers(cfg: kvgen.KVConfig, dev) -> list:
     return layers
 
 
-def stack_e2e(layers, K: int, dev, dist, world: int) -> dict:
+def stack_e2e(layers, K: int, dev, dist, world: int, flags: int = 0) -> dict:
     """The stack end to end through the C ABI with host buffers.  Per step: one
     host-to-device copy of every layer's queries plus the block table, lengths and tail
     ids (one pinned buffer, back to back, 16-byte aligned), the 32 kvz_decode_attention
@@ -631,11 +647,13 @@ def stack_e2e(layers, K: int, dev, dist, world: int) -> dict:
     pin_out2 = [torch.empty(out_shape, dtype=torch.float32).pin_memory() for _ in range(2)]
     status = kvz.new_status(dev)
 
+    kw = {"flags": flags} if flags else {}
+
     def calls(views, out):
         q_, t_, l_, tl_ = views
         for i, W in enumerate(layers):
             kvz.decode_attention(q_[i], t_, l_, tl_, W.metas[0], W.arenas[0], W.pools[0], out[i], status,
-                                 workspace=W0.ws_c)
+                                 workspace=W0.ws_c, **kw)
 
     def serial_step(k):
         d_in2[0].copy_(pin_in, non_blocking=True)
@@ -696,7 +714,8 @@ def stack_e2e(layers, K: int, dev, dist, world: int) -> dict:
                    "copies run on a second stream, overlapping the neighbouring steps (inputs and outputs "
                    "double-buffered); the K steps replayed as one CUDA graph; median of 5 timed runs",
             "serial_value": round(job_throughput(world, logical, K, ms_ser), 2),
-            "serial_how": "the same copies and calls issued back to back on one stream"}
+            "serial_how": "the same copies and calls issued back to back on one stream",
+            "launch": "overlapped (KVZ_ATTN_OVERLAP_PREVIOUS)" if flags else "plain"}
 
 
 def measure_stack(args, dev, local, dist, world: int, rank: int) -> dict:
@@ -715,6 +734,14 @@ def measure_stack(args, dev, local, dist, world: int, rank: int) -> dict:
         for W in layers:
             W.step_r(0)
 
+    def step_co(k):
+        for W in layers:
+            W.step_c(0, flags=OVERLAP)
+
+    def step_ro(k):
+        for W in layers:
+            W.step_r(0, flags=OVERLAP)
+
     for k in range(args.warmup):
         step_c(k)
         step_r(k)
@@ -723,31 +750,43 @@ def measure_stack(args, dev, local, dist, world: int, rank: int) -> dict:
         if int(W.status.item()) != 0:
             raise RuntimeError(f"status {int(W.status.item())}")
     identical = all(torch.equal(W.out, W.out_raw) for W in layers)
+    ref_out = torch.stack([W.out for W in layers]).clone()
     g_c, g_r = graph_of(step_c, K), graph_of(step_r, K)
-    g_c.replay()
-    g_r.replay()
+    g_co, g_ro = graph_of(step_co, K), graph_of(step_ro, K)
+    for g in (g_c, g_r, g_co, g_ro):
+        g.replay()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        soak(g_c, 0.6)
+        soak(g_co, 0.6)
+        ms_co = timed_runs(g_co, dist)
+        ms_ro = timed_runs(g_ro, dist)
         ms_c = timed_runs(g_c, dist)
         ms_r = timed_runs(g_r, dist)
-        soak(g_c, 0.3)
+        soak(g_co, 0.3)
     clocks = clk.summary()
+    if not (torch.equal(torch.stack([W.out for W in layers]), ref_out)
+            and all(torch.equal(W.out, W.out_raw) for W in layers)):
+        raise RuntimeError("overlapped calls changed the stack's outputs")
+    med_co, med_ro = max_over_ranks(dist, [statistics.median(ms_co), statistics.median(ms_ro)], device=dev)
     med_c, med_r = max_over_ranks(dist, [statistics.median(ms_c), statistics.median(ms_r)], device=dev)
-    us_c, us_r = med_c * 1e3 / K, med_r * 1e3 / K
+    us_c, us_r = med_c * 1e3 / K, med_r * 1e3 / K  # plain launches
     logical = sum(W.logical_bytes for W in layers)
     alg = sum(W.alg_bytes_c for W in layers)
     alg_r = sum(W.alg_bytes_r for W in layers)
     blocks = sum(W.blocks for W in layers)
     raw_blocks = sum(W.raw_blocks for W in layers)
     block_bytes = sum(W.block_bytes for W in layers)
-    e2e = stack_e2e(layers, K, dev, dist, world)
-    launch_us = us_c / L  # one attention launch + its merge, averaged over the layers of a step
+    e2e = stack_e2e(layers, K, dev, dist, world, flags=OVERLAP)
+    us_co, us_ro = med_co * 1e3 / K, med_ro * 1e3 / K
+    launch_us = us_co / L  # one attention launch + its merge, averaged over the layers of a step
     achieved = alg / L / (launch_us * 1e-6) / 1e9
-    achieved_r = alg_r / (us_r * 1e-6) / 1e9
+    achieved_r = alg_r / (us_ro * 1e-6) / 1e9
     res = {
-        "value": round(job_throughput(world, logical, K, med_c), 2), "ms_per_step": round(us_c / 1e3, 5),
-        "us_per_step": round(us_c, 2), "raw_us_per_step": round(us_r, 2), "speedup_vs_raw": round(us_r / us_c, 4),
+        "value": round(job_throughput(world, logical, K, med_co), 2), "ms_per_step": round(us_co / 1e3, 5),
+        "launch": "overlapped: every layer's call is kvz_decode_attention_ex with KVZ_ATTN_OVERLAP_PREVIOUS, a "
+                  "programmatic dependent of the previous layer's merge (outputs bit-identical to plain calls); "
+                  "the raw arm the same with kvz_decode_attention_raw_ex",
+        "us_per_step": round(us_co, 2), "raw_us_per_step": round(us_ro, 2), "speedup_vs_raw": round(us_ro / us_co, 4),
         "compressed_fraction": round(1 - raw_blocks / blocks, 5),
         "compressed_bytes_ratio": round(block_bytes / (blocks * 1024), 5),
         "expected_speedup_from_fraction": round(blocks * 1024 / block_bytes, 4),
@@ -761,11 +800,18 @@ def measure_stack(args, dev, local, dist, world: int, rank: int) -> dict:
                             "traffic: dram bytes of one launch on one layer of this stack (ncu summary in profiles/)"},
         "roofline_raw": {"achieved": round(achieved_r, 1), "frac": round(achieved_r / peak, 4),
                          "algorithmic_bytes_per_step": alg_r},
-        "runs": {**runs_summary(ms_c, K), "how": f"{RUNS} timed runs of the {K}-step graph, median reported"},
-        "runs_raw": runs_summary(ms_r, K),
+        "runs": {**runs_summary(ms_co, K), "how": f"{RUNS} timed runs of the {K}-step graph, median reported"},
+        "runs_raw": runs_summary(ms_ro, K),
         "e2e": e2e, "clocks": clocks, "gpu_launches": 2 * L * K,
+        "plain_launches": {
+            "us_per_step": round(us_c, 2), "raw_us_per_step": round(us_r, 2), "speedup_vs_raw": round(us_r / us_c, 4),
+            "logical_GBps": round(job_throughput(world, logical, K, med_c), 2),
+            "roofline_frac": round(alg / L / (us_c / L * 1e-6) / 1e9 / peak, 4),
+            "runs": runs_summary(ms_c, K), "runs_raw": runs_summary(ms_r, K),
+            "how": "the same step with kvz_decode_attention / kvz_decode_attention_raw (each layer's call starts "
+                   "after the previous one has finished)"},
     }
-    del layers, g_c, g_r
+    del layers, g_c, g_r, g_co, g_ro
     torch.cuda.empty_cache()
     return res
 

@@ -30,6 +30,9 @@ STATUS_Q_RANGE = 64
 
 ERR_OUT_OF_SPACE = -7
 
+# attention launch flags (kvz_decode_attention_ex / kvz_decode_attention_raw_ex)
+ATTN_OVERLAP_PREVIOUS = 1
+
 GA_GRANULE = 64
 GA_TILE_BYTES = 3008
 GA_RAW_TILE_BYTES = 4096
@@ -48,6 +51,7 @@ EXPORTS = (
     "kvz_ga_calibrate", "kvz_ga_encode_pages", "kvz_ga_decode_blocks", "kvz_ga_decode_attention",
     "kvz_selftest_bounded_wait", "kvz_encode_sizes", "kvz_alloc_reserve_granules", "kvz_alloc_room",
     "kvz_f8_calibrate", "kvz_f8_encode_pages", "kvz_f8_decode_blocks", "kvz_f8_decode_attention",
+    "kvz_decode_attention_ex", "kvz_decode_attention_raw_ex", "kvz_selftest_late_writer",
 )
 
 
@@ -78,6 +82,11 @@ def _load() -> ctypes.CDLL:
         "kvz_attention_workspace_size": (sz, [Dims, i32, i32, i32]),
         "kvz_decode_attention": (ctypes.c_int, [Dims, i32, i32, P, P, i32, P, P, P, i64, P, u64, P, i64, P, P, sz, P, P]),
         "kvz_decode_attention_raw": (ctypes.c_int, [Dims, i32, i32, P, P, i32, P, P, i64, P, P, sz, P, P]),
+        "kvz_decode_attention_ex": (ctypes.c_int, [Dims, i32, i32, P, P, i32, P, P, P, i64, P, u64, P, i64, P, P, sz,
+                                                   P, ctypes.c_uint32, P]),
+        "kvz_decode_attention_raw_ex": (ctypes.c_int, [Dims, i32, i32, P, P, i32, P, P, i64, P, P, sz, P,
+                                                       ctypes.c_uint32, P]),
+        "kvz_selftest_late_writer": (ctypes.c_int, [P, P, u64, u64, P]),
         "kvz_alloc_create": (ctypes.c_int, [u64, ctypes.c_uint32, i32, i32, ctypes.POINTER(P)]),
         "kvz_alloc_destroy": (None, [P]),
         "kvz_alloc_reserve": (ctypes.c_int, [P, P, P, i32, P, P, P, P, P]),
@@ -228,40 +237,48 @@ def decode_blocks(meta, arena, pages, out, status, stream=None):
 
 
 def decode_attention(q, page_ids, seq_lens, tail_page, meta, arena, raw_pool, out, status, workspace=None,
-                     stream=None):
+                     stream=None, flags: int = 0):
     """Attention over compressed pages page_ids [B][max_pages] plus raw tail pages;
-    q BF16 [B][Hq][128] -> out float32 [B][Hq][128]."""
+    q BF16 [B][Hq][128] -> out float32 [B][Hq][128].  flags (ATTN_OVERLAP_PREVIOUS)
+    selects kvz_decode_attention_ex."""
     B, hq = q.shape[0], q.shape[1]
     hkv = meta.shape[1] if meta.dim() >= 2 else raw_pool.shape[1]
     max_pages = page_ids.shape[1] if page_ids.dim() == 2 else 0
     if workspace is None:
         workspace = torch.empty(attention_workspace_size(hkv, B, hq, max_pages + 1), dtype=torch.uint8,
                                 device=q.device)
-    rc = _lib.kvz_decode_attention(
+    args = (
         _dims(hkv), B, hq, _ptr(q, _BF16, "q"), _ptr(page_ids, torch.int32, "page_ids"), max_pages,
         _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(tail_page, torch.int32, "tail_page"),
         _ptr(meta, _U64, "meta"), meta.numel() // (hkv * 2), _ptr(arena, _U8, "arena"), arena.numel(),
         _ptr(raw_pool, _BF16, "raw_pool"), _pages_of(raw_pool), _ptr(out, torch.float32, "out"),
-        _ptr(workspace, _U8, "workspace"), workspace.numel(), _ptr(status, _U32, "status"), _stream(stream),
+        _ptr(workspace, _U8, "workspace"), workspace.numel(), _ptr(status, _U32, "status"),
     )
-    _check("kvz_decode_attention", rc)
+    if flags:
+        _check("kvz_decode_attention_ex", _lib.kvz_decode_attention_ex(*args, int(flags), _stream(stream)))
+    else:
+        _check("kvz_decode_attention", _lib.kvz_decode_attention(*args, _stream(stream)))
 
 
-def decode_attention_raw(q, page_ids, seq_lens, raw_pool, out, status, workspace=None, stream=None):
-    """The same attention over plain BF16 pages page_ids [B][max_pages] (all pages)."""
+def decode_attention_raw(q, page_ids, seq_lens, raw_pool, out, status, workspace=None, stream=None, flags: int = 0):
+    """The same attention over plain BF16 pages page_ids [B][max_pages] (all pages);
+    flags (ATTN_OVERLAP_PREVIOUS) selects kvz_decode_attention_raw_ex."""
     B, hq = q.shape[0], q.shape[1]
     hkv = raw_pool.shape[1]
     max_pages = page_ids.shape[1]
     if workspace is None:
         workspace = torch.empty(attention_workspace_size(hkv, B, hq, max_pages), dtype=torch.uint8,
                                 device=q.device)
-    rc = _lib.kvz_decode_attention_raw(
+    args = (
         _dims(hkv), B, hq, _ptr(q, _BF16, "q"), _ptr(page_ids, torch.int32, "page_ids"), max_pages,
         _ptr(seq_lens, torch.int32, "seq_lens"), _ptr(raw_pool, _BF16, "raw_pool"), _pages_of(raw_pool),
         _ptr(out, torch.float32, "out"), _ptr(workspace, _U8, "workspace"), workspace.numel(),
-        _ptr(status, _U32, "status"), _stream(stream),
+        _ptr(status, _U32, "status"),
     )
-    _check("kvz_decode_attention_raw", rc)
+    if flags:
+        _check("kvz_decode_attention_raw_ex", _lib.kvz_decode_attention_raw_ex(*args, int(flags), _stream(stream)))
+    else:
+        _check("kvz_decode_attention_raw", _lib.kvz_decode_attention_raw(*args, _stream(stream)))
 
 
 def apply_cursor_updates(idx, pos, end, cursors, stream=None):
@@ -392,6 +409,16 @@ def f8_decode_attention(fmt: int, q, page_ids, seq_lens, tail_page, meta, arena,
         _ptr(status, _U32, "status"), _stream(stream),
     )
     _check("kvz_f8_decode_attention", rc)
+
+
+def selftest_late_writer(src, dst, delay_ns: int, stream=None):
+    """Test helper (kvz_selftest_late_writer): copy src to dst on the device after a delay,
+    letting a programmatic dependent launch begin first."""
+    if src.numel() * src.element_size() != dst.numel() * dst.element_size():
+        raise ValueError("src and dst sizes differ")
+    _check("kvz_selftest_late_writer", _lib.kvz_selftest_late_writer(
+        _ptr(src, None, "src"), _ptr(dst, None, "dst"), src.numel() * src.element_size(), int(delay_ns),
+        _stream(stream)))
 
 
 def selftest_bounded_wait(limit_ns: int, status, out, stream=None):

@@ -128,7 +128,7 @@ struct FormatArgs {
 int run_attention(const FormatArgs &F, const kvz_dims &d, int batch, int hq, const void *q, const int32_t *page_ids,
                   int max_pages, const int32_t *seq_lens, const int32_t *tail_page, int64_t num_meta_pages,
                   const uint8_t *arena, uint64_t arena_bytes, const void *raw_pool, int64_t num_raw_pages, float *out,
-                  void *ws, size_t ws_bytes, uint32_t *status, cudaStream_t stream)
+                  void *ws, size_t ws_bytes, uint32_t *status, cudaStream_t stream, uint32_t flags = 0)
 {
     const int hkv = d.num_kv_heads;
     const int table_pages = F.format != kFmtRaw ? max_pages + 1 : max_pages;
@@ -168,6 +168,7 @@ int run_attention(const FormatArgs &F, const kvz_dims &d, int batch, int hq, con
     P.part_ml = reinterpret_cast<float *>(w);
     P.status = status;
     P.scale_log2 = (float)(1.4426950408889634 / 11.313708498984761);  // log2(e) / sqrt(128)
+    P.overlap = (flags & KVZ_ATTN_OVERLAP_PREVIOUS) ? 1 : 0;
     cudaError_t e = launch_attention(P, F.format, &map, stream);
     return e == cudaSuccess ? KVZ_OK : fail_cuda(e);
 }
@@ -371,6 +372,37 @@ int kvz_decode_attention_raw(kvz_dims dims, int32_t batch, int32_t num_q_heads, 
                          workspace_bytes, status, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int kvz_decode_attention_ex(kvz_dims dims, int32_t batch, int32_t num_q_heads, const void *q, const int32_t *page_ids,
+                            int32_t max_pages, const int32_t *seq_lens, const int32_t *tail_page,
+                            const uint64_t *meta, int64_t num_meta_pages, const uint8_t *arena, uint64_t arena_bytes,
+                            const void *raw_pool, int64_t num_raw_pages, float *out, void *workspace,
+                            size_t workspace_bytes, uint32_t *status, uint32_t flags, kvz_stream_t stream)
+{
+    if (flags & ~KVZ_ATTN_FLAGS_ALL) return KVZ_ERR_INVALID_ARG;
+    int rc = check_attention_common(dims, batch, num_q_heads, q, seq_lens, raw_pool, num_raw_pages, out, workspace,
+                                    status, max_pages, page_ids);
+    if (rc || batch == 0) return rc;
+    if (!tail_page || !meta || !arena || num_meta_pages < 0) return KVZ_ERR_INVALID_ARG;
+    if (!aligned(meta, 16) || !aligned(arena, 256) || !aligned(tail_page, 4)) return KVZ_ERR_ALIGNMENT;
+    return run_attention(FormatArgs{kFmtZf, meta, nullptr, nullptr}, dims, batch, num_q_heads, q, page_ids,
+                         max_pages, seq_lens, tail_page, num_meta_pages, arena, arena_bytes, raw_pool, num_raw_pages,
+                         out, workspace, workspace_bytes, status, reinterpret_cast<cudaStream_t>(stream), flags);
+}
+
+int kvz_decode_attention_raw_ex(kvz_dims dims, int32_t batch, int32_t num_q_heads, const void *q,
+                                const int32_t *page_ids, int32_t max_pages, const int32_t *seq_lens,
+                                const void *raw_pool, int64_t num_raw_pages, float *out, void *workspace,
+                                size_t workspace_bytes, uint32_t *status, uint32_t flags, kvz_stream_t stream)
+{
+    if (flags & ~KVZ_ATTN_FLAGS_ALL) return KVZ_ERR_INVALID_ARG;
+    int rc = check_attention_common(dims, batch, num_q_heads, q, seq_lens, raw_pool, num_raw_pages, out, workspace,
+                                    status, max_pages, page_ids);
+    if (rc || batch == 0) return rc;
+    return run_attention(FormatArgs{kFmtRaw, nullptr, nullptr, nullptr}, dims, batch, num_q_heads, q, page_ids,
+                         max_pages, seq_lens, nullptr, 0, nullptr, 0, raw_pool, num_raw_pages, out, workspace,
+                         workspace_bytes, status, reinterpret_cast<cudaStream_t>(stream), flags);
+}
+
 int kvz_decode_attention_noalloc(kvz_dims dims, int32_t batch, int32_t num_q_heads, const void *q,
                                  const int32_t *page_ids, int32_t max_pages, const int32_t *seq_lens,
                                  const int32_t *tail_page, const uint64_t *meta, int64_t num_meta_pages,
@@ -501,6 +533,16 @@ int kvz_ga_decode_attention(kvz_dims dims, int32_t batch, int32_t num_q_heads, c
     return run_attention(FormatArgs{kFmtGa, nullptr, meta, bases}, dims, batch, num_q_heads, q, page_ids, max_pages,
                          seq_lens, tail_page, num_meta_pages, arena, arena_bytes, raw_pool, num_raw_pages, out,
                          workspace, workspace_bytes, status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kvz_selftest_late_writer(const void *src, void *dst, uint64_t bytes, uint64_t delay_ns, kvz_stream_t stream)
+{
+    if (bytes == 0) return KVZ_OK;
+    if (!src || !dst) return KVZ_ERR_INVALID_ARG;
+    if (!aligned(src, 16) || !aligned(dst, 16) || bytes % 16 != 0) return KVZ_ERR_ALIGNMENT;
+    if (delay_ns > 1000000000ull || bytes > ((uint64_t)1 << 30)) return KVZ_ERR_INVALID_ARG;  // <= 1 s, <= 1 GiB
+    cudaError_t e = launch_late_writer(src, dst, bytes, delay_ns, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? KVZ_OK : fail_cuda(e);
 }
 
 int kvz_selftest_bounded_wait(uint64_t limit_ns, uint32_t *status, uint64_t *out, kvz_stream_t stream)

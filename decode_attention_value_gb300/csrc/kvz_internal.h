@@ -94,6 +94,7 @@ struct AttnParams {
     int32_t *prefix;   // [batch + 1] page prefix per sequence, written by CTA 0
     uint32_t *status;
     float scale_log2;  // log2(e) / sqrt(128)
+    int overlap;       // 1: launched as programmatic dependents (KVZ_ATTN_OVERLAP_PREVIOUS)
 };
 
 inline size_t attn_slots(int batch, int hkv, int grid) { return (size_t)batch * hkv + grid - 1; }
@@ -117,6 +118,7 @@ cudaError_t launch_enc_scan(const EncodeParams &P, cudaStream_t stream);
 cudaError_t launch_ga_encode(const EncodeParams &P, cudaStream_t stream);
 cudaError_t launch_ga_decode(const DecodeParams &P, cudaStream_t stream);
 cudaError_t launch_wait_selftest(uint64_t limit_ns, uint32_t *status, uint64_t *out, cudaStream_t stream);
+cudaError_t launch_late_writer(const void *src, void *dst, uint64_t bytes, uint64_t delay_ns, cudaStream_t stream);
 cudaError_t launch_f8_calibrate(int fmt, int hkv, const uint16_t *raw_pool, int64_t num_raw_pages,
                                 const int32_t *pages, int n, uint8_t *bases, uint32_t *status, cudaStream_t stream);
 cudaError_t launch_f8_encode(int fmt, const EncodeParams &P, cudaStream_t stream);

@@ -2,6 +2,8 @@
 // library uses: one wait on a barrier nobody arrives on (it must give up after the limit,
 // set KVZ_STATUS_TIMEOUT and return) and one on a phase that is already complete (it
 // must return at once).  The kernel exits normally either way; nothing faults or traps.
+// Also a late writer for testing overlapped attention launches: it lets a programmatic
+// dependent launch begin at once, waits a bounded time, then copies a buffer.
 #include "kvz_internal.h"
 
 namespace kvz {
@@ -26,6 +28,24 @@ __global__ void k_wait_selftest(uint64_t limit_ns, uint32_t *status, uint64_t *o
 cudaError_t launch_wait_selftest(uint64_t limit_ns, uint32_t *status, uint64_t *out, cudaStream_t stream)
 {
     k_wait_selftest<<<1, 32, 0, stream>>>(limit_ns, status, out);
+    return cudaGetLastError();
+}
+
+// One block: allow the dependent grid to be scheduled, wait delay_ns (globaltimer), then
+// copy `words` 16-byte words from src to dst.
+__global__ void k_late_writer(const uint4 *src, uint4 *dst, uint64_t words, uint64_t delay_ns)
+{
+    pdl_launch_dependents();
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < delay_ns) {
+    }
+    for (uint64_t i = threadIdx.x; i < words; i += blockDim.x) dst[i] = src[i];
+}
+
+cudaError_t launch_late_writer(const void *src, void *dst, uint64_t bytes, uint64_t delay_ns, cudaStream_t stream)
+{
+    k_late_writer<<<1, 256, 0, stream>>>(static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), bytes / 16,
+                                          delay_ns);
     return cudaGetLastError();
 }
 

@@ -187,6 +187,45 @@ int kvz_decode_attention_raw(kvz_dims dims, int32_t batch, int32_t num_q_heads, 
                              kvz_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
+ * kvz_decode_attention_ex / kvz_decode_attention_raw_ex -- the two attention calls with
+ * launch flags.  flags = 0 is exactly kvz_decode_attention / kvz_decode_attention_raw.
+ * The pages describe no launch mechanics; this is a GB300 launch option.
+ *
+ * KVZ_ATTN_OVERLAP_PREVIOUS: the call's kernels are launched as programmatic dependents
+ * (CUDA programmatic dependent launch), so its attention kernel may begin while the
+ * kernel before it on the stream is still running, and the call's merge kernel lets a
+ * programmatic dependent launched after it begin early.  In a decode step this overlaps
+ * each layer's start-up (lengths, page table, metadata, the first pages of the stream)
+ * with the kernel that produces the layer's queries.  Contract:
+ *  - Read before that kernel has finished: seq_lens, page_ids, tail_page, meta, arena,
+ *    and every raw page except each sequence's last page (the tail page of the
+ *    compressed call; the last page of each sequence in the raw call).  The kernel right
+ *    before this call must not write any of these (in particular, a page-completion
+ *    encode must not be the kernel right before an overlapped call).
+ *  - Read or written only after that kernel has finished and its writes are visible: q,
+ *    each sequence's last page, the workspace and out.  The preceding kernel may write q
+ *    and the step's new token into the last page.
+ *  - status may be OR-ed before that kernel has finished: do not clear it there.
+ *  - A kernel launched after this call as a programmatic dependent must wait for this
+ *    call to complete (griddepcontrol.wait / cudaGridDependencySynchronize) before it
+ *    reads out or reuses the workspace; another overlapped call does so.
+ * Results are bit-identical to flags = 0 (same split, same arithmetic).  Flags outside
+ * KVZ_ATTN_FLAGS_ALL return KVZ_ERR_INVALID_ARG.
+ * --------------------------------------------------------------------------------- */
+#define KVZ_ATTN_OVERLAP_PREVIOUS 1u
+#define KVZ_ATTN_FLAGS_ALL 1u
+int kvz_decode_attention_ex(kvz_dims dims, int32_t batch, int32_t num_q_heads, const void *q,
+                            const int32_t *page_ids, int32_t max_pages, const int32_t *seq_lens,
+                            const int32_t *tail_page, const uint64_t *meta, int64_t num_meta_pages,
+                            const uint8_t *arena, uint64_t arena_bytes, const void *raw_pool,
+                            int64_t num_raw_pages, float *out, void *workspace, size_t workspace_bytes,
+                            uint32_t *status, uint32_t flags, kvz_stream_t stream);
+int kvz_decode_attention_raw_ex(kvz_dims dims, int32_t batch, int32_t num_q_heads, const void *q,
+                                const int32_t *page_ids, int32_t max_pages, const int32_t *seq_lens,
+                                const void *raw_pool, int64_t num_raw_pages, float *out, void *workspace,
+                                size_t workspace_bytes, uint32_t *status, uint32_t flags, kvz_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
  * kvz_decode_attention_noalloc -- kvz_decode_attention for callers that cannot
  * allocate device memory.  The pages describe no such variant; it exists for callers
  * such as runtime plugins whose host framework owns every device allocation, code that
@@ -390,6 +429,13 @@ int kvz_apply_cursor_updates(const int32_t *idx, const uint32_t *pos, const uint
  * return).  out: device uint64[3] = {ns of the first wait, ns of the second,
  * bit 0 = first wait succeeded, bit 1 = second wait succeeded}.  limit_ns in (0, 10 s]. */
 int kvz_selftest_bounded_wait(uint64_t limit_ns, uint32_t *status, uint64_t *out, kvz_stream_t stream);
+
+/* kvz_selftest_late_writer -- test helper with no counterpart on the pages: a kernel that
+ * lets a programmatic dependent launch begin at once, waits delay_ns (<= 1 s) on the
+ * device, then copies `bytes` (a multiple of 16, <= 1 GiB; 16-byte aligned device
+ * pointers) from src to dst.  Launched right before an overlapped attention call, it
+ * checks that the call reads q and the last pages only after the wait. */
+int kvz_selftest_late_writer(const void *src, void *dst, uint64_t bytes, uint64_t delay_ns, kvz_stream_t stream);
 
 /* Text for a KVZ_ERR_* code. */
 const char *kvz_strerror(int code);
