@@ -211,6 +211,69 @@ __global__ void __launch_bounds__(kScanThreads) k_enc_scan(EncodeParams P, int e
 }
 
 // ---------------------------------------------------------------------------------
+// packing of one staged (entry, head) slice: its K group at pair_base, its V group right
+// after, each block eligible (768 B: low bytes + codes) or raw (1024 B), in storage order,
+// and the two 8-byte group words; a group past its cursor's end is not written (offset
+// KVZ_OFFSET_INVALID, KVZ_STATUS_ARENA_FULL).  One warp.
+// ---------------------------------------------------------------------------------
+__device__ __forceinline__ void pack_groups(const EncodeParams &P, const uint8_t *stage, int lane, uint32_t tagsK,
+                                            uint32_t tagsV, uint64_t pair_base, int seq, int dst, int head)
+{
+    const uint32_t gK = group_granules(tagsK), gV = group_granules(tagsV);
+    const uint64_t end = min((uint64_t)P.cursors[2 * seq + 1], P.arena_bytes / kGranule);
+#pragma unroll 1
+    for (int kv = 0; kv < 2; ++kv) {
+        const uint64_t offset0 = pair_base + (kv ? gK : 0);
+        const uint32_t group_tags = kv ? tagsV : tagsK;
+        const bool fits = offset0 + (kv ? gV : gK) <= end;
+        uint32_t before = 0;
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t tag = (group_tags >> (8 * j)) & 0xFFu;
+            if (fits) {
+                uint32_t w[8];
+                gather_block(stage, kv, j, lane, w);
+                uint8_t *blk = P.arena + (offset0 + before) * kGranule;
+                if (tag != 0xFFu) {
+                    const uint32_t b = tag << 1;
+                    uint32_t low[4], code[2];
+#pragma unroll
+                    for (int f = 0; f < 2; ++f) {
+                        uint32_t lo03 = 0, lo47 = 0, cw = 0;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const uint32_t x = (w[f * 4 + i / 2] >> (16 * (i & 1))) & 0xFFFFu;
+                            const uint32_t sg = x >> 15, e = (x >> 7) & 0xFFu, d = (e - b) >> 1;
+                            if (i < 4) {
+                                lo03 |= (x & 0xFFu) << (8 * i);
+                                cw |= ((sg << 7) | d) << (8 * i);
+                            } else {
+                                lo47 |= (x & 0xFFu) << (8 * (i - 4));
+                                cw |= ((sg << 3) | (d << 4)) << (8 * (i - 4));
+                            }
+                        }
+                        low[2 * f] = lo03;
+                        low[2 * f + 1] = lo47;
+                        code[f] = cw;
+                    }
+                    *reinterpret_cast<uint4 *>(blk + 16 * lane) = make_uint4(low[0], low[1], low[2], low[3]);
+                    *reinterpret_cast<uint2 *>(blk + 512 + 8 * lane) = make_uint2(code[0], code[1]);
+                } else {
+                    *reinterpret_cast<uint4 *>(blk + 32 * lane) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4 *>(blk + 32 * lane + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+                }
+            }
+            before += tag_granules(tag);
+        }
+        if (lane == 0) {
+            const uint64_t off_word = fits ? offset0 : (uint64_t)KVZ_OFFSET_INVALID;
+            P.meta[((int64_t)dst * P.hkv + head) * 2 + kv] = off_word | ((uint64_t)group_tags << 32);
+            if (!fits) atomicOr(P.status, KVZ_STATUS_ARENA_FULL);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------
 // launch 3: pack
 // ---------------------------------------------------------------------------------
 // Warp-per-item pack: each warp stages one (entry, head) slice in its own shared-memory
@@ -246,60 +309,8 @@ __global__ void __launch_bounds__(kPackWarps * 32, 2) k_enc_pack_w(EncodeParams 
         __syncwarp();
         // one tag byte per block, as the size pass found them
         const uint64_t tags = P.ws_tags[it];
-        const uint32_t tagsK = (uint32_t)tags, tagsV = (uint32_t)(tags >> 32);
-        const uint32_t gK = group_granules(tagsK), gV = group_granules(tagsV);
-        const uint64_t pair_base = (uint64_t)P.ws_page_base[entry] + before_heads;
-        const uint64_t end = min((uint64_t)P.cursors[2 * seq + 1], P.arena_bytes / kGranule);
-#pragma unroll 1
-        for (int kv = 0; kv < 2; ++kv) {
-            const uint64_t offset0 = pair_base + (kv ? gK : 0);
-            const uint32_t group_tags = kv ? tagsV : tagsK;
-            const bool fits = offset0 + (kv ? gV : gK) <= end;
-            uint32_t before = 0;
-#pragma unroll 1
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t tag = (group_tags >> (8 * j)) & 0xFFu;
-                if (fits) {
-                    uint32_t w[8];
-                    gather_block(stage, kv, j, lane, w);
-                    uint8_t *blk = P.arena + (offset0 + before) * kGranule;
-                    if (tag != 0xFFu) {
-                        const uint32_t b = tag << 1;
-                        uint32_t low[4], code[2];
-#pragma unroll
-                        for (int f = 0; f < 2; ++f) {
-                            uint32_t lo03 = 0, lo47 = 0, cw = 0;
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const uint32_t x = (w[f * 4 + i / 2] >> (16 * (i & 1))) & 0xFFFFu;
-                                const uint32_t sg = x >> 15, e = (x >> 7) & 0xFFu, d = (e - b) >> 1;
-                                if (i < 4) {
-                                    lo03 |= (x & 0xFFu) << (8 * i);
-                                    cw |= ((sg << 7) | d) << (8 * i);
-                                } else {
-                                    lo47 |= (x & 0xFFu) << (8 * (i - 4));
-                                    cw |= ((sg << 3) | (d << 4)) << (8 * (i - 4));
-                                }
-                            }
-                            low[2 * f] = lo03;
-                            low[2 * f + 1] = lo47;
-                            code[f] = cw;
-                        }
-                        *reinterpret_cast<uint4 *>(blk + 16 * lane) = make_uint4(low[0], low[1], low[2], low[3]);
-                        *reinterpret_cast<uint2 *>(blk + 512 + 8 * lane) = make_uint2(code[0], code[1]);
-                    } else {
-                        *reinterpret_cast<uint4 *>(blk + 32 * lane) = make_uint4(w[0], w[1], w[2], w[3]);
-                        *reinterpret_cast<uint4 *>(blk + 32 * lane + 16) = make_uint4(w[4], w[5], w[6], w[7]);
-                    }
-                }
-                before += tag_granules(tag);
-            }
-            if (lane == 0) {
-                const uint64_t off_word = fits ? offset0 : (uint64_t)KVZ_OFFSET_INVALID;
-                P.meta[((int64_t)dst * P.hkv + head) * 2 + kv] = off_word | ((uint64_t)group_tags << 32);
-                if (!fits) atomicOr(P.status, KVZ_STATUS_ARENA_FULL);
-            }
-        }
+        pack_groups(P, stage, lane, (uint32_t)tags, (uint32_t)(tags >> 32),
+                    (uint64_t)P.ws_page_base[entry] + before_heads, seq, dst, head);
     }
 }
 

@@ -50,11 +50,16 @@ def spread_cfg(lo, hi, seed, hkv=2):
     return kvgen.KVConfig(f"spread{lo}-{hi}", 1, 1, 4 * hkv, hkv, 8, spread=(lo, hi), seed=seed)
 
 
+# KV head counts from 1 to 16
 @pytest.mark.parametrize("cfg", [kvgen.C0, spread_cfg(8, 20, 5), spread_cfg(8, 14, 6), spread_cfg(16, 20, 7),
                                  kvgen.KVConfig("llama-like", 1, 1, 32, 8, 6, k_log2_sigma=(-4, 3),
                                                 v_log2_sigma=(-3, 1), k_outlier_channels=4,
-                                                k_outlier_scale=32.0, seed=9)],
-                         ids=lambda c: c.name)
+                                                k_outlier_scale=32.0, seed=9),
+                                 spread_cfg(8, 20, 21, hkv=1), spread_cfg(8, 20, 22, hkv=3),
+                                 kvgen.KVConfig("hkv16-two-pass", 1, 1, 32, 16, 9, k_log2_sigma=(-4, 3),
+                                                v_log2_sigma=(-3, 1), k_outlier_channels=4,
+                                                k_outlier_scale=32.0, seed=23)],
+                         ids=lambda c: f"{c.name}-hkv{c.hkv}")
 def test_encode_bit_exact(kvz, oracle, cfg):
     n = cfg.num_pages
     pool = kvgen.gen_pages(cfg, n)
@@ -81,9 +86,11 @@ def test_encode_extremes_all_eligible_and_all_raw(kvz, oracle):
         assert int(ora[2][0, 0]) == n * 4 * 2 * per_group
 
 
-def test_encode_many_cursors_and_scan_tiles(kvz, oracle):
-    """Thousands of (page, head) pairs -> several scan tiles, segments crossing tiles."""
-    cfg = kvgen.KVConfig("scan", 1, 1, 32, 8, 1200, k_log2_sigma=(-4, 3), v_log2_sigma=(-3, 1),
+@pytest.mark.parametrize("hkv", [8, 16], ids=lambda h: f"hkv{h}")
+def test_encode_many_cursors_and_scan_tiles(kvz, oracle, hkv):
+    """Thousands of (page, head) pairs in ten cursors of 1 to 210 pages: segments that cross
+    the placement scan's tiles."""
+    cfg = kvgen.KVConfig("scan", 1, 1, 2 * hkv, hkv, 1200, k_log2_sigma=(-4, 3), v_log2_sigma=(-3, 1),
                          block_outlier_frac=0.2, seed=13)
     n = cfg.num_pages
     pool = kvgen.gen_pages(cfg, n)
