@@ -453,50 +453,72 @@ def oracle_encode_rate(cfg: kvgen.KVConfig, mib: int = 64, threads: int = 1) -> 
     return threads * pool.nbytes / dt / 1e9
 
 
-def oracle_sample(cfg: kvgen.KVConfig, budget_s: float, seqs_max: int | None = None, threads: int | None = None):
-    """Time the CPU oracle's decode attention (decode of the compressed pages + fp64
-    attention) on the workload's sequences, on all host cores: as many sequences as the
-    budget allows, repeated until about `budget_s` seconds of work have been timed.
-    Returns (logical GB/s, seconds timed, sequences per pass, passes, threads)."""
-    import oracle
+class OracleSample:
+    """The CPU oracle's decode attention (decode of the compressed pages + fp64 attention)
+    on sequences of one layer of the workload: the layer is generated and encoded by the
+    oracle once, then timed in passes on all host cores (the oracle's C calls release the
+    GIL and thread over (sequence, KV head) units)."""
 
-    oracle.build()
-    lay = kvgen.gen_layout(cfg)
-    table, seq_lens = lay["table"].numpy(), lay["seq_lens"].numpy()
-    pool = kvgen.bits(kvgen.gen_pages(cfg, cfg.num_pages))
-    q = kvgen.bits(kvgen.gen_q(cfg))
-    threads = threads or os.cpu_count() or 1
+    def __init__(self, cfg: kvgen.KVConfig, threads: int | None = None):
+        import oracle
 
-    def prepare(sel):
-        full = table[sel, : cfg.full_pages]
-        tail = table[sel, cfg.full_pages] if cfg.tail_max > 0 else np.full(len(sel), -1, np.int32)
+        oracle.build()
+        self.oracle, self.cfg = oracle, cfg
+        lay = kvgen.gen_layout(cfg)
+        self.table, self.seq_lens = lay["table"].numpy(), lay["seq_lens"].numpy()
+        self.pool = kvgen.bits(kvgen.gen_pages(cfg, cfg.num_pages))
+        self.q = kvgen.bits(kvgen.gen_q(cfg))
+        self.threads = threads or os.cpu_count() or 1
+        self.sel, self.prep = None, None
+
+    def _prepare(self, sel):
+        cfg = self.cfg
+        full = self.table[sel, : cfg.full_pages]
+        tail = self.table[sel, cfg.full_pages] if cfg.tail_max > 0 else np.full(len(sel), -1, np.int32)
         meta = np.zeros((cfg.num_pages, cfg.hkv, 2), np.uint64)
         per = (cfg.full_pages + 1) * cfg.hkv * 32
         arena = np.zeros(len(sel) * per * 256, np.uint8)
         cur = np.array([[i * per, (i + 1) * per] for i in range(len(sel))], np.uint32)
         src = full.reshape(-1).astype(np.int32)
         seq = np.repeat(np.arange(len(sel), dtype=np.int32), cfg.full_pages)
-        oracle.encode_pages(pool, src, src, seq, meta, arena, cur, cfg.hkv)
+        self.oracle.encode_pages(self.pool, src, src, seq, meta, arena, cur, cfg.hkv)
         return full, tail, meta, arena
 
-    def run(sel, prep):
+    def _run(self, sel, prep) -> float:
         full, tail, meta, arena = prep
         t0 = time.perf_counter()
-        oracle.decode_attention(q[sel], full, seq_lens[sel], tail, meta, arena, pool, cfg.hkv, nthreads=threads)
+        self.oracle.decode_attention(self.q[sel], full, self.seq_lens[sel], tail, meta, arena, self.pool, self.cfg.hkv,
+                                     nthreads=self.threads)
         return time.perf_counter() - t0
 
-    # calibrate with one sequence (all its KV heads), then size one pass to the budget
-    one = [0]
-    t1 = run(one, prepare(one))
-    n = max(1, min(seqs_max or cfg.batch, cfg.batch, int(budget_s / max(t1, 1e-6) * min(threads, cfg.hkv))))
-    sel = list(range(n))
-    prep = prepare(sel)
-    total, passes = 0.0, 0
-    while passes == 0 or (total < budget_s and passes < 1000):
-        total += run(sel, prep)
-        passes += 1
-    logical = int(seq_lens[sel].sum()) * cfg.hkv * 2 * 128 * 2 * passes
-    return logical / total / 1e9, total, n, passes, threads
+    def size_for(self, budget_s: float, seqs_max: int | None = None):
+        """Pick as many sequences as one pass of about budget_s seconds takes (calibrated on
+        one sequence), encode them once."""
+        one = [0]
+        t1 = self._run(one, self._prepare(one))
+        cfg = self.cfg
+        n = max(1, min(seqs_max or cfg.batch, cfg.batch, int(budget_s / max(t1, 1e-6) * min(self.threads, cfg.hkv))))
+        self.sel = list(range(n))
+        self.prep = self._prepare(self.sel)
+
+    def time(self, budget_s: float):
+        """Passes over the chosen sequences until about budget_s seconds have been timed:
+        (logical GB/s, seconds timed, sequences per pass, passes, threads)."""
+        total, passes = 0.0, 0
+        while passes == 0 or (total < budget_s and passes < 1000):
+            total += self._run(self.sel, self.prep)
+            passes += 1
+        logical = int(self.seq_lens[self.sel].sum()) * self.cfg.hkv * 2 * 128 * 2 * passes
+        return logical / total / 1e9, total, len(self.sel), passes, self.threads
+
+
+def oracle_sample(cfg: kvgen.KVConfig, budget_s: float, seqs_max: int | None = None, threads: int | None = None):
+    """Time the CPU oracle's decode attention on the workload's sequences for about
+    budget_s seconds.  Returns (logical GB/s, seconds timed, sequences per pass, passes,
+    threads)."""
+    o = OracleSample(cfg, threads)
+    o.size_for(budget_s, seqs_max)
+    return o.time(budget_s)
 
 
 # --------------------------------------------------------------------------------------
@@ -1565,10 +1587,12 @@ def run_reference(args, dist, rank, world):
     cfg = layer_cfg("c2-layer" if wl == "c2" else wl)
     K, Wm = args.steps, args.warmup
     per_step_budget = max(0.5, min(4.0, 150.0 / max(1, K + Wm)))
+    sample = OracleSample(cfg)  # the layer generated and encoded by the oracle once
+    sample.size_for(per_step_budget, seqs_max=cfg.batch)
     vals, secs = [], []
     nseq = threads = 0
     for k in range(Wm + K):
-        gbps, dt, nseq, passes, threads = oracle_sample(cfg, per_step_budget, seqs_max=cfg.batch)
+        gbps, dt, nseq, passes, threads = sample.time(per_step_budget)
         if k >= Wm:
             vals.append(gbps)
             secs.append(dt)

@@ -47,10 +47,6 @@ def _attend(kvz, layer, a, q, flags, out_c=None, out_r=None, status=None):
         kvz.decode_attention_raw(q, a.raw_table, a.lens, layer.g_pool, out_r, status, workspace=a.ws_r, flags=flags)
 
 
-def _calls(kvz, layer, a, q, flags, out_c, out_r, status):
-    _attend(kvz, layer, a, q, flags, out_c, out_r, status)
-
-
 CASES = [
     kvgen.C0_TAIL,
     kvgen.KVConfig("ragged-b6", 1, 6, 16, 4, 9, tail_min=1, tail_max=15, k_log2_sigma=(-4, 3), v_log2_sigma=(-3, 1),
@@ -67,10 +63,10 @@ def test_overlap_matches_plain_calls(kvz, oracle, cfg):
     shape = (cfg.batch, cfg.hq, 128)
     outs = {k: torch.empty(shape, dtype=torch.float32, device="cuda") for k in ("c0", "r0", "c1", "r1")}
     st = kvz.new_status()
-    _calls(kvz, layer, a, layer.g_q, 0, outs["c0"], outs["r0"], st)
+    _attend(kvz, layer, a, layer.g_q, 0, outs["c0"], outs["r0"], st)
     # overlapped calls back to back: each also overlaps the previous call's merge
-    _calls(kvz, layer, a, layer.g_q, OVER, outs["c1"], outs["r1"], st)
-    _calls(kvz, layer, a, layer.g_q, OVER, outs["c1"], outs["r1"], st)
+    _attend(kvz, layer, a, layer.g_q, OVER, outs["c1"], outs["r1"], st)
+    _attend(kvz, layer, a, layer.g_q, OVER, outs["c1"], outs["r1"], st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     for k in ("c1", "r1"):
