@@ -21,7 +21,8 @@ layer of the 8K stack compressed against raw, the streaming Qwen3-8B-shaped step
 page-completion encodes and the capacity count, and one 131072-token layer with the
 encode/decode throughput at 1-4 GB.
 
-Timing rules: >= 3 warm-up steps; inputs larger than L2 (the stack) or rotating copies
+Timing rules: 10 warm-up steps and 50 timed steps per run by default (at least 3 warm-up
+steps whatever the flags); inputs larger than L2 (the stack) or rotating copies
 of the KV (single layers: 3 copies, > L2) so every step reads cold data; CUDA events on
 the launching stream, synchronize on both sides, max over ranks.  `--impl reference`
 times the CPU oracle on the same configuration (the reference arm of this build).
@@ -1622,8 +1623,8 @@ def run_reference(args, dist, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="kvz", choices=["kvz", "reference"])
     ap.add_argument("--workload", default="c2", choices=["c2", "c2-layer", "c1", "c4", "c3", "serve"],
                     help="c2: the full 32-layer 8K step (default headline); c2-layer / c1 / c4: one layer as the "
