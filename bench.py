@@ -198,6 +198,7 @@ def config_dict(workload: str, world: int) -> dict:
         cfg = kvgen.C3
         return {"workload": cfg.name, "layers": cfg.layers, "batch": cfg.batch, "q_heads": cfg.hq,
                 "kv_heads": cfg.hkv, "head_dim": 128, "page_tokens": 16, "prompt_tokens": 2048,
+                "launch": "overlapped layer calls (layer 0 of a step plain: it follows the appends and encodes)",
                 "parallelism": par}
     cfg = layer_cfg(workload)
     return {"workload": cfg.name + ("" if workload == "c1" else "-one-layer"), "layers": 1, "batch": cfg.batch,
@@ -933,14 +934,17 @@ def measure_stream(args, dev, local, world: int) -> dict:
             ev = torch.cuda.Event()
             ev.record()
             pending = (ticket, ev)
+        # layer 0 follows the tail append and the encodes: a plain launch; every later layer
+        # follows the previous layer's attention and overlaps its start-up with it
         for layer in range(L):
             kvz.decode_attention(qs[layer], full_table, seq_lens[t], tails[t], meta[layer], arena, raw[layer], out_c,
-                                 status, workspace=ws_c)
+                                 status, workspace=ws_c, flags=OVERLAP if layer else 0)
 
     def step_raw(t):
         append(t)
         for layer in range(L):
-            kvz.decode_attention_raw(qs[layer], table, seq_lens[t], raw[layer], out_r, status, workspace=ws_r)
+            kvz.decode_attention_raw(qs[layer], table, seq_lens[t], raw[layer], out_r, status, workspace=ws_r,
+                                     flags=OVERLAP if layer else 0)
 
     def run(step_fn):
         times = []

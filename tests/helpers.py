@@ -102,19 +102,19 @@ class Layer:
         tp = self.raw_table().shape[1] if raw else self.full.shape[1] + 1
         return torch.empty(self.kvz.attention_workspace_size(hkv, B, hq, tp), dtype=torch.uint8, device="cuda")
 
-    def run_compressed(self, out=None, meta=None, status=None):
+    def run_compressed(self, out=None, meta=None, status=None, flags=0):
         out = torch.empty((self.cfg.batch, self.cfg.hq, 128), dtype=torch.float32, device="cuda") if out is None else out
         st = self.status if status is None else status
         self.kvz.decode_attention(self.g_q, self.full.cuda(), self.seq_lens.cuda(), self.tail.cuda(),
                                   self.meta if meta is None else meta, self.arena, self.g_pool, out, st,
-                                  workspace=self.workspace(False))
+                                  workspace=self.workspace(False), flags=flags)
         return out
 
-    def run_raw(self, out=None, status=None):
+    def run_raw(self, out=None, status=None, flags=0):
         out = torch.empty((self.cfg.batch, self.cfg.hq, 128), dtype=torch.float32, device="cuda") if out is None else out
         st = self.status if status is None else status
         self.kvz.decode_attention_raw(self.g_q, self.raw_table().cuda(), self.seq_lens.cuda(), self.g_pool,
-                                      out, st, workspace=self.workspace(True))
+                                      out, st, workspace=self.workspace(True), flags=flags)
         return out
 
     def oracle_attention(self, oracle, nthreads=8, meta=None):
