@@ -209,3 +209,96 @@ def test_encode_sizes_match_the_oracle_placement(kvz, oracle, cfg):
     torch.cuda.synchronize()
     assert int(st.item()) == kvz.STATUS_BAD_INDEX
     assert (g_sizes.cpu() == 0).all()
+
+
+def _large_case(hkv, n, seed, cursors=10):
+    """A pool of n pages (70-110 MB of BF16), placed through `cursors` cursors of ragged run
+    lengths, shuffled sources and destinations."""
+    cfg = kvgen.KVConfig("large", 1, 1, 2 * hkv, hkv, n, k_log2_sigma=(-4, 3), v_log2_sigma=(-3, 1),
+                         block_outlier_frac=0.2, seed=seed)
+    pool = kvgen.gen_pages(cfg, n)
+    rng = np.random.default_rng(seed)
+    cuts = np.sort(rng.choice(np.arange(1, n), cursors - 1, replace=False))
+    sizes = np.diff(np.concatenate([[0], cuts, [n]]))
+    seq = np.repeat(np.arange(cursors, dtype=np.int32), sizes)
+    worst = sizes.astype(np.int64) * hkv * 2 * 16
+    starts = np.concatenate([[7], 7 + np.cumsum(worst + 5)[:-1]])
+    cur = np.stack([starts, starts + worst], 1).astype(np.uint32)
+    return pool, rng.permutation(n).astype(np.int32), rng.permutation(n).astype(np.int32), seq, cur
+
+
+@pytest.mark.parametrize("hkv,n", [(1, 9000), (2, 5000), (8, 1700)], ids=lambda v: str(v))
+def test_encode_large_inputs(kvz, oracle, hkv, n):
+    """Inputs larger than L2 through ragged cursors: bytes, metadata and cursors against
+    the oracle."""
+    pool, src, dst, seq, cur = _large_case(hkv, n, seed=50 + hkv)
+    gpu, ora = encode_both(kvz, oracle, pool, src, dst, seq, n, int(cur[-1, 1]) * 256, cur)
+    assert_same(gpu, ora)
+
+
+def test_encode_large_arena_full_and_bad_index(kvz, oracle):
+    hkv, n = 8, 1500
+    pool, src, dst, seq, cur = _large_case(hkv, n, seed=61)
+    # the fourth cursor's region holds a third of its worst case: some of its groups, in
+    # the middle of the input, do not fit
+    cur = cur.copy()
+    cur[3, 1] = cur[3, 0] + (cur[3, 1] - cur[3, 0]) // 3
+    gpu, ora = encode_both(kvz, oracle, pool, src, dst, seq, n, int(cur[-1, 1]) * 256, cur)
+    assert ora[3] == oracle.ARENA_FULL
+    assert_same(gpu, ora)
+    # a source page out of range: nothing is written, cursors unchanged
+    bad = src.copy()
+    bad[n // 2] = n + 3
+    gpu, ora = encode_both(kvz, oracle, pool, bad, dst, seq, n, int(cur[-1, 1]) * 256, cur)
+    assert ora[3] == oracle.BAD_INDEX
+    assert_same(gpu, ora)
+
+
+def test_encode_reused_workspace_and_graph(kvz, oracle):
+    """Two calls through one workspace, then the same call captured in a CUDA graph and
+    replayed: the per-call state in the workspace (validation word, page-size sums) is
+    reset by every call."""
+    hkv, n = 4, 2400
+    pool, src, dst, seq, cur = _large_case(hkv, n, seed=71)
+    arena_bytes = int(cur[-1, 1]) * 256
+    o_meta = np.zeros((n, hkv, 2), np.uint64)
+    o_arena = np.zeros(arena_bytes, np.uint8)
+    o_cur = cur.copy()
+    assert oracle.encode_pages(kvgen.bits(pool), src, dst, seq, o_meta, o_arena, o_cur, hkv) == 0
+    g_pool = pool.cuda()
+    g_src, g_dst, g_seq = (torch.from_numpy(a).cuda() for a in (src, dst, seq))
+    ws = torch.empty(kvz.encode_workspace_size(hkv, n), dtype=torch.uint8, device="cuda")
+    meta = torch.zeros((n, hkv, 2), dtype=torch.int64, device="cuda")
+    arena = torch.zeros(arena_bytes, dtype=torch.uint8, device="cuda")
+    cursors = torch.zeros((len(cur), 2), dtype=torch.int32, device="cuda")
+    st = kvz.new_status()
+    cur0 = torch.from_numpy(cur.view(np.int32).copy()).cuda()
+
+    def call():
+        cursors.copy_(cur0)
+        meta.zero_()
+        arena.zero_()
+        kvz.encode_pages(g_pool, g_src, g_dst, g_seq, meta, arena, cursors, st, workspace=ws)
+
+    def check(what):
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0, what
+        assert np.array_equal(cursors.cpu().numpy().view(np.uint32), o_cur), what
+        assert np.array_equal(meta.cpu().numpy().view(np.uint64), o_meta), what
+        assert np.array_equal(arena.cpu().numpy(), o_arena), what
+
+    for k in range(2):
+        call()
+        check(f"eager call {k}")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call()  # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    check("side-stream call")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    for k in range(2):
+        g.replay()
+        check(f"graph replay {k}")
