@@ -264,8 +264,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
         if (lane == 31) pref[B] = incl;
     }
     __syncthreads();
-    if (blockIdx.x == 0 && !P.overlap)
-        for (int b = tid; b <= B; b += kThreads) P.prefix[b] = pref[b];
 
     const int64_t T = (int64_t)hkv * pref[B];
     const int64_t C = gridDim.x, c = blockIdx.x;
@@ -448,13 +446,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
     float *mlv = reinterpret_cast<float *>(smem + Smem::ml);
     float *mo = reinterpret_cast<float *>(smem + Smem::mo);
     bool ok = true;
-    if (P.overlap) {
-        // overlapped launch: q, the workspace and the outputs belong to the kernel before
-        // this one until it has finished
-        pdl_wait_primary();
-        if (blockIdx.x == 0)
-            for (int b = tid; b <= B; b += kConsumers * 32) P.prefix[b] = pref[b];
-    }
+    // overlapped launch: q, the workspace and the outputs belong to the kernel before this
+    // one until it has finished
+    if (P.overlap) pdl_wait_primary();
     int64_t x = lo, ibase = 0;
     while (x < hi) {
         const PageLoc L = locate(pref, B, hkv, x);
@@ -967,14 +961,38 @@ template <int kGroups>
 __global__ void __launch_bounds__(128 * kGroups, 1) k_attn_merge(const AttnParams P)
 {
     __shared__ float gm[kGroups][4], gl[kGroups][4], go[kGroups][4][128];
-    if (P.overlap) {
-        pdl_launch_dependents();  // the next overlapped call may place its CTAs
-        pdl_wait_primary();       // the attention grid's partials and prefix are complete
-    }
+    __shared__ int s_cnt[kGroups * 4][3];
+    if (P.overlap) pdl_launch_dependents();  // the next overlapped call may place its CTAs
     const int u = blockIdx.x, hkv = P.hkv, G = P.G;
     const int b = u / hkv, kvh = u % hkv, d = threadIdx.x & 127, grp = threadIdx.x >> 7;
-    const int32_t pb = P.prefix[b], pb1 = P.prefix[b + 1], pB = P.prefix[P.batch];
-    const int64_t n = pb1 - pb;
+    // pages of the sequences before b, of b, and of all, from the lengths (the attention
+    // kernel's count), before the wait: the lengths were complete before the call started
+    int pb = 0, nb = 0, pB = 0;
+    for (int i = threadIdx.x; i < P.batch; i += blockDim.x) {
+        const int L = P.seq_lens[i];
+        const int pages = L > 0 ? (L + kPage - 1) / kPage : 0;
+        pB += pages;
+        pb += i < b ? pages : 0;
+        nb += i == b ? pages : 0;
+    }
+    pb = __reduce_add_sync(0xffffffffu, pb);
+    nb = __reduce_add_sync(0xffffffffu, nb);
+    pB = __reduce_add_sync(0xffffffffu, pB);
+    if ((threadIdx.x & 31) == 0) {
+        s_cnt[threadIdx.x >> 5][0] = pb;
+        s_cnt[threadIdx.x >> 5][1] = nb;
+        s_cnt[threadIdx.x >> 5][2] = pB;
+    }
+    __syncthreads();
+    pb = nb = pB = 0;
+#pragma unroll
+    for (int w = 0; w < kGroups * 4; ++w) {
+        pb += s_cnt[w][0];
+        nb += s_cnt[w][1];
+        pB += s_cnt[w][2];
+    }
+    if (P.overlap) pdl_wait_primary();  // the attention grid's partials are complete
+    const int64_t n = nb;
     const int64_t T = (int64_t)hkv * pB;
     const int64_t C = P.grid;
     float *out = P.out + ((int64_t)b * hkv * G + (int64_t)kvh * G) * kDim;

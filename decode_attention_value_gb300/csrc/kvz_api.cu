@@ -160,8 +160,6 @@ int run_attention(const FormatArgs &F, const kvz_dims &d, int batch, int hq, con
     P.num_raw_pages = num_raw_pages;
     P.out = out;
     uint8_t *w = static_cast<uint8_t *>(ws);
-    P.prefix = reinterpret_cast<int32_t *>(w);
-    w += attn_ws_prefix_bytes(batch);
     const size_t slots = attn_slots(batch, hkv, grid);
     P.part_o = reinterpret_cast<float *>(w);
     w += slots * attn_slot_heads(hq / hkv) * 128 * 4;

@@ -91,7 +91,6 @@ struct AttnParams {
     float *out;
     float *part_o;     // [slots][4 or 8][128] (heads per slot: attn_slot_heads(G))
     float *part_ml;    // [slots][4 or 8][2]
-    int32_t *prefix;   // [batch + 1] page prefix per sequence, written by CTA 0
     uint32_t *status;
     float scale_log2;  // log2(e) / sqrt(128)
     int overlap;       // 1: launched as programmatic dependents (KVZ_ATTN_OVERLAP_PREVIOUS)
@@ -101,14 +100,12 @@ inline size_t attn_slots(int batch, int hkv, int grid) { return (size_t)batch * 
 // heads per partial slot: 4 for G <= 4, 8 for G = 5..8
 inline int attn_slot_heads(int G) { return G > 4 ? 8 : 4; }
 
-// workspace layout: prefix (batch+1 int32, rounded to 16 B), part_o, part_ml
-inline size_t attn_ws_prefix_bytes(int batch) { return ((size_t)(batch + 1) * 4 + 15) / 16 * 16; }
+// workspace layout: part_o, part_ml
 inline size_t attn_ws_bytes(int batch, int hkv, int grid, int G = 4)
 {
-    size_t pre = attn_ws_prefix_bytes(batch);
     size_t slots = attn_slots(batch, hkv, grid);
     const size_t gs = (size_t)attn_slot_heads(G);
-    return pre + slots * gs * 128 * 4 + slots * gs * 2 * 4;
+    return slots * gs * 128 * 4 + slots * gs * 2 * 4;
 }
 
 cudaError_t launch_encode(const EncodeParams &P, cudaStream_t stream);
