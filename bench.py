@@ -160,7 +160,9 @@ def profiled_traffic(workload: str, kernel: str = "compressed"):
     """dram bytes per launch of an attention kernel ("compressed" = 12-bit groups,
     "tiles" = group-adaptive tiles) from the committed ncu summary, if it was taken on
     the current kernel source."""
-    p = os.path.join(ROOT, "profiles", f"k_attn_{kernel}_{workload}.md")
+    # the C2 profile is of one layer of the stack: the c2-layer workload's kernel launch
+    name = {"c2-layer": "c2"}.get(workload, workload)
+    p = os.path.join(ROOT, "profiles", f"k_attn_{kernel}_{name}.md")
     if not os.path.exists(p):
         return None
     vals = {}
