@@ -18,8 +18,8 @@ figure through the C ABI with host buffers (every layer's queries in, every laye
 output back, each step), the CPU oracle on the host cores, and as extra keys: one C1
 layer (batch 32, 2K context) with encode / standalone decode / decompress-first, one
 layer of the 8K stack compressed against raw, the streaming Qwen3-8B-shaped step with
-page-completion encodes and the capacity count, and one 131072-token layer with the
-encode/decode throughput at 1-4 GB.
+page-completion encodes and the capacity count, one 131072-token layer with the
+encode/decode throughput at 1-4 GB, and the full 32-layer 131072-token step.
 
 Timing rules: 10 warm-up steps and 50 timed steps per run by default (at least 3 warm-up
 steps whatever the flags); inputs larger than L2 (the stack) or rotating copies
@@ -744,9 +744,10 @@ def stack_e2e(layers, K: int, dev, dist, world: int, flags: int = 0) -> dict:
             "launch": "overlapped (KVZ_ATTN_OVERLAP_PREVIOUS)" if flags else "plain"}
 
 
-def measure_stack(args, dev, local, dist, world: int, rank: int) -> dict:
-    """The full 32-layer 8K decode step, compressed and raw, plus its end-to-end leg."""
-    cfg = kvgen.C2
+def measure_stack(args, dev, local, dist, world: int, rank: int, cfg: kvgen.KVConfig = kvgen.C2,
+                  profile: str = "c2", e2e_leg: bool = True) -> dict:
+    """A full decode step over every layer of a stack (the 32-layer 8K step by default),
+    compressed and raw, overlapped and plain calls, plus its end-to-end leg."""
     peak, peak_kind = measured_peaks()
     layers = stack_layers(cfg, dev)
     L = cfg.layers
@@ -802,7 +803,7 @@ def measure_stack(args, dev, local, dist, world: int, rank: int) -> dict:
     blocks = sum(W.blocks for W in layers)
     raw_blocks = sum(W.raw_blocks for W in layers)
     block_bytes = sum(W.block_bytes for W in layers)
-    e2e = stack_e2e(layers, K, dev, dist, world, flags=OVERLAP)
+    e2e = stack_e2e(layers, K, dev, dist, world, flags=OVERLAP) if e2e_leg else None
     us_co, us_ro = med_co * 1e3 / K, med_ro * 1e3 / K
     launch_us = us_co / L  # one attention launch + its merge, averaged over the layers of a step
     achieved = alg / L / (launch_us * 1e-6) / 1e9
@@ -819,16 +820,17 @@ def measure_stack(args, dev, local, dist, world: int, rank: int) -> dict:
         "bit_identical_compressed_vs_raw": identical,
         "compressed_GB": round(block_bytes / 1e9, 3), "logical_GB_per_step": round(logical / 1e9, 3),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic("c2"), "peak_kind": peak_kind,
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(profile), "peak_kind": peak_kind,
                      "kernel": "k_attn<12-bit groups> + k_attn_merge (one layer's call)",
                      "launch_us": round(launch_us, 3), "algorithmic_bytes_per_launch": round(alg / L),
-                     "how": "algorithmic bytes of one layer's call (mean over the 32 layers) / (median step time / 32); "
-                            "traffic: dram bytes of one launch on one layer of this stack (ncu summary in profiles/)"},
+                     "how": f"algorithmic bytes of one layer's call (mean over the {L} layers) / (median step time / "
+                            f"{L}); traffic: dram bytes of one launch on one layer of this stack (ncu summary in "
+                            "profiles/)"},
         "roofline_raw": {"achieved": round(achieved_r, 1), "frac": round(achieved_r / peak, 4),
                          "algorithmic_bytes_per_step": alg_r},
         "runs": {**runs_summary(ms_co, K), "how": f"{RUNS} timed runs of the {K}-step graph, median reported"},
         "runs_raw": runs_summary(ms_ro, K),
-        "e2e": e2e, "clocks": clocks, "gpu_launches": 2 * L * K,
+        "clocks": clocks, "gpu_launches": 2 * L * K,
         "plain_launches": {
             "us_per_step": round(us_c, 2), "raw_us_per_step": round(us_r, 2), "speedup_vs_raw": round(us_r / us_c, 4),
             "logical_GBps": round(job_throughput(world, logical, K, med_c), 2),
@@ -837,6 +839,8 @@ def measure_stack(args, dev, local, dist, world: int, rank: int) -> dict:
             "how": "the same step with kvz_decode_attention / kvz_decode_attention_raw (each layer's call starts "
                    "after the previous one has finished)"},
     }
+    if e2e is not None:
+        res["e2e"] = e2e
     del layers, g_c, g_r, g_co, g_ro
     torch.cuda.empty_cache()
     return res
@@ -1484,7 +1488,8 @@ def base_line(workload: str, world: int, args, value: float, us_step: float) -> 
 def run_default(args, dist, rank, world, local):
     """Headline: the full 32-layer 8K decode step (C2).  Extra keys: one C1 layer, one
     layer of the 8K stack, one 131072-token layer with the codec throughput at 1-4 GB,
-    and the streaming C3 step with page-completion encodes and the capacity count."""
+    the streaming C3 step with page-completion encodes and the capacity count, and the
+    full 32-layer 131072-token step (C4)."""
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     S = measure_stack(args, dev, local, dist, world, rank)
@@ -1506,6 +1511,12 @@ def run_default(args, dist, rank, world, local):
         del flush
         torch.cuda.empty_cache()
         extras["c3_streaming"] = measure_stream(args, dev, local, world)
+        # the 131072-token stack: every layer's call of one decode step (32 x ~0.92 GB compressed)
+        S4 = measure_stack(args, dev, local, dist, world, rank, cfg=kvgen.C4, profile="c4", e2e_leg=False)
+        extras["c4_stack"] = {"workload": kvgen.C4.name + "-full-stack", "layers": kvgen.C4.layers,
+                              "batch": kvgen.C4.batch, "context_tokens": kvgen.C4.full_pages * 16,
+                              "logical_GBps": S4["value"],
+                              **{k: v for k, v in S4.items() if k not in ("value", "ms_per_step", "launch")}}
     cpu = None
     cfg1 = kvgen.KVConfig(**{**kvgen.C2.__dict__, "layers": 1})
     if rank == 0 and not args.no_cpu_baseline:
