@@ -9,7 +9,7 @@ import pytest
 import torch
 
 import kvgen
-from helpers import Layer, check_attention
+from helpers import F8Layer, GaLayer, Layer, check_attention
 
 pytestmark = pytest.mark.gpu
 
@@ -28,7 +28,7 @@ def kvz():
 
 def _case(i: int):
     rng = np.random.default_rng(9000 + i)
-    hkv = int(rng.choice([1, 2, 4, 8]))
+    hkv = int(rng.choice([1, 2, 4, 8, 16]))
     G = int(rng.integers(1, 9))
     batch = int(rng.integers(1, 41))
     full = int(rng.integers(0, 33))
@@ -89,3 +89,51 @@ def test_random_shapes_match_oracle(kvz, oracle, i):
     empty = [b for b, L in enumerate(lens) if L == 0]
     if empty:
         assert not out_c[empty].any(), f"{what}: empty sequences must give zero outputs"
+
+
+def _u32(t):
+    return t.cpu().numpy().view(np.uint32)
+
+
+@pytest.mark.parametrize("i", range(8))
+def test_random_shapes_group_adaptive_tiles(kvz, oracle, i):
+    """The group-adaptive tile format on the same random draws: calibration bases, tile
+    entries and bytes and cursors bit for bit, attention within the tolerance of the fp64
+    oracle and bit-identical to the raw kernel."""
+    cfg, lens, _ = _case(100 + i)
+    base = Layer(cfg, None, seq_lens=lens)
+    ga = GaLayer(base, oracle)
+    what = f"{cfg.name} tiles (B={cfg.batch}, Hkv={cfg.hkv}, G={cfg.hq // cfg.hkv}, pages={cfg.full_pages})"
+    assert np.array_equal(ga.bases.cpu().numpy(), ga.o_bases), what + ": bases"
+    assert np.array_equal(_u32(ga.meta), ga.o_meta), what + ": entries"
+    assert np.array_equal(ga.arena.cpu().numpy(), ga.o_arena), what + ": tile bytes"
+    assert np.array_equal(_u32(ga.cursors), ga.o_cursors), what + ": cursors"
+    out_g = ga.run()
+    out_r = base.run_raw()
+    torch.cuda.synchronize()
+    assert int(ga.status.item()) == 0 and int(base.status.item()) == 0, what
+    ref, st = ga.oracle_attention(oracle)
+    assert st == 0
+    check_attention(out_g, ref, what)
+    assert torch.equal(out_g, out_r), what + ": tile and raw outputs differ"
+
+
+@pytest.mark.parametrize("fmt", [1, 2], ids=["e4m3", "e5m2"])
+@pytest.mark.parametrize("i", range(4))
+def test_random_shapes_fp8_tiles(kvz, oracle, fmt, i):
+    """FP8 pages on the same random draws: bases, entries, tile bytes and cursors bit for
+    bit, attention within the tolerance of the fp64 oracle over the FP8 values."""
+    cfg, lens, _ = _case(200 + i)
+    base = Layer(cfg, None, seq_lens=lens)
+    f8 = F8Layer(base, fmt, oracle)
+    what = f"{cfg.name} fp8 {fmt} (B={cfg.batch}, Hkv={cfg.hkv}, G={cfg.hq // cfg.hkv}, pages={cfg.full_pages})"
+    assert np.array_equal(f8.bases.cpu().numpy(), f8.o_bases), what + ": bases"
+    assert np.array_equal(_u32(f8.meta), f8.o_meta), what + ": entries"
+    assert np.array_equal(f8.arena.cpu().numpy(), f8.o_arena), what + ": tile bytes"
+    assert np.array_equal(_u32(f8.cursors), f8.o_cursors), what + ": cursors"
+    got = f8.run()
+    torch.cuda.synchronize()
+    assert int(f8.status.item()) == 0, what
+    ref, st = f8.oracle_attention(oracle)
+    assert st == 0
+    check_attention(got, ref, what)
