@@ -403,8 +403,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                         if (d_kind == kKindPair) {
                             const uint32_t bK = d_bytes & 0xFFFFu, bV = d_bytes >> 16;
                             mbar_arrive_expect_tx(fullbar, bK + bV);
-                            bulk_copy_g2s_hint(dst, P.arena + d_srcK, bK, fullbar, stream_once);
-                            bulk_copy_g2s_hint(dst + 4096, P.arena + d_srcV, bV, fullbar, stream_once);
+                            if (!kTiles && d_srcV == d_srcK + bK) {
+                                // 12-bit groups: V right after K in the stage; one copy when the
+                                // encoder placed them next to each other (pages encoded together)
+                                bulk_copy_g2s_hint(dst, P.arena + d_srcK, bK + bV, fullbar, stream_once);
+                            } else {
+                                bulk_copy_g2s_hint(dst, P.arena + d_srcK, bK, fullbar, stream_once);
+                                bulk_copy_g2s_hint(dst + (kTiles ? 4096u : bK), P.arena + d_srcV, bV, fullbar,
+                                                   stream_once);
+                            }
                         } else if (d_kind == kKindRaw) {
                             mbar_arrive_expect_tx(fullbar, kStageBytes);
                             tensor_copy_2d_g2s_hint(dst, &tmap, 0, (int32_t)d_srcK, fullbar, stream_once);
@@ -774,7 +781,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) k_attn(const AttnParams 
                         pv(o[2 * j + 1], a1);
                     }
                 } else if (!kTiles && kCompressed && inf.kind == kKindPair) {
-                    uint32_t off = 4096;
+                    uint32_t off = group_granules(inf.tagsK) * kGranule;  // V right after K
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const uint32_t tag = (inf.tagsV >> (8 * j)) & 0xFFu;
