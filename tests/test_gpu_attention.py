@@ -220,3 +220,60 @@ def test_corrupt_metadata_fuzz(kvz, oracle):
     ref, ost = layer.oracle_attention(oracle, meta=o_meta)
     assert ost == 8
     check_attention(out, ref, "fuzzed metadata")
+
+
+def test_concurrent_streams_and_host_threads(kvz, oracle):
+    """Calls on two streams at once, each with its own workspace and output, and calls
+    from two host threads: the library keeps no per-call state outside its arguments, so
+    every output equals the one from sequential calls, bit for bit."""
+    import threading
+
+    cfgs = [kvgen.KVConfig("conc-a", 1, 12, 32, 8, 40, tail_min=1, tail_max=15, k_log2_sigma=(-4, 3),
+                           v_log2_sigma=(-3, 1), seed=71),
+            kvgen.KVConfig("conc-b", 1, 5, 16, 2, 90, tail_min=1, tail_max=15, spread=(8, 20), seed=72)]
+    layers = [Layer(c, oracle) for c in cfgs]
+    want = []
+    for layer in layers:
+        out_c, out_r = layer.run_compressed(), layer.run_raw()
+        torch.cuda.synchronize()
+        assert torch.equal(out_c, out_r)
+        ref, st = layer.oracle_attention(oracle)
+        assert st == 0
+        check_attention(out_c, ref, layer.cfg.name)
+        want.append(out_c.clone())
+
+    # two streams, both layers and both kernels on each, several rounds
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    outs = []
+    for rnd in range(3):
+        for k, layer in enumerate(layers):
+            s = streams[(k + rnd) % 2]
+            with torch.cuda.stream(s):
+                outs.append((k, layer.run_compressed(), layer.run_raw()))
+    torch.cuda.synchronize()
+    for k, out_c, out_r in outs:
+        assert torch.equal(out_c, want[k]) and torch.equal(out_r, want[k]), cfgs[k].name
+
+    # two host threads, each with its own stream
+    errors, results = [], {}
+
+    def worker(k):
+        try:
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                res = [layers[k].run_compressed() for _ in range(4)]
+            s.synchronize()
+            results[k] = res
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(k,)) for k in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for k in range(2):
+        assert all(torch.equal(o, want[k]) for o in results[k]), cfgs[k].name
+    assert all(int(layer.status.item()) == 0 for layer in layers)
